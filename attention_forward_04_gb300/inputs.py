@@ -1,0 +1,86 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module only draws numbers: it holds none of the attention arithmetic, and it
+is the one module that both the GPU tests/benchmark and the oracle side use.
+
+Recipe (the same for every caller): for a workload with seed base ``s`` the
+three tensors are drawn with ``torch.Generator().manual_seed(s + t)`` for
+t = 0 (Q), 1 (K), 2 (V) as ``torch.randn(..., dtype=float32)`` on the CPU,
+multiplied by the workload's Q/K multiplier (1, or 2 for the long-sequence
+workload; multiplying by 2 is exact in binary floating point), then cast to the
+workload's storage dtype.  Shapes follow the pages' workloads: [B, H, N, D]
+with N = 4096 and d = 128 (the shape the pages analyse), d = 64, and N up to
+16k.  There is no dataset on the pages; everything here is synthetic.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    D: int
+    dtype: str          # "fp32" or "bf16" (storage and I/O type)
+    causal: bool
+    seed: int           # seed base: Q uses seed, K seed+1, V seed+2
+    qk_mult: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def flops(self) -> float:
+        """Attention FLOPs counted as 4*B*H*N^2*D, halved for the causal mask."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.D
+        return f / 2 if self.causal else f
+
+    def with_(self, **kw) -> "Workload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return Workload(**d)
+
+
+TORCH_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}
+
+# The five workloads; seeds are 1000*c + {0,1,2} for workload number c.
+WORKLOADS = {
+    "fp32_b1h1n256d64": Workload("fp32_b1h1n256d64", 1, 1, 256, 64, "fp32", False, 1000),
+    "bf16_b2h8n1024d64": Workload("bf16_b2h8n1024d64", 2, 8, 1024, 64, "bf16", False, 2000),
+    "bf16_b4h16n4096d128": Workload("bf16_b4h16n4096d128", 4, 16, 4096, 128, "bf16", False, 3000),
+    "bf16_b8h32n4096d128_causal": Workload("bf16_b8h32n4096d128_causal", 8, 32, 4096, 128,
+                                           "bf16", True, 4000),
+    "bf16_b1h32n16384d128_x2": Workload("bf16_b1h32n16384d128_x2", 1, 32, 16384, 128, "bf16",
+                                        False, 5000, 2.0),
+    "bf16_b1h32n16384d128_x2_causal": Workload("bf16_b1h32n16384d128_x2_causal", 1, 32, 16384,
+                                               128, "bf16", True, 5000, 2.0),
+}
+
+# The workload the throughput metric is quoted on.
+HEADLINE = "bf16_b4h16n4096d128"
+
+
+def make_qkv(w: Workload, seed_offset: int = 0):
+    """Q, K, V as CPU tensors of shape [B, H, N, D] in the workload's dtype."""
+    shape = (w.B, w.H, w.N, w.D)
+    out = []
+    for t in range(3):
+        g = torch.Generator().manual_seed(w.seed + seed_offset + t)
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if t < 2 and w.qk_mult != 1.0:
+            x = x * w.qk_mult
+        out.append(x.to(TORCH_DTYPES[w.dtype]).contiguous())
+    return tuple(out)
+
+
+def make_shape(B, H, N, D, dtype="bf16", seed=7, qk_mult=1.0):
+    """Seeded Q, K, V for an arbitrary shape (edge cases in the tests)."""
+    w = Workload("adhoc", B, H, N, D, dtype, False, seed, qk_mult)
+    return make_qkv(w)
