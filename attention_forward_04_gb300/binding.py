@@ -1,0 +1,131 @@
+"""ctypes binding of libfa.so (include/fa.h): argument marshalling only.
+
+Every step of the attention forward runs in the library's CUDA kernels; this module
+turns torch tensors into pointers, sizes and a stream handle.  torch provides device
+memory and streams, nothing else.  If the library is missing the import fails loudly:
+there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_FP32, FA_BF16, FA_FP16 = 0, 1, 2
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_MISALIGNED",
+          4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+
+# Every symbol include/fa.h declares, with its ctypes signature.
+_c = ctypes
+SIGNATURES = {
+    "fa_fwd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                          _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_float, _c.c_int,
+                          _c.c_int, _c.c_void_p]),
+    "fa_status_string": (_c.c_char_p, [_c.c_int]),
+    "fa_last_cuda_error": (_c.c_char_p, []),
+    "fa_check_device_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
+    "fa_set_watchdog": (_c.c_int, [_c.c_uint64, _c.c_int]),
+    "fa_version": (_c.c_int, []),
+}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, detail: str = ""):
+        self.status = status
+        msg = STATUS.get(status, "FA_ERR_UNKNOWN(%d)" % status)
+        super().__init__(msg + (": " + detail if detail else ""))
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfa.so and declare every exported signature. Raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None and path == LIB_PATH:
+            return _lib
+        if not os.path.exists(path):
+            raise FileNotFoundError(
+                "libfa.so not found at %s: build it first (attention_forward_04_gb300.build)" % path)
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path == LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def _dtype_code(t):
+    import torch
+    codes = {torch.float32: FA_FP32, torch.bfloat16: FA_BF16, torch.float16: FA_FP16}
+    if t.dtype not in codes:
+        raise TypeError("unsupported dtype %s (fp32, bf16 or fp16)" % t.dtype)
+    return codes[t.dtype]
+
+
+def _check(status: int):
+    if status != 0:
+        lib = load_library()
+        detail = lib.fa_last_cuda_error().decode() if status == 4 else ""
+        raise FaError(status, detail)
+
+
+def fwd_ptr(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, stream=0) -> int:
+    """Raw pointer form of fa_fwd; returns the status code."""
+    return int(load_library().fa_fwd(q, k, v, o, lse, B, H, N, D, float(scale), int(causal),
+                                      int(dtype), stream))
+
+
+def fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Attention forward through the C ABI.
+
+    q, k, v: CUDA tensors [B, H, N, D], contiguous, one dtype (fp32, bf16 or fp16).
+    Returns (o [B,H,N,D] in the input dtype, lse [B,H,N] fp32).  The call is
+    asynchronous on ``stream`` (default: torch's current stream).
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, D] shape")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous [B, H, N, D]")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    with torch.cuda.device(q.device):
+        _check(fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, D, scale, causal, _dtype_code(q), handle))
+    return out, lse
+
+
+def check_device_status(stream=None):
+    """Synchronise the stream and return (status, detail words) of the kernel watchdog."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    detail = (ctypes.c_uint32 * 4)()
+    st = int(load_library().fa_check_device_status(handle, detail))
+    return st, list(detail)
+
+
+def set_watchdog(wait_limit_cycles: int = 0, inject_stall: int = 0):
+    _check(int(load_library().fa_set_watchdog(int(wait_limit_cycles), int(inject_stall))))

@@ -1,0 +1,202 @@
+// fa_api.cu -- the C ABI (include/fa.h): argument checks, TMA descriptor encoding,
+// persistent-grid sizing and kernel dispatch.  No call allocates device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWaitLimit = 1ull << 32;  // SM cycles (~2 s)
+
+thread_local char g_last_cuda_error[256] = "";
+
+std::atomic<unsigned long long> g_wait_limit{kDefaultWaitLimit};
+std::atomic<int> g_inject_stall{0};
+
+struct DeviceInfo {
+    std::once_flag once;
+    cudaError_t err = cudaSuccess;
+    int sm_count = 0;
+    int major = 0, minor = 0;
+    std::once_flag prepared[2][2][2];  // [D==128][causal][f16]
+    cudaError_t prepare_err[2][2][2] = {};
+};
+DeviceInfo g_dev[kMaxDevices];
+
+int fail_cuda(cudaError_t e, const char* what) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%d)", what,
+                  cudaGetErrorString(e), (int)e);
+    return FA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static cudaError_t e0 = cudaSuccess;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        e0 = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                              &q);
+        if (e0 == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else if (e0 == cudaSuccess)
+            e0 = cudaErrorSymbolNotFound;
+    });
+    *err = e0;
+    return fn;
+}
+
+// [BH, N, D] 16-bit tensor viewed as a 3-D map (innermost D); box {64, 128, 1} with the
+// 128-byte swizzle the tensor-core kernel expects.  Rows past N read as zero.
+bool encode_map(CUtensorMap* map, const void* base, int64_t bh, int64_t n, int64_t d, bool f16,
+                PFN_cuTensorMapEncodeTiled_v12000 fn) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(n * d * 2)};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_version(void) { return 100; }
+
+const char* fa_status_string(int status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+const char* fa_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall) {
+    if (inject_stall != 0 && inject_stall != 1) return FA_ERR_INVALID_ARG;
+    g_wait_limit.store(wait_limit_cycles ? (unsigned long long)wait_limit_cycles : kDefaultWaitLimit);
+    g_inject_stall.store(inject_stall);
+    return FA_OK;
+}
+
+int fa_check_device_status(void* stream, uint32_t* detail) {
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
+    uint32_t w[4] = {0, 0, 0, 0};
+    e = fa::tc_status_read_reset(w);
+    if (e != cudaSuccess) return fail_cuda(e, "status word");
+    if (detail) std::memcpy(detail, w, sizeof(w));
+    return (w[0] & 1u) ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+           int64_t N, int64_t D, float scale, int causal, int dtype, void* stream) {
+    // ---- argument checks: no CUDA call before these pass
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
+    if (B > 0x7FFFFFFFLL || H > 0x7FFFFFFFLL || B * H > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL)
+        return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const size_t esize = dtype == FA_FP32 ? 4 : 2;
+    const size_t tbytes = (size_t)BH * (size_t)N * (size_t)D * esize;
+    const size_t lbytes = (size_t)BH * (size_t)N * sizeof(float);
+    if (tbytes / esize / (size_t)D / (size_t)N != (size_t)BH) return FA_ERR_INVALID_ARG;
+    if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) ||
+        overlaps(o, tbytes, v, tbytes) || overlaps(lse, lbytes, q, tbytes) ||
+        overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
+        overlaps(lse, lbytes, o, tbytes))
+        return FA_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, static_cast<const void*>(o)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_MISALIGNED;
+    const bool tc = dtype != FA_FP32;
+    int units = 0;
+    if (tc) {
+        units = fa::tc_units((int)BH, (int)N, causal != 0);
+        if (units < 0) return FA_ERR_UNSUPPORTED;
+    }
+
+    // ---- device properties (once per device)
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    DeviceInfo& di = g_dev[dev];
+    std::call_once(di.once, [&] {
+        di.err = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (di.err == cudaSuccess)
+            di.err = cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (di.err == cudaSuccess)
+            di.err = cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    });
+    if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
+    if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;  // built for sm_103a only
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    if (!tc) {
+        e = fa::simt_launch((int)D, causal != 0, static_cast<const float*>(q),
+                            static_cast<const float*>(k), static_cast<const float*>(v),
+                            static_cast<float*>(o), lse, (int)BH, (int)N, scale, st);
+        return e == cudaSuccess ? FA_OK : fail_cuda(e, "fp32 kernel launch");
+    }
+
+    const bool f16 = dtype == FA_FP16;
+    const int di128 = D == 128, dic = causal != 0, dif = f16;
+    std::call_once(di.prepared[di128][dic][dif],
+                   [&] { di.prepare_err[di128][dic][dif] = fa::tc_prepare((int)D, dic, f16); });
+    if (di.prepare_err[di128][dic][dif] != cudaSuccess)
+        return fail_cuda(di.prepare_err[di128][dic][dif], "cudaFuncSetAttribute");
+
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
+    if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
+    fa::TcParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_map(&p.tmap_q, q, BH, N, D, f16, fn) || !encode_map(&p.tmap_k, k, BH, N, D, f16, fn) ||
+        !encode_map(&p.tmap_v, v, BH, N, D, f16, fn))
+        return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    p.o = o;
+    p.lse = lse;
+    p.n = (int)N;
+    p.bh = (int)BH;
+    p.npairs = (int)((N + 255) / 256);
+    p.nkv = (int)((N + 127) / 128);
+    p.units = units;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit = g_wait_limit.load();
+    p.inject_stall = g_inject_stall.load();
+    const int grid = units < di.sm_count ? units : di.sm_count;
+    e = fa::tc_launch((int)D, dic, f16, p, grid, st);
+    return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch");
+}
+
+}  // extern "C"

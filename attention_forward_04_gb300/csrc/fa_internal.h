@@ -1,0 +1,48 @@
+// fa_internal.h -- declarations shared by the C-ABI layer (fa_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Launch parameters of the tensor-core kernel (bf16/fp16 storage, D = 64 or 128).
+struct TcParams {
+    CUtensorMap tmap_q;  // 3-D maps over the [B*H, N, D] view, innermost D; box {64, 128, 1},
+    CUtensorMap tmap_k;  // 128-byte swizzle, zero fill outside the tensor (ragged N)
+    CUtensorMap tmap_v;
+    void* o;             // [B*H, N, D] output, same element type as the inputs
+    float* lse;          // [B*H, N] fp32
+    int n;               // sequence length N
+    int bh;              // B*H
+    int npairs;          // ceil(N / 256): query-tile pairs per slice
+    int nkv;             // ceil(N / 128): key/value tiles per slice
+    int units;           // work units of the persistent schedule
+    float scale_log2;    // scale * log2(e)
+    unsigned long long wait_limit;  // cycles a single wait may spin before giving up
+    int inject_stall;    // failure-detection test hook (see fa_set_watchdog)
+};
+
+// Work units of the persistent schedule for a given shape.
+int tc_units(int bh, int n, bool causal);
+
+// Dynamic shared memory the tensor-core kernel needs for head dimension D.
+int tc_smem_bytes(int D);
+
+// One-time per device: raise the dynamic shared-memory limit of the kernel instance.
+cudaError_t tc_prepare(int D, bool causal, bool f16);
+
+// Launch the tensor-core kernel with `grid` persistent CTAs on `stream`.
+cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
+                      cudaStream_t stream);
+
+// Copy the device status word (4 words) of the tensor-core kernels to `out` and clear it.
+cudaError_t tc_status_read_reset(uint32_t out[4]);
+
+// fp32 SIMT kernel: q, k, v, o [B*H, N, D] fp32, lse [B*H, N].
+cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, const float* v,
+                        float* o, float* lse, int bh, int n, float scale, cudaStream_t stream);
+
+}  // namespace fa

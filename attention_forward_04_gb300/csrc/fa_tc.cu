@@ -1,0 +1,613 @@
+// fa_tc.cu -- FlashAttention forward on the GB300 5th-generation tensor cores.
+//
+// What it computes: O = softmax(scale * Q K^T) V and LSE per row, for every (b, h) slice
+// of [B, H, N, D] bf16/fp16 tensors ("KingOfEgg: Flash Attention v1" §1.1-§1.2), tile
+// by tile with the online-softmax (m, l, O) recurrence so that no N x N matrix ever
+// reaches HBM ("08 · FlashAttention" §二; "第 13 课：GPU 内核与 FlashAttention"
+// Figure 13-2: query blocks outside, key/value blocks inside, O written once).
+//
+// Design (one persistent CTA per SM, 10 warps, warp-specialised):
+//   * warp 9 (loader): TMA loads of two 128-row query tiles (A and B) per work item and
+//     a ring of 128-key K and V tiles, each completion counted on an mbarrier
+//     (the asynchronous double-buffered copy of "pwwt.cn: FlashAttention 与内存墙" §3.3,
+//     here as TMA + mbarrier instead of cp.async groups).
+//   * warp 8 (MMA issuer, one thread): tcgen05.mma  S_t = Q_t K_j^T  into TMEM, and
+//     O_t += P_t V_j  with P_t read straight from TMEM; completion is signalled with
+//     tcgen05.commit onto mbarriers.  Issue order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
+//     PV_B(j) S_B(j+1) | ... so the softmax of one tile overlaps the products of the other.
+//   * warps 0-3 / 4-7 (softmax of tile A / tile B): one thread per query row (TMEM lane =
+//     row).  Running max m and sum l stay in registers; exp2 with scale*log2(e) folded
+//     into one FMA; P is rounded to the input type and stored back into TMEM over S.
+//     The max is only raised when it grows by more than 2^8 (log2 units), and only then
+//     is O rescaled in TMEM ("08 · FlashAttention" §五 and "第 13 课" §4B: old output
+//     multiplied by exp(m_old - m_new) when a larger maximum appears; keeping a stale
+//     reference is exact after the final division, since O and l share it).
+//   * epilogue: O / l (one division per row at the end, "第 13 课" exercise; "pwwt.cn"
+//     §2.2), LSE = (m + log2 l) * ln 2, stored from registers.
+//   * causal: key tiles entirely after a query tile are skipped, only the diagonal tile
+//     is masked ("08 · FlashAttention" §四 is_causal).  Work units pair a heavy and a
+//     light query-tile pair of the same slice, so every unit costs about the same.
+//
+// Every mbarrier wait is bounded: a wait that runs past its limit raises a CTA-wide abort
+// flag and a device status word, every role then leaves its loop, in-flight copies and
+// products are drained (bounded as well), TMEM is freed, and the kernel returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kBM = 128;            // query rows per tile = TMEM lanes
+constexpr int kBN = 128;            // keys per K/V tile
+constexpr int kSoftmaxWarps = 8;    // warps 0-3: tile A, warps 4-7: tile B
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kPanelCols = 64;      // 16-bit elements per 128-byte swizzled row
+constexpr int kPanelBytes = kBM * 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleLog2 = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Roles recorded in the status word when a wait gives up.
+constexpr uint32_t kRoleSoftmax = 1, kRoleMma = 2, kRoleLoad = 3;
+
+// Device status word: [0] flags (1 = a wait ran out), [1] role, [2] CTA, [3] wait id.
+__device__ unsigned int g_status[4];
+
+template <int D>
+struct Geo {
+    static constexpr int kPanels = D / kPanelCols;
+    static constexpr int kTileBytes = kPanels * kPanelBytes;   // one 128 x D tile
+    static constexpr int kSlots = (D == 128) ? 4 : 8;          // K/V ring depth
+    static constexpr int kKVOff = 2 * kTileBytes;               // after Q_A, Q_B
+    static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+    // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_done[2] drain
+    static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 1;
+    static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
+    static constexpr int kSmemBytes = kMiscOff + 16 + 1024;     // + alignment slack
+    static constexpr uint32_t col_s(int t) { return (uint32_t)t * kBN; }
+    static constexpr uint32_t col_o(int t) { return 2u * kBN + (uint32_t)t * D; }
+};
+
+// Barrier indices.
+template <int D> __device__ __forceinline__ int b_q_full(int t) { return t; }
+template <int D> __device__ __forceinline__ int b_q_empty(int t) { return 2 + t; }
+template <int D> __device__ __forceinline__ int b_kv_full(uint32_t i) { return 4 + (int)(i % Geo<D>::kSlots); }
+template <int D> __device__ __forceinline__ int b_kv_empty(uint32_t i) { return 4 + Geo<D>::kSlots + (int)(i % Geo<D>::kSlots); }
+template <int D> __device__ __forceinline__ int b_s_full(int t) { return 4 + 2 * Geo<D>::kSlots + t; }
+template <int D> __device__ __forceinline__ int b_p_full(int t) { return 6 + 2 * Geo<D>::kSlots + t; }
+template <int D> __device__ __forceinline__ int b_o_done(int t) { return 8 + 2 * Geo<D>::kSlots + t; }
+template <int D> __device__ __forceinline__ int b_drain() { return 10 + 2 * Geo<D>::kSlots; }
+
+// Ring position i -> phase parity of its slot.
+template <int D> __device__ __forceinline__ uint32_t ring_parity(uint32_t i) {
+    return (i / Geo<D>::kSlots) & 1u;
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B both bf16
+// (or both fp16), A K-major, B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major, bool f16) {
+    return (1u << 4)                                   // D format: f32
+           | ((f16 ? 0u : 1u) << 7)                    // A format: f16 = 0, bf16 = 1
+           | ((f16 ? 0u : 1u) << 10)                   // B format
+           | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
+           | ((uint32_t)(N >> 3) << 17)                // N / 8
+           | ((uint32_t)(M >> 4) << 24);               // M / 16
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
+// CU_TENSOR_MAP_SWIZZLE_128B; tiles start on 1024-byte boundaries).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// ----------------------------------------------------------------- work schedule
+struct Item {
+    int bh;    // slice b*H + h
+    int pair;  // query rows [256*pair, 256*pair + 256): tile A = first 128, tile B = next 128
+    int nA;    // key/value tiles tile A visits
+    int nB;    // key/value tiles tile B visits (nB >= nA)
+};
+
+// Non-causal: one unit per (slice, pair), slice-major so concurrently running CTAs share
+// the K/V of a few slices in L2.  Causal: unit (slice, q) holds pairs npairs-1-q and q,
+// heavy first; every unit then costs about the same.
+template <bool CAUSAL>
+__device__ __forceinline__ int unit_items(const TcParams& p, int u) {
+    if (!CAUSAL) return 1;
+    const int half = (p.npairs + 1) / 2;
+    const int q = u % half;
+    return (p.npairs - 1 - q != q) ? 2 : 1;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ Item unit_item(const TcParams& p, int u, int s) {
+    Item it;
+    if (!CAUSAL) {
+        it.bh = u / p.npairs;
+        it.pair = u % p.npairs;
+        it.nA = p.nkv;
+        it.nB = p.nkv;
+        return it;
+    }
+    const int half = (p.npairs + 1) / 2;
+    it.bh = u / half;
+    const int q = u % half;
+    it.pair = (s == 0) ? (p.npairs - 1 - q) : q;
+    it.nA = min(2 * it.pair + 1, p.nkv);
+    it.nB = min(2 * it.pair + 2, p.nkv);
+    return it;
+}
+
+// ----------------------------------------------------------------- bounded waits
+struct Ctl {
+    uint32_t bars;                 // smem address of barrier 0
+    volatile int* abort;           // CTA-wide abort flag (shared memory)
+    unsigned long long limit;      // cycles
+};
+
+__device__ __forceinline__ uint32_t bar_addr(const Ctl& c, int i) { return c.bars + 8u * (uint32_t)i; }
+
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort,
+                                       unsigned long long limit, uint32_t role, uint32_t id) {
+    const long long t0 = clock64();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if ((unsigned long long)(clock64() - t0) > limit) {
+            *abort = 1;
+            if (atomicCAS(&g_status[0], 0u, 1u) == 0u) {
+                g_status[1] = role;
+                g_status[2] = blockIdx.x;
+                g_status[3] = id;
+            }
+            __threadfence();
+            return false;
+        }
+    }
+}
+
+// Wait for the phase with `parity` of barrier `i`; false if the CTA is aborting.
+__device__ __forceinline__ bool wait(const Ctl& c, int i, uint32_t parity, uint32_t role) {
+    const uint32_t bar = bar_addr(c, i);
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_slow(bar, parity, c.abort, c.limit, role, (uint32_t)i);
+}
+
+// Warp-wide wait: every lane waits, and the outcome is made uniform across the warp so
+// that no lane reaches a .sync.aligned tcgen05 instruction without the others.
+__device__ __forceinline__ bool wait_warp(const Ctl& c, int i, uint32_t parity, uint32_t role) {
+    const bool ok = wait(c, i, parity, role);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
+// Teardown wait: bounded by time only (ignores the abort flag).
+__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
+    const long long t0 = clock64();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if ((unsigned long long)(clock64() - t0) > limit) return false;
+    }
+    return true;
+}
+
+// ----------------------------------------------------------------- MMA issue
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem,
+                                         uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (uint32_t)(kk / 4) * kPanelBytes + (uint32_t)(kk % 4) * 32u;
+        ptx::mma_ss(d_tmem, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
+                    idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         uint32_t idesc, bool accumulate) {
+#pragma unroll
+    for (int kk = 0; kk < kBN / 16; ++kk) {
+        // V tile: rows = keys (K dimension), 128 B = 64 head-dim values per row (MN-major);
+        // 8-key groups 1024 B apart, 64-column panels kPanelBytes apart.
+        ptx::mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u,
+                    sw128_desc(v_smem + (uint32_t)kk * 16u * 128u, kPanelBytes, 1024), idesc,
+                    (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+// ----------------------------------------------------------------- roles
+template <int D, bool CAUSAL, bool F16>
+__device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_t sbase) {
+    using G = Geo<D>;
+    constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false, F16);
+    constexpr uint32_t idesc_pv = make_idesc(kBM, D, true, F16);
+    const uint32_t sQ[2] = {sbase, sbase + (uint32_t)G::kTileBytes};
+    const uint32_t tS[2] = {tmem + G::col_s(0), tmem + G::col_s(1)};
+    const uint32_t tO[2] = {tmem + G::col_o(0), tmem + G::col_o(1)};
+    auto slot = [&](uint32_t i) {
+        return sbase + (uint32_t)G::kKVOff + (i % G::kSlots) * (uint32_t)G::kTileBytes;
+    };
+    uint32_t kv = 0, q_cnt = 0, p_cnt0 = 0, p_cnt1 = 0;
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const int nsub = unit_items<CAUSAL>(p, u);
+        for (int sub = 0; sub < nsub; ++sub) {
+            const Item it = unit_item<CAUSAL>(p, u, sub);
+            if (!wait(c, b_q_full<D>(0), q_cnt & 1u, kRoleMma)) goto out;
+            if (!wait(c, b_q_full<D>(1), q_cnt & 1u, kRoleMma)) goto out;
+            ++q_cnt;
+            if (!wait(c, b_kv_full<D>(kv), ring_parity<D>(kv), kRoleMma)) goto out;
+            ptx::tc_fence_after();
+            issue_qk<D>(tS[0], sQ[0], slot(kv), idesc_qk);
+            ptx::mma_commit(bar_addr(c, b_s_full<D>(0)));
+            if (it.nA == 1) ptx::mma_commit(bar_addr(c, b_q_empty<D>(0)));
+            issue_qk<D>(tS[1], sQ[1], slot(kv), idesc_qk);
+            ptx::mma_commit(bar_addr(c, b_s_full<D>(1)));
+            if (it.nB == 1) ptx::mma_commit(bar_addr(c, b_q_empty<D>(1)));
+            ptx::mma_commit(bar_addr(c, b_kv_empty<D>(kv)));
+            ++kv;
+
+            for (int j = 0; j < it.nB; ++j) {
+                const uint32_t vpos = kv;        // V_j
+                const uint32_t kpos = kv + 1;    // K_{j+1}
+                const bool more = j + 1 < it.nB;
+                if (!wait(c, b_kv_full<D>(vpos), ring_parity<D>(vpos), kRoleMma)) goto out;
+                ptx::tc_fence_after();
+                if (j < it.nA) {
+                    if (!wait(c, b_p_full<D>(0), p_cnt0 & 1u, kRoleMma)) goto out;
+                    ++p_cnt0;
+                    ptx::tc_fence_after();
+                    issue_pv<D>(tO[0], tS[0], slot(vpos), idesc_pv, j > 0);
+                    ptx::mma_commit(bar_addr(c, b_o_done<D>(0)));
+                }
+                if (more) {
+                    if (!wait(c, b_kv_full<D>(kpos), ring_parity<D>(kpos), kRoleMma)) goto out;
+                    ptx::tc_fence_after();
+                }
+                if (j + 1 < it.nA) {
+                    issue_qk<D>(tS[0], sQ[0], slot(kpos), idesc_qk);
+                    ptx::mma_commit(bar_addr(c, b_s_full<D>(0)));
+                    if (j + 2 == it.nA) ptx::mma_commit(bar_addr(c, b_q_empty<D>(0)));
+                }
+                if (!wait(c, b_p_full<D>(1), p_cnt1 & 1u, kRoleMma)) goto out;
+                ++p_cnt1;
+                ptx::tc_fence_after();
+                issue_pv<D>(tO[1], tS[1], slot(vpos), idesc_pv, j > 0);
+                ptx::mma_commit(bar_addr(c, b_o_done<D>(1)));
+                ptx::mma_commit(bar_addr(c, b_kv_empty<D>(vpos)));
+                ++kv;
+                if (more) {
+                    issue_qk<D>(tS[1], sQ[1], slot(kpos), idesc_qk);
+                    ptx::mma_commit(bar_addr(c, b_s_full<D>(1)));
+                    if (j + 2 == it.nB) ptx::mma_commit(bar_addr(c, b_q_empty<D>(1)));
+                    ptx::mma_commit(bar_addr(c, b_kv_empty<D>(kpos)));
+                    ++kv;
+                }
+            }
+        }
+    }
+out:
+    // Every product issued so far must finish before TMEM is released.
+    ptx::mma_commit(bar_addr(c, b_drain<D>()));
+    wait_drain(bar_addr(c, b_drain<D>()), 0, c.limit);
+}
+
+template <int D, bool CAUSAL>
+__device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
+    using G = Geo<D>;
+    const uint32_t sQ[2] = {sbase, sbase + (uint32_t)G::kTileBytes};
+    auto slot = [&](uint32_t i) {
+        return sbase + (uint32_t)G::kKVOff + (i % G::kSlots) * (uint32_t)G::kTileBytes;
+    };
+    uint32_t kv = 0, q_cnt = 0;
+    uint32_t q_issued[2] = {0, 0};  // Q loads issued per tile buffer
+    const uint32_t skipped = (p.inject_stall == 1 && blockIdx.x == 0) ? 0u : 0xFFFFFFFFu;
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const int nsub = unit_items<CAUSAL>(p, u);
+        for (int sub = 0; sub < nsub; ++sub) {
+            const Item it = unit_item<CAUSAL>(p, u, sub);
+            for (int t = 0; t < 2; ++t) {
+                if (!wait(c, b_q_empty<D>(t), (q_cnt & 1u) ^ 1u, kRoleLoad)) goto out;
+                const uint32_t fb = bar_addr(c, b_q_full<D>(t));
+                ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
+#pragma unroll
+                for (int pc = 0; pc < G::kPanels; ++pc)
+                    ptx::tma_load_3d(sQ[t] + (uint32_t)pc * kPanelBytes, &p.tmap_q, fb, pc * kPanelCols,
+                                     it.pair * 2 * kBM + t * kBM, it.bh);
+                ++q_issued[t];
+            }
+            ++q_cnt;
+            for (int j = 0; j < it.nB; ++j) {
+                for (int w = 0; w < 2; ++w) {  // K_j then V_j
+                    if (!wait(c, b_kv_empty<D>(kv), ring_parity<D>(kv) ^ 1u, kRoleLoad)) goto out;
+                    if (kv != skipped) {
+                        const uint32_t fb = bar_addr(c, b_kv_full<D>(kv));
+                        ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
+                        const CUtensorMap* map = (w == 0) ? &p.tmap_k : &p.tmap_v;
+#pragma unroll
+                        for (int pc = 0; pc < G::kPanels; ++pc)
+                            ptx::tma_load_3d(slot(kv) + (uint32_t)pc * kPanelBytes, map, fb,
+                                             pc * kPanelCols, j * kBN, it.bh);
+                    }
+                    ++kv;
+                }
+            }
+        }
+    }
+out:
+    // No TMA copy may still be writing shared memory when the CTA exits: wait for the
+    // last fill of every ring slot and of both query buffers.
+    for (uint32_t i = (kv > (uint32_t)G::kSlots ? kv - G::kSlots : 0u); i < kv; ++i)
+        if (i != skipped) wait_drain(bar_addr(c, b_kv_full<D>(i)), ring_parity<D>(i), c.limit);
+    for (int t = 0; t < 2; ++t)
+        if (q_issued[t] > 0) wait_drain(bar_addr(c, b_q_full<D>(t)), (q_issued[t] - 1u) & 1u, c.limit);
+}
+
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (F16) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    } else {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// One 128-key tile of one row: running max update, exp2, row sum, P packed to 16-bit.
+// s[]: raw (unscaled) scores; keys kbase + c with kbase + c >= limit are invisible.
+template <bool MASK, bool F16>
+__device__ __forceinline__ void softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
+                                             float sl2, float& m_run, float& l_run, float& alpha,
+                                             uint32_t (&pk)[64]) {
+    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int c = 0; c < 128; ++c) {
+        float x = u2f(s[c]);
+        if (MASK && kbase + c >= limit) x = -INFINITY;
+        mx[c & 3] = fmaxf(mx[c & 3], x);
+    }
+    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;  // log2 units
+    float m_new = m_run;
+    alpha = 1.0f;
+    if (mt > m_run + kRescaleLog2) {
+        m_new = mt;
+        alpha = ptx::ex2(m_run - mt);
+    }
+    const float neg = -m_new;
+    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < 128; c += 2) {
+        float p0 = ptx::ex2(fmaf(u2f(s[c]), sl2, neg));
+        float p1 = ptx::ex2(fmaf(u2f(s[c + 1]), sl2, neg));
+        if (MASK) {
+            if (kbase + c >= limit) p0 = 0.f;
+            if (kbase + c + 1 >= limit) p1 = 0.f;
+        }
+        sum[(c >> 1) & 3] += p0 + p1;
+        pk[c >> 1] = pack2<F16>(p0, p1);
+    }
+    l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+    m_run = m_new;
+}
+
+template <int D, bool CAUSAL, bool F16>
+__device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int warp, int lane) {
+    using G = Geo<D>;
+    const int t = warp / 4;                       // 0: tile A, 1: tile B
+    const int lane_base = (warp % 4) * 32;        // this warp's TMEM lane quarter
+    const uint32_t tl = (uint32_t)lane_base << 16;
+    const uint32_t tS = tmem + tl + G::col_s(t);
+    const uint32_t tO = tmem + tl + G::col_o(t);
+    uint32_t s_cnt = 0, o_cnt = 0;
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const int nsub = unit_items<CAUSAL>(p, u);
+        for (int sub = 0; sub < nsub; ++sub) {
+            const Item it = unit_item<CAUSAL>(p, u, sub);
+            const int n = t == 0 ? it.nA : it.nB;
+            const int row = it.pair * 2 * kBM + t * kBM + lane_base + lane;
+            const int limit = CAUSAL ? min(row + 1, p.n) : p.n;   // visible keys: j < limit
+            float m_run = -INFINITY, l_run = 0.0f;
+
+            for (int j = 0; j < n; ++j) {
+                if (!wait_warp(c, b_s_full<D>(t), s_cnt & 1u, kRoleSoftmax)) return;
+                ++s_cnt;
+                if (j > 0) {  // O_t += P(j-1) V(j-1) is complete before S(j) is (issue order)
+                    if (!wait_warp(c, b_o_done<D>(t), o_cnt & 1u, kRoleSoftmax)) return;
+                    ++o_cnt;
+                }
+                ptx::tc_fence_after();
+                uint32_t s[128];
+                ptx::tmem_ld128_wait(tS, s);
+                const int kbase = j * kBN;
+                float alpha;
+                uint32_t pk[64];
+                if (__any_sync(0xFFFFFFFFu, kbase + kBN > limit))
+                    softmax_tile<true, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, alpha, pk);
+                else
+                    softmax_tile<false, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, alpha, pk);
+                __syncwarp();
+                // P over the first 64 columns of this tile's S region (two 16-bit values per column).
+                ptx::tmem_st16(tS + 0, &pk[0]);
+                ptx::tmem_st16(tS + 16, &pk[16]);
+                ptx::tmem_st16(tS + 32, &pk[32]);
+                ptx::tmem_st16(tS + 48, &pk[48]);
+                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    // The running max rose: rescale this row of O by alpha in TMEM.
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32_wait(tO + (uint32_t)cc * 32u, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
+                        ptx::tmem_st32(tO + (uint32_t)cc * 32u, o);
+                    }
+                }
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, b_p_full<D>(t)));
+            }
+
+            // Epilogue: O / l and LSE for this row.
+            if (!wait_warp(c, b_o_done<D>(t), o_cnt & 1u, kRoleSoftmax)) return;
+            ++o_cnt;
+            ptx::tc_fence_after();
+            const bool live = row < p.n;
+            const float inv_l = 1.0f / l_run;
+            const size_t grow = (size_t)it.bh * (size_t)p.n + (size_t)(live ? row : 0);
+            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + grow * D;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                ptx::tmem_ld32_wait(tO + (uint32_t)cc * 32u, o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<F16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+                if (live) {
+                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
+            }
+            if (live) p.lse[grow] = (m_run + log2f(l_run)) * kLn2;
+            __syncwarp();
+        }
+    }
+}
+
+template <int D, bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constant__ TcParams p) {
+    using G = Geo<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::kMiscOff + 4);
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    Ctl c;
+    c.bars = sbase + (uint32_t)G::kBarOff;
+    c.abort = abort_flag;
+    c.limit = p.wait_limit;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            ptx::mbar_init(bar_addr(c, b_q_full<D>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_q_empty<D>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_s_full<D>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_p_full<D>(t)), 128);
+            ptx::mbar_init(bar_addr(c, b_o_done<D>(t)), 1);
+        }
+        for (int s = 0; s < G::kSlots; ++s) {
+            ptx::mbar_init(bar_addr(c, b_kv_full<D>(s)), 1);
+            ptx::mbar_init(bar_addr(c, b_kv_empty<D>(s)), 1);
+        }
+        ptx::mbar_init(bar_addr(c, b_drain<D>()), 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kLoadWarp && lane == 0) {
+        ptx::prefetch_tensormap(&p.tmap_q);
+        ptx::prefetch_tensormap(&p.tmap_k);
+        ptx::prefetch_tensormap(&p.tmap_v);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp < kSoftmaxWarps) {
+        softmax_role<D, CAUSAL, F16>(p, c, tmem, warp, lane);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_role<D, CAUSAL, F16>(p, c, tmem, sbase);
+        __syncwarp();
+    } else {
+        if (lane == 0) load_role<D, CAUSAL>(p, c, sbase);
+        __syncwarp();
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int D, bool CAUSAL, bool F16>
+cudaError_t prepare_one() {
+    return cudaFuncSetAttribute(fa_tc_kernel<D, CAUSAL, F16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSmemBytes);
+}
+
+template <int D, bool CAUSAL, bool F16>
+cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t stream) {
+    fa_tc_kernel<D, CAUSAL, F16><<<grid, kThreads, Geo<D>::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t dispatch(bool causal, bool f16, bool prepare, const TcParams* p, int grid,
+                     cudaStream_t stream) {
+    if (prepare) {
+        if (causal) return f16 ? prepare_one<D, true, true>() : prepare_one<D, true, false>();
+        return f16 ? prepare_one<D, false, true>() : prepare_one<D, false, false>();
+    }
+    if (causal)
+        return f16 ? launch_one<D, true, true>(*p, grid, stream)
+                   : launch_one<D, true, false>(*p, grid, stream);
+    return f16 ? launch_one<D, false, true>(*p, grid, stream)
+               : launch_one<D, false, false>(*p, grid, stream);
+}
+
+}  // namespace
+
+int tc_units(int bh, int n, bool causal) {
+    const long long npairs = (n + 2 * kBM - 1) / (2 * kBM);
+    const long long u = causal ? (long long)bh * ((npairs + 1) / 2) : (long long)bh * npairs;
+    return u > 0x7FFFFFFFLL ? -1 : (int)u;
+}
+
+int tc_smem_bytes(int D) { return D == 64 ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes; }
+
+cudaError_t tc_prepare(int D, bool causal, bool f16) {
+    return D == 64 ? dispatch<64>(causal, f16, true, nullptr, 0, nullptr)
+                   : dispatch<128>(causal, f16, true, nullptr, 0, nullptr);
+}
+
+cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
+                      cudaStream_t stream) {
+    return D == 64 ? dispatch<64>(causal, f16, false, &p, grid, stream)
+                   : dispatch<128>(causal, f16, false, &p, grid, stream);
+}
+
+cudaError_t tc_status_read_reset(uint32_t out[4]) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int) * 4);
+    if (e != cudaSuccess) return e;
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_status, zero, sizeof(zero));
+}
+
+}  // namespace fa

@@ -1,0 +1,423 @@
+#!/usr/bin/env python
+"""Throughput of the attention forward on GB300, one JSON line on stdout.
+
+A step is one whole forward pass (one fa_fwd call) over one batch of synthetic
+[B, H, N, D] inputs.  Default workload: bf16, B=4, H=16, N=4096, D=128, non-causal,
+scale 1/sqrt(128) -- the shape the pages analyse, and the workload the throughput
+metric is quoted on.  Metric: attention TFLOPS = 4*B*H*N^2*D / t (halved when causal).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank is an independent replica on its own GPU (the
+forward has no exchange step), per-GPU work is fixed ("scaling": "weak"), and value
+is the total work of all ranks over the max-over-ranks time.
+
+Timing: W untimed warm-up steps, then exactly K steps between a barrier +
+cudaDeviceSynchronize on both sides, timed with CUDA events on the launching stream.
+Consecutive steps alternate between two input sets of 192 MiB each (together larger
+than the 129 MB L2), so no step starts with its inputs resident in L2.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SRC = os.path.join(ROOT, "attention_forward_04_gb300", "csrc", "fa_tc.cu")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_traffic(workload: str):
+    """dram read+write bytes per launch from an ncu capture, if it matches this kernel source."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(workload)
+    if not e or e.get("kernel_sha256_16") != kernel_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons for one GPU."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            self.samples.append((time.monotonic(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:  # timed region shorter than the sampling period: nearest samples
+            inside = [s for (t, s) in self.samples if t0 - 0.5 <= t <= t1 + 0.5]
+            window = "around-timed"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            for name, val in zip(names, s[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(inside[0][2]), "reasons": sorted(reasons),
+                "power_w_max": max((num(s[3]) or 0.0) for s in inside),
+                "samples": len(inside), "window": window}
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def time_oracle(w, budget_s: float, max_rows: int | None = None):
+    """Time the fp64 oracle on a bounded sample of the workload: whole query rows of
+    slice (0, 0), as many as fit the budget.  Returns (tflops, seconds, rows, threads)."""
+    import numpy as np
+    import oracle
+    from attention_forward_04_gb300.inputs import make_qkv
+    q, k, v = make_qkv(w.with_(B=1, H=1))
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    threads = oracle.default_threads()
+
+    def flops_rows(rows):
+        keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+        return float(np.sum(4.0 * keys * w.D))
+
+    # probe with a small row count, then size the sample to the budget
+    rows = np.arange(min(w.N, 64), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q64, k64, v64, w.scale, w.causal, np.zeros_like(rows), rows, threads)
+    dt = time.perf_counter() - t0
+    per_row = dt / len(rows)
+    n = int(max(1, min(w.N, budget_s / max(per_row, 1e-9))))
+    if max_rows:
+        n = min(n, max_rows)
+    rows = np.linspace(0, w.N - 1, n).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q64, k64, v64, w.scale, w.causal, np.zeros_like(rows), rows, threads)
+    dt = time.perf_counter() - t0
+    return flops_rows(rows) / dt / 1e12, dt, n, threads
+
+
+def run_reference(args, w):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import oracle
+    from attention_forward_04_gb300.inputs import make_qkv
+    oracle.build()
+    q, k, v = make_qkv(w.with_(B=1, H=1))
+    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    threads = oracle.default_threads()
+    # size each step so the whole run ends within about two minutes
+    probe = np.arange(min(w.N, 16), dtype=np.int64)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q64, k64, v64, w.scale, w.causal, np.zeros_like(probe), probe, threads)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    per_step_budget = min(2.0, 120.0 / max(1, args.steps + args.warmup))
+    nrows = int(max(1, min(w.N, per_step_budget / max(per_row, 1e-9))))
+    rng = np.random.default_rng(0)
+    flops = 0.0
+    elapsed = 0.0
+    for step in range(args.warmup + args.steps):
+        rows = np.sort(rng.choice(w.N, size=nrows, replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q64, k64, v64, w.scale, w.causal, np.zeros_like(rows), rows, threads)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            elapsed += dt
+            keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
+            flops += float(np.sum(4.0 * keys * w.D))
+    value = flops / elapsed / 1e12
+    sample = ("%d random query rows of one (b, h) slice per step (of %d rows x %d slices), "
+              "fp64 three-pass oracle, %d threads" % (nrows, w.N, w.B * w.H, threads))
+    line = {"impl": "reference", "metric": "attention fwd TFLOPS (4*B*H*N^2*D/t)", "value": value,
+            "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w, gpus):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+            "dtype": w.dtype, "scale": w.scale, "qk_mult": w.qk_mult,
+            "layout": "[B,H,N,D] contiguous", "parallelism": "replicas x%d" % gpus,
+            "l2": "two alternating input sets of %.0f MiB each (> 129 MB L2); no flush"
+                  % (3 * w.B * w.H * w.N * w.D * (4 if w.dtype == "fp32" else 2) / 2**20)}
+
+
+# ------------------------------------------------------------------ main GPU leg
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from attention_forward_04_gb300.inputs import HEADLINE, WORKLOADS
+    w = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    rank, local_rank, world = dist_env()
+    import torch
+    import torch.distributed as dist
+    from attention_forward_04_gb300 import binding, build
+    from attention_forward_04_gb300.inputs import TORCH_DTYPES, make_qkv
+
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist.barrier()
+    else:
+        torch.cuda.set_device(0)
+    binding.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    code = {"fp32": binding.FA_FP32, "bf16": binding.FA_BF16, "fp16": binding.FA_FP16}[w.dtype]
+    B, H, N, D = w.B, w.H, w.N, w.D
+
+    sets = []
+    for s in range(2):
+        q, k, v = make_qkv(w, seed_offset=100 * s + 10 * rank)
+        sets.append(tuple(t.to(dev) for t in (q, k, v)))
+    host_set = make_qkv(w, seed_offset=10 * rank)
+    o = torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype], device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+
+    def step(i):
+        q, k, v = sets[i & 1]
+        st = binding.fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                             lse.data_ptr(), B, H, N, D, w.scale, int(w.causal), code, sh)
+        if st != 0:
+            raise binding.FaError(st)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, detail = binding.check_device_status()
+    if st != 0:
+        raise RuntimeError("kernel watchdog after warm-up: %d %s" % (st, detail))
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.monotonic()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.15)
+    sampler.stop()
+    ms_local = ev0.elapsed_time(ev1)
+    st, detail = binding.check_device_status()
+    if st != 0:
+        raise RuntimeError("kernel watchdog in timed region: %d %s" % (st, detail))
+
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flops_step = w.flops
+    value = flops_step * args.steps * world / (ms / 1e3) / 1e12
+    per_launch_ms = ms_local / args.steps
+
+    # ---- end to end through the public API: pinned host inputs -> device -> fa.fwd -> host
+    hq, hk, hv = (t.pin_memory() for t in host_set)
+    ho = torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype]).pin_memory()
+    hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in host_set)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv.copy_(hv, non_blocking=True)
+        binding.fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops_step * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops_step / (per_launch_ms / 1e3) / 1e12
+    traffic = load_traffic(w.name)
+    if w.dtype == "fp32":
+        roof = {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s",
+                "frac": None, "traffic": traffic,
+                "note": "fp32 SIMT path; FFMA peak derived in DESIGN.md"}
+    else:
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % peak_src
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
+                "hbm_gbs_algorithmic": (3 + 1) * B * H * N * D * 2 / (per_launch_ms / 1e3) / 1e9}
+
+    cpu = None
+    if world == 1 or rank == 0:
+        try:
+            tfl, secs, rows, threads = time_oracle(w, args.cpu_budget)
+            cpu = {"value": tfl, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                   "sample": "%d query rows spread over slice (0,0) of %s (%d rows x %d slices), "
+                             "fp64 three-pass oracle, %.1f s" % (rows, w.name, N, B * H, secs)}
+        except Exception as ex:  # the CPU leg must not hide the GPU number
+            cpu = {"value": None, "unit": "TFLOPS", "cores": None, "kind": "oracle",
+                   "sample": "failed: %s" % ex}
+
+    clocks = sampler.summary(t_wall0, t_wall1)
+    line = {
+        "metric": "attention fwd TFLOPS (4*B*H*N^2*D/t)",
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded torch.randn, cast to %s)" % w.dtype,
+        "config": config_of(w, world),
+        "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "ms_per_step": e2e_ms / args.e2e_steps},
+        "gpu_launches": args.steps,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "pct_of_peak": 100.0 * achieved / peak if w.dtype != "fp32" else None,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,106 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) FlashAttention forward library (libfa.so).
+ *
+ * The operation (one call = one whole forward pass over a batch of heads):
+ *   For every slice (b, h) of [B, H, N, D] tensors Q, K, V and every query row i,
+ *     O[b,h,i,:] = sum_j softmax_j(scale * Q[b,h,i,:] . K[b,h,j,:]) * V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp(scale * Q[b,h,i,:] . K[b,h,j,:])
+ *   with j over all N keys, or over j <= i when `causal` is set.
+ *   Sources: "KingOfEgg: Flash Attention v1" (dandandamowang.xyz) §1.1 (scaled
+ *   dot-product attention) and §1.2 (the [B, H, N, D] layout); "08 · FlashAttention"
+ *   §二 (tiles plus online softmax, the N x N matrix never reaches HBM) and §四
+ *   (`is_causal`).  LSE is the natural-log row normaliser m + ln l of the scaled
+ *   scores; the pages keep m and l separately ("KingOfEgg" §5.2), and one fp32
+ *   value per row carries both.
+ *
+ * All calls are host calls.  No call allocates device memory.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Storage type of Q, K, V and O.  LSE is always fp32. */
+typedef enum {
+    FA_FP32 = 0, /* fp32 in, fp32 out; SIMT fp32 arithmetic (no TF32)                  */
+    FA_BF16 = 1, /* bf16 in, bf16 out; tensor-core products, fp32 accumulation/softmax */
+    FA_FP16 = 2  /* fp16 in, fp16 out; same arithmetic as FA_BF16                       */
+} fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, size out of range, bad flag, output overlaps an input */
+    FA_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (D, dtype, GPU model)       */
+    FA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned (TMA needs 16 B)             */
+    FA_ERR_CUDA = 4,        /* a CUDA runtime call or the kernel launch failed                      */
+    FA_ERR_TIMEOUT = 5      /* a kernel wait ran past its limit (reported by fa_check_device_status) */
+} fa_status;
+
+/*
+ * fa_fwd -- attention forward pass, asynchronous on `stream`.
+ *
+ *   q, k, v : device pointers, [B, H, N, D] contiguous (row-major), element type `dtype`.
+ *   o       : device pointer, [B, H, N, D] contiguous, element type `dtype`; written fully.
+ *   lse     : device pointer, [B, H, N] contiguous fp32; written fully.
+ *   B, H, N : >= 1.  B*H < 2^31 and N < 2^31.  Any N is accepted (a ragged last tile is
+ *             masked; keys >= N never contribute).
+ *   D       : head dimension, 64 or 128.
+ *   scale   : finite, >= 0 (normally 1/sqrt(D)).
+ *   causal  : 0 = all keys; 1 = key j <= query i (square N x N).
+ *   dtype   : an fa_dtype value.
+ *   stream  : a cudaStream_t (CUstream) cast to void*, or NULL for the legacy default stream.
+ *
+ * Ownership: the caller owns every buffer and keeps it alive until the stream has
+ * finished the call.  o and lse need no initialisation.  o and lse must not overlap
+ * q, k, v or each other.  The call allocates nothing and does not synchronise.
+ *
+ * Errors: arguments are checked before any CUDA call; on a bad argument nothing is
+ * launched and FA_ERR_INVALID_ARG / FA_ERR_UNSUPPORTED / FA_ERR_MISALIGNED is returned.
+ * A failed launch returns FA_ERR_CUDA (see fa_last_cuda_error).  Faults inside the
+ * kernel never trap: every wait in the kernel is bounded, and a wait that runs out sets
+ * a device status word that fa_check_device_status reports as FA_ERR_TIMEOUT.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int64_t B, int64_t H, int64_t N, int64_t D,
+           float scale, int causal, int dtype, void* stream);
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* fa_status_string(int status);
+
+/* Text of the last CUDA error seen by this library in the calling thread, or "". */
+const char* fa_last_cuda_error(void);
+
+/*
+ * fa_check_device_status -- synchronises `stream`, then reads and clears the device
+ * status word the tensor-core kernels set when a bounded wait runs out.
+ * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_CUDA if the synchronisation itself failed.
+ * If `detail` is not NULL it receives 4 words: flags, role that gave up, CTA index, wait id.
+ */
+int fa_check_device_status(void* stream, uint32_t* detail);
+
+/*
+ * fa_set_watchdog -- failure-detection control for the tensor-core kernels (affects
+ * launches made after the call, in this process).
+ *   wait_limit_cycles : SM clock cycles any single wait may spin before the kernel gives
+ *                       up; 0 restores the default (2^32 cycles, about two seconds).
+ *   inject_stall      : 0 = normal.  1 = in CTA 0 the loader withholds the first K/V tile
+ *                       load of its first work item, so the waits for it run out.  This
+ *                       exists so tests can check that a stuck pipeline ends with
+ *                       FA_ERR_TIMEOUT instead of a hang; the outputs of that call are
+ *                       then undefined.
+ * Returns FA_OK, or FA_ERR_INVALID_ARG for an unknown inject_stall value.
+ */
+int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall);
+
+/* Library ABI version (major * 100 + minor). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

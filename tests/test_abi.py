@@ -1,0 +1,92 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol that
+include/fa.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_forward_04_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_status_string" in names
+    assert set(names) == set(binding.SIGNATURES), names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_version() >= 100
+    for code, name in binding.STATUS.items():
+        assert lib.fa_status_string(code).decode() == name
+    assert lib.fa_status_string(99).decode() == "FA_ERR_UNKNOWN"
+
+
+# Fake, 16-byte aligned, non-overlapping addresses: validation must fail before any of
+# them is used.  Each case below is rejected by a host-side check.
+BASE = 1 << 40
+SZ = 1 << 30
+
+
+def call(lib, q=BASE, k=BASE + SZ, v=BASE + 2 * SZ, o=BASE + 3 * SZ, lse=BASE + 4 * SZ,
+         B=1, H=1, N=128, D=128, scale=0.1, causal=0, dtype=1):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, D, scale, causal, dtype, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(v=0), INVALID), (dict(o=0), INVALID),
+    (dict(lse=0), INVALID),
+    (dict(B=0), INVALID), (dict(H=0), INVALID), (dict(N=0), INVALID), (dict(N=-5), INVALID),
+    (dict(B=1 << 31), INVALID), (dict(B=1 << 16, H=1 << 16), INVALID),
+    (dict(causal=2), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID), (dict(scale=-0.5), INVALID),
+    (dict(dtype=7), INVALID), (dict(dtype=-1), INVALID),
+    (dict(D=96), UNSUPPORTED), (dict(D=32), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
+    (dict(q=BASE + 8), MISALIGNED), (dict(o=BASE + 3 * SZ + 4), MISALIGNED),
+    (dict(lse=BASE + 4 * SZ + 2), MISALIGNED),
+    (dict(o=BASE), INVALID),                       # o aliases q
+    (dict(o=BASE + SZ + 64), INVALID),             # o overlaps k
+    (dict(lse=BASE + 2 * SZ + 16), INVALID),       # lse inside v
+    (dict(lse=BASE + 3 * SZ), INVALID),            # lse aliases o
+])
+def test_bad_arguments_rejected_before_cuda(lib, kw, expect):
+    assert call(lib, **kw) == expect
+
+
+def test_watchdog_control_validation(lib):
+    assert lib.fa_set_watchdog(0, 5) == INVALID
+    assert lib.fa_set_watchdog(0, 0) == OK
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 8, 64)
+    with pytest.raises(ValueError):
+        binding.fwd(x, x, x)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(FileNotFoundError):
+        binding.load_library(str(tmp_path / "nope.so"))

@@ -1,0 +1,180 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances, written here and applied element by element:
+  * fp32 storage (SIMT fp32 path): max |O - O_oracle| <= 1e-5, max |LSE - LSE_oracle| <= 1e-5.
+  * bf16 / fp16 storage (tensor-core path, fp32 accumulation and softmax):
+    max |O - O_oracle| <= 2e-2, max |LSE - LSE_oracle| <= 1e-3.
+The oracle reads the same stored (dtype-rounded) inputs, converted exactly to fp64.
+
+Small shapes are compared in full; the full-size workloads are compared on sampled
+rows (rows are independent, so a sampled oracle row is exactly the full oracle's row):
+every tile boundary row and a seeded random set of rows, in several slices.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from attention_forward_04_gb300 import binding, build
+from attention_forward_04_gb300.inputs import WORKLOADS, make_qkv, make_shape
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"fp32": (1e-5, 1e-5), "bf16": (2e-2, 1e-3), "fp16": (2e-2, 1e-3)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu_lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    binding.load_library()
+
+
+def f64(t):
+    return t.to(torch.float64).numpy()
+
+
+def run_gpu(q, k, v, scale, causal):
+    o, lse = binding.fwd(q.cuda(), k.cuda(), v.cuda(), scale=scale, causal=causal)
+    torch.cuda.synchronize()
+    st, detail = binding.check_device_status()
+    assert st == 0, (st, detail)
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def assert_close(o, lse, o_ref, lse_ref, dtype, what=""):
+    tol_o, tol_l = TOL[dtype]
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse)), what
+    eo = np.abs(o - o_ref)
+    el = np.abs(lse - lse_ref)
+    io = np.unravel_index(np.argmax(eo), eo.shape)
+    assert eo.max() <= tol_o, "%s O max err %.3e at %s (mean %.3e)" % (what, eo.max(), io, eo.mean())
+    assert el.max() <= tol_l, "%s LSE max err %.3e (mean %.3e)" % (what, el.max(), el.mean())
+
+
+def full_compare(q, k, v, scale, causal, dtype, what=""):
+    o, lse = run_gpu(q, k, v, scale, causal)
+    o_ref, lse_ref = oracle.attention_fwd(f64(q), f64(k), f64(v), scale, causal)
+    assert_close(o, lse, o_ref, lse_ref, dtype, what)
+
+
+# ------------------------------------------------------------ small and edge shapes
+EDGE_N = [1, 17, 127, 128, 129, 255, 256, 257, 383, 640, 1000]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("N", EDGE_N)
+def test_bf16_edge_shapes(N, D, causal):
+    q, k, v = make_shape(1, 2, N, D, "bf16", seed=N * 7 + D)
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "bf16", "N=%d D=%d causal=%d" % (N, D, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("N", [1, 33, 200, 256, 300])
+def test_fp32_edge_shapes(N, D, causal):
+    q, k, v = make_shape(2, 1, N, D, "fp32", seed=N * 11 + D)
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "fp32", "N=%d D=%d causal=%d" % (N, D, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_fp16(D, causal):
+    q, k, v = make_shape(2, 3, 700, D, "fp16", seed=99 + D)
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "fp16")
+
+
+def test_many_slices_persistent_schedule():
+    """More work units than SMs: every CTA runs several items back to back."""
+    q, k, v = make_shape(3, 70, 300, 64, "bf16", seed=5)
+    full_compare(q, k, v, 0.125, False, "bf16")
+    full_compare(q, k, v, 0.125, True, "bf16")
+
+
+def test_large_scores_force_rescales():
+    """Scores with a wide spread and growing row maxima make the running max move by
+    more than the lazy threshold many times."""
+    q, k, v = make_shape(1, 2, 1500, 128, "bf16", seed=17, qk_mult=3.0)
+    # keys grow in magnitude along the sequence so the max keeps rising
+    ramp = torch.linspace(0.2, 3.0, 1500).view(1, 1, 1500, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    full_compare(q, k, v, 1.0 / math.sqrt(128), False, "bf16")
+    full_compare(q, k, v, 1.0 / math.sqrt(128), True, "bf16")
+
+
+def test_zero_scale_uniform_weights():
+    q, k, v = make_shape(1, 1, 300, 128, "bf16", seed=23)
+    full_compare(q, k, v, 0.0, False, "bf16")
+    full_compare(q, k, v, 0.0, True, "bf16")
+
+
+def test_constant_value_column_on_gpu():
+    q, k, v = make_shape(1, 2, 777, 128, "bf16", seed=29)
+    v[..., 3] = 1.5
+    o, _ = run_gpu(q, k, v, 1.0 / math.sqrt(128), True)
+    assert np.max(np.abs(o[..., 3] - 1.5)) <= TOL["bf16"][0]
+
+
+def test_deterministic_rerun():
+    q, k, v = make_shape(2, 4, 1000, 128, "bf16", seed=31)
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    o1, l1 = binding.fwd(qc, kc, vc, causal=True)
+    o2, l2 = binding.fwd(qc, kc, vc, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_non_default_stream():
+    q, k, v = make_shape(1, 2, 500, 64, "bf16", seed=37)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+        o, lse = binding.fwd(qc, kc, vc, stream=s)
+    s.synchronize()
+    o_ref, lse_ref = oracle.attention_fwd(f64(q), f64(k), f64(v), 0.125, False)
+    assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16")
+
+
+# ------------------------------------------------------------ the five workloads
+def sampled_rows(N, seed, extra=24):
+    rows = {0, 1, N - 1, N - 2}
+    for b in range(128, N, 128):
+        rows.update({b - 1, b})
+    rng = np.random.default_rng(seed)
+    rows.update(rng.integers(0, N, size=extra).tolist())
+    return sorted(r for r in rows if 0 <= r < N)
+
+
+@pytest.mark.parametrize("name", ["fp32_b1h1n256d64", "bf16_b2h8n1024d64"])
+def test_small_workloads_full(name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w)
+    full_compare(q, k, v, w.scale, w.causal, w.dtype, name)
+
+
+@pytest.mark.parametrize("name", ["bf16_b4h16n4096d128", "bf16_b8h32n4096d128_causal",
+                                  "bf16_b1h32n16384d128_x2", "bf16_b1h32n16384d128_x2_causal"])
+def test_full_size_workloads_sampled(name):
+    w = WORKLOADS[name]
+    q, k, v = make_qkv(w)
+    o, lse = binding.fwd(q.cuda(), k.cuda(), v.cuda(), scale=w.scale, causal=w.causal)
+    torch.cuda.synchronize()
+    st, detail = binding.check_device_status()
+    assert st == 0, (st, detail)
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+    BH = w.B * w.H
+    rng = np.random.default_rng(w.seed)
+    slices = sorted({0, BH - 1, *rng.integers(0, BH, size=4).tolist()})
+    for s in slices:
+        b, h = divmod(s, w.H)
+        rows = np.array(sampled_rows(w.N, w.seed + s))
+        o_ref, l_ref = oracle.attention_rows(f64(q[b:b + 1, h:h + 1]), f64(k[b:b + 1, h:h + 1]),
+                                             f64(v[b:b + 1, h:h + 1]), w.scale, w.causal,
+                                             np.zeros_like(rows), rows)
+        og = o[b, h, rows].float().cpu().numpy().astype(np.float64)
+        lg = lse[b, h, rows].cpu().numpy().astype(np.float64)
+        assert_close(og, lg, o_ref, l_ref, w.dtype, "%s slice %d" % (name, s))
