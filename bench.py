@@ -147,34 +147,29 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def time_oracle(w, budget_s: float, max_rows: int | None = None):
-    """Time the fp64 oracle on a bounded sample of the workload: whole query rows of
-    slice (0, 0), as many as fit the budget.  Returns (tflops, seconds, rows, threads)."""
+def time_oracle(w, budget_s: float, host_qkv):
+    """Time the fp64 oracle, as it stands, on a bounded sample of the workload: whole
+    (b, h) slices, as many as fit the time budget (at least one).
+    Returns (tflops, seconds, slices, threads)."""
     import numpy as np
     import oracle
-    from attention_forward_04_gb300.inputs import make_qkv
-    q, k, v = make_qkv(w.with_(B=1, H=1))
-    q64, k64, v64 = (t.double().numpy() for t in (q, k, v))
+    BH = w.B * w.H
+    q, k, v = (t.reshape(1, BH, w.N, w.D) for t in host_qkv)
     threads = oracle.default_threads()
-
-    def flops_rows(rows):
-        keys = (rows + 1) if w.causal else np.full_like(rows, w.N)
-        return float(np.sum(4.0 * keys * w.D))
-
-    # probe with a small row count, then size the sample to the budget
-    rows = np.arange(min(w.N, 64), dtype=np.int64)
+    # estimate the cost of one slice from a probe of 64 rows spread over the slice
+    rows = np.unique(np.linspace(0, w.N - 1, min(w.N, 64)).astype(np.int64))
+    q0, k0, v0 = (t[:, :1].double().numpy() for t in (q, k, v))
     t0 = time.perf_counter()
-    oracle.attention_rows(q64, k64, v64, w.scale, w.causal, np.zeros_like(rows), rows, threads)
-    dt = time.perf_counter() - t0
-    per_row = dt / len(rows)
-    n = int(max(1, min(w.N, budget_s / max(per_row, 1e-9))))
-    if max_rows:
-        n = min(n, max_rows)
-    rows = np.linspace(0, w.N - 1, n).astype(np.int64)
+    oracle.attention_rows(q0, k0, v0, w.scale, w.causal, np.zeros_like(rows), rows, threads)
+    per_row = (time.perf_counter() - t0) / len(rows)
+    per_slice = per_row * w.N
+    ns = int(max(1, min(BH, budget_s // max(per_slice, 1e-9))))
+    qs, ks, vs = (t[:, :ns].double().numpy() for t in (q, k, v))
     t0 = time.perf_counter()
-    oracle.attention_rows(q64, k64, v64, w.scale, w.causal, np.zeros_like(rows), rows, threads)
+    oracle.attention_fwd(qs, ks, vs, w.scale, w.causal, threads)
     dt = time.perf_counter() - t0
-    return flops_rows(rows) / dt / 1e12, dt, n, threads
+    flops = w.flops * ns / BH
+    return flops / dt / 1e12, dt, ns, threads
 
 
 def run_reference(args, w):
@@ -235,12 +230,13 @@ def config_of(w, gpus):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of CPU oracle timing (0 skips the CPU leg)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -374,9 +370,12 @@ def main():
     achieved = flops_step / (per_launch_ms / 1e3) / 1e12
     traffic = load_traffic(w.name)
     if w.dtype == "fp32":
-        roof = {"bound": "alu", "achieved": achieved, "peak": None, "unit": "TFLOP/s",
-                "frac": None, "traffic": traffic,
-                "note": "fp32 SIMT path; FFMA peak derived in DESIGN.md"}
+        # fp32 FFMA peak: SMs x 128 fp32 lanes x 2 FLOP x max SM clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = sms * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": traffic,
+                "peak_source": "derived: %d SMs x 128 fp32 lanes x 2 FLOP x max SM clock" % sms}
     else:
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
@@ -386,12 +385,13 @@ def main():
                 "hbm_gbs_algorithmic": (3 + 1) * B * H * N * D * 2 / (per_launch_ms / 1e3) / 1e9}
 
     cpu = None
-    if world == 1 or rank == 0:
+    if args.cpu_budget > 0:
         try:
-            tfl, secs, rows, threads = time_oracle(w, args.cpu_budget)
+            tfl, secs, ns, threads = time_oracle(w, args.cpu_budget, host_set)
             cpu = {"value": tfl, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-                   "sample": "%d query rows spread over slice (0,0) of %s (%d rows x %d slices), "
-                             "fp64 three-pass oracle, %.1f s" % (rows, w.name, N, B * H, secs)}
+                   "sample": "%d of %d (b,h) slices of %s (N=%d, D=%d, causal=%s), whole "
+                             "slices, fp64 three-pass oracle, %.1f s"
+                             % (ns, B * H, w.name, N, D, w.causal, secs)}
         except Exception as ex:  # the CPU leg must not hide the GPU number
             cpu = {"value": None, "unit": "TFLOPS", "cores": None, "kind": "oracle",
                    "sample": "failed: %s" % ex}
