@@ -200,41 +200,46 @@ __device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned 
 }
 
 // ----------------------------------------------------------------- MMA issue
+// Descriptors are built once per buffer; a K step only adds a constant to the start
+// address field (addresses stay below 256 KB, so the 14-bit field never carries).
+// All lanes of the MMA warp execute these; one elected lane issues.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem,
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc,
                                          uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (uint32_t)(kk / 4) * kPanelBytes + (uint32_t)(kk % 4) * 32u;
-        ptx::mma_ss(d_tmem, sw128_desc(q_smem + off, 16, 1024), sw128_desc(k_smem + off, 16, 1024),
-                    idesc, kk > 0 ? 1u : 0u);
+        const uint64_t off = ((uint64_t)(kk / 4) * kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
+        ptx::mma_ss_elect(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          uint32_t idesc, bool accumulate) {
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
         // V tile: rows = keys (K dimension), 128 B = 64 head-dim values per row (MN-major);
-        // 8-key groups 1024 B apart, 64-column panels kPanelBytes apart.
-        ptx::mma_ts(d_tmem, p_tmem + (uint32_t)kk * 8u,
-                    sw128_desc(v_smem + (uint32_t)kk * 16u * 128u, kPanelBytes, 1024), idesc,
-                    (accumulate || kk > 0) ? 1u : 0u);
+        // 16 keys = 2048 B per K step; 64-column panels kPanelBytes apart (LBO).
+        ptx::mma_ts_elect(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)((kk * 2048) >> 4),
+                          idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
 // ----------------------------------------------------------------- roles
+// MMA issuer: the whole warp runs this loop (waits are warp-uniform), one lane issues.
 template <int D, bool CAUSAL, bool F16>
 __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_t sbase) {
     using G = Geo<D>;
     constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false, F16);
     constexpr uint32_t idesc_pv = make_idesc(kBM, D, true, F16);
-    const uint32_t sQ[2] = {sbase, sbase + (uint32_t)G::kTileBytes};
+    const uint64_t dQ[2] = {sw128_desc(sbase, 16, 1024),
+                            sw128_desc(sbase + (uint32_t)G::kTileBytes, 16, 1024)};
+    const uint64_t dK0 = sw128_desc(sbase + (uint32_t)G::kKVOff, 16, 1024);       // K-major
+    const uint64_t dV0 = sw128_desc(sbase + (uint32_t)G::kKVOff, kPanelBytes, 1024);  // MN-major
     const uint32_t tS[2] = {tmem + G::col_s(0), tmem + G::col_s(1)};
     const uint32_t tO[2] = {tmem + G::col_o(0), tmem + G::col_o(1)};
-    auto slot = [&](uint32_t i) {
-        return sbase + (uint32_t)G::kKVOff + (i % G::kSlots) * (uint32_t)G::kTileBytes;
+    auto slot_off = [&](uint32_t i) {  // descriptor offset of ring slot i
+        return (uint64_t)((i % G::kSlots) * (uint32_t)G::kTileBytes) >> 4;
     };
     uint32_t kv = 0, q_cnt = 0, p_cnt0 = 0, p_cnt1 = 0;
 
@@ -242,54 +247,54 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
         const int nsub = unit_items<CAUSAL>(p, u);
         for (int sub = 0; sub < nsub; ++sub) {
             const Item it = unit_item<CAUSAL>(p, u, sub);
-            if (!wait(c, b_q_full<D>(0), q_cnt & 1u, kRoleMma)) goto out;
-            if (!wait(c, b_q_full<D>(1), q_cnt & 1u, kRoleMma)) goto out;
+            if (!wait_warp(c, b_q_full<D>(0), q_cnt & 1u, kRoleMma)) goto out;
+            if (!wait_warp(c, b_q_full<D>(1), q_cnt & 1u, kRoleMma)) goto out;
             ++q_cnt;
-            if (!wait(c, b_kv_full<D>(kv), ring_parity<D>(kv), kRoleMma)) goto out;
+            if (!wait_warp(c, b_kv_full<D>(kv), ring_parity<D>(kv), kRoleMma)) goto out;
             ptx::tc_fence_after();
-            issue_qk<D>(tS[0], sQ[0], slot(kv), idesc_qk);
-            ptx::mma_commit(bar_addr(c, b_s_full<D>(0)));
-            if (it.nA == 1) ptx::mma_commit(bar_addr(c, b_q_empty<D>(0)));
-            issue_qk<D>(tS[1], sQ[1], slot(kv), idesc_qk);
-            ptx::mma_commit(bar_addr(c, b_s_full<D>(1)));
-            if (it.nB == 1) ptx::mma_commit(bar_addr(c, b_q_empty<D>(1)));
-            ptx::mma_commit(bar_addr(c, b_kv_empty<D>(kv)));
+            issue_qk<D>(tS[0], dQ[0], dK0 + slot_off(kv), idesc_qk);
+            ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(0)));
+            if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(0)));
+            issue_qk<D>(tS[1], dQ[1], dK0 + slot_off(kv), idesc_qk);
+            ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(1)));
+            if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(1)));
+            ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(kv)));
             ++kv;
 
             for (int j = 0; j < it.nB; ++j) {
                 const uint32_t vpos = kv;        // V_j
                 const uint32_t kpos = kv + 1;    // K_{j+1}
                 const bool more = j + 1 < it.nB;
-                if (!wait(c, b_kv_full<D>(vpos), ring_parity<D>(vpos), kRoleMma)) goto out;
+                if (!wait_warp(c, b_kv_full<D>(vpos), ring_parity<D>(vpos), kRoleMma)) goto out;
                 ptx::tc_fence_after();
                 if (j < it.nA) {
-                    if (!wait(c, b_p_full<D>(0), p_cnt0 & 1u, kRoleMma)) goto out;
+                    if (!wait_warp(c, b_p_full<D>(0), p_cnt0 & 1u, kRoleMma)) goto out;
                     ++p_cnt0;
                     ptx::tc_fence_after();
-                    issue_pv<D>(tO[0], tS[0], slot(vpos), idesc_pv, j > 0);
-                    ptx::mma_commit(bar_addr(c, b_o_done<D>(0)));
+                    issue_pv<D>(tO[0], tS[0], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                    ptx::mma_commit_elect(bar_addr(c, b_o_done<D>(0)));
                 }
                 if (more) {
-                    if (!wait(c, b_kv_full<D>(kpos), ring_parity<D>(kpos), kRoleMma)) goto out;
+                    if (!wait_warp(c, b_kv_full<D>(kpos), ring_parity<D>(kpos), kRoleMma)) goto out;
                     ptx::tc_fence_after();
                 }
                 if (j + 1 < it.nA) {
-                    issue_qk<D>(tS[0], sQ[0], slot(kpos), idesc_qk);
-                    ptx::mma_commit(bar_addr(c, b_s_full<D>(0)));
-                    if (j + 2 == it.nA) ptx::mma_commit(bar_addr(c, b_q_empty<D>(0)));
+                    issue_qk<D>(tS[0], dQ[0], dK0 + slot_off(kpos), idesc_qk);
+                    ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(0)));
+                    if (j + 2 == it.nA) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(0)));
                 }
-                if (!wait(c, b_p_full<D>(1), p_cnt1 & 1u, kRoleMma)) goto out;
+                if (!wait_warp(c, b_p_full<D>(1), p_cnt1 & 1u, kRoleMma)) goto out;
                 ++p_cnt1;
                 ptx::tc_fence_after();
-                issue_pv<D>(tO[1], tS[1], slot(vpos), idesc_pv, j > 0);
-                ptx::mma_commit(bar_addr(c, b_o_done<D>(1)));
-                ptx::mma_commit(bar_addr(c, b_kv_empty<D>(vpos)));
+                issue_pv<D>(tO[1], tS[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                ptx::mma_commit_elect(bar_addr(c, b_o_done<D>(1)));
+                ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(vpos)));
                 ++kv;
                 if (more) {
-                    issue_qk<D>(tS[1], sQ[1], slot(kpos), idesc_qk);
-                    ptx::mma_commit(bar_addr(c, b_s_full<D>(1)));
-                    if (j + 2 == it.nB) ptx::mma_commit(bar_addr(c, b_q_empty<D>(1)));
-                    ptx::mma_commit(bar_addr(c, b_kv_empty<D>(kpos)));
+                    issue_qk<D>(tS[1], dQ[1], dK0 + slot_off(kpos), idesc_qk);
+                    ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(1)));
+                    if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(1)));
+                    ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(kpos)));
                     ++kv;
                 }
             }
@@ -297,8 +302,9 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
     }
 out:
     // Every product issued so far must finish before TMEM is released.
-    ptx::mma_commit(bar_addr(c, b_drain<D>()));
+    ptx::mma_commit_elect(bar_addr(c, b_drain<D>()));
     wait_drain(bar_addr(c, b_drain<D>()), 0, c.limit);
+    __syncwarp();
 }
 
 template <int D, bool CAUSAL>
@@ -366,41 +372,76 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-// One 128-key tile of one row: running max update, exp2, row sum, P packed to 16-bit.
-// s[]: raw (unscaled) scores; keys kbase + c with kbase + c >= limit are invisible.
-template <bool MASK, bool F16>
-__device__ __forceinline__ void softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
-                                             float sl2, float& m_run, float& l_run, float& alpha,
-                                             uint32_t (&pk)[64]) {
+// Row maximum of the raw scores of one 128-key tile; invisible keys (kbase + c >= limit)
+// are left out.
+template <bool MASK>
+__device__ __forceinline__ float tile_row_max(const uint32_t (&s)[128], int kbase, int limit) {
     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    if (MASK) {
 #pragma unroll
-    for (int c = 0; c < 128; ++c) {
-        float x = u2f(s[c]);
-        if (MASK && kbase + c >= limit) x = -INFINITY;
-        mx[c & 3] = fmaxf(mx[c & 3], x);
-    }
-    const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;  // log2 units
-    float m_new = m_run;
-    alpha = 1.0f;
-    if (mt > m_run + kRescaleLog2) {
-        m_new = mt;
-        alpha = ptx::ex2(m_run - mt);
-    }
-    const float neg = -m_new;
-    float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int c = 0; c < 128; ++c) {
+            const float x = (kbase + c < limit) ? u2f(s[c]) : -INFINITY;
+            mx[c & 3] = fmaxf(mx[c & 3], x);
+        }
+    } else {
 #pragma unroll
-    for (int c = 0; c < 128; c += 2) {
-        float p0 = ptx::ex2(fmaf(u2f(s[c]), sl2, neg));
-        float p1 = ptx::ex2(fmaf(u2f(s[c + 1]), sl2, neg));
+        for (int c = 0; c < 128; c += 8) {
+            mx[0] = ptx::max3(mx[0], u2f(s[c]), u2f(s[c + 1]));
+            mx[1] = ptx::max3(mx[1], u2f(s[c + 2]), u2f(s[c + 3]));
+            mx[2] = ptx::max3(mx[2], u2f(s[c + 4]), u2f(s[c + 5]));
+            mx[3] = ptx::max3(mx[3], u2f(s[c + 6]), u2f(s[c + 7]));
+        }
+    }
+    return ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+}
+
+// p = 2^(s * sl2 - m) for columns [C0, C0 + 64), packed to 16-bit pairs into pk[C0/2 ...],
+// partial row sums into acc (four fp32 pairs).  Invisible keys give p = 0.
+template <int C0, bool MASK, bool F16>
+__device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[128], int kbase, int limit,
+                                              float sl2, float neg_m, float (&acc)[8],
+                                              uint32_t (&pk)[64]) {
+#pragma unroll
+    for (int c = C0; c < C0 + 64; c += 2) {
+        float x0, x1;
+        ptx::fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), sl2, neg_m);
+        float p0 = ptx::ex2(x0);
+        float p1 = ptx::ex2(x1);
         if (MASK) {
             if (kbase + c >= limit) p0 = 0.f;
             if (kbase + c + 1 >= limit) p1 = 0.f;
         }
-        sum[(c >> 1) & 3] += p0 + p1;
+        const int a = ((c >> 1) & 3) * 2;
+        ptx::add2(acc[a], acc[a + 1], p0, p1);
         pk[c >> 1] = pack2<F16>(p0, p1);
     }
-    l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
-    m_run = m_new;
+}
+
+// One 128-key tile of one row: running-max update (raised only when the tile max exceeds
+// it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tS (64
+// columns, two 16-bit values per column) in two halves.  Returns the O rescale factor.
+template <bool MASK, bool F16>
+__device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
+                                              float sl2, float& m_run, float& l_run,
+                                              uint32_t tS) {
+    const float mt = tile_row_max<MASK>(s, kbase, limit) * sl2;  // log2 units
+    float alpha = 1.0f;
+    if (mt > m_run + kRescaleLog2) {
+        alpha = ptx::ex2(m_run - mt);   // m_run = -inf on the first tile: alpha = 0
+        m_run = mt;
+    }
+    const float neg_m = -m_run;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    uint32_t pk[64];
+    tile_exp_half<0, MASK, F16>(s, kbase, limit, sl2, neg_m, acc, pk);
+    __syncwarp();
+    ptx::tmem_st32p(tS, &pk[0]);
+    tile_exp_half<64, MASK, F16>(s, kbase, limit, sl2, neg_m, acc, pk);
+    __syncwarp();
+    ptx::tmem_st32p(tS + 32, &pk[32]);
+    const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    l_run = l_run * alpha + sum;
+    return alpha;
 }
 
 template <int D, bool CAUSAL, bool F16>
@@ -433,18 +474,11 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                 uint32_t s[128];
                 ptx::tmem_ld128_wait(tS, s);
                 const int kbase = j * kBN;
-                float alpha;
-                uint32_t pk[64];
-                if (__any_sync(0xFFFFFFFFu, kbase + kBN > limit))
-                    softmax_tile<true, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, alpha, pk);
-                else
-                    softmax_tile<false, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, alpha, pk);
-                __syncwarp();
-                // P over the first 64 columns of this tile's S region (two 16-bit values per column).
-                ptx::tmem_st16(tS + 0, &pk[0]);
-                ptx::tmem_st16(tS + 16, &pk[16]);
-                ptx::tmem_st16(tS + 32, &pk[32]);
-                ptx::tmem_st16(tS + 48, &pk[48]);
+                // P goes over the first 64 columns of this tile's S region.
+                const float alpha =
+                    __any_sync(0xFFFFFFFFu, kbase + kBN > limit)
+                        ? softmax_tile<true, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tS)
+                        : softmax_tile<false, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tS);
                 if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                     // The running max rose: rescale this row of O by alpha in TMEM.
 #pragma unroll 1
@@ -541,8 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     if (warp < kSoftmaxWarps) {
         softmax_role<D, CAUSAL, F16>(p, c, tmem, warp, lane);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_role<D, CAUSAL, F16>(p, c, tmem, sbase);
-        __syncwarp();
+        mma_role<D, CAUSAL, F16>(p, c, tmem, sbase);
     } else {
         if (lane == 0) load_role<D, CAUSAL>(p, c, sbase);
         __syncwarp();
