@@ -18,12 +18,15 @@
 //   * warps 0-3 / 4-7 (softmax of tile A / tile B): one thread per query row (TMEM lane =
 //     row).  Running max m and sum l stay in registers; exp2 with scale*log2(e) folded
 //     into one FMA; P is rounded to the input type and stored back into TMEM over S.
-//     The max is only raised when it grows by more than 2^8 (log2 units), and only then
+//     The max is only raised when it grows by more than 2^16 (2^8 for fp16), and only then
 //     is O rescaled in TMEM ("08 · FlashAttention" §五 and "第 13 课" §4B: old output
 //     multiplied by exp(m_old - m_new) when a larger maximum appears; keeping a stale
 //     reference is exact after the final division, since O and l share it).
 //   * epilogue: O / l (one division per row at the end, "第 13 课" exercise; "pwwt.cn"
-//     §2.2), LSE = (m + log2 l) * ln 2, stored from registers.
+//     §2.2), staged per warp through shared memory so that every global store writes
+//     whole 128-byte lines; LSE = (m + log2 l) * ln 2.
+//   * item prologue: Q_A, then K_0, then Q_B are loaded, so S_A(0) starts as early as
+//     possible when a CTA moves to its next work item.
 //   * causal: key tiles entirely after a query tile are skipped, only the diagonal tile
 //     is masked ("08 · FlashAttention" §四 is_causal).  Work units pair a heavy and a
 //     light query-tile pair of the same slice, so every unit costs about the same.
@@ -53,7 +56,10 @@ constexpr int kThreads = 320;
 constexpr int kPanelCols = 64;      // 16-bit elements per 128-byte swizzled row
 constexpr int kPanelBytes = kBM * 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleLog2 = 8.0f;
+// The running reference is raised only when a tile max exceeds it by more than this many
+// log2 units, so stored P values stay below 2^kRescaleLog2: 16 for bf16 P (exponent range
+// of fp32), 8 for fp16 P (largest fp16 is 65504).
+template <bool F16> struct Lazy { static constexpr float kRescaleLog2 = F16 ? 8.0f : 16.0f; };
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Roles recorded in the status word when a wait gives up.
@@ -68,12 +74,20 @@ struct Geo {
     static constexpr int kTileBytes = kPanels * kPanelBytes;   // one 128 x D tile
     static constexpr int kSlots = (D == 128) ? 4 : 8;          // K/V ring depth
     static constexpr int kKVOff = 2 * kTileBytes;               // after Q_A, Q_B
-    static constexpr int kBarOff = kKVOff + kSlots * kTileBytes;
+    // O staging: one 4 KB slot per softmax warp (its 32 rows x one 64-column panel, rows
+    // of 128 B with the 16-byte chunks XOR-swizzled by row so both the row-wise writes and
+    // the row-contiguous reads are free of bank conflicts)
+    static constexpr int kStageOff = kKVOff + kSlots * kTileBytes;
+    static constexpr int kStageSlot = 4096;
+    static constexpr int kBarOff = kStageOff + kSoftmaxWarps * kStageSlot;
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_done[2] drain
     static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 1;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;     // + alignment slack
     static constexpr uint32_t col_s(int t) { return (uint32_t)t * kBN; }
+    // P (16-bit pairs) overwrites the upper 64 columns of its S region, so S columns 0-63
+    // stay readable until the next S product
+    static constexpr uint32_t col_p(int t) { return (uint32_t)t * kBN + 64u; }
     static constexpr uint32_t col_o(int t) { return 2u * kBN + (uint32_t)t * D; }
 };
 
@@ -237,6 +251,7 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
     const uint64_t dK0 = sw128_desc(sbase + (uint32_t)G::kKVOff, 16, 1024);       // K-major
     const uint64_t dV0 = sw128_desc(sbase + (uint32_t)G::kKVOff, kPanelBytes, 1024);  // MN-major
     const uint32_t tS[2] = {tmem + G::col_s(0), tmem + G::col_s(1)};
+    const uint32_t tP[2] = {tmem + G::col_p(0), tmem + G::col_p(1)};
     const uint32_t tO[2] = {tmem + G::col_o(0), tmem + G::col_o(1)};
     auto slot_off = [&](uint32_t i) {  // descriptor offset of ring slot i
         return (uint64_t)((i % G::kSlots) * (uint32_t)G::kTileBytes) >> 4;
@@ -248,13 +263,14 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
         for (int sub = 0; sub < nsub; ++sub) {
             const Item it = unit_item<CAUSAL>(p, u, sub);
             if (!wait_warp(c, b_q_full<D>(0), q_cnt & 1u, kRoleMma)) goto out;
-            if (!wait_warp(c, b_q_full<D>(1), q_cnt & 1u, kRoleMma)) goto out;
-            ++q_cnt;
             if (!wait_warp(c, b_kv_full<D>(kv), ring_parity<D>(kv), kRoleMma)) goto out;
             ptx::tc_fence_after();
             issue_qk<D>(tS[0], dQ[0], dK0 + slot_off(kv), idesc_qk);
             ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(0)));
             if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(0)));
+            if (!wait_warp(c, b_q_full<D>(1), q_cnt & 1u, kRoleMma)) goto out;
+            ++q_cnt;
+            ptx::tc_fence_after();
             issue_qk<D>(tS[1], dQ[1], dK0 + slot_off(kv), idesc_qk);
             ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(1)));
             if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(1)));
@@ -271,7 +287,7 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
                     if (!wait_warp(c, b_p_full<D>(0), p_cnt0 & 1u, kRoleMma)) goto out;
                     ++p_cnt0;
                     ptx::tc_fence_after();
-                    issue_pv<D>(tO[0], tS[0], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                    issue_pv<D>(tO[0], tP[0], dV0 + slot_off(vpos), idesc_pv, j > 0);
                     ptx::mma_commit_elect(bar_addr(c, b_o_done<D>(0)));
                 }
                 if (more) {
@@ -286,7 +302,7 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
                 if (!wait_warp(c, b_p_full<D>(1), p_cnt1 & 1u, kRoleMma)) goto out;
                 ++p_cnt1;
                 ptx::tc_fence_after();
-                issue_pv<D>(tO[1], tS[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                issue_pv<D>(tO[1], tP[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
                 ptx::mma_commit_elect(bar_addr(c, b_o_done<D>(1)));
                 ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(vpos)));
                 ++kv;
@@ -322,8 +338,9 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
         const int nsub = unit_items<CAUSAL>(p, u);
         for (int sub = 0; sub < nsub; ++sub) {
             const Item it = unit_item<CAUSAL>(p, u, sub);
-            for (int t = 0; t < 2; ++t) {
-                if (!wait(c, b_q_empty<D>(t), (q_cnt & 1u) ^ 1u, kRoleLoad)) goto out;
+            // Q_A first, then K_0 (so S_A(0) can start), then Q_B, then V_0, K_1, V_1, ...
+            auto load_q = [&](int t) -> bool {
+                if (!wait(c, b_q_empty<D>(t), (q_cnt & 1u) ^ 1u, kRoleLoad)) return false;
                 const uint32_t fb = bar_addr(c, b_q_full<D>(t));
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
 #pragma unroll
@@ -331,8 +348,9 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                     ptx::tma_load_3d(sQ[t] + (uint32_t)pc * kPanelBytes, &p.tmap_q, fb, pc * kPanelCols,
                                      it.pair * 2 * kBM + t * kBM, it.bh);
                 ++q_issued[t];
-            }
-            ++q_cnt;
+                return true;
+            };
+            if (!load_q(0)) goto out;
             for (int j = 0; j < it.nB; ++j) {
                 for (int w = 0; w < 2; ++w) {  // K_j then V_j
                     if (!wait(c, b_kv_empty<D>(kv), ring_parity<D>(kv) ^ 1u, kRoleLoad)) goto out;
@@ -346,8 +364,10 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                                              pc * kPanelCols, j * kBN, it.bh);
                     }
                     ++kv;
+                    if (j == 0 && w == 0 && !load_q(1)) goto out;
                 }
             }
+            ++q_cnt;
         }
     }
 out:
@@ -376,23 +396,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // are left out.
 template <bool MASK>
 __device__ __forceinline__ float tile_row_max(const uint32_t (&s)[128], int kbase, int limit) {
-    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float mx[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
     if (MASK) {
 #pragma unroll
         for (int c = 0; c < 128; ++c) {
             const float x = (kbase + c < limit) ? u2f(s[c]) : -INFINITY;
-            mx[c & 3] = fmaxf(mx[c & 3], x);
+            mx[c & 7] = fmaxf(mx[c & 7], x);
         }
     } else {
+        // eight independent chains keep the dependent depth short
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-            mx[0] = ptx::max3(mx[0], u2f(s[c]), u2f(s[c + 1]));
-            mx[1] = ptx::max3(mx[1], u2f(s[c + 2]), u2f(s[c + 3]));
-            mx[2] = ptx::max3(mx[2], u2f(s[c + 4]), u2f(s[c + 5]));
-            mx[3] = ptx::max3(mx[3], u2f(s[c + 6]), u2f(s[c + 7]));
-        }
+        for (int c = 0; c < 128; c += 2)
+            mx[(c >> 1) & 7] = ptx::max3(mx[(c >> 1) & 7], u2f(s[c]), u2f(s[c + 1]));
     }
-    return ptx::max3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+    return fmaxf(ptx::max3(mx[0], mx[1], mx[2]), fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
 // p = 2^(s * sl2 - m) for columns [C0, C0 + 64), packed to 16-bit pairs into pk[C0/2 ...],
@@ -418,15 +437,15 @@ __device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[128], int kbas
 }
 
 // One 128-key tile of one row: running-max update (raised only when the tile max exceeds
-// it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tS (64
+// it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tP (64
 // columns, two 16-bit values per column) in two halves.  Returns the O rescale factor.
 template <bool MASK, bool F16>
 __device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
                                               float sl2, float& m_run, float& l_run,
-                                              uint32_t tS) {
+                                              uint32_t tP) {
     const float mt = tile_row_max<MASK>(s, kbase, limit) * sl2;  // log2 units
     float alpha = 1.0f;
-    if (mt > m_run + kRescaleLog2) {
+    if (mt > m_run + Lazy<F16>::kRescaleLog2) {
         alpha = ptx::ex2(m_run - mt);   // m_run = -inf on the first tile: alpha = 0
         m_run = mt;
     }
@@ -435,22 +454,24 @@ __device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbas
     uint32_t pk[64];
     tile_exp_half<0, MASK, F16>(s, kbase, limit, sl2, neg_m, acc, pk);
     __syncwarp();
-    ptx::tmem_st32p(tS, &pk[0]);
+    ptx::tmem_st32p(tP, &pk[0]);
     tile_exp_half<64, MASK, F16>(s, kbase, limit, sl2, neg_m, acc, pk);
     __syncwarp();
-    ptx::tmem_st32p(tS + 32, &pk[32]);
+    ptx::tmem_st32p(tP + 32, &pk[32]);
     const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     l_run = l_run * alpha + sum;
     return alpha;
 }
 
 template <int D, bool CAUSAL, bool F16>
-__device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int warp, int lane) {
+__device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int warp, int lane,
+                             uint32_t stage) {
     using G = Geo<D>;
     const int t = warp / 4;                       // 0: tile A, 1: tile B
     const int lane_base = (warp % 4) * 32;        // this warp's TMEM lane quarter
     const uint32_t tl = (uint32_t)lane_base << 16;
     const uint32_t tS = tmem + tl + G::col_s(t);
+    const uint32_t tP = tmem + tl + G::col_p(t);
     const uint32_t tO = tmem + tl + G::col_o(t);
     uint32_t s_cnt = 0, o_cnt = 0;
 
@@ -474,11 +495,10 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                 uint32_t s[128];
                 ptx::tmem_ld128_wait(tS, s);
                 const int kbase = j * kBN;
-                // P goes over the first 64 columns of this tile's S region.
+                const bool mask = __any_sync(0xFFFFFFFFu, kbase + kBN > limit);
                 const float alpha =
-                    __any_sync(0xFFFFFFFFu, kbase + kBN > limit)
-                        ? softmax_tile<true, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tS)
-                        : softmax_tile<false, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tS);
+                    mask ? softmax_tile<true, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tP)
+                         : softmax_tile<false, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tP);
                 if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                     // The running max rose: rescale this row of O by alpha in TMEM.
 #pragma unroll 1
@@ -495,31 +515,45 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                 ptx::mbar_arrive(bar_addr(c, b_p_full<D>(t)));
             }
 
-            // Epilogue: O / l and LSE for this row.
+            // Epilogue: O / l, one 64-column panel at a time through this warp's staging
+            // slot, so the global stores are row-contiguous: each store instruction writes
+            // four whole 128-byte lines (rows past N are skipped); LSE from registers.
             if (!wait_warp(c, b_o_done<D>(t), o_cnt & 1u, kRoleSoftmax)) return;
             ++o_cnt;
             ptx::tc_fence_after();
-            const bool live = row < p.n;
             const float inv_l = 1.0f / l_run;
-            const size_t grow = (size_t)it.bh * (size_t)p.n + (size_t)(live ? row : 0);
-            uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + grow * D;
+            const int row0 = it.pair * 2 * kBM + t * kBM + lane_base;   // first row of the warp
+            uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)it.bh * (size_t)p.n * D;
 #pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                ptx::tmem_ld32_wait(tO + (uint32_t)cc * 32u, o);
-                uint32_t w[16];
+            for (int pc = 0; pc < D / 64; ++pc) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    w[i] = pack2<F16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
-                if (live) {
-                    uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32_wait(tO + (uint32_t)(pc * 64 + h * 32), o);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack2<F16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t chunk = (uint32_t)(h * 4 + i) ^ (uint32_t)(lane & 7);
+                        ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
+                                          w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
                 }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int r = 4 * k + (lane >> 3);   // row within the warp's 32
+                    const int ch = lane & 7;             // 16-byte chunk within the 128-byte row
+                    const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u +
+                                                      (uint32_t)((ch ^ (r & 7)) * 16));
+                    if (row0 + r < p.n)
+                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * D + pc * 64 + ch * 8) = v;
+                }
+                __syncwarp();
             }
-            if (live) p.lse[grow] = (m_run + log2f(l_run)) * kLn2;
+            if (row < p.n) p.lse[(size_t)it.bh * (size_t)p.n + (size_t)row] = (m_run + log2f(l_run)) * kLn2;
             __syncwarp();
         }
     }
@@ -573,7 +607,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kSoftmaxWarps) {
-        softmax_role<D, CAUSAL, F16>(p, c, tmem, warp, lane);
+        softmax_role<D, CAUSAL, F16>(p, c, tmem, warp, lane,
+                                     sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
     } else if (warp == kMmaWarp) {
         mma_role<D, CAUSAL, F16>(p, c, tmem, sbase);
     } else {
