@@ -218,6 +218,27 @@ def run_reference(args, w):
     return 0
 
 
+def aggregate_over_ranks(ms_local: float, units_local: float, steps: int, world: int,
+                         all_reduce_max=None):
+    """Whole-job throughput of independent replicas: every rank timed its own `steps` steps
+    (ms_local); the job time is the slowest rank's, and the value is the units all ranks
+    processed (units_local per step per rank) over that time, in units per second.
+    all_reduce_max(x) returns the max of x over ranks (None for a single process)."""
+    ms = ms_local if all_reduce_max is None or world == 1 else float(all_reduce_max(ms_local))
+    return ms, units_local * steps * world / (ms / 1e3)
+
+
+def torch_all_reduce_max(device):
+    import torch
+    import torch.distributed as dist
+
+    def f(x):
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return f
+
+
 def config_of(w, gpus):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
             "dtype": w.dtype, "scale": w.scale, "qk_mult": w.qk_mult,
@@ -317,13 +338,10 @@ def main():
     if st != 0:
         raise RuntimeError("kernel watchdog in timed region: %d %s" % (st, detail))
 
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
     flops_step = w.flops
-    value = flops_step * args.steps * world / (ms / 1e3) / 1e12
+    reduce_max = torch_all_reduce_max(dev) if world > 1 else None
+    ms, per_s = aggregate_over_ranks(ms_local, flops_step, args.steps, world, reduce_max)
+    value = per_s / 1e12
     per_launch_ms = ms_local / args.steps
 
     # ---- end to end through the public API: pinned host inputs -> device -> fa.fwd -> host
@@ -351,12 +369,9 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = flops_step * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    e2e_ms, e2e_per_s = aggregate_over_ranks(e0.elapsed_time(e1), flops_step, args.e2e_steps,
+                                             world, reduce_max)
+    e2e_value = e2e_per_s / 1e12
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
 
