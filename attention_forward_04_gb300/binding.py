@@ -25,6 +25,12 @@ SIGNATURES = {
     "fa_fwd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                           _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_float, _c.c_int,
                           _c.c_int, _c.c_void_p]),
+    "fa_fwd_bnhd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                               _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_float,
+                               _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_fwd_varlen": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                 _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
+                                 _c.c_int64, _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_last_cuda_error": (_c.c_char_p, []),
     "fa_check_device_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
@@ -113,6 +119,66 @@ def fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     with torch.cuda.device(q.device):
         _check(fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, D, scale, causal, _dtype_code(q), handle))
+    return out, lse
+
+
+def _common(q, k, v, ndim):
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dim() != ndim or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one %d-D shape" % ndim)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+
+
+def _stream_handle(q, stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def fwd_bnhd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
+    """Forward pass over token-major tensors q, k, v [B, N, H, D] (fa_fwd_bnhd).
+
+    Returns (o [B, N, H, D], lse [B, H, N] fp32)."""
+    import torch
+    _common(q, k, v, 4)
+    B, N, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_fwd_bnhd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                              out.data_ptr(), lse.data_ptr(), B, N, H, D,
+                                              float(scale), int(causal), _dtype_code(q),
+                                              _stream_handle(q, stream))))
+    return out, lse
+
+
+def fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, out=None, lse=None,
+               stream=None):
+    """Forward pass over packed sequences (fa_fwd_varlen).
+
+    q, k, v: [total, H, D]; cu_seqlens: int32 CUDA tensor [batch + 1] of token offsets.
+    Returns (o [total, H, D], lse [H, total] fp32)."""
+    import torch
+    _common(q, k, v, 3)
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1):
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    T, H, D = q.shape
+    batch = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                out.data_ptr(), lse.data_ptr(),
+                                                cu_seqlens.data_ptr(), batch, int(max_seqlen), T,
+                                                H, D, float(scale), int(causal), _dtype_code(q),
+                                                _stream_handle(q, stream))))
     return out, lse
 
 

@@ -58,13 +58,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
     return fn;
 }
 
-// [BH, N, D] 16-bit tensor viewed as a 3-D map (innermost D); box {64, 128, 1} with the
-// 128-byte swizzle the tensor-core kernel expects.  Rows past N read as zero.
-bool encode_map(CUtensorMap* map, const void* base, int64_t bh, int64_t n, int64_t d, bool f16,
-                PFN_cuTensorMapEncodeTiled_v12000 fn) {
-    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
-    cuuint64_t strides[2] = {(cuuint64_t)(d * 2), (cuuint64_t)(n * d * 2)};
-    cuuint32_t box[3] = {64, 128, 1};
+// 16-bit tensor viewed as a 3-D TMA map whose box lands in shared memory as 128 rows of
+// 64 head-dim values (128 bytes, 128-byte swizzle), which the tensor-core kernel expects.
+//   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, 128, 1}; rows past N read as zero.
+//   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, 128}; tokens past T read
+//   as zero (tokens of the next packed sequence are masked by the kernel instead).
+bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int64_t n, int64_t h,
+                int64_t t, int64_t d, bool f16, PFN_cuTensorMapEncodeTiled_v12000 fn) {
+    cuuint64_t dims[3], strides[2];
+    cuuint32_t box[3];
+    if (layout == 0) {
+        dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)n; dims[2] = (cuuint64_t)bh;
+        strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(n * d * 2);
+        box[0] = 64; box[1] = 128; box[2] = 1;
+    } else {
+        dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)h; dims[2] = (cuuint64_t)t;
+        strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(h * d * 2);
+        box[0] = 64; box[1] = 1; box[2] = 128;
+    }
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -82,7 +93,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
-int fa_version(void) { return 100; }
+int fa_version(void) { return 110; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -115,34 +126,55 @@ int fa_check_device_status(void* stream, uint32_t* detail) {
     return (w[0] & 1u) ? FA_ERR_TIMEOUT : FA_OK;
 }
 
-int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
-           int64_t N, int64_t D, float scale, int causal, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One forward request in any of the three layouts.
+struct Request {
+    const void *q, *k, *v;
+    void* o;
+    float* lse;
+    int64_t B, H, N, D;    // N: sequence length, or the longest packed sequence
+    int64_t T;             // token-major layouts: tokens (B*N, or the packed total)
+    int layout;            // 0: [B, H, N, D]; 1: token-major [T, H, D]
+    const int* cu;         // packed sequences: [B + 1] token offsets (device), else null
+    float scale;
+    int causal, dtype;
+    void* stream;
+};
+
+int forward(const Request& r) {
     // ---- argument checks: no CUDA call before these pass
-    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
-    if (B < 1 || H < 1 || N < 1) return FA_ERR_INVALID_ARG;
-    if (B > 0x7FFFFFFFLL || H > 0x7FFFFFFFLL || B * H > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL)
+    if (!r.q || !r.k || !r.v || !r.o || !r.lse) return FA_ERR_INVALID_ARG;
+    if (r.B < 1 || r.H < 1 || r.N < 1 || r.T < 1) return FA_ERR_INVALID_ARG;
+    if (r.B > 0x7FFFFFFFLL || r.H > 0x7FFFFFFFLL || r.B * r.H > 0x7FFFFFFFLL ||
+        r.N > 0x7FFFFFFFLL || r.T > 0x7FFFFFFFLL)
         return FA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-    const int64_t BH = B * H;
-    const size_t esize = dtype == FA_FP32 ? 4 : 2;
-    const size_t tbytes = (size_t)BH * (size_t)N * (size_t)D * esize;
-    const size_t lbytes = (size_t)BH * (size_t)N * sizeof(float);
-    if (tbytes / esize / (size_t)D / (size_t)N != (size_t)BH) return FA_ERR_INVALID_ARG;
-    if (overlaps(o, tbytes, q, tbytes) || overlaps(o, tbytes, k, tbytes) ||
-        overlaps(o, tbytes, v, tbytes) || overlaps(lse, lbytes, q, tbytes) ||
-        overlaps(lse, lbytes, k, tbytes) || overlaps(lse, lbytes, v, tbytes) ||
-        overlaps(lse, lbytes, o, tbytes))
+    if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
+    if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (r.D != 64 && r.D != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = r.B * r.H;
+    const size_t esize = r.dtype == FA_FP32 ? 4 : 2;
+    const int64_t rows = r.layout == 0 ? BH * r.N : r.T * r.H;   // rows of D elements
+    if (rows / r.H != (r.layout == 0 ? r.B * r.N : r.T)) return FA_ERR_INVALID_ARG;
+    const size_t tbytes = (size_t)rows * (size_t)r.D * esize;
+    const size_t lbytes = (size_t)(r.cu ? r.T * r.H : BH * r.N) * sizeof(float);
+    if (tbytes / esize / (size_t)r.D != (size_t)rows) return FA_ERR_INVALID_ARG;
+    if (overlaps(r.o, tbytes, r.q, tbytes) || overlaps(r.o, tbytes, r.k, tbytes) ||
+        overlaps(r.o, tbytes, r.v, tbytes) || overlaps(r.lse, lbytes, r.q, tbytes) ||
+        overlaps(r.lse, lbytes, r.k, tbytes) || overlaps(r.lse, lbytes, r.v, tbytes) ||
+        overlaps(r.lse, lbytes, r.o, tbytes))
         return FA_ERR_INVALID_ARG;
-    for (const void* ptr : {q, k, v, static_cast<const void*>(o)})
+    for (const void* ptr : {r.q, r.k, r.v, static_cast<const void*>(r.o)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_MISALIGNED;
-    if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_MISALIGNED;
-    const bool tc = dtype != FA_FP32;
+    if ((reinterpret_cast<uintptr_t>(r.lse) & 3u) || (reinterpret_cast<uintptr_t>(r.cu) & 3u))
+        return FA_ERR_MISALIGNED;
+    const bool tc = r.dtype != FA_FP32;
     int units = 0;
     if (tc) {
-        units = fa::tc_units((int)BH, (int)N, causal != 0);
+        units = fa::tc_units((int)BH, (int)r.N, r.causal != 0);
         if (units < 0) return FA_ERR_UNSUPPORTED;
     }
 
@@ -161,19 +193,26 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     });
     if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
     if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;  // built for sm_103a only
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaStream_t st = static_cast<cudaStream_t>(r.stream);
+
+    fa::SliceLayout g;
+    g.layout = r.layout;
+    g.cu_seqlens = r.cu;
+    g.heads = (int)r.H;
+    g.total = (int)r.T;
+    g.n = (int)r.N;
 
     if (!tc) {
-        e = fa::simt_launch((int)D, causal != 0, static_cast<const float*>(q),
-                            static_cast<const float*>(k), static_cast<const float*>(v),
-                            static_cast<float*>(o), lse, (int)BH, (int)N, scale, st);
+        e = fa::simt_launch((int)r.D, r.causal != 0, static_cast<const float*>(r.q),
+                            static_cast<const float*>(r.k), static_cast<const float*>(r.v),
+                            static_cast<float*>(r.o), r.lse, (int)BH, g, r.scale, st);
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "fp32 kernel launch");
     }
 
-    const bool f16 = dtype == FA_FP16;
-    const int di128 = D == 128, dic = causal != 0, dif = f16;
+    const bool f16 = r.dtype == FA_FP16;
+    const int di128 = r.D == 128, dic = r.causal != 0, dif = f16;
     std::call_once(di.prepared[di128][dic][dif],
-                   [&] { di.prepare_err[di128][dic][dif] = fa::tc_prepare((int)D, dic, f16); });
+                   [&] { di.prepare_err[di128][dic][dif] = fa::tc_prepare((int)r.D, dic, f16); });
     if (di.prepare_err[di128][dic][dif] != cudaSuccess)
         return fail_cuda(di.prepare_err[di128][dic][dif], "cudaFuncSetAttribute");
 
@@ -181,22 +220,52 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
     if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
     fa::TcParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!encode_map(&p.tmap_q, q, BH, N, D, f16, fn) || !encode_map(&p.tmap_k, k, BH, N, D, f16, fn) ||
-        !encode_map(&p.tmap_v, v, BH, N, D, f16, fn))
+    if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, f16, fn) ||
+        !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, f16, fn) ||
+        !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, f16, fn))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    p.o = o;
-    p.lse = lse;
-    p.n = (int)N;
+    p.o = r.o;
+    p.lse = r.lse;
+    p.layout = r.layout;
+    p.cu_seqlens = r.cu;
+    p.heads = (int)r.H;
+    p.total = (int)r.T;
+    p.n = (int)r.N;
     p.bh = (int)BH;
-    p.npairs = (int)((N + 255) / 256);
-    p.nkv = (int)((N + 127) / 128);
+    p.npairs = (int)((r.N + 255) / 256);
+    p.nkv = (int)((r.N + 127) / 128);
     p.units = units;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2 = r.scale * 1.4426950408889634f;
     p.wait_limit = g_wait_limit.load();
     p.inject_stall = g_inject_stall.load();
     const int grid = units < di.sm_count ? units : di.sm_count;
-    e = fa::tc_launch((int)D, dic, f16, p, grid, st);
+    e = fa::tc_launch((int)r.D, dic, f16, p, grid, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
+           int64_t N, int64_t D, float scale, int causal, int dtype, void* stream) {
+    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 0, nullptr, scale, causal, dtype, stream};
+    return forward(r);
+}
+
+int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+                int64_t N, int64_t H, int64_t D, float scale, int causal, int dtype, void* stream) {
+    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 1, nullptr, scale, causal, dtype, stream};
+    return forward(r);
+}
+
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total,
+                  int64_t H, int64_t D, float scale, int causal, int dtype, void* stream) {
+    if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+    const Request r{q, k, v, o, lse, batch, H, max_seqlen, D, total, 1, cu_seqlens, scale, causal,
+                    dtype, stream};
+    return forward(r);
 }
 
 }  // extern "C"

@@ -13,12 +13,16 @@ struct TcParams {
     CUtensorMap tmap_q;  // 3-D maps over the [B*H, N, D] view, innermost D; box {64, 128, 1},
     CUtensorMap tmap_k;  // 128-byte swizzle, zero fill outside the tensor (ragged N)
     CUtensorMap tmap_v;
-    void* o;             // [B*H, N, D] output, same element type as the inputs
-    float* lse;          // [B*H, N] fp32
-    int n;               // sequence length N
+    void* o;             // output, same element type and layout as the inputs
+    float* lse;          // fp32 LSE: [B, H, N], or [H, total] for packed sequences
+    int layout;          // 0: [B, H, N, D] slices; 1: token-major [tokens, H, D]
+    const int* cu_seqlens;  // packed sequences: [B + 1] token offsets (device), else null
+    int heads;           // H
+    int total;           // tokens in the token-major view (B*N, or the packed total)
+    int n;               // sequence length N (packed sequences: the longest allowed length)
     int bh;              // B*H
-    int npairs;          // ceil(N / 256): query-tile pairs per slice
-    int nkv;             // ceil(N / 128): key/value tiles per slice
+    int npairs;          // ceil(N / 256): query-tile pairs per slice (at most)
+    int nkv;             // ceil(N / 128): key/value tiles per slice (at most)
     int units;           // work units of the persistent schedule
     float scale_log2;    // scale * log2(e)
     unsigned long long wait_limit;  // cycles a single wait may spin before giving up
@@ -41,8 +45,18 @@ cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
 // Copy the device status word (4 words) of the tensor-core kernels to `out` and clear it.
 cudaError_t tc_status_read_reset(uint32_t out[4]);
 
-// fp32 SIMT kernel: q, k, v, o [B*H, N, D] fp32, lse [B*H, N].
+// Geometry shared by both paths: where row r of slice (b, h) lives.
+struct SliceLayout {
+    int layout;             // 0: [B, H, N, D]; 1: token-major [tokens, H, D]
+    const int* cu_seqlens;  // packed sequences (device), else null
+    int heads;              // H
+    int total;              // tokens in the token-major view
+    int n;                  // N, or the longest allowed packed length
+};
+
+// fp32 SIMT kernel over the same layouts (fp32 storage).
 cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, const float* v,
-                        float* o, float* lse, int bh, int n, float scale, cudaStream_t stream);
+                        float* o, float* lse, int bh, const SliceLayout& g, float scale,
+                        cudaStream_t stream);
 
 }  // namespace fa

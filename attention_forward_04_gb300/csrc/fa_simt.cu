@@ -7,6 +7,9 @@
 // FlashAttention" Figure 13-2): each CTA owns 32 query rows of one (b, h) slice, keeps
 // (m, l, O) on chip for the whole key loop, and writes O and LSE once.
 //
+// Layouts: [B, H, N, D] slices, or token-major [tokens, H, D] (fixed length N, or packed
+// sequences with token offsets cu_seqlens), as in the tensor-core path.
+//
 // CTA = 128 threads = 32 rows x 4 threads.  Thread q of a row owns head-dim columns
 // q, q+4, q+8, ... (interleaved, so the 4 threads of a row hit 4 different banks when
 // reading a shared K/V row).  Per key tile of 32 keys: partial dot products are summed
@@ -30,8 +33,8 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
                                                            const float* __restrict__ k,
                                                            const float* __restrict__ v,
                                                            float* __restrict__ o,
-                                                           float* __restrict__ lse, int n,
-                                                           float scale) {
+                                                           float* __restrict__ lse,
+                                                           const SliceLayout g, float scale) {
     constexpr int DQ = D / 4;  // columns per thread
     __shared__ __align__(16) float Ks[kKeys][D];
     __shared__ __align__(16) float Vs[kKeys][D];
@@ -39,17 +42,32 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
     const int tid = threadIdx.x;
     const int r = tid / 4;         // row within the CTA
     const int qd = tid % 4;        // column phase: columns qd + 4*i
-    const int nblk = (n + kRows - 1) / kRows;
+    const int nblk = (g.n + kRows - 1) / kRows;
     const int bh = (int)(blockIdx.x / (unsigned)nblk);     // slice b*H + h
     const int blk = (int)(blockIdx.x % (unsigned)nblk);    // row block within the slice
-    const size_t slice = (size_t)bh * (size_t)n * D;
+    const int b = bh / g.heads, h = bh % g.heads;
+    // Length and first token of the slice; packed offsets are clamped to [0, total] and
+    // lengths to the declared maximum, so malformed offsets cannot move an access out of bounds.
+    int n = g.n, tok0 = b * g.n;
+    if (g.cu_seqlens != nullptr) {
+        int s0 = g.cu_seqlens[b], s1 = g.cu_seqlens[b + 1];
+        s0 = min(max(s0, 0), g.total);
+        s1 = min(max(s1, s0), g.total);
+        n = min(s1 - s0, g.n);
+        tok0 = s0;
+    }
+    if (blk * kRows >= n) return;   // the whole block lies past the end of the sequence
+    // row j of the slice starts at element slice + j * rs
+    const size_t rs = g.layout == 0 ? (size_t)D : (size_t)g.heads * D;
+    const size_t slice = g.layout == 0 ? (size_t)bh * (size_t)g.n * D : ((size_t)tok0 * g.heads + h) * D;
+    const size_t lse0 = g.cu_seqlens != nullptr ? (size_t)h * g.total + tok0 : (size_t)bh * g.n;
     const int row = blk * kRows + r;
     const bool live = row < n;
 
     float qv[DQ], acc[DQ];
 #pragma unroll
     for (int i = 0; i < DQ; ++i) {
-        qv[i] = live ? q[slice + (size_t)row * D + qd + 4 * i] : 0.0f;
+        qv[i] = live ? q[slice + (size_t)row * rs + qd + 4 * i] : 0.0f;
         acc[i] = 0.0f;
     }
     float m = -INFINITY, l = 0.0f;
@@ -66,8 +84,8 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
             const int kc = (idx % (D / 4)) * 4;
             float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
             if (k0 + kr < n) {
-                kx = *reinterpret_cast<const float4*>(k + slice + (size_t)(k0 + kr) * D + kc);
-                vx = *reinterpret_cast<const float4*>(v + slice + (size_t)(k0 + kr) * D + kc);
+                kx = *reinterpret_cast<const float4*>(k + slice + (size_t)(k0 + kr) * rs + kc);
+                vx = *reinterpret_cast<const float4*>(v + slice + (size_t)(k0 + kr) * rs + kc);
             }
             *reinterpret_cast<float4*>(&Ks[kr][kc]) = kx;
             *reinterpret_cast<float4*>(&Vs[kr][kc]) = vx;
@@ -112,29 +130,30 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
     if (live) {
         const float inv_l = 1.0f / l;
 #pragma unroll
-        for (int i = 0; i < DQ; ++i) o[slice + (size_t)row * D + qd + 4 * i] = acc[i] * inv_l;
-        if (qd == 0) lse[(size_t)bh * n + row] = m + logf(l);
+        for (int i = 0; i < DQ; ++i) o[slice + (size_t)row * rs + qd + 4 * i] = acc[i] * inv_l;
+        if (qd == 0) lse[lse0 + row] = m + logf(l);
     }
 }
 
 template <int D, bool CAUSAL>
 cudaError_t launch(const float* q, const float* k, const float* v, float* o, float* lse, int bh,
-                   int n, float scale, cudaStream_t stream) {
-    const long long blocks = (long long)((n + kRows - 1) / kRows) * bh;
+                   const SliceLayout& g, float scale, cudaStream_t stream) {
+    const long long blocks = (long long)((g.n + kRows - 1) / kRows) * bh;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    fa_simt_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, lse, n, scale);
+    fa_simt_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, lse, g, scale);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, const float* v,
-                        float* o, float* lse, int bh, int n, float scale, cudaStream_t stream) {
+                        float* o, float* lse, int bh, const SliceLayout& g, float scale,
+                        cudaStream_t stream) {
     if (D == 64)
-        return causal ? launch<64, true>(q, k, v, o, lse, bh, n, scale, stream)
-                      : launch<64, false>(q, k, v, o, lse, bh, n, scale, stream);
-    return causal ? launch<128, true>(q, k, v, o, lse, bh, n, scale, stream)
-                  : launch<128, false>(q, k, v, o, lse, bh, n, scale, stream);
+        return causal ? launch<64, true>(q, k, v, o, lse, bh, g, scale, stream)
+                      : launch<64, false>(q, k, v, o, lse, bh, g, scale, stream);
+    return causal ? launch<128, true>(q, k, v, o, lse, bh, g, scale, stream)
+                  : launch<128, false>(q, k, v, o, lse, bh, g, scale, stream);
 }
 
 }  // namespace fa

@@ -127,39 +127,102 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
 // ----------------------------------------------------------------- work schedule
 struct Item {
     int bh;    // slice b*H + h
+    int h;     // head
     int pair;  // query rows [256*pair, 256*pair + 256): tile A = first 128, tile B = next 128
     int nA;    // key/value tiles tile A visits
     int nB;    // key/value tiles tile B visits (nB >= nA)
+    int len;   // sequence length of the slice
+    int tok0;  // token-major layout: token index of row 0 of the slice
 };
 
-// Non-causal: one unit per (slice, pair), slice-major so concurrently running CTAs share
-// the K/V of a few slices in L2.  Causal: unit (slice, q) holds pairs npairs-1-q and q,
-// heavy first; every unit then costs about the same.
-template <bool CAUSAL>
-__device__ __forceinline__ int unit_items(const TcParams& p, int u) {
-    if (!CAUSAL) return 1;
-    const int half = (p.npairs + 1) / 2;
-    const int q = u % half;
-    return (p.npairs - 1 - q != q) ? 2 : 1;
+// Length and first token of slice bh.  Packed offsets are clamped to [0, total] and lengths
+// to the declared maximum, so malformed offsets cannot move any access out of bounds.
+template <int MODE>
+__device__ __forceinline__ void slice_geometry(const TcParams& p, int bh, int& len, int& tok0) {
+    if (MODE == 0) {   // [B, H, N, D]: every slice has N rows
+        len = p.n;
+        tok0 = 0;
+        return;
+    }
+    const int b = bh / p.heads;
+    if (p.cu_seqlens != nullptr) {
+        int s0 = __ldg(p.cu_seqlens + b), s1 = __ldg(p.cu_seqlens + b + 1);
+        s0 = min(max(s0, 0), p.total);
+        s1 = min(max(s1, s0), p.total);
+        len = min(s1 - s0, p.n);
+        tok0 = s0;
+    } else {
+        len = p.n;
+        tok0 = b * p.n;
+    }
 }
 
-template <bool CAUSAL>
+// Work units: non-causal, one unit per (slice, pair), slice-major so concurrently running
+// CTAs share the K/V of a few slices in L2.  Causal: unit (slice, q) holds pairs
+// npairs-1-q and q of that slice, heavy first, so every unit costs about the same.  Units
+// past the end of a (shorter) packed sequence hold nothing.  unit_count gives the number of
+// items of unit u, unit_item the s-th one (computed on demand to keep registers free).
+template <bool CAUSAL, int MODE>
+__device__ __forceinline__ int unit_count(const TcParams& p, int u) {
+    if (MODE == 0) {   // [B, H, N, D]: every unit is full
+        if (!CAUSAL) return 1;
+        const int q = u % ((p.npairs + 1) / 2);
+        return (p.npairs - 1 - q != q) ? 2 : 1;
+    }
+    const int per_slice = CAUSAL ? (p.npairs + 1) / 2 : p.npairs;
+    const int q = u % per_slice;
+    int len, tok0;
+    slice_geometry<MODE>(p, u / per_slice, len, tok0);
+    const int npairs = (len + 2 * kBM - 1) / (2 * kBM);
+    if (!CAUSAL) return q < npairs ? 1 : 0;
+    if (q >= (npairs + 1) / 2) return 0;
+    return (npairs - 1 - q != q) ? 2 : 1;
+}
+
+template <bool CAUSAL, int MODE>
 __device__ __forceinline__ Item unit_item(const TcParams& p, int u, int s) {
+    const int per_slice = CAUSAL ? (p.npairs + 1) / 2 : p.npairs;
     Item it;
-    if (!CAUSAL) {
-        it.bh = u / p.npairs;
-        it.pair = u % p.npairs;
-        it.nA = p.nkv;
-        it.nB = p.nkv;
+    if (MODE == 0) {   // [B, H, N, D]: slices of N rows, no head or token bookkeeping
+        it.bh = u / per_slice;
+        const int q = u % per_slice;
+        it.h = 0;
+        it.len = p.n;
+        it.tok0 = 0;
+        it.pair = CAUSAL ? ((s == 0) ? (p.npairs - 1 - q) : q) : q;
+        it.nA = CAUSAL ? min(2 * it.pair + 1, p.nkv) : p.nkv;
+        it.nB = CAUSAL ? min(2 * it.pair + 2, p.nkv) : p.nkv;
         return it;
     }
-    const int half = (p.npairs + 1) / 2;
-    it.bh = u / half;
-    const int q = u % half;
-    it.pair = (s == 0) ? (p.npairs - 1 - q) : q;
-    it.nA = min(2 * it.pair + 1, p.nkv);
-    it.nB = min(2 * it.pair + 2, p.nkv);
+    it.bh = u / per_slice;
+    it.h = it.bh % p.heads;
+    const int q = u % per_slice;
+    slice_geometry<MODE>(p, it.bh, it.len, it.tok0);
+    const int npairs = (it.len + 2 * kBM - 1) / (2 * kBM);
+    const int nkv = (it.len + kBN - 1) / kBN;
+    if (!CAUSAL) {
+        it.pair = q;
+        it.nA = nkv;
+        it.nB = nkv;
+    } else {
+        it.pair = (s == 0) ? (npairs - 1 - q) : q;
+        it.nA = min(2 * it.pair + 1, nkv);
+        it.nB = min(2 * it.pair + 2, nkv);
+    }
     return it;
+}
+
+// TMA coordinates (dims 1 and 2) of row `row` of the item's slice.
+template <int MODE>
+__device__ __forceinline__ void tile_coords(const TcParams& p, const Item& it, int row, int& c1,
+                                            int& c2) {
+    if (MODE == 0) {
+        c1 = row;
+        c2 = it.bh;
+    } else {
+        c1 = it.h;
+        c2 = it.tok0 + row;
+    }
 }
 
 // ----------------------------------------------------------------- bounded waits
@@ -241,7 +304,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint6
 
 // ----------------------------------------------------------------- roles
 // MMA issuer: the whole warp runs this loop (waits are warp-uniform), one lane issues.
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_t sbase) {
     using G = Geo<D>;
     constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false, F16);
@@ -259,9 +322,9 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
     uint32_t kv = 0, q_cnt = 0, p_cnt0 = 0, p_cnt1 = 0;
 
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const int nsub = unit_items<CAUSAL>(p, u);
+        const int nsub = unit_count<CAUSAL, MODE>(p, u);
         for (int sub = 0; sub < nsub; ++sub) {
-            const Item it = unit_item<CAUSAL>(p, u, sub);
+            const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
             if (!wait_warp(c, b_q_full<D>(0), q_cnt & 1u, kRoleMma)) goto out;
             if (!wait_warp(c, b_kv_full<D>(kv), ring_parity<D>(kv), kRoleMma)) goto out;
             ptx::tc_fence_after();
@@ -323,7 +386,7 @@ out:
     __syncwarp();
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, int MODE>
 __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
     using G = Geo<D>;
     const uint32_t sQ[2] = {sbase, sbase + (uint32_t)G::kTileBytes};
@@ -335,18 +398,20 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
     const uint32_t skipped = (p.inject_stall == 1 && blockIdx.x == 0) ? 0u : 0xFFFFFFFFu;
 
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const int nsub = unit_items<CAUSAL>(p, u);
+        const int nsub = unit_count<CAUSAL, MODE>(p, u);
         for (int sub = 0; sub < nsub; ++sub) {
-            const Item it = unit_item<CAUSAL>(p, u, sub);
+            const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
             // Q_A first, then K_0 (so S_A(0) can start), then Q_B, then V_0, K_1, V_1, ...
             auto load_q = [&](int t) -> bool {
                 if (!wait(c, b_q_empty<D>(t), (q_cnt & 1u) ^ 1u, kRoleLoad)) return false;
                 const uint32_t fb = bar_addr(c, b_q_full<D>(t));
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
+                int c1, c2;
+                tile_coords<MODE>(p, it, it.pair * 2 * kBM + t * kBM, c1, c2);
 #pragma unroll
                 for (int pc = 0; pc < G::kPanels; ++pc)
                     ptx::tma_load_3d(sQ[t] + (uint32_t)pc * kPanelBytes, &p.tmap_q, fb, pc * kPanelCols,
-                                     it.pair * 2 * kBM + t * kBM, it.bh);
+                                     c1, c2);
                 ++q_issued[t];
                 return true;
             };
@@ -358,10 +423,12 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                         const uint32_t fb = bar_addr(c, b_kv_full<D>(kv));
                         ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
                         const CUtensorMap* map = (w == 0) ? &p.tmap_k : &p.tmap_v;
+                        int c1, c2;
+                        tile_coords<MODE>(p, it, j * kBN, c1, c2);
 #pragma unroll
                         for (int pc = 0; pc < G::kPanels; ++pc)
                             ptx::tma_load_3d(slot(kv) + (uint32_t)pc * kPanelBytes, map, fb,
-                                             pc * kPanelCols, j * kBN, it.bh);
+                                             pc * kPanelCols, c1, c2);
                     }
                     ++kv;
                     if (j == 0 && w == 0 && !load_q(1)) goto out;
@@ -463,7 +530,7 @@ __device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbas
     return alpha;
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int warp, int lane,
                              uint32_t stage) {
     using G = Geo<D>;
@@ -476,12 +543,14 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
     uint32_t s_cnt = 0, o_cnt = 0;
 
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-        const int nsub = unit_items<CAUSAL>(p, u);
+        const int nsub = unit_count<CAUSAL, MODE>(p, u);
         for (int sub = 0; sub < nsub; ++sub) {
-            const Item it = unit_item<CAUSAL>(p, u, sub);
+            const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
             const int n = t == 0 ? it.nA : it.nB;
             const int row = it.pair * 2 * kBM + t * kBM + lane_base + lane;
-            const int limit = CAUSAL ? min(row + 1, p.n) : p.n;   // visible keys: j < limit
+            // sequence length: the kernel parameter for [B, H, N, D] (no register held)
+            const int len = MODE == 0 ? p.n : it.len;
+            const int limit = CAUSAL ? min(row + 1, len) : len;   // visible keys: j < limit
             float m_run = -INFINITY, l_run = 0.0f;
 
             for (int j = 0; j < n; ++j) {
@@ -523,7 +592,11 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             ptx::tc_fence_after();
             const float inv_l = 1.0f / l_run;
             const int row0 = it.pair * 2 * kBM + t * kBM + lane_base;   // first row of the warp
-            uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)it.bh * (size_t)p.n * D;
+            // row r of the slice: obase + r * ostride (elements)
+            const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
+            uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +
+                              (MODE == 0 ? (size_t)it.bh * (size_t)p.n * D
+                                         : ((size_t)it.tok0 * p.heads + it.h) * D);
 #pragma unroll 1
             for (int pc = 0; pc < D / 64; ++pc) {
 #pragma unroll
@@ -548,18 +621,24 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                     const int ch = lane & 7;             // 16-byte chunk within the 128-byte row
                     const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u +
                                                       (uint32_t)((ch ^ (r & 7)) * 16));
-                    if (row0 + r < p.n)
-                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * D + pc * 64 + ch * 8) = v;
+                    if (row0 + r < (MODE == 0 ? p.n : it.len))
+                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * ostride + pc * 64 + ch * 8) = v;
                 }
                 __syncwarp();
             }
-            if (row < p.n) p.lse[(size_t)it.bh * (size_t)p.n + (size_t)row] = (m_run + log2f(l_run)) * kLn2;
+            if (row < (MODE == 0 ? p.n : it.len)) {
+                // [B, H, N] rows, or [H, total] for packed sequences
+                const size_t lrow = (MODE == 1 && p.cu_seqlens != nullptr)
+                                        ? (size_t)it.h * (size_t)p.total + (size_t)it.tok0 + (size_t)row
+                                        : (size_t)it.bh * (size_t)p.n + (size_t)row;
+                p.lse[lrow] = (m_run + log2f(l_run)) * kLn2;
+            }
             __syncwarp();
         }
     }
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constant__ TcParams p) {
     using G = Geo<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -607,12 +686,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kSoftmaxWarps) {
-        softmax_role<D, CAUSAL, F16>(p, c, tmem, warp, lane,
+        softmax_role<D, CAUSAL, F16, MODE>(p, c, tmem, warp, lane,
                                      sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
     } else if (warp == kMmaWarp) {
-        mma_role<D, CAUSAL, F16>(p, c, tmem, sbase);
+        mma_role<D, CAUSAL, F16, MODE>(p, c, tmem, sbase);
     } else {
-        if (lane == 0) load_role<D, CAUSAL>(p, c, sbase);
+        if (lane == 0) load_role<D, CAUSAL, MODE>(p, c, sbase);
         __syncwarp();
     }
 
@@ -624,30 +703,36 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     }
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(fa_tc_kernel<D, CAUSAL, F16>,
+    return cudaFuncSetAttribute(fa_tc_kernel<D, CAUSAL, F16, MODE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSmemBytes);
 }
 
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t stream) {
-    fa_tc_kernel<D, CAUSAL, F16><<<grid, kThreads, Geo<D>::kSmemBytes, stream>>>(p);
+    fa_tc_kernel<D, CAUSAL, F16, MODE><<<grid, kThreads, Geo<D>::kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <int D>
-cudaError_t dispatch(bool causal, bool f16, bool prepare, const TcParams* p, int grid,
-                     cudaStream_t stream) {
+template <int D, bool CAUSAL, bool F16>
+cudaError_t dispatch_mode(int mode, bool prepare, const TcParams* p, int grid, cudaStream_t stream) {
     if (prepare) {
-        if (causal) return f16 ? prepare_one<D, true, true>() : prepare_one<D, true, false>();
-        return f16 ? prepare_one<D, false, true>() : prepare_one<D, false, false>();
+        cudaError_t e = prepare_one<D, CAUSAL, F16, 0>();
+        return e != cudaSuccess ? e : prepare_one<D, CAUSAL, F16, 1>();
     }
+    return mode == 0 ? launch_one<D, CAUSAL, F16, 0>(*p, grid, stream)
+                     : launch_one<D, CAUSAL, F16, 1>(*p, grid, stream);
+}
+
+template <int D>
+cudaError_t dispatch(bool causal, bool f16, int mode, bool prepare, const TcParams* p, int grid,
+                     cudaStream_t stream) {
     if (causal)
-        return f16 ? launch_one<D, true, true>(*p, grid, stream)
-                   : launch_one<D, true, false>(*p, grid, stream);
-    return f16 ? launch_one<D, false, true>(*p, grid, stream)
-               : launch_one<D, false, false>(*p, grid, stream);
+        return f16 ? dispatch_mode<D, true, true>(mode, prepare, p, grid, stream)
+                   : dispatch_mode<D, true, false>(mode, prepare, p, grid, stream);
+    return f16 ? dispatch_mode<D, false, true>(mode, prepare, p, grid, stream)
+               : dispatch_mode<D, false, false>(mode, prepare, p, grid, stream);
 }
 
 }  // namespace
@@ -661,14 +746,14 @@ int tc_units(int bh, int n, bool causal) {
 int tc_smem_bytes(int D) { return D == 64 ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes; }
 
 cudaError_t tc_prepare(int D, bool causal, bool f16) {
-    return D == 64 ? dispatch<64>(causal, f16, true, nullptr, 0, nullptr)
-                   : dispatch<128>(causal, f16, true, nullptr, 0, nullptr);
+    return D == 64 ? dispatch<64>(causal, f16, 0, true, nullptr, 0, nullptr)
+                   : dispatch<128>(causal, f16, 0, true, nullptr, 0, nullptr);
 }
 
 cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
                       cudaStream_t stream) {
-    return D == 64 ? dispatch<64>(causal, f16, false, &p, grid, stream)
-                   : dispatch<128>(causal, f16, false, &p, grid, stream);
+    return D == 64 ? dispatch<64>(causal, f16, p.layout, false, &p, grid, stream)
+                   : dispatch<128>(causal, f16, p.layout, false, &p, grid, stream);
 }
 
 cudaError_t tc_status_read_reset(uint32_t out[4]) {

@@ -68,6 +68,41 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int64_t B, int64_t H, int64_t N, int64_t D,
            float scale, int causal, int dtype, void* stream);
 
+/*
+ * fa_fwd_bnhd -- the same forward pass over token-major tensors.
+ *
+ *   q, k, v, o : device pointers, [B, N, H, D] contiguous ("batch, sequence, head, dim"):
+ *                row i of head h of batch b starts at element ((b*N + i)*H + h)*D.  Reading
+ *                and writing this layout directly saves the [B,N,H,D] <-> [B,H,N,D] copies
+ *                around the attention ("pwwt.cn: FlashAttention 与内存墙" §5.2).
+ *   lse        : device pointer, [B, H, N] contiguous fp32.
+ *   Everything else as fa_fwd (same limits, ownership, errors, asynchrony).
+ */
+int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse,
+                int64_t B, int64_t N, int64_t H, int64_t D,
+                float scale, int causal, int dtype, void* stream);
+
+/*
+ * fa_fwd_varlen -- the forward pass over packed sequences of different lengths, without
+ * padding ("08 · FlashAttention" §四: packing with cu_seqlens instead of a padding mask).
+ *
+ *   q, k, v, o : device pointers, [total, H, D] contiguous: the tokens of all sequences one
+ *                after another; sequence b owns tokens cu_seqlens[b] .. cu_seqlens[b+1]-1.
+ *   lse        : device pointer, [H, total] contiguous fp32 (entry h*total + token).
+ *   cu_seqlens : device pointer, batch + 1 int32 values: 0 = cu[0] <= cu[1] <= ... <=
+ *                cu[batch] = total, and cu[b+1] - cu[b] <= max_seqlen.  Each sequence
+ *                attends only to its own tokens (causal: token j <= token i within it).
+ *                Empty sequences are allowed.  The kernel clamps offsets to [0, total] and
+ *                lengths to max_seqlen, so malformed offsets give wrong results but never an
+ *                access outside the tensors; they are not otherwise checked (checking would
+ *                need a device-to-host copy).
+ *   batch, max_seqlen, total, H : >= 1; batch*H < 2^31; total < 2^31.
+ *   Everything else as fa_fwd.
+ */
+int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                  const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total,
+                  int64_t H, int64_t D, float scale, int causal, int dtype, void* stream);
+
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(int status);
 
@@ -97,7 +132,7 @@ int fa_check_device_status(void* stream, uint32_t* detail);
 int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall);
 
 /* Library ABI version (major * 100 + minor). */
-int fa_version(void);
+int fa_version(void);   /* 110: adds fa_fwd_bnhd and fa_fwd_varlen */
 
 #ifdef __cplusplus
 }

@@ -75,6 +75,33 @@ def test_bad_arguments_rejected_before_cuda(lib, kw, expect):
     assert call(lib, **kw) == expect
 
 
+def test_varlen_and_bnhd_argument_checks(lib):
+    T, H, D = 1000, 4, 128
+    args = dict(q=BASE, k=BASE + SZ, v=BASE + 2 * SZ, o=BASE + 3 * SZ, lse=BASE + 4 * SZ)
+    cu = BASE + 5 * SZ
+
+    def varlen(cu=cu, batch=3, maxlen=512, total=T, H=H, D=D, dtype=1, **kw):
+        a = dict(args, **kw)
+        return lib.fa_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], cu, batch, maxlen,
+                                 total, H, D, 0.1, 0, dtype, None)
+    assert varlen(cu=0) == INVALID
+    assert varlen(cu=cu + 2) == MISALIGNED
+    assert varlen(batch=0) == INVALID
+    assert varlen(maxlen=0) == INVALID
+    assert varlen(total=0) == INVALID
+    assert varlen(H=0) == INVALID
+    assert varlen(D=80) == UNSUPPORTED
+    assert varlen(dtype=9) == INVALID
+    assert varlen(o=BASE + SZ) == INVALID            # o aliases k
+    assert varlen(q=BASE + 4) == MISALIGNED
+    assert lib.fa_fwd_bnhd(0, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
+                           2, 128, 4, 128, 0.1, 0, 1, None) == INVALID
+    assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
+                           2, 128, 4, 96, 0.1, 0, 1, None) == UNSUPPORTED
+    assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
+                           2, 0, 4, 128, 0.1, 0, 1, None) == INVALID
+
+
 def test_watchdog_control_validation(lib):
     assert lib.fa_set_watchdog(0, 5) == INVALID
     assert lib.fa_set_watchdog(0, 0) == OK
