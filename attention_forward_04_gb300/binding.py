@@ -31,6 +31,11 @@ SIGNATURES = {
     "fa_fwd_varlen": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                  _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
                                  _c.c_int64, _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_bwd_workspace_bytes": (_c.c_int64, [_c.c_int64, _c.c_int64, _c.c_int64]),
+    "fa_bwd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                          _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                          _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
+                          _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_last_cuda_error": (_c.c_char_p, []),
     "fa_check_device_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
@@ -180,6 +185,45 @@ def fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, out=No
                                                 H, D, float(scale), int(causal), _dtype_code(q),
                                                 _stream_handle(q, stream))))
     return out, lse
+
+
+def bwd_workspace_bytes(B, H, N) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(int(B), int(H), int(N)))
+
+
+def bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """Attention backward through the C ABI (fa_bwd).
+
+    q, k, v, o, dout: CUDA tensors [B, H, N, D], contiguous, bf16 or fp16; o and lse are the
+    forward's outputs.  Returns (dq, dk, dv) in the input dtype.  ``workspace`` (a uint8
+    CUDA tensor of at least bwd_workspace_bytes(B, H, N) bytes) is allocated when omitted.
+    """
+    import torch
+    _common(q, k, v, 4)
+    for t in (o, dout):
+        if not t.is_cuda or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("o and dout must be contiguous CUDA tensors shaped and typed like q")
+    B, H, N, D = q.shape
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, N)
+    if need < 0:
+        raise FaError(1, "B, H or N out of range")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         dout.data_ptr(), lse.data_ptr(), dq.data_ptr(),
+                                         dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                                         workspace.numel() * workspace.element_size(), B, H, N,
+                                         D, float(scale), int(causal), _dtype_code(q),
+                                         _stream_handle(q, stream))))
+    return dq, dk, dv
 
 
 def check_device_status(stream=None):

@@ -31,6 +31,8 @@ struct DeviceInfo {
     int major = 0, minor = 0;
     std::once_flag prepared[2][2][2];  // [D==128][causal][f16]
     cudaError_t prepare_err[2][2][2] = {};
+    std::once_flag bwd_prepared[2][2][2];
+    cudaError_t bwd_prepare_err[2][2][2] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -93,7 +95,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
-int fa_version(void) { return 110; }
+int fa_version(void) { return 120; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -119,9 +121,11 @@ int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall) {
 int fa_check_device_status(void* stream, uint32_t* detail) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-    uint32_t w[4] = {0, 0, 0, 0};
+    uint32_t w[4] = {0, 0, 0, 0}, wb[4] = {0, 0, 0, 0};
     e = fa::tc_status_read_reset(w);
+    if (e == cudaSuccess) e = fa::bwd_status_read_reset(wb);
     if (e != cudaSuccess) return fail_cuda(e, "status word");
+    if (!(w[0] & 1u) && (wb[0] & 1u)) std::memcpy(w, wb, sizeof(w));   // report the backward's
     if (detail) std::memcpy(detail, w, sizeof(w));
     return (w[0] & 1u) ? FA_ERR_TIMEOUT : FA_OK;
 }
@@ -257,6 +261,100 @@ int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse
                 int64_t N, int64_t H, int64_t D, float scale, int causal, int dtype, void* stream) {
     const Request r{q, k, v, o, lse, B, H, N, D, B * N, 1, nullptr, scale, causal, dtype, stream};
     return forward(r);
+}
+
+int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+    if (B < 1 || H < 1 || N < 1 || B > 0x7FFFFFFFLL || H > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL ||
+        B * H > 0x7FFFFFFFLL)
+        return -1;
+    const int64_t bytes = B * H * N * (int64_t)sizeof(float);   // delta rows
+    return (bytes + 255) / 256 * 256;
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace, int64_t workspace_bytes,
+           int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal, int dtype,
+           void* stream) {
+    // ---- argument checks: no CUDA call before these pass
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+        return FA_ERR_INVALID_ARG;
+    const int64_t need = fa_bwd_workspace_bytes(B, H, N);
+    if (need < 0) return FA_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
+    if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (dtype == FA_FP32) return FA_ERR_UNSUPPORTED;   // backward: 16-bit storage only
+    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    const int64_t BH = B * H;
+    const size_t tbytes = (size_t)BH * (size_t)N * (size_t)D * 2;
+    const size_t lbytes = (size_t)BH * (size_t)N * sizeof(float);
+    if (tbytes / 2 / (size_t)D / (size_t)N != (size_t)BH) return FA_ERR_INVALID_ARG;
+    const void* ins[7] = {q, k, v, o, dout, lse, workspace};
+    const size_t in_bytes[7] = {tbytes, tbytes, tbytes, tbytes, tbytes, lbytes, (size_t)need};
+    void* outs[3] = {dq, dk, dv};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 7; ++b)
+            if (overlaps(outs[a], tbytes, ins[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(outs[a], tbytes, outs[b], tbytes)) return FA_ERR_INVALID_ARG;
+    }
+    if (overlaps(workspace, (size_t)need, q, tbytes) || overlaps(workspace, (size_t)need, k, tbytes) ||
+        overlaps(workspace, (size_t)need, v, tbytes) || overlaps(workspace, (size_t)need, o, tbytes) ||
+        overlaps(workspace, (size_t)need, dout, tbytes) || overlaps(workspace, (size_t)need, lse, lbytes))
+        return FA_ERR_INVALID_ARG;
+    for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(dq),
+                            static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_MISALIGNED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return FA_ERR_MISALIGNED;
+
+    // ---- device
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    DeviceInfo& di = g_dev[dev];
+    std::call_once(di.once, [&] {
+        di.err = cudaDeviceGetAttribute(&di.sm_count, cudaDevAttrMultiProcessorCount, dev);
+        if (di.err == cudaSuccess)
+            di.err = cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (di.err == cudaSuccess)
+            di.err = cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    });
+    if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
+    if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;
+    const bool f16 = dtype == FA_FP16;
+    const int di128 = D == 128, dic = causal != 0, dif = f16;
+    std::call_once(di.bwd_prepared[di128][dic][dif],
+                   [&] { di.bwd_prepare_err[di128][dic][dif] = fa::bwd_prepare((int)D, dic, f16); });
+    if (di.bwd_prepare_err[di128][dic][dif] != cudaSuccess)
+        return fail_cuda(di.bwd_prepare_err[di128][dic][dif], "cudaFuncSetAttribute (backward)");
+    PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
+    if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
+
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!encode_map(&p.tmap_q, q, 0, BH, N, H, B * N, D, f16, fn) ||
+        !encode_map(&p.tmap_k, k, 0, BH, N, H, B * N, D, f16, fn) ||
+        !encode_map(&p.tmap_v, v, 0, BH, N, H, B * N, D, f16, fn) ||
+        !encode_map(&p.tmap_do, dout, 0, BH, N, H, B * N, D, f16, fn))
+        return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    p.lse = lse;
+    p.delta = static_cast<const float*>(workspace);
+    p.dq = dq;
+    p.dk = dk;
+    p.dv = dv;
+    p.n = (int)N;
+    p.ntiles = (int)((N + 127) / 128);
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit = g_wait_limit.load();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = fa::bwd_delta_launch((int)D, f16, o, dout, static_cast<float*>(workspace), (long long)BH * N, st);
+    if (e != cudaSuccess) return fail_cuda(e, "backward delta launch");
+    e = fa::bwd_launch((int)D, dic, f16, p, (int)BH, st);
+    return e == cudaSuccess ? FA_OK : fail_cuda(e, "backward kernel launch");
 }
 
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -29,6 +29,35 @@ struct TcParams {
     int inject_stall;    // failure-detection test hook (see fa_set_watchdog)
 };
 
+// Launch parameters of the backward kernels ([B*H, N, D] bf16/fp16, D = 64 or 128).
+struct BwdParams {
+    CUtensorMap tmap_q;   // 3-D maps over [B*H, N, D] exactly as the forward's
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    CUtensorMap tmap_do;
+    const float* lse;     // [B*H, N] natural-log LSE of the forward
+    const float* delta;   // [B*H, N] rowsum(dO * O), written by the first backward kernel
+    void* dq;             // [B*H, N, D] outputs, input element type
+    void* dk;
+    void* dv;
+    int n;                // sequence length N
+    int ntiles;           // ceil(N / 128)
+    float scale;          // softmax scale
+    float scale_log2;     // scale * log2(e)
+    unsigned long long wait_limit;
+};
+
+// delta[r] = sum_d dO[r, d] * O[r, d] for rows r < rows (fp32 from 16-bit inputs).
+cudaError_t bwd_delta_launch(int D, bool f16, const void* o, const void* dout, float* delta,
+                             long long rows, cudaStream_t stream);
+// Raise the dynamic shared-memory limit of the backward tensor-core kernels (once).
+cudaError_t bwd_prepare(int D, bool causal, bool f16);
+// dQ (one CTA per 128-query tile) and dK, dV (one CTA per 128-key tile), B*H*ntiles CTAs each.
+cudaError_t bwd_launch(int D, bool causal, bool f16, const BwdParams& p, int bh,
+                       cudaStream_t stream);
+// Status word of the backward kernels (same meaning as the forward's).
+cudaError_t bwd_status_read_reset(uint32_t out[4]);
+
 // Work units of the persistent schedule for a given shape.
 int tc_units(int bh, int n, bool causal);
 

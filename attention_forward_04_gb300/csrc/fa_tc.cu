@@ -43,9 +43,12 @@
 
 #include "fa_internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace fa {
 namespace {
+
+using namespace tc;
 
 constexpr int kBM = 128;            // query rows per tile = TMEM lanes
 constexpr int kBN = 128;            // keys per K/V tile
@@ -53,17 +56,12 @@ constexpr int kSoftmaxWarps = 8;    // warps 0-3: tile A, warps 4-7: tile B
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kThreads = 320;
-constexpr int kPanelCols = 64;      // 16-bit elements per 128-byte swizzled row
-constexpr int kPanelBytes = kBM * 128;
 constexpr uint32_t kTmemCols = 512;
 // The running reference is raised only when a tile max exceeds it by more than this many
 // log2 units, so stored P values stay below 2^kRescaleLog2: 16 for bf16 P (exponent range
 // of fp32), 8 for fp16 P (largest fp16 is 65504).
 template <bool F16> struct Lazy { static constexpr float kRescaleLog2 = F16 ? 8.0f : 16.0f; };
-constexpr float kLn2 = 0.6931471805599453f;
 
-// Roles recorded in the status word when a wait gives up.
-constexpr uint32_t kRoleSoftmax = 1, kRoleMma = 2, kRoleLoad = 3;
 
 // Device status word: [0] flags (1 = a wait ran out), [1] role, [2] CTA, [3] wait id.
 __device__ unsigned int g_status[4];
@@ -104,24 +102,6 @@ template <int D> __device__ __forceinline__ int b_drain() { return 10 + 2 * Geo<
 // Ring position i -> phase parity of its slot.
 template <int D> __device__ __forceinline__ uint32_t ring_parity(uint32_t i) {
     return (i / Geo<D>::kSlots) & 1u;
-}
-
-// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, A and B both bf16
-// (or both fp16), A K-major, B K-major or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool b_mn_major, bool f16) {
-    return (1u << 4)                                   // D format: f32
-           | ((f16 ? 0u : 1u) << 7)                    // A format: f16 = 0, bf16 = 1
-           | ((f16 ? 0u : 1u) << 10)                   // B format
-           | ((b_mn_major ? 1u : 0u) << 16)            // B major-ness
-           | ((uint32_t)(N >> 3) << 17)                // N / 8
-           | ((uint32_t)(M >> 4) << 24);               // M / 16
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (the layout TMA writes with
-// CU_TENSOR_MAP_SWIZZLE_128B; tiles start on 1024-byte boundaries).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // ----------------------------------------------------------------- work schedule
@@ -223,57 +203,6 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, const Item& it, i
         c1 = it.h;
         c2 = it.tok0 + row;
     }
-}
-
-// ----------------------------------------------------------------- bounded waits
-struct Ctl {
-    uint32_t bars;                 // smem address of barrier 0
-    volatile int* abort;           // CTA-wide abort flag (shared memory)
-    unsigned long long limit;      // cycles
-};
-
-__device__ __forceinline__ uint32_t bar_addr(const Ctl& c, int i) { return c.bars + 8u * (uint32_t)i; }
-
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int* abort,
-                                       unsigned long long limit, uint32_t role, uint32_t id) {
-    const long long t0 = clock64();
-    while (true) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if ((unsigned long long)(clock64() - t0) > limit) {
-            *abort = 1;
-            if (atomicCAS(&g_status[0], 0u, 1u) == 0u) {
-                g_status[1] = role;
-                g_status[2] = blockIdx.x;
-                g_status[3] = id;
-            }
-            __threadfence();
-            return false;
-        }
-    }
-}
-
-// Wait for the phase with `parity` of barrier `i`; false if the CTA is aborting.
-__device__ __forceinline__ bool wait(const Ctl& c, int i, uint32_t parity, uint32_t role) {
-    const uint32_t bar = bar_addr(c, i);
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    return wait_slow(bar, parity, c.abort, c.limit, role, (uint32_t)i);
-}
-
-// Warp-wide wait: every lane waits, and the outcome is made uniform across the warp so
-// that no lane reaches a .sync.aligned tcgen05 instruction without the others.
-__device__ __forceinline__ bool wait_warp(const Ctl& c, int i, uint32_t parity, uint32_t role) {
-    const bool ok = wait(c, i, parity, role);
-    return __all_sync(0xFFFFFFFFu, ok);
-}
-
-// Teardown wait: bounded by time only (ignores the abort flag).
-__device__ __noinline__ bool wait_drain(uint32_t bar, uint32_t parity, unsigned long long limit) {
-    const long long t0 = clock64();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if ((unsigned long long)(clock64() - t0) > limit) return false;
-    }
-    return true;
 }
 
 // ----------------------------------------------------------------- MMA issue
@@ -444,19 +373,6 @@ out:
         if (i != skipped) wait_drain(bar_addr(c, b_kv_full<D>(i)), ring_parity<D>(i), c.limit);
     for (int t = 0; t < 2; ++t)
         if (q_issued[t] > 0) wait_drain(bar_addr(c, b_q_full<D>(t)), (q_issued[t] - 1u) & 1u, c.limit);
-}
-
-__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
-
-template <bool F16>
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
-    if constexpr (F16) {
-        __half2 h = __floats2half2_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    } else {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
 }
 
 // Row maximum of the raw scores of one 128-key tile; invisible keys (kbase + c >= limit)
@@ -654,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     c.bars = sbase + (uint32_t)G::kBarOff;
     c.abort = abort_flag;
     c.limit = p.wait_limit;
+    c.status = g_status;
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {

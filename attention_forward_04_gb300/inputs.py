@@ -8,7 +8,8 @@ three tensors are drawn with ``torch.Generator().manual_seed(s + t)`` for
 t = 0 (Q), 1 (K), 2 (V) as ``torch.randn(..., dtype=float32)`` on the CPU,
 multiplied by the workload's Q/K multiplier (1, or 2 for the long-sequence
 workload; multiplying by 2 is exact in binary floating point), then cast to the
-workload's storage dtype.  Shapes follow the pages' workloads: [B, H, N, D]
+workload's storage dtype.  The backward's upstream gradient dO is drawn the same way
+with t = 3 (no multiplier).  Shapes follow the pages' workloads: [B, H, N, D]
 with N = 4096 and d = 128 (the shape the pages analyse), d = 64, and N up to
 16k.  There is no dataset on the pages; everything here is synthetic.
 """
@@ -84,3 +85,15 @@ def make_shape(B, H, N, D, dtype="bf16", seed=7, qk_mult=1.0):
     """Seeded Q, K, V for an arbitrary shape (edge cases in the tests)."""
     w = Workload("adhoc", B, H, N, D, dtype, False, seed, qk_mult)
     return make_qkv(w)
+
+
+def make_dout(w: Workload, seed_offset: int = 0):
+    """dO = dL/dO for the backward: CPU tensor [B, H, N, D] in the workload's dtype."""
+    g = torch.Generator().manual_seed(w.seed + seed_offset + 3)
+    x = torch.randn((w.B, w.H, w.N, w.D), generator=g, dtype=torch.float32)
+    return x.to(TORCH_DTYPES[w.dtype]).contiguous()
+
+
+def make_shape_dout(B, H, N, D, dtype="bf16", seed=7):
+    """Seeded dO for an arbitrary shape (same recipe as make_dout)."""
+    return make_dout(Workload("adhoc", B, H, N, D, dtype, False, seed))

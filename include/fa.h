@@ -104,6 +104,47 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   int64_t H, int64_t D, float scale, int causal, int dtype, void* stream);
 
 /* Human-readable name of a status code (static string; never NULL). */
+/*
+ * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for a [B, H, N, D]
+ * problem (one fp32 value per query row, rounded up to 256 bytes); -1 if B, H or N is out
+ * of range.  Pure host arithmetic.
+ */
+int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
+
+/*
+ * fa_bwd -- attention backward pass, asynchronous on `stream`.
+ *
+ * Given dO = dL/dO for the forward above, writes the gradients of L:
+ *     P = exp(scale * Q K^T - LSE) (causal: P_ij = 0 for j > i),
+ *     delta_i = sum_d dO_id O_id,  dS = P * (dO V^T - delta),
+ *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+ * P is rebuilt from the forward's LSE instead of being stored ("08 · FlashAttention" §三
+ * 反向传播; "第 13 课：FlashAttention" §4B); the formulas are the chain rule through the
+ * softmax of "KingOfEgg: Flash Attention v1" §1.1.
+ *
+ *   q, k, v, o, dout : device pointers, [B, H, N, D] contiguous, element type `dtype`;
+ *                      o and lse are the outputs of fa_fwd on the same q, k, v, scale, causal.
+ *   lse              : device pointer, [B, H, N] fp32 (fa_fwd's lse).
+ *   dq, dk, dv       : device pointers, [B, H, N, D] contiguous, element type `dtype`;
+ *                      written fully (no accumulation into existing contents).
+ *   workspace        : device pointer of at least fa_bwd_workspace_bytes(B, H, N) bytes,
+ *                      16-byte aligned; scratch for delta, needs no initialisation, and
+ *                      must not be shared by two calls in flight at once.
+ *   B, H, N, scale, causal, stream : as for fa_fwd.
+ *   D                : 64 or 128.
+ *   dtype            : FA_BF16 or FA_FP16 (FA_FP32 returns FA_ERR_UNSUPPORTED).
+ *
+ * Arithmetic: products on the tensor cores from 16-bit operands (P and dS are rounded to
+ * `dtype` before their products, like P in the forward), fp32 accumulation, results
+ * rounded to `dtype`.  No atomics: results do not depend on scheduling.
+ * Errors: as fa_fwd; additionally FA_ERR_INVALID_ARG when the workspace is too small or any
+ * output overlaps an input, the workspace or another output.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace,
+           int64_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, float scale,
+           int causal, int dtype, void* stream);
+
 const char* fa_status_string(int status);
 
 /* Text of the last CUDA error seen by this library in the calling thread, or "". */
@@ -132,7 +173,7 @@ int fa_check_device_status(void* stream, uint32_t* detail);
 int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall);
 
 /* Library ABI version (major * 100 + minor). */
-int fa_version(void);   /* 110: adds fa_fwd_bnhd and fa_fwd_varlen */
+int fa_version(void);   /* 120: adds fa_bwd and fa_bwd_workspace_bytes */
 
 #ifdef __cplusplus
 }

@@ -117,3 +117,39 @@ def test_binding_refuses_cpu_tensors():
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(FileNotFoundError):
         binding.load_library(str(tmp_path / "nope.so"))
+
+
+def bwd_call(lib, ws_bytes=None, B=1, H=2, N=300, D=128, scale=0.1, causal=0, dtype=1, **ptr):
+    names = ["q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws"]
+    addr = {n: BASE + i * SZ for i, n in enumerate(names)}
+    addr.update(ptr)
+    if ws_bytes is None:
+        ws_bytes = lib.fa_bwd_workspace_bytes(B, H, N)
+    return lib.fa_bwd(addr["q"], addr["k"], addr["v"], addr["o"], addr["do"], addr["lse"],
+                      addr["dq"], addr["dk"], addr["dv"], addr["ws"], ws_bytes, B, H, N, D, scale,
+                      causal, dtype, None)
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.fa_bwd_workspace_bytes(2, 3, 100) == 2 * 3 * 100 * 4 // 256 * 256 + 256
+    assert lib.fa_bwd_workspace_bytes(1, 1, 64) == 256
+    assert lib.fa_bwd_workspace_bytes(1, 1, 128) == 512
+    assert lib.fa_bwd_workspace_bytes(0, 1, 1) == -1
+    assert lib.fa_bwd_workspace_bytes(1, 1, -1) == -1
+    assert lib.fa_bwd_workspace_bytes(1 << 16, 1 << 16, 1) == -1
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=0), INVALID), (dict(do=0), INVALID), (dict(lse=0), INVALID), (dict(dv=0), INVALID),
+    (dict(ws=0), INVALID), (dict(ws_bytes=100), INVALID), (dict(N=0), INVALID),
+    (dict(causal=3), INVALID), (dict(scale=float("nan")), INVALID), (dict(dtype=9), INVALID),
+    (dict(dtype=0), UNSUPPORTED), (dict(D=96), UNSUPPORTED),
+    (dict(dq=BASE), INVALID),                      # dq aliases q
+    (dict(dk=BASE + 6 * SZ + 128), INVALID),       # dk overlaps dq
+    (dict(dv=BASE + 9 * SZ), INVALID),             # dv aliases the workspace
+    (dict(ws=BASE + 4 * SZ + 512), INVALID),       # workspace inside dout
+    (dict(do=BASE + 4 * SZ + 8), MISALIGNED), (dict(ws=BASE + 9 * SZ + 4), MISALIGNED),
+    (dict(lse=BASE + 5 * SZ + 2), MISALIGNED),
+])
+def test_bwd_bad_arguments_rejected_before_cuda(lib, kw, expect):
+    assert bwd_call(lib, **kw) == expect
