@@ -247,6 +247,230 @@ def config_of(w, gpus):
                   % (3 * w.B * w.H * w.N * w.D * (4 if w.dtype == "fp32" else 2) / 2**20)}
 
 
+# ------------------------------------------------------------------ backward
+BWD_METRIC = "attention bwd TFLOPS (10*B*H*N^2*D/t)"
+
+
+def bwd_flops(w) -> float:
+    """Algorithmic backward FLOPs: five N x N x D products per slice (S, dP, dV, dQ, dK),
+    2*N^2*D each, halved for the causal mask.  The kernels recompute S and dP once more
+    (seven products); that extra work is not counted."""
+    return 2.5 * w.flops
+
+
+def time_oracle_bwd(w, budget_s: float, host):
+    """The fp64 backward oracle, as it stands, on whole (b, h) slices within the budget."""
+    from oracle.backward import attention_bwd
+    q, k, v, do = (t.reshape(1, w.B * w.H, w.N, w.D) for t in host)
+    args = [t[:, :1].double().numpy() for t in (q, k, v, do)]
+    t0 = time.perf_counter()
+    attention_bwd(*args, w.scale, w.causal)
+    per_slice = time.perf_counter() - t0
+    ns = int(max(1, min(w.B * w.H, budget_s // max(per_slice, 1e-9))))
+    args = [t[:, :ns].double().numpy() for t in (q, k, v, do)]
+    t0 = time.perf_counter()
+    attention_bwd(*args, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    return bwd_flops(w) * ns / (w.B * w.H) / dt / 1e12, dt, ns
+
+
+def run_reference_bwd(args, w):
+    """The backward oracle timed as the reference arm: whole slices, bounded per step."""
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    from oracle.backward import attention_bwd
+    from attention_forward_04_gb300.inputs import make_dout, make_qkv
+    one = w.with_(B=1, H=1)
+    args64 = [t.double().numpy() for t in (*make_qkv(one), make_dout(one))]
+    elapsed = 0.0
+    steps = 0
+    for step in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        attention_bwd(*args64, w.scale, w.causal)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            elapsed += dt
+            steps += 1
+        if elapsed > 120.0:
+            break
+    value = bwd_flops(w) / (w.B * w.H) * steps / elapsed / 1e12
+    sample = "one whole (b, h) slice per step (of %d), fp64 numpy backward oracle" % (w.B * w.H)
+    line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": elapsed / steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": dict(config_of(w, args.gpus), op="bwd"),
+            "cpu_baseline": {"value": value, "unit": "TFLOPS",
+                             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_bwd(args, w):
+    """Backward pass: a step is one fa_bwd call (delta, dQ and dK/dV kernels) over resident
+    Q, K, V, O, LSE, dO; the forward that produces O and LSE runs before timing."""
+    rank, local_rank, world = dist_env()
+    import torch
+    import torch.distributed as dist
+    from attention_forward_04_gb300 import binding, build
+    from attention_forward_04_gb300.inputs import TORCH_DTYPES, make_dout, make_qkv
+
+    if w.dtype == "fp32":
+        raise SystemExit("the backward serves bf16 and fp16 storage only")
+    if rank == 0:
+        build.build()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        dist.barrier()
+    else:
+        torch.cuda.set_device(0)
+    lib = binding.load_library()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    code = {"bf16": binding.FA_BF16, "fp16": binding.FA_FP16}[w.dtype]
+    B, H, N, D = w.B, w.H, w.N, w.D
+    sets = []
+    for s in range(2):
+        q, k, v = (t.to(dev) for t in make_qkv(w, seed_offset=100 * s + 10 * rank))
+        do = make_dout(w, seed_offset=100 * s + 10 * rank).to(dev)
+        o, lse = binding.fwd(q, k, v, scale=w.scale, causal=w.causal)
+        sets.append((q, k, v, o, lse, do))
+    grads = [torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype], device=dev) for _ in range(3)]
+    wsb = binding.bwd_workspace_bytes(B, H, N)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+    def step(i):
+        q, k, v, o, lse, do = sets[i & 1]
+        st = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                        lse.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(),
+                        grads[2].data_ptr(), ws.data_ptr(), wsb, B, H, N, D, w.scale,
+                        int(w.causal), code, sh)
+        if st != 0:
+            raise binding.FaError(st)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    st, detail = binding.check_device_status()
+    if st != 0:
+        raise RuntimeError("kernel watchdog after warm-up: %d %s" % (st, detail))
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.monotonic()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.monotonic()
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.15)
+    sampler.stop()
+    ms_local = ev0.elapsed_time(ev1)
+    st, detail = binding.check_device_status()
+    if st != 0:
+        raise RuntimeError("kernel watchdog in timed region: %d %s" % (st, detail))
+    flops_step = bwd_flops(w)
+    reduce_max = torch_all_reduce_max(dev) if world > 1 else None
+    ms, per_s = aggregate_over_ranks(ms_local, flops_step, args.steps, world, reduce_max)
+    per_call_ms = ms_local / args.steps
+
+    # ---- end to end: pinned host Q, K, V, O, LSE, dO -> device -> fa_bwd -> host dQ, dK, dV
+    host = [t.cpu().pin_memory() for t in sets[0]]
+    hgrads = [torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype]).pin_memory()
+              for _ in range(3)]
+    dbuf = [torch.empty_like(t, device=dev) for t in host]
+
+    def e2e_step():
+        for d_, h_ in zip(dbuf, host):
+            d_.copy_(h_, non_blocking=True)
+        q, k, v, o, lse, do = dbuf
+        binding.bwd(q, k, v, o, lse, do, scale=w.scale, causal=w.causal, dq=grads[0],
+                    dk=grads[1], dv=grads[2], workspace=ws, stream=stream)
+        for h_, d_ in zip(hgrads, grads):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms, e2e_per_s = aggregate_over_ranks(e0.elapsed_time(e1), flops_step, args.e2e_steps,
+                                             world, reduce_max)
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in hgrads)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops_step / (per_call_ms / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None,
+            "kernel": "whole fa_bwd call (delta, dQ and dK/dV kernels); per-kernel shares "
+                      "in the ncu launch list",
+            "peak_source": "%s bf16 dense burst" % peak_src,
+            "executed_tflops": 3.5 * w.flops / (per_call_ms / 1e3) / 1e12}
+    cpu = None
+    if args.cpu_budget > 0:
+        try:
+            tfl, secs, ns = time_oracle_bwd(w, args.cpu_budget, [t.cpu() for t in
+                                                                 (sets[0][0], sets[0][1],
+                                                                  sets[0][2], sets[0][5])])
+            cpu = {"value": tfl, "unit": "TFLOPS", "cores": len(os.sched_getaffinity(0)),
+                   "kind": "oracle",
+                   "sample": "%d of %d (b,h) slices of %s, whole slices, fp64 numpy backward "
+                             "oracle, %.1f s (cores: numpy's BLAS threads)" % (ns, B * H, w.name,
+                                                                               secs)}
+        except Exception as ex:
+            cpu = {"value": None, "unit": "TFLOPS", "cores": None, "kind": "oracle",
+                   "sample": "failed: %s" % ex}
+    line = {
+        "metric": BWD_METRIC, "value": per_s / 1e12, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded torch.randn, cast to %s)" % w.dtype,
+        "config": dict(config_of(w, world), op="bwd",
+                       l2="two alternating input sets (Q, K, V, O, dO, LSE) of %.0f MiB each "
+                          "(> 129 MB L2); no flush" % ((5 * D * 2 + 4) * B * H * N / 2**20)),
+        "e2e": {"value": e2e_per_s / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "ms_per_step": e2e_ms / args.e2e_steps},
+        "gpu_launches": 3 * args.steps,
+        "roofline": roof, "cpu_baseline": cpu,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 # ------------------------------------------------------------------ main GPU leg
 def main():
     ap = argparse.ArgumentParser()
@@ -258,11 +482,17 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle timing (0 skips the CPU leg)")
+    ap.add_argument("--op", default="fwd", choices=["fwd", "bwd"],
+                    help="fwd: the forward pass (default); bwd: the backward pass (fa_bwd)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     from attention_forward_04_gb300.inputs import HEADLINE, WORKLOADS
     w = WORKLOADS[args.workload or HEADLINE]
+    if args.op == "bwd":
+        if args.impl == "reference":
+            return run_reference_bwd(args, w)
+        return run_bwd(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
 
