@@ -36,6 +36,10 @@ SIGNATURES = {
                           _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                           _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
                           _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_bwd_noalloc": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                  _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                  _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
+                                  _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_last_cuda_error": (_c.c_char_p, []),
     "fa_check_device_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
@@ -223,6 +227,21 @@ def bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=No
                                          workspace.numel() * workspace.element_size(), B, H, N,
                                          D, float(scale), int(causal), _dtype_code(q),
                                          _stream_handle(q, stream))))
+    return dq, dk, dv
+
+
+def bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, stream=None):
+    """fa_bwd_noalloc: the backward with library-owned scratch.  The caller provides the
+    gradient buffers dq, dk, dv (same shape and dtype as q); nothing is allocated."""
+    import torch
+    _common(q, k, v, 4)
+    B, H, N, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_bwd_noalloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
+            float(scale), int(causal), _dtype_code(q), _stream_handle(q, stream))))
     return dq, dk, dv
 
 

@@ -145,6 +145,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int64_t workspace_bytes, int64_t B, int64_t H, int64_t N, int64_t D, float scale,
            int causal, int dtype, void* stream);
 
+/*
+ * fa_bwd_noalloc -- fa_bwd with its scratch taken from a fixed array inside the library
+ * instead of from the caller.  The pages have no counterpart: it serves callers that
+ * cannot provide or allocate device memory at the call site (a pool holding all free HBM,
+ * code running inside an allocator, a stream that must not wait on cudaMalloc).
+ *
+ *   Arguments, results, arithmetic and errors: as fa_bwd, without workspace arguments.
+ *   Limit: fa_bwd_workspace_bytes(B, H, N) <= FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (4 MiB, i.e.
+ *          B*H*N <= 1,048,576 query rows); larger problems return FA_ERR_UNSUPPORTED before
+ *          any CUDA call.
+ *   Allocation: none, by this call or anything it calls.
+ *   Set-up: the first call on each device looks up that device's copy of the array
+ *          (cudaGetSymbolAddress) and keeps the address; make that first call before any
+ *          stream capture begins on the device.
+ *   Concurrency: every call on one device uses the same array.  Two calls whose work can
+ *          overlap on the device (different streams not ordered by events, or two host
+ *          threads' streams) race on it and give wrong results; order them on one stream.
+ */
+#define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (4 * 1024 * 1024)
+int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                   const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                   int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+                   int dtype, void* stream);
+
 const char* fa_status_string(int status);
 
 /* Text of the last CUDA error seen by this library in the calling thread, or "". */
