@@ -8,14 +8,19 @@
 //
 // Three kernels, no atomics (results do not depend on scheduling):
 //   * delta: one warp per row, rowsum(dO * O) in fp32;
-//   * dQ: one CTA per 128-query tile; per 128-key tile the MMA warp computes S = Q K^T and
-//     dP = dO V^T into TMEM, the four elementwise warps (TMEM lane = query row) form
-//     P and dS = P (dP - delta) and write dS (16-bit) back over dP, and the MMA warp
-//     accumulates dQ += dS K with K read as the MN-major operand;
-//   * dK, dV: one CTA per 128-key tile; per 128-query tile S^T = K Q^T and dP^T = V dO^T
-//     (TMEM lane = key row), the elementwise warps write P^T and dS^T (16-bit) over them,
-//     and the MMA warp accumulates dV += P^T dO and dK += dS^T Q.
-// Warps: 0-3 elementwise, 4 MMA issuer (converged, one elected lane issues), 5 TMA loader.
+//   * dQ: one CTA per 128-query tile.  Q and dO are copied once into TMEM and serve as the
+//     A operands of S = Q K_j^T and dP = dO V_j^T, so those products read only K_j / V_j
+//     from shared memory; the elementwise warps (TMEM lane = query row) form P, then
+//     dS = P (dP - delta), written (16-bit) over dP, and dQ += dS K_j reads K_j as the
+//     MN-major operand;
+//   * dK, dV: one CTA per 128-key tile with K, V fixed in shared memory; per query tile
+//     S^T = K Q_i^T and dP^T = V dO_i^T (TMEM lane = key row), P^T written over S^T feeds
+//     dV += P^T dO_i, and dS^T written over dP^T feeds dK += dS^T Q_i.
+// All products are M = 128, N = 128 (or N = D), K = 16 steps.  The MMA warp staggers them
+// so that each elementwise phase overlaps products of the neighbouring phase: the next S
+// is issued as soon as the elementwise warps have read the current one.
+// Warps: 0-7 elementwise (warp w: TMEM lanes 32 (w % 4).., columns 64 (w / 4).. of each
+// 128-column tile), 8 MMA issuer (converged, one elected lane issues), 9 TMA loader.
 // Every wait is bounded as in the forward kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -36,104 +41,133 @@ using namespace tc;
 // Device status word: [0] flags (1 = a wait ran out), [1] role, [2] CTA, [3] wait id.
 __device__ unsigned int g_status[4];
 
-constexpr int kT = 128;          // tile rows (TMEM lanes) and tile columns
-constexpr int kThreads = 192;
-constexpr int kMmaWarp = 4;
-constexpr int kLoadWarp = 5;
-constexpr int kSlots = 4;        // ring of streamed tiles (two per step)
+constexpr int kT = 128;          // tile rows (TMEM lanes) and streamed tile rows
+constexpr int kThreads = 320;
+constexpr int kEwThreads = 256;  // warps 0-7
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D>
+// Shared memory of one kernel: FIXED 128 x D tiles, then a ring of SLOTS streamed tiles,
+// then (dK/dV) the staged per-column vectors, then the barriers.
+template <int D, int FIXED, int SLOTS>
 struct BGeo {
     static constexpr int kPanels = D / kPanelCols;
     static constexpr int kTile = kPanels * kPanelBytes;        // one 128 x D tile
-    static constexpr int kRingOff = 2 * kTile;                 // after the two fixed tiles
-    static constexpr int kStageOff = kRingOff + kSlots * kTile;
-    static constexpr int kVecOff = kStageOff + 4 * 4096;       // per-column LSE/delta (dK/dV)
-    static constexpr int kBarOff = kVecOff + 2 * 2 * kT * 4;
-    // barriers: fixed_full, ring_full[S], ring_empty[S], s_full, ew_full, done, drain
-    static constexpr int kNumBars = 1 + 2 * kSlots + 4;
+    static constexpr int kSlots = SLOTS;
+    static constexpr int kRingOff = FIXED * kTile;
+    // epilogue staging (4 KB per elementwise warp) reuses the ring: it starts only after
+    // every product, hence every read of the ring, has completed
+    static constexpr int kStageOff = kRingOff;
+    static constexpr int kVecOff = kRingOff + SLOTS * kTile;   // 2 x 256 floats (dK/dV)
+    static constexpr int kBarOff = kVecOff + 2 * 256 * 4;
+    // barriers: fixed_full, ring_full[S], ring_empty[S], then the named ones below
+    static constexpr int kNumBars = 1 + 2 * SLOTS + 7;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
-    // TMEM columns: S (or S^T), dP (or dP^T), accumulator 0 (dQ or dV), accumulator 1 (dK)
-    static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+    static_assert(kSmemBytes <= 232448, "shared memory");
+    static_assert(8 * 4096 <= SLOTS * kTile, "staging fits the ring");
+
+    static constexpr int fixed_full() { return 0; }
+    static constexpr int ring_full(uint32_t i) { return 1 + (int)(i % SLOTS); }
+    static constexpr int ring_empty(uint32_t i) { return 1 + SLOTS + (int)(i % SLOTS); }
+    static constexpr int s_ready() { return 1 + 2 * SLOTS; }    // S (S^T) in TMEM
+    static constexpr int dp_ready() { return 2 + 2 * SLOTS; }   // dP (dP^T) in TMEM
+    static constexpr int x_ready() { return 3 + 2 * SLOTS; }    // dQ: S read; dK/dV: P^T stored
+    static constexpr int ds_ready() { return 4 + 2 * SLOTS; }   // dS (dS^T) stored
+    static constexpr int qdo_ready() { return 5 + 2 * SLOTS; }  // dQ: Q, dO copied into TMEM
+    static constexpr int done() { return 6 + 2 * SLOTS; }
+    static constexpr int drain() { return 7 + 2 * SLOTS; }
+    static __device__ __forceinline__ uint32_t ring_par(uint32_t i) { return (i / SLOTS) & 1u; }
 };
 
-constexpr int b_fixed_full() { return 0; }
-constexpr int b_ring_full(uint32_t i) { return 1 + (int)(i % kSlots); }
-constexpr int b_ring_empty(uint32_t i) { return 1 + kSlots + (int)(i % kSlots); }
-constexpr int b_s_full() { return 1 + 2 * kSlots; }
-constexpr int b_ew_full() { return 2 + 2 * kSlots; }
-constexpr int b_done() { return 3 + 2 * kSlots; }
-constexpr int b_drain() { return 4 + 2 * kSlots; }
-__device__ __forceinline__ uint32_t ring_par(uint32_t i) { return (i / kSlots) & 1u; }
+template <int D> using GeoDq = BGeo<D, 0, 6>;      // Q, dO pass through ring slots 0, 1
+template <int D> using GeoDkdv = BGeo<D, 2, 4>;    // K, V fixed
 
 // ----------------------------------------------------------------- MMA helpers
-// D_tmem (+)= A[128 x D] * B[128 x D]^T with both operands K-major in shared memory.
-template <int D>
-__device__ __forceinline__ void mma_nt(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc) {
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = ((uint64_t)(kk / 4) * kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
-        ptx::mma_ss_elect(d_tmem, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
-    }
+// K-major B: 16-element K step inside a 128-byte panel row, panels of 16 KB.
+__device__ __forceinline__ uint64_t kmaj_step(int kk) {
+    return ((uint64_t)(kk / 4) * kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
 }
 
-// acc_tmem (+)= A_tmem[128 x 128] * B, B a 128 x D shared tile read as the MN-major operand.
-__device__ __forceinline__ void mma_tn(uint32_t acc_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, bool accumulate) {
+// D_tmem = A[128 x D] * B[128 x D]^T, A and B K-major in shared memory.
+template <int D>
+__device__ __forceinline__ void mma_ss_nt(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+        ptx::mma_ss_elect(d_tmem, a_desc + kmaj_step(kk), b_desc + kmaj_step(kk), idesc,
+                          kk > 0 ? 1u : 0u);
+}
+
+// D_tmem = A_tmem[128 x D] * B[128 x D]^T, A in TMEM (16-bit pairs per column, D/2
+// columns), B K-major in shared memory.
+template <int D>
+__device__ __forceinline__ void mma_ts_nt(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc) {
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk)
+        ptx::mma_ts_elect(d_tmem, a_tmem + (uint32_t)kk * 8u, b_desc + kmaj_step(kk), idesc,
+                          kk > 0 ? 1u : 0u);
+}
+
+// acc_tmem (+)= A_tmem[128 x 128] * B, B a 128 x D tile read as the MN-major operand (16
+// rows = 2 KB per K step).  A holds 16-bit values packed two per TMEM column in two blocks
+// of 32 columns (64 values each) at a_tmem and a_tmem + 64, one per elementwise warp of
+// the lane quarter.
+__device__ __forceinline__ void mma_ts_tn(uint32_t acc_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, bool accumulate) {
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
-        ptx::mma_ts_elect(acc_tmem, a_tmem + (uint32_t)kk * 8u,
+        ptx::mma_ts_elect(acc_tmem, a_tmem + (uint32_t)(kk >> 2) * 64u + (uint32_t)(kk & 3) * 8u,
                           b_desc + (uint64_t)((kk * 2048) >> 4), idesc,
                           (accumulate || kk > 0) ? 1u : 0u);
 }
 
 // ----------------------------------------------------------------- epilogue
-// This warp's 32 TMEM lanes x D fp32 columns at t_acc, times mul, rounded to 16 bits, to
-// global rows base + r * D (r < 32, only rows with row0 + r < nrows), through a 4 KB
-// staging slot so every store instruction writes whole 128-byte lines.
+// This warp's 32 TMEM lanes x 64 fp32 columns at t_acc, times mul, rounded to 16 bits, to
+// global rows base + r * D (r < 32, only rows with row0 + r < nrows; base points at the
+// panel's first column), through a 4 KB staging slot so every store instruction writes
+// whole 128-byte lines.
 template <int D, bool F16>
 __device__ __forceinline__ void store_rows(uint32_t t_acc, float mul, uint32_t stage,
                                            uint16_t* base, int row0, int nrows, int lane) {
-#pragma unroll 1
-    for (int pc = 0; pc < D / 64; ++pc) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t o[32];
-            ptx::tmem_ld32_wait(t_acc + (uint32_t)(pc * 64 + h * 32), o);
-            uint32_t w[16];
+    for (int h = 0; h < 2; ++h) {
+        uint32_t o[32];
+        ptx::tmem_ld32_wait(t_acc + (uint32_t)(h * 32), o);
+        uint32_t w[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack2<F16>(u2f(o[2 * i]) * mul, u2f(o[2 * i + 1]) * mul);
+        for (int i = 0; i < 16; ++i) w[i] = pack2<F16>(u2f(o[2 * i]) * mul, u2f(o[2 * i + 1]) * mul);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t chunk = (uint32_t)(h * 4 + i) ^ (uint32_t)(lane & 7);
-                ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
-                                  w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-            }
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t chunk = (uint32_t)(h * 4 + i) ^ (uint32_t)(lane & 7);
+            ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
+                              w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
         }
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int r = 4 * k + (lane >> 3);
-            const int ch = lane & 7;
-            const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) * 16));
-            if (row0 + r < nrows)
-                *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * D + pc * 64 + ch * 8) = v;
-        }
-        __syncwarp();
     }
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = 4 * k + (lane >> 3);
+        const int ch = lane & 7;
+        const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) * 16));
+        if (row0 + r < nrows)
+            *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * D + ch * 8) = v;
+    }
+    __syncwarp();
 }
 
-// Named barrier 1 over the 128 elementwise threads (warps 0-3) that also ANDs a predicate.
+// Named barrier 1 over the 256 elementwise threads (warps 0-7) that also ANDs a predicate:
+// a stop decision taken here is common to all eight warps, so no warp is ever left at a
+// barrier that a warp which gave up will not reach.
 __device__ __forceinline__ bool ew_barrier_and(bool ok) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)ok)
@@ -147,9 +181,8 @@ struct Setup {
     uint32_t sbase, tmem;
 };
 
-template <int D>
-__device__ __forceinline__ Setup setup_cta(uint8_t* smem_raw, const BwdParams& p, int ew_count) {
-    using G = BGeo<D>;
+template <class G>
+__device__ __forceinline__ Setup setup_cta(uint8_t* smem_raw, const BwdParams& p) {
     Setup su;
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -161,15 +194,18 @@ __device__ __forceinline__ Setup setup_cta(uint8_t* smem_raw, const BwdParams& p
     su.c.status = g_status;
     const int warp = threadIdx.x / 32;
     if (threadIdx.x == 0) {
-        ptx::mbar_init(bar_addr(su.c, b_fixed_full()), 1);
-        for (int s = 0; s < kSlots; ++s) {
-            ptx::mbar_init(bar_addr(su.c, b_ring_full(s)), 1);
-            ptx::mbar_init(bar_addr(su.c, b_ring_empty(s)), 1);
+        ptx::mbar_init(bar_addr(su.c, G::fixed_full()), 1);
+        for (int s = 0; s < G::kSlots; ++s) {
+            ptx::mbar_init(bar_addr(su.c, G::ring_full(s)), 1);
+            ptx::mbar_init(bar_addr(su.c, G::ring_empty(s)), 1);
         }
-        ptx::mbar_init(bar_addr(su.c, b_s_full()), 1);
-        ptx::mbar_init(bar_addr(su.c, b_ew_full()), ew_count);
-        ptx::mbar_init(bar_addr(su.c, b_done()), 1);
-        ptx::mbar_init(bar_addr(su.c, b_drain()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::s_ready()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::dp_ready()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::x_ready()), kEwThreads);
+        ptx::mbar_init(bar_addr(su.c, G::ds_ready()), kEwThreads);
+        ptx::mbar_init(bar_addr(su.c, G::qdo_ready()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::done()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::drain()), 1);
         *su.c.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -193,48 +229,54 @@ __device__ __forceinline__ void teardown_cta(const Setup& su) {
     }
 }
 
-// Loader: two fixed tiles (rows fixed_row of maps f0, f1), then per step two streamed tiles
-// (rows 128 * (first + s) of maps r0, r1) through the ring.  Waits for its own copies before
-// returning, so no copy is in flight when the CTA leaves.
+// One 128 x D tile (rows row.. of `map`, slice bh) into shared memory at dst, completing
+// on barrier bar (whose expected bytes the caller has set).
 template <int D>
-__device__ void load_tiles(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
-                           const CUtensorMap* f1, int fixed_row, const CUtensorMap* r0,
-                           const CUtensorMap* r1, int first, int steps, int bh) {
-    using G = BGeo<D>;
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int row, int bh) {
+#pragma unroll
+    for (int pc = 0; pc < D / kPanelCols; ++pc)
+        ptx::tma_load_3d(dst + (uint32_t)pc * kPanelBytes, map, bar, pc * kPanelCols, row, bh);
+}
+
+// Loader: optionally two fixed tiles (f0, f1 at fixed_row), then `count` streamed tiles
+// through the ring; item(i, &map, &row) names the i-th.  Waits for its own copies before
+// returning, so no copy is in flight when the CTA leaves.
+template <int D, class G, class Item>
+__device__ void load_role(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
+                          const CUtensorMap* f1, int fixed_row, int count, int bh, Item item) {
     uint32_t pos = 0;
-    const uint32_t fb = bar_addr(c, b_fixed_full());
-    ptx::mbar_arrive_expect_tx(fb, 2u * G::kTile);
-#pragma unroll
-    for (int pc = 0; pc < G::kPanels; ++pc) {
-        ptx::tma_load_3d(sbase + (uint32_t)pc * kPanelBytes, f0, fb, pc * kPanelCols, fixed_row, bh);
-        ptx::tma_load_3d(sbase + (uint32_t)G::kTile + (uint32_t)pc * kPanelBytes, f1, fb,
-                         pc * kPanelCols, fixed_row, bh);
+    const uint32_t fb = bar_addr(c, G::fixed_full());
+    if (f0) {
+        ptx::mbar_arrive_expect_tx(fb, 2u * G::kTile);
+        load_tile<D>(sbase, f0, fb, fixed_row, bh);
+        load_tile<D>(sbase + (uint32_t)G::kTile, f1, fb, fixed_row, bh);
     }
-    for (int s = 0; s < steps; ++s) {
-        for (int w = 0; w < 2; ++w) {
-            if (!wait(c, b_ring_empty(pos), ring_par(pos) ^ 1u, kRoleLoad)) goto out;
-            const uint32_t bar = bar_addr(c, b_ring_full(pos));
-            const uint32_t dst = sbase + (uint32_t)G::kRingOff + (pos % kSlots) * (uint32_t)G::kTile;
-            ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
-#pragma unroll
-            for (int pc = 0; pc < G::kPanels; ++pc)
-                ptx::tma_load_3d(dst + (uint32_t)pc * kPanelBytes, w == 0 ? r0 : r1, bar,
-                                 pc * kPanelCols, (first + s) * kT, bh);
-            ++pos;
-        }
+    for (; (int)pos < count; ++pos) {
+        if (!wait(c, G::ring_empty(pos), G::ring_par(pos) ^ 1u, kRoleLoad)) break;
+        const uint32_t bar = bar_addr(c, G::ring_full(pos));
+        const CUtensorMap* map;
+        int row;
+        item((int)pos, map, row);
+        ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
+        load_tile<D>(sbase + (uint32_t)G::kRingOff + (pos % G::kSlots) * (uint32_t)G::kTile, map,
+                     bar, row, bh);
     }
-out:
-    wait_drain(fb, 0, c.limit);
-    for (uint32_t i = (pos > (uint32_t)kSlots ? pos - kSlots : 0u); i < pos; ++i)
-        wait_drain(bar_addr(c, b_ring_full(i)), ring_par(i), c.limit);
+    if (f0) wait_drain(fb, 0, c.limit);
+    for (uint32_t i = (pos > (uint32_t)G::kSlots ? pos - G::kSlots : 0u); i < pos; ++i)
+        wait_drain(bar_addr(c, G::ring_full(i)), G::ring_par(i), c.limit);
 }
 
 // ----------------------------------------------------------------- dQ kernel
+// TMEM columns (D = 128; D = 64 halves the first two): Q [0, D/2), dO [D/2, D),
+// S [D, D+128), dP [D+128, D+256), dQ accumulator [D+256, 2D+256).
+// Ring items: 0 = Q, 1 = dO, then K_j = 2 + 2j, V_j = 3 + 2j.
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
-    using G = BGeo<D>;
+    using G = GeoDq<D>;
+    constexpr uint32_t kColQ = 0, kColDO = D / 2, kColS = D, kColDP = D + 128, kColAcc = D + 256;
     extern __shared__ uint8_t smem_raw[];
-    const Setup su = setup_cta<D>(smem_raw, p, 128);
+    const Setup su = setup_cta<G>(smem_raw, p);
     const Ctl& c = su.c;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x / p.ntiles, qt = blockIdx.x % p.ntiles;
@@ -243,93 +285,153 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 
     if (warp == kLoadWarp) {
         if (lane == 0)
-            load_tiles<D>(c, su.sbase, &p.tmap_q, &p.tmap_do, qt * kT, &p.tmap_k, &p.tmap_v, 0,
-                          nkv, bh);
+            load_role<D, G>(c, su.sbase, nullptr, nullptr, 0, 2 + 2 * nkv, bh,
+                            [&](int i, const CUtensorMap*& m, int& row) {
+                                if (i < 2) { m = i == 0 ? &p.tmap_q : &p.tmap_do; row = qt * kT; }
+                                else { m = (i & 1) ? &p.tmap_v : &p.tmap_k; row = ((i - 2) >> 1) * kT; }
+                            });
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
         constexpr uint32_t id_tn = make_idesc(kT, D, true, F16);
-        const uint64_t dQ = sw128_desc(su.sbase, 16, 1024);
-        const uint64_t dDO = sw128_desc(su.sbase + (uint32_t)G::kTile, 16, 1024);
-        const uint64_t dRing = sw128_desc(su.sbase + (uint32_t)G::kRingOff, 16, 1024);
-        const uint64_t dRingMN = sw128_desc(su.sbase + (uint32_t)G::kRingOff, kPanelBytes, 1024);
-        auto slot_off = [](uint32_t i) { return (uint64_t)((i % kSlots) * (uint32_t)G::kTile) >> 4; };
-        if (!wait_warp(c, b_fixed_full(), 0, kRoleMma)) goto mma_out;
+        const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
+        auto kdesc = [&](uint32_t pos) {   // K-major view of a ring tile
+            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, 16, 1024);
+        };
+        auto mdesc = [&](uint32_t pos) {   // MN-major view of a ring tile
+            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, kPanelBytes, 1024);
+        };
+        auto issue_s = [&](int j) -> bool {    // S = Q K_j^T
+            const uint32_t pos = 2u + 2u * (uint32_t)j;
+            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            ptx::tc_fence_after();
+            mma_ts_nt<D>(tm + kColS, tm + kColQ, kdesc(pos), id_nt);
+            ptx::mma_commit_elect(bar_addr(c, G::s_ready()));
+            return true;
+        };
+        auto issue_dp = [&](int j) -> bool {   // dP = dO V_j^T; V_j is then done
+            const uint32_t pos = 3u + 2u * (uint32_t)j;
+            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            ptx::tc_fence_after();
+            mma_ts_nt<D>(tm + kColDP, tm + kColDO, kdesc(pos), id_nt);
+            ptx::mma_commit_elect(bar_addr(c, G::dp_ready()));
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(pos)));
+            return true;
+        };
+        if (!wait_warp(c, G::qdo_ready(), 0, kRoleMma)) goto mma_out;
+        ptx::tc_fence_after();
+        if (!issue_s(0) || !issue_dp(0)) goto mma_out;
         for (int j = 0; j < nkv; ++j) {
-            const uint32_t kpos = 2u * j, vpos = 2u * j + 1u;
-            if (!wait_warp(c, b_ring_full(kpos), ring_par(kpos), kRoleMma)) goto mma_out;
+            const uint32_t par = (uint32_t)j & 1u;
+            if (!wait_warp(c, G::x_ready(), par, kRoleMma)) goto mma_out;   // S(j) read
+            if (j + 1 < nkv && !issue_s(j + 1)) goto mma_out;
+            if (!wait_warp(c, G::ds_ready(), par, kRoleMma)) goto mma_out;
             ptx::tc_fence_after();
-            mma_nt<D>(tm + G::kColS, dQ, dRing + slot_off(kpos), id_nt);          // S = Q K^T
-            if (!wait_warp(c, b_ring_full(vpos), ring_par(vpos), kRoleMma)) goto mma_out;
-            ptx::tc_fence_after();
-            mma_nt<D>(tm + G::kColDP, dDO, dRing + slot_off(vpos), id_nt);        // dP = dO V^T
-            ptx::mma_commit_elect(bar_addr(c, b_s_full()));
-            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(vpos)));
-            if (!wait_warp(c, b_ew_full(), (uint32_t)j & 1u, kRoleMma)) goto mma_out;
-            ptx::tc_fence_after();
-            mma_tn(tm + G::kColAcc0, tm + G::kColDP, dRingMN + slot_off(kpos), id_tn, j > 0);  // dQ += dS K
-            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(kpos)));
+            const uint32_t kpos = 2u + 2u * (uint32_t)j;
+            mma_ts_tn(tm + kColAcc, tm + kColDP, mdesc(kpos), id_tn, j > 0);   // dQ += dS K_j
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(kpos)));
+            if (j + 1 < nkv && !issue_dp(j + 1)) goto mma_out;
         }
-        ptx::mma_commit_elect(bar_addr(c, b_done()));
+        ptx::mma_commit_elect(bar_addr(c, G::done()));
     mma_out:
-        ptx::mma_commit_elect(bar_addr(c, b_drain()));
-        wait_drain(bar_addr(c, b_drain()), 0, c.limit);
+        ptx::mma_commit_elect(bar_addr(c, G::drain()));
+        wait_drain(bar_addr(c, G::drain()), 0, c.limit);
         __syncwarp();
     } else {
-        // elementwise: thread = query row
-        const int r = warp * 32 + lane;
+        // elementwise: thread = query row r; this warp's 64 of the 128 keys of each tile
+        const int quarter = warp & 3, ch = warp >> 2;
+        const int r = quarter * 32 + lane;
         const int i = qt * kT + r;
         const bool live = i < p.n;
         const size_t row = (size_t)bh * p.n + (live ? i : 0);
         const float lse2 = live ? p.lse[row] * kLog2e : 0.0f;
         const float dlt = live ? p.delta[row] : 0.0f;
         const int limit = CAUSAL ? min(i + 1, p.n) : p.n;    // visible keys: key < limit
-        const uint32_t tl = (uint32_t)(warp * 32) << 16;
-        for (int j = 0; j < nkv; ++j) {
-            if (!wait_warp(c, b_s_full(), (uint32_t)j & 1u, kRoleSoftmax)) goto ew_out;
-            ptx::tc_fence_after();
-            const bool mask = __any_sync(0xFFFFFFFFu, j * kT + kT > limit);
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t sv[32], dp[32];
-                ptx::tmem_ld32x2_wait(tm + tl + G::kColS + 32u * ch, tm + tl + G::kColDP + 32u * ch, sv, dp);
-                uint32_t pk[16];
+        const uint32_t tl = (uint32_t)(quarter * 32) << 16;
+        const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
+        {
+            // Q and dO rows into TMEM as 16-bit pairs (this warp: one 64-column panel)
+            const bool ok = wait_warp(c, G::ring_full(0), 0, kRoleSoftmax) &&
+                            wait_warp(c, G::ring_full(1), 0, kRoleSoftmax);
+            if (ok && ch < D / 64) {
 #pragma unroll
-                for (int cc = 0; cc < 32; cc += 2) {
-                    const int key = j * kT + ch * 32 + cc;
-                    float p0 = ptx::ex2(fmaf(u2f(sv[cc]), p.scale_log2, -lse2));
-                    float p1 = ptx::ex2(fmaf(u2f(sv[cc + 1]), p.scale_log2, -lse2));
-                    if (mask) {
-                        if (key >= limit) p0 = 0.0f;
-                        if (key + 1 >= limit) p1 = 0.0f;
+                for (int t = 0; t < 2; ++t) {
+                    const uint32_t src = ring + (uint32_t)t * G::kTile + (uint32_t)ch * kPanelBytes +
+                                         (uint32_t)r * 128u;
+                    uint32_t w[32];
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 v = ptx::ld_shared_v4(src + (uint32_t)((cc ^ (r & 7)) * 16));
+                        w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
                     }
-                    pk[cc >> 1] = pack2<F16>(p0 * (u2f(dp[cc]) - dlt), p1 * (u2f(dp[cc + 1]) - dlt));
+                    ptx::tmem_st32(tm + tl + (t == 0 ? kColQ : kColDO) + 32u * (uint32_t)ch, w);
                 }
-                __syncwarp();
-                // dS over dP columns 16ch.. (dP columns already loaded)
-                ptx::tmem_st16(tm + tl + G::kColDP + 16u * ch, pk);
+                ptx::tmem_wait_st();
             }
-            ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(c, b_ew_full()));
+            if (!ew_barrier_and(ok)) goto ew_out;
+            if (threadIdx.x == 0) {
+                ptx::mbar_arrive(bar_addr(c, G::ring_empty(0)));
+                ptx::mbar_arrive(bar_addr(c, G::ring_empty(1)));
+                ptx::mbar_arrive(bar_addr(c, G::qdo_ready()));
+            }
         }
-        if (!wait_warp(c, b_done(), 0, kRoleSoftmax)) goto ew_out;
+        for (int j = 0; j < nkv; ++j) {
+            const uint32_t par = (uint32_t)j & 1u;
+            const int key0 = j * kT + 64 * ch;
+            const bool mask = __any_sync(0xFFFFFFFFu, key0 + 64 > limit);
+            float pr[64];
+            {   // phase a: P from S
+                if (!wait_warp(c, G::s_ready(), par, kRoleSoftmax)) goto ew_out;
+                ptx::tc_fence_after();
+                uint32_t sv[64];
+                ptx::tmem_ld64_wait(tm + tl + kColS + 64u * (uint32_t)ch, sv);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, G::x_ready()));   // S may be overwritten
+#pragma unroll
+                for (int cc = 0; cc < 64; ++cc) {
+                    pr[cc] = ptx::ex2(fmaf(u2f(sv[cc]), p.scale_log2, -lse2));
+                    if (mask && key0 + cc >= limit) pr[cc] = 0.0f;
+                }
+            }
+            {   // phase b: dS = P (dP - delta), 16-bit, over this warp's dP columns
+                if (!wait_warp(c, G::dp_ready(), par, kRoleSoftmax)) goto ew_out;
+                ptx::tc_fence_after();
+                uint32_t dp[64];
+                const uint32_t tp = tm + tl + kColDP + 64u * (uint32_t)ch;
+                ptx::tmem_ld64_wait(tp, dp);
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 2)
+                    pk[cc >> 1] = pack2<F16>(pr[cc] * (u2f(dp[cc]) - dlt),
+                                             pr[cc + 1] * (u2f(dp[cc + 1]) - dlt));
+                ptx::tmem_st32(tp, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, G::ds_ready()));
+            }
+        }
+        if (!wait_warp(c, G::done(), 0, kRoleSoftmax)) goto ew_out;
         ptx::tc_fence_after();
-        store_rows<D, F16>(tm + tl + G::kColAcc0, p.scale,
-                           su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
-                           reinterpret_cast<uint16_t*>(p.dq) + (size_t)bh * p.n * D, qt * kT + warp * 32,
-                           p.n, lane);
+        if (ch < D / 64)   // one 64-column panel of dQ per warp
+            store_rows<D, F16>(tm + tl + kColAcc + 64u * (uint32_t)ch, p.scale,
+                               su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
+                               reinterpret_cast<uint16_t*>(p.dq) + (size_t)bh * p.n * D + 64 * ch,
+                               qt * kT + quarter * 32, p.n, lane);
     ew_out:;
     }
     teardown_cta(su);
 }
 
 // ----------------------------------------------------------------- dK, dV kernel
+// TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256+D), dK [256+D, 256+2D).
+// Ring items: Q_i = 2s, dO_i = 2s + 1 for query tile i = i0 + s.
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
-    using G = BGeo<D>;
+    using G = GeoDkdv<D>;
+    constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     extern __shared__ uint8_t smem_raw[];
-    const Setup su = setup_cta<D>(smem_raw, p, 128);
+    const Setup su = setup_cta<G>(smem_raw, p);
     const Ctl& c = su.c;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int bh = blockIdx.x / p.ntiles, kt = blockIdx.x % p.ntiles;
@@ -339,103 +441,147 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 
     if (warp == kLoadWarp) {
         if (lane == 0)
-            load_tiles<D>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, &p.tmap_q, &p.tmap_do, i0, nq,
-                          bh);
+            load_role<D, G>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, 2 * nq, bh,
+                            [&](int i, const CUtensorMap*& m, int& row) {
+                                m = (i & 1) ? &p.tmap_do : &p.tmap_q;
+                                row = (i0 + (i >> 1)) * kT;
+                            });
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
         constexpr uint32_t id_tn = make_idesc(kT, D, true, F16);
         const uint64_t dK = sw128_desc(su.sbase, 16, 1024);
         const uint64_t dV = sw128_desc(su.sbase + (uint32_t)G::kTile, 16, 1024);
-        const uint64_t dRing = sw128_desc(su.sbase + (uint32_t)G::kRingOff, 16, 1024);
-        const uint64_t dRingMN = sw128_desc(su.sbase + (uint32_t)G::kRingOff, kPanelBytes, 1024);
-        auto slot_off = [](uint32_t i) { return (uint64_t)((i % kSlots) * (uint32_t)G::kTile) >> 4; };
-        if (!wait_warp(c, b_fixed_full(), 0, kRoleMma)) goto mma_out;
+        const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
+        auto kdesc = [&](uint32_t pos) {
+            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, 16, 1024);
+        };
+        auto mdesc = [&](uint32_t pos) {
+            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, kPanelBytes, 1024);
+        };
+        auto issue_st = [&](int s) -> bool {    // S^T = K Q_i^T
+            const uint32_t pos = 2u * (uint32_t)s;
+            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            ptx::tc_fence_after();
+            mma_ss_nt<D>(tm + kColS, dK, kdesc(pos), id_nt);
+            ptx::mma_commit_elect(bar_addr(c, G::s_ready()));
+            return true;
+        };
+        auto issue_dpt = [&](int s) -> bool {   // dP^T = V dO_i^T
+            const uint32_t pos = 2u * (uint32_t)s + 1u;
+            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            ptx::tc_fence_after();
+            mma_ss_nt<D>(tm + kColDP, dV, kdesc(pos), id_nt);
+            ptx::mma_commit_elect(bar_addr(c, G::dp_ready()));
+            return true;
+        };
+        if (!wait_warp(c, G::fixed_full(), 0, kRoleMma)) goto mma_out;
+        if (!issue_st(0) || !issue_dpt(0)) goto mma_out;
         for (int s = 0; s < nq; ++s) {
-            const uint32_t qpos = 2u * s, dopos = 2u * s + 1u;
-            if (!wait_warp(c, b_ring_full(qpos), ring_par(qpos), kRoleMma)) goto mma_out;
+            const uint32_t par = (uint32_t)s & 1u, qpos = 2u * (uint32_t)s, dopos = qpos + 1u;
+            if (!wait_warp(c, G::x_ready(), par, kRoleMma)) goto mma_out;   // P^T stored
             ptx::tc_fence_after();
-            mma_nt<D>(tm + G::kColS, dK, dRing + slot_off(qpos), id_nt);         // S^T = K Q^T
-            if (!wait_warp(c, b_ring_full(dopos), ring_par(dopos), kRoleMma)) goto mma_out;
+            mma_ts_tn(tm + kColDV, tm + kColS, mdesc(dopos), id_tn, s > 0);   // dV += P^T dO_i
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(dopos)));
+            if (s + 1 < nq && !issue_st(s + 1)) goto mma_out;
+            if (!wait_warp(c, G::ds_ready(), par, kRoleMma)) goto mma_out;
             ptx::tc_fence_after();
-            mma_nt<D>(tm + G::kColDP, dV, dRing + slot_off(dopos), id_nt);       // dP^T = V dO^T
-            ptx::mma_commit_elect(bar_addr(c, b_s_full()));
-            if (!wait_warp(c, b_ew_full(), (uint32_t)s & 1u, kRoleMma)) goto mma_out;
-            ptx::tc_fence_after();
-            mma_tn(tm + G::kColAcc0, tm + G::kColS, dRingMN + slot_off(dopos), id_tn, s > 0);   // dV += P^T dO
-            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(dopos)));
-            mma_tn(tm + G::kColAcc1, tm + G::kColDP, dRingMN + slot_off(qpos), id_tn, s > 0);   // dK += dS^T Q
-            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(qpos)));
+            mma_ts_tn(tm + kColDK, tm + kColDP, mdesc(qpos), id_tn, s > 0);   // dK += dS^T Q_i
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(qpos)));
+            if (s + 1 < nq && !issue_dpt(s + 1)) goto mma_out;
         }
-        ptx::mma_commit_elect(bar_addr(c, b_done()));
+        ptx::mma_commit_elect(bar_addr(c, G::done()));
     mma_out:
-        ptx::mma_commit_elect(bar_addr(c, b_drain()));
-        wait_drain(bar_addr(c, b_drain()), 0, c.limit);
+        ptx::mma_commit_elect(bar_addr(c, G::drain()));
+        wait_drain(bar_addr(c, G::drain()), 0, c.limit);
         __syncwarp();
     } else {
-        // elementwise: thread = key row; columns = the 128 queries of the current tile
-        const int r = warp * 32 + lane;
+        // elementwise: thread = key row r; this warp's 64 of the 128 queries of each tile
+        const int quarter = warp & 3, ch = warp >> 2;
+        const int r = quarter * 32 + lane;
         const int key = kt * kT + r;
-        const uint32_t tl = (uint32_t)(warp * 32) << 16;
+        const uint32_t tl = (uint32_t)(quarter * 32) << 16;
+        const int t = threadIdx.x;   // 0..255
         float* vec = reinterpret_cast<float*>(smem_raw + (su.sbase - ptx::smem_addr(smem_raw)) + G::kVecOff);
-        // per-column LSE (log2 units) and delta of query tile i0 + s, staged in shared memory;
-        // the next tile's pair is fetched one step ahead into registers
-        auto fetch = [&](int s, float& l2, float& d) {
-            const int q = (i0 + s) * kT + r;
+        // Per-column LSE (log2 units) and delta of each query tile, staged in shared
+        // memory: thread t < 128 stages the LSE of query t of the tile, thread 128 + t its
+        // delta.  The next tile's value is fetched one step ahead into a register.
+        auto fetch = [&](int s) -> float {
+            const int q = (i0 + s) * kT + (t & (kT - 1));
             const bool ok = s < nq && q < p.n;
-            l2 = ok ? p.lse[(size_t)bh * p.n + q] * kLog2e : INFINITY;   // p = 0 past N
-            d = ok ? p.delta[(size_t)bh * p.n + q] : 0.0f;
+            if (t < kT) return ok ? p.lse[(size_t)bh * p.n + q] * kLog2e : INFINITY;   // p = 0 past N
+            return ok ? p.delta[(size_t)bh * p.n + q] : 0.0f;
         };
-        float l2_next, d_next;
-        fetch(0, l2_next, d_next);
+        float next = fetch(0);
+        bool failed = false;
         for (int s = 0; s < nq; ++s) {
-            float* vl = vec + (s & 1) * 2 * kT;   // [0, 128): LSE * log2 e, [128, 256): delta
-            vl[r] = l2_next;
-            vl[kT + r] = d_next;
-            // One barrier over the four elementwise warps publishes the staged vectors and
-            // makes the stop decision common to all four, so no warp is left at a barrier
-            // that a warp which gave up will never reach.
-            const bool ok = wait_warp(c, b_s_full(), (uint32_t)s & 1u, kRoleSoftmax);
+            const uint32_t par = (uint32_t)s & 1u;
+            float* vl = vec + par * 256;   // [0, 128): LSE * log2 e, [128, 256): delta
+            vl[t] = next;
+            const bool ok = !failed && wait_warp(c, G::s_ready(), par, kRoleSoftmax);
             if (!ew_barrier_and(ok)) goto ew_out;
             ptx::tc_fence_after();
-            fetch(s + 1, l2_next, d_next);
-            const int qbase = (i0 + s) * kT;
+            next = fetch(s + 1);
+            const int qbase = (i0 + s) * kT + 64 * ch;
             const bool diag = CAUSAL && (i0 + s == kt);   // queries before this key are masked
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t sv[32], dp[32];
-                ptx::tmem_ld32x2_wait(tm + tl + G::kColS + 32u * ch, tm + tl + G::kColDP + 32u * ch, sv, dp);
-                uint32_t pp[16], pd[16];
+            const float4* l4 = reinterpret_cast<const float4*>(vl + 64 * ch);
+            const float4* d4 = reinterpret_cast<const float4*>(vl + kT + 64 * ch);
+            float pr[64];
+            {   // phase a: P^T from S^T, 16-bit over this warp's S^T columns
+                const uint32_t ts = tm + tl + kColS + 64u * (uint32_t)ch;
+                uint32_t sv[64];
+                ptx::tmem_ld64_wait(ts, sv);
 #pragma unroll
-                for (int cc = 0; cc < 32; cc += 2) {
-                    const int col = ch * 32 + cc;
-                    float p0 = ptx::ex2(fmaf(u2f(sv[cc]), p.scale_log2, -vl[col]));
-                    float p1 = ptx::ex2(fmaf(u2f(sv[cc + 1]), p.scale_log2, -vl[col + 1]));
-                    if (diag) {
-                        if (qbase + col < key) p0 = 0.0f;
-                        if (qbase + col + 1 < key) p1 = 0.0f;
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const float4 l = l4[c4];
+                    const float lv[4] = {l.x, l.y, l.z, l.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = c4 * 4 + e;
+                        pr[cc] = ptx::ex2(fmaf(u2f(sv[cc]), p.scale_log2, -lv[e]));
+                        if (diag && qbase + cc < key) pr[cc] = 0.0f;
                     }
-                    pp[cc >> 1] = pack2<F16>(p0, p1);
-                    pd[cc >> 1] = pack2<F16>(p0 * (u2f(dp[cc]) - vl[kT + col]),
-                                             p1 * (u2f(dp[cc + 1]) - vl[kT + col + 1]));
                 }
-                __syncwarp();
-                ptx::tmem_st16(tm + tl + G::kColS + 16u * ch, pp);    // P^T over S^T columns
-                ptx::tmem_st16(tm + tl + G::kColDP + 16u * ch, pd);   // dS^T over dP^T columns
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 2) pk[cc >> 1] = pack2<F16>(pr[cc], pr[cc + 1]);
+                ptx::tmem_st32(ts, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, G::x_ready()));
             }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(c, b_ew_full()));
+            {   // phase b: dS^T = P^T (dP^T - delta), 16-bit over this warp's dP^T columns
+                if (!wait_warp(c, G::dp_ready(), par, kRoleSoftmax)) { failed = true; continue; }
+                ptx::tc_fence_after();
+                const uint32_t tp = tm + tl + kColDP + 64u * (uint32_t)ch;
+                uint32_t dp[64];
+                ptx::tmem_ld64_wait(tp, dp);
+                uint32_t pk[32];
+#pragma unroll
+                for (int c4 = 0; c4 < 16; ++c4) {
+                    const float4 d = d4[c4];
+                    const int cc = c4 * 4;
+                    pk[cc >> 1] = pack2<F16>(pr[cc] * (u2f(dp[cc]) - d.x), pr[cc + 1] * (u2f(dp[cc + 1]) - d.y));
+                    pk[(cc >> 1) + 1] = pack2<F16>(pr[cc + 2] * (u2f(dp[cc + 2]) - d.z),
+                                                   pr[cc + 3] * (u2f(dp[cc + 3]) - d.w));
+                }
+                ptx::tmem_st32(tp, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, G::ds_ready()));
+            }
         }
-        if (!wait_warp(c, b_done(), 0, kRoleSoftmax)) goto ew_out;
+        if (failed) goto ew_out;
+        if (!wait_warp(c, G::done(), 0, kRoleSoftmax)) goto ew_out;
         ptx::tc_fence_after();
-        {
+        if (ch < D / 64) {   // one 64-column panel of dV and of dK per warp
             const uint32_t stage = su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u;
-            const int row0 = kt * kT + warp * 32;
-            store_rows<D, F16>(tm + tl + G::kColAcc0, 1.0f, stage,
-                               reinterpret_cast<uint16_t*>(p.dv) + (size_t)bh * p.n * D, row0, p.n, lane);
-            store_rows<D, F16>(tm + tl + G::kColAcc1, p.scale, stage,
-                               reinterpret_cast<uint16_t*>(p.dk) + (size_t)bh * p.n * D, row0, p.n, lane);
+            const int row0 = kt * kT + quarter * 32;
+            const size_t off = (size_t)bh * p.n * D + 64 * ch;
+            store_rows<D, F16>(tm + tl + kColDV + 64u * (uint32_t)ch, 1.0f, stage,
+                               reinterpret_cast<uint16_t*>(p.dv) + off, row0, p.n, lane);
+            store_rows<D, F16>(tm + tl + kColDK + 64u * (uint32_t)ch, p.scale, stage,
+                               reinterpret_cast<uint16_t*>(p.dk) + off, row0, p.n, lane);
         }
     ew_out:;
     }
@@ -475,20 +621,20 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
 template <int D, bool CAUSAL, bool F16>
 cudaError_t prepare3() {
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL, F16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, BGeo<D>::kSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, GeoDq<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(bwd_dkdv_kernel<D, CAUSAL, F16>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, BGeo<D>::kSmemBytes);
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, GeoDkdv<D>::kSmemBytes);
 }
 
 template <int D, bool CAUSAL, bool F16>
 cudaError_t launch3(const BwdParams& p, int bh, cudaStream_t stream) {
     const long long ctas = (long long)bh * p.ntiles;
     if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    bwd_dq_kernel<D, CAUSAL, F16><<<(unsigned)ctas, kThreads, BGeo<D>::kSmemBytes, stream>>>(p);
+    bwd_dq_kernel<D, CAUSAL, F16><<<(unsigned)ctas, kThreads, GeoDq<D>::kSmemBytes, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    bwd_dkdv_kernel<D, CAUSAL, F16><<<(unsigned)ctas, kThreads, BGeo<D>::kSmemBytes, stream>>>(p);
+    bwd_dkdv_kernel<D, CAUSAL, F16><<<(unsigned)ctas, kThreads, GeoDkdv<D>::kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
