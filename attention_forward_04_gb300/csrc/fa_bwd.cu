@@ -8,17 +8,19 @@
 //
 // Three kernels, no atomics (results do not depend on scheduling):
 //   * delta: one warp per row, rowsum(dO * O) in fp32;
-//   * dQ: one CTA per 128-query tile.  Q and dO are copied once into TMEM and serve as the
-//     A operands of S = Q K_j^T and dP = dO V_j^T, so those products read only K_j / V_j
-//     from shared memory; the elementwise warps (TMEM lane = query row) form P, then
-//     dS = P (dP - delta), written (16-bit) over dP, and dQ += dS K_j reads K_j as the
-//     MN-major operand;
+//   * dQ: one CTA per 128-query tile.  Q is copied once into TMEM and serves as the A
+//     operand of S = Q K_j^T (dO stays in shared memory for dP = dO V_j^T); the
+//     elementwise warps (TMEM lane = query row) form P, then dS = P (dP - delta) into a
+//     TMEM region of its own (16-bit), so dP of the next key tile can start while dQ +=
+//     dS K_j (K_j read as the MN-major operand) waits for dS;
 //   * dK, dV: one CTA per 128-key tile with K, V fixed in shared memory; per query tile
 //     S^T = K Q_i^T and dP^T = V dO_i^T (TMEM lane = key row), P^T written over S^T feeds
 //     dV += P^T dO_i, and dS^T written over dP^T feeds dK += dS^T Q_i.
 // All products are M = 128, N = 128 (or N = D), K = 16 steps.  The MMA warp staggers them
 // so that each elementwise phase overlaps products of the neighbouring phase: the next S
-// is issued as soon as the elementwise warps have read the current one.
+// is issued as soon as the elementwise warps have read the current one.  Streamed tiles
+// pass through a 4-slot ring whose two slots per step swap roles every other step, so the
+// tile needed first two steps later lands in the slot that is released first.
 // Warps: 0-7 elementwise (warp w: TMEM lanes 32 (w % 4).., columns 64 (w / 4).. of each
 // 128-column tile), 8 MMA issuer (converged, one elected lane issues), 9 TMA loader.
 // Every wait is bounded as in the forward kernel.
@@ -49,8 +51,8 @@ constexpr int kLoadWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Shared memory of one kernel: FIXED 128 x D tiles, then a ring of SLOTS streamed tiles,
-// then (dK/dV) the staged per-column vectors, then the barriers.
+// Shared memory: FIXED fixed 128 x D tiles, a ring of SLOTS streamed tiles, the staged
+// per-column vectors (dK/dV), then the barriers.
 template <int D, int FIXED, int SLOTS>
 struct BGeo {
     static constexpr int kPanels = D / kPanelCols;
@@ -60,30 +62,41 @@ struct BGeo {
     // epilogue staging (4 KB per elementwise warp) reuses the ring: it starts only after
     // every product, hence every read of the ring, has completed
     static constexpr int kStageOff = kRingOff;
-    static constexpr int kVecOff = kRingOff + SLOTS * kTile;   // 2 x 256 floats (dK/dV)
-    static constexpr int kBarOff = kVecOff + 2 * 256 * 4;
-    // barriers: fixed_full, ring_full[S], ring_empty[S], then the named ones below
-    static constexpr int kNumBars = 1 + 2 * SLOTS + 7;
+    static constexpr int kVecOff = kRingOff + kSlots * kTile;  // 2 x 256 floats (dK/dV only)
+    static constexpr int kBarOff = kVecOff + (FIXED == 2 ? 2 * 256 * 4 : 0);
+    // barriers: fixed_full, ring_full[4], ring_empty[4], then the named ones below
+    static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
     static_assert(kSmemBytes <= 232448, "shared memory");
-    static_assert(8 * 4096 <= SLOTS * kTile, "staging fits the ring");
+    static_assert(8 * 4096 <= kSlots * kTile, "staging fits the ring");
 
     static constexpr int fixed_full() { return 0; }
-    static constexpr int ring_full(uint32_t i) { return 1 + (int)(i % SLOTS); }
-    static constexpr int ring_empty(uint32_t i) { return 1 + SLOTS + (int)(i % SLOTS); }
-    static constexpr int s_ready() { return 1 + 2 * SLOTS; }    // S (S^T) in TMEM
-    static constexpr int dp_ready() { return 2 + 2 * SLOTS; }   // dP (dP^T) in TMEM
-    static constexpr int x_ready() { return 3 + 2 * SLOTS; }    // dQ: S read; dK/dV: P^T stored
-    static constexpr int ds_ready() { return 4 + 2 * SLOTS; }   // dS (dS^T) stored
-    static constexpr int qdo_ready() { return 5 + 2 * SLOTS; }  // dQ: Q, dO copied into TMEM
-    static constexpr int done() { return 6 + 2 * SLOTS; }
-    static constexpr int drain() { return 7 + 2 * SLOTS; }
-    static __device__ __forceinline__ uint32_t ring_par(uint32_t i) { return (i / SLOTS) & 1u; }
+    static constexpr int ring_full(uint32_t slot) { return 1 + (int)slot; }
+    static constexpr int ring_empty(uint32_t slot) { return 1 + kSlots + (int)slot; }
+    // cyclic use (dQ): streamed tile `pos` in slot pos % SLOTS, its (pos / SLOTS)-th fill
+    static __device__ __forceinline__ uint32_t cyc_slot(uint32_t pos) { return pos % SLOTS; }
+    static __device__ __forceinline__ uint32_t cyc_par(uint32_t pos) { return (pos / SLOTS) & 1u; }
+    static constexpr int s_ready() { return 1 + 2 * kSlots; }    // S (S^T) in TMEM
+    static constexpr int dp_ready() { return 2 + 2 * kSlots; }   // dP (dP^T) in TMEM
+    static constexpr int x_ready() { return 3 + 2 * kSlots; }    // dQ: S read; dK/dV: P^T stored
+    static constexpr int ds_ready() { return 4 + 2 * kSlots; }   // dS (dS^T) stored
+    static constexpr int q_ready() { return 5 + 2 * kSlots; }    // dQ: Q copied into TMEM
+    static constexpr int dp_free() { return 6 + 2 * kSlots; }    // dQ: dP read
+    static constexpr int ds_free() { return 7 + 2 * kSlots; }    // dQ: dQ product read dS
+    static constexpr int done() { return 8 + 2 * kSlots; }
+    static constexpr int drain() { return 9 + 2 * kSlots; }
 };
 
-template <int D> using GeoDq = BGeo<D, 0, 6>;      // Q, dO pass through ring slots 0, 1
-template <int D> using GeoDkdv = BGeo<D, 2, 4>;    // K, V fixed
+template <int D> using GeoDq = BGeo<D, 1, 6>;     // dO fixed; Q, then K_j, V_j, streamed
+template <int D> using GeoDkdv = BGeo<D, 2, 4>;   // K, V fixed; Q_i, dO_i streamed
+
+// The dK/dV ring: step j streams tile A_j (needed first, released last) and B_j (needed
+// second, released first).  A_j takes the slot B_{j-2} used and B_j the slot A_{j-2} used,
+// so every slot is filled once per two steps.
+__device__ __forceinline__ uint32_t slot_a(int j) { return 2u * (uint32_t)(j & 1) + ((uint32_t)(j >> 1) & 1u); }
+__device__ __forceinline__ uint32_t slot_b(int j) { return 2u * (uint32_t)(j & 1) + 1u - ((uint32_t)(j >> 1) & 1u); }
+__device__ __forceinline__ uint32_t slot_par(int j) { return (uint32_t)(j >> 1) & 1u; }
 
 // ----------------------------------------------------------------- MMA helpers
 // K-major B: 16-element K step inside a 128-byte panel row, panels of 16 KB.
@@ -114,13 +127,15 @@ __device__ __forceinline__ void mma_ts_nt(uint32_t d_tmem, uint32_t a_tmem, uint
 
 // acc_tmem (+)= A_tmem[128 x 128] * B, B a 128 x D tile read as the MN-major operand (16
 // rows = 2 KB per K step).  A holds 16-bit values packed two per TMEM column in two blocks
-// of 32 columns (64 values each) at a_tmem and a_tmem + 64, one per elementwise warp of
-// the lane quarter.
+// of 32 columns (64 values each), one per elementwise warp of the lane quarter, at a_tmem
+// and a_tmem + BLOCK (BLOCK = 32: contiguous; 64: over the first half of each 64-column
+// fp32 block the values were computed from).
+template <uint32_t BLOCK>
 __device__ __forceinline__ void mma_ts_tn(uint32_t acc_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, bool accumulate) {
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
-        ptx::mma_ts_elect(acc_tmem, a_tmem + (uint32_t)(kk >> 2) * 64u + (uint32_t)(kk & 3) * 8u,
+        ptx::mma_ts_elect(acc_tmem, a_tmem + (uint32_t)(kk >> 2) * BLOCK + (uint32_t)(kk & 3) * 8u,
                           b_desc + (uint64_t)((kk * 2048) >> 4), idesc,
                           (accumulate || kk > 0) ? 1u : 0u);
 }
@@ -203,7 +218,9 @@ __device__ __forceinline__ Setup setup_cta(uint8_t* smem_raw, const BwdParams& p
         ptx::mbar_init(bar_addr(su.c, G::dp_ready()), 1);
         ptx::mbar_init(bar_addr(su.c, G::x_ready()), kEwThreads);
         ptx::mbar_init(bar_addr(su.c, G::ds_ready()), kEwThreads);
-        ptx::mbar_init(bar_addr(su.c, G::qdo_ready()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::q_ready()), 1);
+        ptx::mbar_init(bar_addr(su.c, G::dp_free()), kEwThreads);
+        ptx::mbar_init(bar_addr(su.c, G::ds_free()), 1);
         ptx::mbar_init(bar_addr(su.c, G::done()), 1);
         ptx::mbar_init(bar_addr(su.c, G::drain()), 1);
         *su.c.abort = 0;
@@ -239,42 +256,75 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
         ptx::tma_load_3d(dst + (uint32_t)pc * kPanelBytes, map, bar, pc * kPanelCols, row, bh);
 }
 
-// Loader: optionally two fixed tiles (f0, f1 at fixed_row), then `count` streamed tiles
-// through the ring; item(i, &map, &row) names the i-th.  Waits for its own copies before
-// returning, so no copy is in flight when the CTA leaves.
-template <int D, class G, class Item>
-__device__ void load_role(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
-                          const CUtensorMap* f1, int fixed_row, int count, int bh, Item item) {
-    uint32_t pos = 0;
+// dK/dV loader: the two fixed tiles (f0, f1 at fixed_row), then for steps j < steps the
+// tiles A_j (map ma) and B_j (map mb), rows first_row + 128 j, through the paired ring.
+// Waits for its own copies before returning, so no copy is in flight when the CTA leaves.
+template <int D>
+__device__ void load_pairs(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
+                           const CUtensorMap* f1, int fixed_row, const CUtensorMap* ma,
+                           const CUtensorMap* mb, int first_row, int steps, int bh) {
+    using G = GeoDkdv<D>;
     const uint32_t fb = bar_addr(c, G::fixed_full());
-    if (f0) {
-        ptx::mbar_arrive_expect_tx(fb, 2u * G::kTile);
-        load_tile<D>(sbase, f0, fb, fixed_row, bh);
-        load_tile<D>(sbase + (uint32_t)G::kTile, f1, fb, fixed_row, bh);
+    ptx::mbar_arrive_expect_tx(fb, 2u * G::kTile);
+    load_tile<D>(sbase, f0, fb, fixed_row, bh);
+    load_tile<D>(sbase + (uint32_t)G::kTile, f1, fb, fixed_row, bh);
+    int issued = 0;   // tiles issued, A and B alternating
+    for (int j = 0; j < steps; ++j) {
+        for (int w = 0; w < 2; ++w) {
+            const uint32_t slot = w == 0 ? slot_a(j) : slot_b(j);
+            if (!wait(c, G::ring_empty(slot), slot_par(j) ^ 1u, kRoleLoad)) goto out;
+            const uint32_t bar = bar_addr(c, G::ring_full(slot));
+            ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
+            load_tile<D>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, w == 0 ? ma : mb,
+                         bar, first_row + j * kT, bh);
+            ++issued;
+        }
     }
-    for (; (int)pos < count; ++pos) {
-        if (!wait(c, G::ring_empty(pos), G::ring_par(pos) ^ 1u, kRoleLoad)) break;
-        const uint32_t bar = bar_addr(c, G::ring_full(pos));
-        const CUtensorMap* map;
-        int row;
-        item((int)pos, map, row);
+out:
+    wait_drain(fb, 0, c.limit);
+    // copies of the last two steps may still be in flight
+    for (int k = (issued > 4 ? issued - 4 : 0); k < issued; ++k) {
+        const int j = k >> 1;
+        wait_drain(bar_addr(c, G::ring_full((k & 1) ? slot_b(j) : slot_a(j))), slot_par(j), c.limit);
+    }
+}
+
+// dQ loader: the fixed tile dO (rows fixed_row), then streamed tile 0 = Q (rows fixed_row)
+// and tiles 1 + 2j = K_j, 2 + 2j = V_j (rows 128 j) through the cyclic ring.  Waits for its
+// own copies before returning.
+template <int D>
+__device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fixed_row, int nkv,
+                        int bh) {
+    using G = GeoDq<D>;
+    const uint32_t fb = bar_addr(c, G::fixed_full());
+    ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTile);
+    load_tile<D>(sbase, &p.tmap_do, fb, fixed_row, bh);
+    const uint32_t count = 1u + 2u * (uint32_t)nkv;
+    uint32_t pos = 0;
+    for (; pos < count; ++pos) {
+        const uint32_t slot = G::cyc_slot(pos);
+        if (!wait(c, G::ring_empty(slot), G::cyc_par(pos) ^ 1u, kRoleLoad)) break;
+        const uint32_t bar = bar_addr(c, G::ring_full(slot));
+        const CUtensorMap* map = pos == 0 ? &p.tmap_q : ((pos & 1u) ? &p.tmap_k : &p.tmap_v);
+        const int row = pos == 0 ? fixed_row : (int)((pos - 1u) >> 1) * kT;
         ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
-        load_tile<D>(sbase + (uint32_t)G::kRingOff + (pos % G::kSlots) * (uint32_t)G::kTile, map,
-                     bar, row, bh);
+        load_tile<D>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, map, bar, row, bh);
     }
-    if (f0) wait_drain(fb, 0, c.limit);
+    wait_drain(fb, 0, c.limit);
     for (uint32_t i = (pos > (uint32_t)G::kSlots ? pos - G::kSlots : 0u); i < pos; ++i)
-        wait_drain(bar_addr(c, G::ring_full(i)), G::ring_par(i), c.limit);
+        wait_drain(bar_addr(c, G::ring_full(G::cyc_slot(i))), G::cyc_par(i), c.limit);
 }
 
 // ----------------------------------------------------------------- dQ kernel
-// TMEM columns (D = 128; D = 64 halves the first two): Q [0, D/2), dO [D/2, D),
-// S [D, D+128), dP [D+128, D+256), dQ accumulator [D+256, 2D+256).
-// Ring items: 0 = Q, 1 = dO, then K_j = 2 + 2j, V_j = 3 + 2j.
+// TMEM columns: Q [0, D/2), dS [D/2, D/2+64), S [D/2+64, +128), dP [D/2+192, +128),
+// dQ accumulator [D/2+320, +D)  (512 columns at D = 128).
+// Shared memory: dO fixed; ring: Q (copied to TMEM, then released), K_j, V_j.
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using G = GeoDq<D>;
-    constexpr uint32_t kColQ = 0, kColDO = D / 2, kColS = D, kColDP = D + 128, kColAcc = D + 256;
+    constexpr uint32_t kColQ = 0, kColDS = D / 2, kColS = D / 2 + 64, kColDP = kColS + 128,
+                       kColAcc = kColDP + 128;
+    static_assert(kColAcc + D <= kTmemCols, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
     const Setup su = setup_cta<G>(smem_raw, p);
     const Ctl& c = su.c;
@@ -285,52 +335,52 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 
     if (warp == kLoadWarp) {
         if (lane == 0)
-            load_role<D, G>(c, su.sbase, nullptr, nullptr, 0, 2 + 2 * nkv, bh,
-                            [&](int i, const CUtensorMap*& m, int& row) {
-                                if (i < 2) { m = i == 0 ? &p.tmap_q : &p.tmap_do; row = qt * kT; }
-                                else { m = (i & 1) ? &p.tmap_v : &p.tmap_k; row = ((i - 2) >> 1) * kT; }
-                            });
+            load_dq<D>(c, su.sbase, p, qt * kT, nkv, bh);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
         constexpr uint32_t id_tn = make_idesc(kT, D, true, F16);
+        const uint64_t dDO = sw128_desc(su.sbase, 16, 1024);
         const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
-        auto kdesc = [&](uint32_t pos) {   // K-major view of a ring tile
-            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, 16, 1024);
+        auto kdesc = [&](uint32_t pos) {
+            return sw128_desc(ring + G::cyc_slot(pos) * (uint32_t)G::kTile, 16, 1024);
         };
-        auto mdesc = [&](uint32_t pos) {   // MN-major view of a ring tile
-            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, kPanelBytes, 1024);
+        auto mdesc = [&](uint32_t pos) {
+            return sw128_desc(ring + G::cyc_slot(pos) * (uint32_t)G::kTile, kPanelBytes, 1024);
         };
-        auto issue_s = [&](int j) -> bool {    // S = Q K_j^T
-            const uint32_t pos = 2u + 2u * (uint32_t)j;
-            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+        auto issue_s = [&](int j) -> bool {    // S = Q K_j^T (Q from TMEM)
+            const uint32_t pos = 1u + 2u * (uint32_t)j;
+            if (!wait_warp(c, G::ring_full(G::cyc_slot(pos)), G::cyc_par(pos), kRoleMma)) return false;
             ptx::tc_fence_after();
             mma_ts_nt<D>(tm + kColS, tm + kColQ, kdesc(pos), id_nt);
             ptx::mma_commit_elect(bar_addr(c, G::s_ready()));
             return true;
         };
         auto issue_dp = [&](int j) -> bool {   // dP = dO V_j^T; V_j is then done
-            const uint32_t pos = 3u + 2u * (uint32_t)j;
-            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            const uint32_t pos = 2u + 2u * (uint32_t)j;
+            if (!wait_warp(c, G::ring_full(G::cyc_slot(pos)), G::cyc_par(pos), kRoleMma)) return false;
             ptx::tc_fence_after();
-            mma_ts_nt<D>(tm + kColDP, tm + kColDO, kdesc(pos), id_nt);
+            mma_ss_nt<D>(tm + kColDP, dDO, kdesc(pos), id_nt);
             ptx::mma_commit_elect(bar_addr(c, G::dp_ready()));
-            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(pos)));
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(G::cyc_slot(pos))));
             return true;
         };
-        if (!wait_warp(c, G::qdo_ready(), 0, kRoleMma)) goto mma_out;
+        if (!wait_warp(c, G::fixed_full(), 0, kRoleMma)) goto mma_out;
+        if (!wait_warp(c, G::q_ready(), 0, kRoleMma)) goto mma_out;
         ptx::tc_fence_after();
         if (!issue_s(0) || !issue_dp(0)) goto mma_out;
         for (int j = 0; j < nkv; ++j) {
             const uint32_t par = (uint32_t)j & 1u;
-            if (!wait_warp(c, G::x_ready(), par, kRoleMma)) goto mma_out;   // S(j) read
+            if (!wait_warp(c, G::x_ready(), par, kRoleMma)) goto mma_out;    // S(j) read
             if (j + 1 < nkv && !issue_s(j + 1)) goto mma_out;
+            if (!wait_warp(c, G::dp_free(), par, kRoleMma)) goto mma_out;    // dP(j) read
+            if (j + 1 < nkv && !issue_dp(j + 1)) goto mma_out;
             if (!wait_warp(c, G::ds_ready(), par, kRoleMma)) goto mma_out;
             ptx::tc_fence_after();
-            const uint32_t kpos = 2u + 2u * (uint32_t)j;
-            mma_ts_tn(tm + kColAcc, tm + kColDP, mdesc(kpos), id_tn, j > 0);   // dQ += dS K_j
-            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(kpos)));
-            if (j + 1 < nkv && !issue_dp(j + 1)) goto mma_out;
+            const uint32_t kpos = 1u + 2u * (uint32_t)j;
+            mma_ts_tn<32>(tm + kColAcc, tm + kColDS, mdesc(kpos), id_tn, j > 0);   // dQ += dS K_j
+            ptx::mma_commit_elect(bar_addr(c, G::ds_free()));
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(G::cyc_slot(kpos))));
         }
         ptx::mma_commit_elect(bar_addr(c, G::done()));
     mma_out:
@@ -348,32 +398,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         const float dlt = live ? p.delta[row] : 0.0f;
         const int limit = CAUSAL ? min(i + 1, p.n) : p.n;    // visible keys: key < limit
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-        const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
         {
-            // Q and dO rows into TMEM as 16-bit pairs (this warp: one 64-column panel)
-            const bool ok = wait_warp(c, G::ring_full(0), 0, kRoleSoftmax) &&
-                            wait_warp(c, G::ring_full(1), 0, kRoleSoftmax);
+            // Q rows (streamed tile 0) into TMEM as 16-bit pairs (this warp: one 64-column
+            // panel); the ring slot is then released
+            const bool ok = wait_warp(c, G::ring_full(0), 0, kRoleSoftmax);
             if (ok && ch < D / 64) {
+                const uint32_t src = su.sbase + (uint32_t)G::kRingOff + (uint32_t)ch * kPanelBytes +
+                                     (uint32_t)r * 128u;
+                uint32_t w[32];
 #pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    const uint32_t src = ring + (uint32_t)t * G::kTile + (uint32_t)ch * kPanelBytes +
-                                         (uint32_t)r * 128u;
-                    uint32_t w[32];
-#pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint4 v = ptx::ld_shared_v4(src + (uint32_t)((cc ^ (r & 7)) * 16));
-                        w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
-                    }
-                    ptx::tmem_st32(tm + tl + (t == 0 ? kColQ : kColDO) + 32u * (uint32_t)ch, w);
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 v = ptx::ld_shared_v4(src + (uint32_t)((cc ^ (r & 7)) * 16));
+                    w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
                 }
+                ptx::tmem_st32(tm + tl + kColQ + 32u * (uint32_t)ch, w);
                 ptx::tmem_wait_st();
             }
             ptx::tc_fence_before();
             if (!ew_barrier_and(ok)) goto ew_out;
             if (threadIdx.x == 0) {
                 ptx::mbar_arrive(bar_addr(c, G::ring_empty(0)));
-                ptx::mbar_arrive(bar_addr(c, G::ring_empty(1)));
-                ptx::mbar_arrive(bar_addr(c, G::qdo_ready()));
+                ptx::mbar_arrive(bar_addr(c, G::q_ready()));
             }
         }
         for (int j = 0; j < nkv; ++j) {
@@ -389,23 +434,37 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar_addr(c, G::x_ready()));   // S may be overwritten
 #pragma unroll
-                for (int cc = 0; cc < 64; ++cc) {
-                    pr[cc] = ptx::ex2(fmaf(u2f(sv[cc]), p.scale_log2, -lse2));
-                    if (mask && key0 + cc >= limit) pr[cc] = 0.0f;
+                for (int cc = 0; cc < 64; cc += 2) {
+                    float x0, x1;
+                    ptx::fma2(x0, x1, u2f(sv[cc]), u2f(sv[cc + 1]), p.scale_log2, -lse2);
+                    pr[cc] = ptx::ex2(x0);
+                    pr[cc + 1] = ptx::ex2(x1);
+                }
+                if (mask) {
+#pragma unroll
+                    for (int cc = 0; cc < 64; ++cc)
+                        if (key0 + cc >= limit) pr[cc] = 0.0f;
                 }
             }
-            {   // phase b: dS = P (dP - delta), 16-bit, over this warp's dP columns
+            {   // phase b: dS = P (dP - delta), 16-bit, into this warp's half of the dS region
                 if (!wait_warp(c, G::dp_ready(), par, kRoleSoftmax)) goto ew_out;
                 ptx::tc_fence_after();
                 uint32_t dp[64];
-                const uint32_t tp = tm + tl + kColDP + 64u * (uint32_t)ch;
-                ptx::tmem_ld64_wait(tp, dp);
+                ptx::tmem_ld64_wait(tm + tl + kColDP + 64u * (uint32_t)ch, dp);
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, G::dp_free()));   // dP may be overwritten
                 uint32_t pk[32];
 #pragma unroll
-                for (int cc = 0; cc < 64; cc += 2)
-                    pk[cc >> 1] = pack2<F16>(pr[cc] * (u2f(dp[cc]) - dlt),
-                                             pr[cc + 1] * (u2f(dp[cc + 1]) - dlt));
-                ptx::tmem_st32(tp, pk);
+                for (int cc = 0; cc < 64; cc += 2) {
+                    float d0 = u2f(dp[cc]), d1 = u2f(dp[cc + 1]);
+                    ptx::add2(d0, d1, -dlt, -dlt);
+                    ptx::mul2(d0, d1, pr[cc], pr[cc + 1]);
+                    pk[cc >> 1] = pack2<F16>(d0, d1);
+                }
+                // the previous dQ product must have read the dS region
+                if (j > 0 && !wait_warp(c, G::ds_free(), par ^ 1u, kRoleSoftmax)) goto ew_out;
+                ptx::tc_fence_after();
+                ptx::tmem_st32(tm + tl + kColDS + 32u * (uint32_t)ch, pk);
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar_addr(c, G::ds_ready()));
@@ -425,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 
 // ----------------------------------------------------------------- dK, dV kernel
 // TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256+D), dK [256+D, 256+2D).
-// Ring items: Q_i = 2s, dO_i = 2s + 1 for query tile i = i0 + s.
+// Shared memory: K, V fixed; ring A_s = Q_i, B_s = dO_i for query tile i = i0 + s.
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using G = GeoDkdv<D>;
@@ -441,11 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 
     if (warp == kLoadWarp) {
         if (lane == 0)
-            load_role<D, G>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, 2 * nq, bh,
-                            [&](int i, const CUtensorMap*& m, int& row) {
-                                m = (i & 1) ? &p.tmap_do : &p.tmap_q;
-                                row = (i0 + (i >> 1)) * kT;
-                            });
+            load_pairs<D>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, &p.tmap_q, &p.tmap_do,
+                          i0 * kT, nq, bh);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
@@ -453,41 +509,35 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const uint64_t dK = sw128_desc(su.sbase, 16, 1024);
         const uint64_t dV = sw128_desc(su.sbase + (uint32_t)G::kTile, 16, 1024);
         const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
-        auto kdesc = [&](uint32_t pos) {
-            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, 16, 1024);
-        };
-        auto mdesc = [&](uint32_t pos) {
-            return sw128_desc(ring + (pos % G::kSlots) * (uint32_t)G::kTile, kPanelBytes, 1024);
-        };
+        auto kdesc = [&](uint32_t slot) { return sw128_desc(ring + slot * (uint32_t)G::kTile, 16, 1024); };
+        auto mdesc = [&](uint32_t slot) { return sw128_desc(ring + slot * (uint32_t)G::kTile, kPanelBytes, 1024); };
         auto issue_st = [&](int s) -> bool {    // S^T = K Q_i^T
-            const uint32_t pos = 2u * (uint32_t)s;
-            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            if (!wait_warp(c, G::ring_full(slot_a(s)), slot_par(s), kRoleMma)) return false;
             ptx::tc_fence_after();
-            mma_ss_nt<D>(tm + kColS, dK, kdesc(pos), id_nt);
+            mma_ss_nt<D>(tm + kColS, dK, kdesc(slot_a(s)), id_nt);
             ptx::mma_commit_elect(bar_addr(c, G::s_ready()));
             return true;
         };
         auto issue_dpt = [&](int s) -> bool {   // dP^T = V dO_i^T
-            const uint32_t pos = 2u * (uint32_t)s + 1u;
-            if (!wait_warp(c, G::ring_full(pos), G::ring_par(pos), kRoleMma)) return false;
+            if (!wait_warp(c, G::ring_full(slot_b(s)), slot_par(s), kRoleMma)) return false;
             ptx::tc_fence_after();
-            mma_ss_nt<D>(tm + kColDP, dV, kdesc(pos), id_nt);
+            mma_ss_nt<D>(tm + kColDP, dV, kdesc(slot_b(s)), id_nt);
             ptx::mma_commit_elect(bar_addr(c, G::dp_ready()));
             return true;
         };
         if (!wait_warp(c, G::fixed_full(), 0, kRoleMma)) goto mma_out;
         if (!issue_st(0) || !issue_dpt(0)) goto mma_out;
         for (int s = 0; s < nq; ++s) {
-            const uint32_t par = (uint32_t)s & 1u, qpos = 2u * (uint32_t)s, dopos = qpos + 1u;
+            const uint32_t par = (uint32_t)s & 1u;
             if (!wait_warp(c, G::x_ready(), par, kRoleMma)) goto mma_out;   // P^T stored
             ptx::tc_fence_after();
-            mma_ts_tn(tm + kColDV, tm + kColS, mdesc(dopos), id_tn, s > 0);   // dV += P^T dO_i
-            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(dopos)));
+            mma_ts_tn<64>(tm + kColDV, tm + kColS, mdesc(slot_b(s)), id_tn, s > 0);   // dV += P^T dO_i
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(slot_b(s))));
             if (s + 1 < nq && !issue_st(s + 1)) goto mma_out;
             if (!wait_warp(c, G::ds_ready(), par, kRoleMma)) goto mma_out;
             ptx::tc_fence_after();
-            mma_ts_tn(tm + kColDK, tm + kColDP, mdesc(qpos), id_tn, s > 0);   // dK += dS^T Q_i
-            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(qpos)));
+            mma_ts_tn<64>(tm + kColDK, tm + kColDP, mdesc(slot_a(s)), id_tn, s > 0);   // dK += dS^T Q_i
+            ptx::mma_commit_elect(bar_addr(c, G::ring_empty(slot_a(s))));
             if (s + 1 < nq && !issue_dpt(s + 1)) goto mma_out;
         }
         ptx::mma_commit_elect(bar_addr(c, G::done()));
@@ -534,13 +584,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
                 for (int c4 = 0; c4 < 16; ++c4) {
                     const float4 l = l4[c4];
-                    const float lv[4] = {l.x, l.y, l.z, l.w};
+                    const int cc = 4 * c4;
+                    float x0, x1, x2, x3;
+                    ptx::fma2v(x0, x1, u2f(sv[cc]), u2f(sv[cc + 1]), p.scale_log2, p.scale_log2, -l.x, -l.y);
+                    ptx::fma2v(x2, x3, u2f(sv[cc + 2]), u2f(sv[cc + 3]), p.scale_log2, p.scale_log2, -l.z, -l.w);
+                    pr[cc] = ptx::ex2(x0);
+                    pr[cc + 1] = ptx::ex2(x1);
+                    pr[cc + 2] = ptx::ex2(x2);
+                    pr[cc + 3] = ptx::ex2(x3);
+                }
+                if (diag) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int cc = c4 * 4 + e;
-                        pr[cc] = ptx::ex2(fmaf(u2f(sv[cc]), p.scale_log2, -lv[e]));
-                        if (diag && qbase + cc < key) pr[cc] = 0.0f;
-                    }
+                    for (int cc = 0; cc < 64; ++cc)
+                        if (qbase + cc < key) pr[cc] = 0.0f;
                 }
                 uint32_t pk[32];
 #pragma unroll
@@ -560,10 +616,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
 #pragma unroll
                 for (int c4 = 0; c4 < 16; ++c4) {
                     const float4 d = d4[c4];
-                    const int cc = c4 * 4;
-                    pk[cc >> 1] = pack2<F16>(pr[cc] * (u2f(dp[cc]) - d.x), pr[cc + 1] * (u2f(dp[cc + 1]) - d.y));
-                    pk[(cc >> 1) + 1] = pack2<F16>(pr[cc + 2] * (u2f(dp[cc + 2]) - d.z),
-                                                   pr[cc + 3] * (u2f(dp[cc + 3]) - d.w));
+                    const int cc = 4 * c4;
+                    float a0 = u2f(dp[cc]), a1 = u2f(dp[cc + 1]), a2 = u2f(dp[cc + 2]), a3 = u2f(dp[cc + 3]);
+                    ptx::add2(a0, a1, -d.x, -d.y);
+                    ptx::add2(a2, a3, -d.z, -d.w);
+                    ptx::mul2(a0, a1, pr[cc], pr[cc + 1]);
+                    ptx::mul2(a2, a3, pr[cc + 2], pr[cc + 3]);
+                    pk[cc >> 1] = pack2<F16>(a0, a1);
+                    pk[(cc >> 1) + 1] = pack2<F16>(a2, a3);
                 }
                 ptx::tmem_st32(tp, pk);
                 ptx::tmem_wait_st();

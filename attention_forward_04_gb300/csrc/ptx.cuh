@@ -273,6 +273,23 @@ __device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
         : "+f"(a0), "+f"(a1)
         : "f"(b0), "f"(b1));
 }
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ void fma2v(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                      float c0, float c1) {
+    asm("{\n\t.reg .b64 x, y, z, r;\n\t"
+        "mov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\tmov.b64 z, {%6, %7};\n\t"
+        "fma.rn.f32x2 r, x, y, z;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (a0, a1) *= (b0, b1)
+__device__ __forceinline__ void mul2(float& a0, float& a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 x, y, r;\n\t"
+        "mov.b64 x, {%0, %1};\n\tmov.b64 y, {%2, %3};\n\t"
+        "mul.rn.f32x2 r, x, y;\n\tmov.b64 {%0, %1}, r;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
