@@ -36,7 +36,10 @@ if ROOT not in sys.path:
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SRC = os.path.join(ROOT, "attention_forward_04_gb300", "csrc", "fa_tc.cu")
+_CSRC = os.path.join(ROOT, "attention_forward_04_gb300", "csrc")
+# sources whose change invalidates a stored traffic capture
+KERNEL_SRCS = {"fwd": [os.path.join(_CSRC, f) for f in ("fa_tc.cu", "tc_common.cuh", "ptx.cuh")],
+               "bwd": [os.path.join(_CSRC, f) for f in ("fa_bwd.cu", "tc_common.cuh", "ptx.cuh")]}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -57,20 +60,24 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def kernel_hash(op: str = "fwd") -> str:
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS[op]:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
-def load_traffic(workload: str):
-    """dram read+write bytes per launch from an ncu capture, if it matches this kernel source."""
+def load_traffic(key: str, op: str = "fwd"):
+    """dram read+write bytes per launch (per call for the backward) from an ncu capture, if
+    it matches the current kernel sources."""
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
     except (OSError, ValueError):
         return None
-    e = t.get(workload)
-    if not e or e.get("kernel_sha256_16") != kernel_hash():
+    e = t.get(key)
+    if not e or e.get("kernel_sha256_16") != kernel_hash(op):
         return None
     return e.get("bytes_per_launch")
 
@@ -431,7 +438,7 @@ def run_bwd(args, w):
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops_step / (per_call_ms / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": None,
+            "frac": achieved / peak, "traffic": load_traffic("bwd:" + w.name, "bwd"),
             "kernel": "whole fa_bwd call (delta, dQ and dK/dV kernels); per-kernel shares "
                       "in the ncu launch list",
             "peak_source": "%s bf16 dense burst" % peak_src,
