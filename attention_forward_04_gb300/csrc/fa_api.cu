@@ -33,6 +33,8 @@ struct DeviceInfo {
     cudaError_t prepare_err[2][2][2] = {};
     std::once_flag bwd_prepared[2][2][2];
     cudaError_t bwd_prepare_err[2][2][2] = {};
+    std::once_flag prepared256[2][2];  // [causal][f16]
+    cudaError_t prepare256_err[2][2] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -62,17 +64,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 
 // 16-bit tensor viewed as a 3-D TMA map whose box lands in shared memory as 128 rows of
 // 64 head-dim values (128 bytes, 128-byte swizzle), which the tensor-core kernel expects.
-//   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, 128, 1}; rows past N read as zero.
+//   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, rows, 1} (rows = 128, or 64 for the
+//   D = 256 kernel); rows past N read as zero.
 //   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, 128}; tokens past T read
 //   as zero (tokens of the next packed sequence are masked by the kernel instead).
 bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int64_t n, int64_t h,
-                int64_t t, int64_t d, bool f16, PFN_cuTensorMapEncodeTiled_v12000 fn) {
+                int64_t t, int64_t d, bool f16, PFN_cuTensorMapEncodeTiled_v12000 fn,
+                cuuint32_t rows = 128) {
     cuuint64_t dims[3], strides[2];
     cuuint32_t box[3];
     if (layout == 0) {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)n; dims[2] = (cuuint64_t)bh;
         strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(n * d * 2);
-        box[0] = 64; box[1] = 128; box[2] = 1;
+        box[0] = 64; box[1] = rows; box[2] = 1;
     } else {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)h; dims[2] = (cuuint64_t)t;
         strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(h * d * 2);
@@ -121,11 +125,13 @@ int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall) {
 int fa_check_device_status(void* stream, uint32_t* detail) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-    uint32_t w[4] = {0, 0, 0, 0}, wb[4] = {0, 0, 0, 0};
+    uint32_t w[4] = {0, 0, 0, 0}, wb[4] = {0, 0, 0, 0}, w256[4] = {0, 0, 0, 0};
     e = fa::tc_status_read_reset(w);
     if (e == cudaSuccess) e = fa::bwd_status_read_reset(wb);
+    if (e == cudaSuccess) e = fa::tc256_status_read_reset(w256);
     if (e != cudaSuccess) return fail_cuda(e, "status word");
     if (!(w[0] & 1u) && (wb[0] & 1u)) std::memcpy(w, wb, sizeof(w));   // report the backward's
+    if (!(w[0] & 1u) && (w256[0] & 1u)) std::memcpy(w, w256, sizeof(w));
     if (detail) std::memcpy(detail, w, sizeof(w));
     return (w[0] & 1u) ? FA_ERR_TIMEOUT : FA_OK;
 }
@@ -158,7 +164,9 @@ int forward(const Request& r) {
     if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
     if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (r.D != 64 && r.D != 128) return FA_ERR_UNSUPPORTED;
+    if (r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
+    // D = 256: 16-bit storage, [B, H, N, D] layout only
+    if (r.D == 256 && (r.dtype == FA_FP32 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;
     const size_t esize = r.dtype == FA_FP32 ? 4 : 2;
     const int64_t rows = r.layout == 0 ? BH * r.N : r.T * r.H;   // rows of D elements
@@ -177,7 +185,7 @@ int forward(const Request& r) {
         return FA_ERR_MISALIGNED;
     const bool tc = r.dtype != FA_FP32;
     int units = 0;
-    if (tc) {
+    if (tc && r.D != 256) {
         units = fa::tc_units((int)BH, (int)r.N, r.causal != 0);
         if (units < 0) return FA_ERR_UNSUPPORTED;
     }
@@ -215,6 +223,28 @@ int forward(const Request& r) {
 
     const bool f16 = r.dtype == FA_FP16;
     const int di128 = r.D == 128, dic = r.causal != 0, dif = f16;
+    if (r.D == 256) {
+        std::call_once(di.prepared256[dic][dif],
+                       [&] { di.prepare256_err[dic][dif] = fa::tc256_prepare(dic, f16); });
+        if (di.prepare256_err[dic][dif] != cudaSuccess)
+            return fail_cuda(di.prepare256_err[dic][dif], "cudaFuncSetAttribute (D = 256)");
+        PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
+        if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
+        fa::TcParams p;
+        std::memset(&p, 0, sizeof(p));
+        if (!encode_map(&p.tmap_q, r.q, 0, BH, r.N, r.H, r.T, r.D, f16, fn, 64) ||
+            !encode_map(&p.tmap_k, r.k, 0, BH, r.N, r.H, r.T, r.D, f16, fn, 64) ||
+            !encode_map(&p.tmap_v, r.v, 0, BH, r.N, r.H, r.T, r.D, f16, fn, 64))
+            return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+        p.o = r.o;
+        p.lse = r.lse;
+        p.n = (int)r.N;
+        p.bh = (int)BH;
+        p.scale_log2 = r.scale * 1.4426950408889634f;
+        p.wait_limit = g_wait_limit.load();
+        e = fa::tc256_launch(dic, f16, p, st);
+        return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch (D = 256)");
+    }
     std::call_once(di.prepared[di128][dic][dif],
                    [&] { di.prepare_err[di128][dic][dif] = fa::tc_prepare((int)r.D, dic, f16); });
     if (di.prepare_err[di128][dic][dif] != cudaSuccess)

@@ -1,0 +1,414 @@
+// fa_tc256.cu -- attention forward for head dimension D = 256 on the GB300 tensor cores.
+//
+// Same computation as the D = 64/128 kernel ("08 · FlashAttention" §二: tiles plus the
+// online (m, l, O) softmax; "KingOfEgg" §1.1 for the definition), with a layout sized for
+// D = 256: the two-query-tile schedule of the smaller head dimensions would need 2 x 256
+// TMEM columns of O alone.  Here one CTA owns one 128-row query tile and all 512 columns:
+//     Q [0, 128)       the query tile as 16-bit pairs (A operand of S = Q K^T)
+//     S/P buffer 0     [128, 192)   64 keys: fp32 scores, then P (16-bit) over them
+//     S/P buffer 1     [192, 256)
+//     O                [256, 512)   fp32 accumulator
+// Keys advance 64 at a time.  S(j+2) is issued right after O += P(j) V_j, so the softmax
+// of step j+1 overlaps both products.  Every product reads only one operand from shared
+// memory (K_j or V_j), which keeps shared-memory bandwidth below the tensor rate.
+// Warps: 0-3 softmax (thread = query row = TMEM lane), 4 MMA issuer, 5 TMA loader.
+// Every wait is bounded; a wait that runs out sets this unit's status word.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace fa {
+namespace {
+
+using namespace tc;
+
+__device__ unsigned int g_status[4];
+
+constexpr int D = 256;
+constexpr int kBM = 128;                       // query rows per CTA
+constexpr int kBN = 64;                        // keys per step
+constexpr int kThreads = 192;
+constexpr int kMmaWarp = 4, kLoadWarp = 5;
+constexpr int kSlots = 6;
+constexpr int kPanel64 = 64 * 128;             // 64 rows x 64 16-bit columns (8 KB)
+constexpr int kTile = 4 * kPanel64;            // 64 x 256 tile (32 KB)
+constexpr int kStageOff = kSlots * kTile;      // 4 warps x 4 KB epilogue staging
+constexpr int kBarOff = kStageOff + 4 * 4096;
+// barriers: ring_full[6], ring_empty[6], s_full[2], p_full[2], o_done, q_ready, drain
+constexpr int kNumBars = 2 * kSlots + 7;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;
+constexpr int kSmemBytes = kMiscOff + 16 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256, kTmemCols = 512;
+
+constexpr int b_ring_full(uint32_t pos) { return (int)(pos % kSlots); }
+constexpr int b_ring_empty(uint32_t pos) { return kSlots + (int)(pos % kSlots); }
+constexpr int b_s_full(uint32_t b) { return 2 * kSlots + (int)b; }
+constexpr int b_p_full(uint32_t b) { return 2 * kSlots + 2 + (int)b; }
+constexpr int b_o_done() { return 2 * kSlots + 4; }
+constexpr int b_q_ready() { return 2 * kSlots + 5; }
+constexpr int b_drain() { return 2 * kSlots + 6; }
+__device__ __forceinline__ uint32_t ring_par(uint32_t pos) { return (pos / kSlots) & 1u; }
+
+// Streamed tiles: 0 and 1 are the two 64-row halves of the Q tile, then K_j = 2 + 2j and
+// V_j = 3 + 2j.
+__device__ __forceinline__ uint32_t pos_k(int j) { return 2u + 2u * (uint32_t)j; }
+__device__ __forceinline__ uint32_t pos_v(int j) { return 3u + 2u * (uint32_t)j; }
+
+template <bool F16> struct Lazy { static constexpr float kRescaleLog2 = F16 ? 8.0f : 16.0f; };
+
+// Named barrier 1 over the 128 softmax threads that also ANDs a predicate, so a stop
+// decision is common to the four warps.
+__device__ __forceinline__ bool sm_barrier_and(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
+// One 64-key step of one row: running-max update (raised only when the step's maximum
+// exceeds it by more than 2^kRescaleLog2), p = 2^(s * sl2 - m), row sum, and P packed to
+// 16-bit pairs.  Keys at or past `limit` count as absent (MASK).  Eight independent max
+// chains and four paired sum chains keep the dependent depth short.  Returns the factor
+// the row's O and l must be scaled by.
+template <bool MASK, bool F16>
+__device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0, int limit,
+                                              float sl2, float& m_run, float& l_run,
+                                              uint32_t (&pk)[32]) {
+    float mx[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 2) {
+        float a = u2f(s[cc]), b = u2f(s[cc + 1]);
+        if (MASK) {
+            if (key0 + cc >= limit) a = -INFINITY;
+            if (key0 + cc + 1 >= limit) b = -INFINITY;
+        }
+        mx[(cc >> 1) & 7] = ptx::max3(mx[(cc >> 1) & 7], a, b);
+    }
+    const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]),
+                           fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+    float alpha = 1.0f;
+    if (mt > m_run + Lazy<F16>::kRescaleLog2) {
+        alpha = ptx::ex2(m_run - mt);   // 0 on the first step (m_run = -inf)
+        m_run = mt;
+    }
+    const float neg_m = -m_run;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int cc = 0; cc < 64; cc += 2) {
+        float x0, x1;
+        ptx::fma2(x0, x1, u2f(s[cc]), u2f(s[cc + 1]), sl2, neg_m);
+        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+        if (MASK) {
+            if (key0 + cc >= limit) p0 = 0.0f;
+            if (key0 + cc + 1 >= limit) p1 = 0.0f;
+        }
+        const int a = ((cc >> 1) & 3) * 2;
+        ptx::add2(acc[a], acc[a + 1], p0, p1);
+        pk[cc >> 1] = pack2<F16>(p0, p1);
+    }
+    const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+    l_run = l_run * alpha + sum;
+    return alpha;
+}
+
+struct Work {
+    int bh, qt, nkv;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ Work work_of(const TcParams& p) {
+    const int ntiles = (p.n + kBM - 1) / kBM;
+    Work w;
+    if (CAUSAL) {
+        // heaviest query tiles first (work grows with the tile index)
+        w.qt = ntiles - 1 - (int)(blockIdx.x / (unsigned)p.bh);
+        w.bh = (int)(blockIdx.x % (unsigned)p.bh);
+    } else {
+        // slice-major: CTAs resident together share one slice's K and V through L2
+        w.bh = (int)(blockIdx.x / (unsigned)ntiles);
+        w.qt = (int)(blockIdx.x % (unsigned)ntiles);
+    }
+    const int keys = CAUSAL ? min(p.n, (w.qt + 1) * kBM) : p.n;
+    w.nkv = (keys + kBN - 1) / kBN;
+    return w;
+}
+
+template <bool CAUSAL, bool F16>
+__global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = ptx::smem_addr(smem);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kMiscOff);
+    Ctl c;
+    c.bars = sbase + (uint32_t)kBarOff;
+    c.abort = reinterpret_cast<volatile int*>(smem + kMiscOff + 4);
+    c.limit = p.wait_limit;
+    c.status = g_status;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kSlots; ++s) {
+            ptx::mbar_init(bar_addr(c, b_ring_full(s)), 1);
+            ptx::mbar_init(bar_addr(c, b_ring_empty(s)), 1);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_addr(c, b_s_full(b)), 1);
+            ptx::mbar_init(bar_addr(c, b_p_full(b)), 128);
+        }
+        ptx::mbar_init(bar_addr(c, b_o_done()), 1);
+        ptx::mbar_init(bar_addr(c, b_q_ready()), 1);
+        ptx::mbar_init(bar_addr(c, b_drain()), 1);
+        *c.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tm = *tmem_slot;
+    const Work w = work_of<CAUSAL>(p);
+    const uint32_t ring = sbase;
+
+    if (warp == kLoadWarp) {
+        if (lane == 0) {
+            const uint32_t count = 2u + 2u * (uint32_t)w.nkv;
+            uint32_t pos = 0;
+            for (; pos < count; ++pos) {
+                if (!wait(c, b_ring_empty(pos), ring_par(pos) ^ 1u, kRoleLoad)) break;
+                const uint32_t bar = bar_addr(c, b_ring_full(pos));
+                const CUtensorMap* map = pos < 2 ? &p.tmap_q : ((pos & 1u) ? &p.tmap_v : &p.tmap_k);
+                const int row = pos < 2 ? w.qt * kBM + (int)pos * 64 : (int)((pos - 2u) >> 1) * kBN;
+                const uint32_t dst = ring + (pos % kSlots) * (uint32_t)kTile;
+                ptx::mbar_arrive_expect_tx(bar, (uint32_t)kTile);
+#pragma unroll
+                for (int pc = 0; pc < 4; ++pc)
+                    ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, row, w.bh);
+            }
+            for (uint32_t i = (pos > (uint32_t)kSlots ? pos - kSlots : 0u); i < pos; ++i)
+                wait_drain(bar_addr(c, b_ring_full(i)), ring_par(i), c.limit);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        constexpr uint32_t id_qk = make_idesc(kBM, kBN, false, F16);
+        constexpr uint32_t id_pv = make_idesc(kBM, D, true, F16);
+        auto kdesc = [&](uint32_t pos) {   // K-major 64 x 256 tile
+            return sw128_desc(ring + (pos % kSlots) * (uint32_t)kTile, 16, 1024);
+        };
+        auto vdesc = [&](uint32_t pos) {   // the same tile read as the MN-major operand
+            return sw128_desc(ring + (pos % kSlots) * (uint32_t)kTile, kPanel64, 1024);
+        };
+        // S(j) = Q K_j^T into buffer j % 2; K_j is then done
+        auto issue_s = [&](int j) -> bool {
+            const uint32_t pos = pos_k(j), b = (uint32_t)j & 1u;
+            if (!wait_warp(c, b_ring_full(pos), ring_par(pos), kRoleMma)) return false;
+            ptx::tc_fence_after();
+            const uint64_t kd = kdesc(pos);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::mma_ts_elect(tm + kColS + 64u * b, tm + kColQ + (uint32_t)kk * 8u,
+                                  kd + (((uint64_t)(kk / 4) * kPanel64 + (uint64_t)(kk % 4) * 32u) >> 4),
+                                  id_qk, kk > 0 ? 1u : 0u);
+            ptx::mma_commit_elect(bar_addr(c, b_s_full(b)));
+            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(pos)));
+            return true;
+        };
+        if (!wait_warp(c, b_q_ready(), 0, kRoleMma)) goto mma_out;
+        ptx::tc_fence_after();
+        if (!issue_s(0)) goto mma_out;
+        if (w.nkv > 1 && !issue_s(1)) goto mma_out;
+        for (int j = 0; j < w.nkv; ++j) {
+            const uint32_t b = (uint32_t)j & 1u, vpos = pos_v(j);
+            if (!wait_warp(c, b_p_full(b), (uint32_t)(j >> 1) & 1u, kRoleMma)) goto mma_out;
+            if (!wait_warp(c, b_ring_full(vpos), ring_par(vpos), kRoleMma)) goto mma_out;
+            ptx::tc_fence_after();
+            const uint64_t vd = vdesc(vpos);
+#pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+                ptx::mma_ts_elect(tm + kColO, tm + kColS + 64u * b + (uint32_t)kk * 8u,
+                                  vd + (uint64_t)((kk * 2048) >> 4), id_pv,
+                                  (j > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit_elect(bar_addr(c, b_o_done()));
+            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(vpos)));
+            if (j + 2 < w.nkv && !issue_s(j + 2)) goto mma_out;
+        }
+    mma_out:
+        ptx::mma_commit_elect(bar_addr(c, b_drain()));
+        wait_drain(bar_addr(c, b_drain()), 0, c.limit);
+        __syncwarp();
+    } else {
+        // softmax: thread = query row r (TMEM lane r)
+        const int r = warp * 32 + lane;
+        const int i = w.qt * kBM + r;
+        const int limit = CAUSAL ? min(i + 1, p.n) : p.n;      // visible keys: key < limit
+        const uint32_t tl = (uint32_t)(warp * 32) << 16;
+        const float sl2 = p.scale_log2;
+        {
+            // Q row r into TMEM as 16-bit pairs; the two ring slots are then released
+            const bool ok = wait_warp(c, b_ring_full(0), 0, kRoleSoftmax) &&
+                            wait_warp(c, b_ring_full(1), 0, kRoleSoftmax);
+            if (ok) {
+                const int lr = r & 63;
+                const uint32_t src = ring + (uint32_t)(r >> 6) * kTile + (uint32_t)lr * 128u;
+#pragma unroll
+                for (int pc = 0; pc < 4; ++pc) {
+                    uint32_t q[32];
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 v = ptx::ld_shared_v4(src + (uint32_t)pc * kPanel64 +
+                                                          (uint32_t)((cc ^ (lr & 7)) * 16));
+                        q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
+                    }
+                    ptx::tmem_st32(tm + tl + kColQ + 32u * (uint32_t)pc, q);
+                }
+                ptx::tmem_wait_st();
+            }
+            ptx::tc_fence_before();
+            if (!sm_barrier_and(ok)) goto sm_out;
+            if (threadIdx.x == 0) {
+                ptx::mbar_arrive(bar_addr(c, b_ring_empty(0)));
+                ptx::mbar_arrive(bar_addr(c, b_ring_empty(1)));
+                ptx::mbar_arrive(bar_addr(c, b_q_ready()));
+            }
+        }
+        {
+            float m_run = -INFINITY, l_run = 0.0f;   // reference max (log2 units) and row sum
+            for (int j = 0; j < w.nkv; ++j) {
+                const uint32_t b = (uint32_t)j & 1u;
+                const uint32_t tS = tm + tl + kColS + 64u * b;
+                if (!wait_warp(c, b_s_full(b), (uint32_t)(j >> 1) & 1u, kRoleSoftmax)) goto sm_out;
+                ptx::tc_fence_after();
+                uint32_t s[64];
+                ptx::tmem_ld64_wait(tS, s);
+                const int key0 = j * kBN;
+                const bool mask = __any_sync(0xFFFFFFFFu, key0 + kBN > limit);
+                uint32_t pk[32];
+                const float alpha =
+                    mask ? softmax_step<true, F16>(s, key0, limit, sl2, m_run, l_run, pk)
+                         : softmax_step<false, F16>(s, key0, limit, sl2, m_run, l_run, pk);
+                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    // The reference rose: O += P(j-1) V_{j-1} must be complete, then this
+                    // row of O is rescaled in TMEM.  (O += P(j-2) V is already complete: S(j)
+                    // was issued after it, so the parity wait below cannot be two phases
+                    // behind.)
+                    if (!wait_warp(c, b_o_done(), (uint32_t)(j - 1) & 1u, kRoleSoftmax)) goto sm_out;
+                    ptx::tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)cc * 32u, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+                        ptx::tmem_st32(tm + tl + kColO + (uint32_t)cc * 32u, o);
+                    }
+                }
+                __syncwarp();
+                ptx::tmem_st32(tS, pk);   // P over this buffer's first 32 columns
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar_addr(c, b_p_full(b)));
+            }
+            // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.
+            // A parity wait is only sound while the barrier is at most one phase behind the
+            // awaited one.  Here O += P(nkv-3) V is known complete (S(nkv-1) was issued
+            // after it), so wait for the last two products one at a time.
+            if (w.nkv >= 2 && !wait_warp(c, b_o_done(), (uint32_t)(w.nkv - 2) & 1u, kRoleSoftmax))
+                goto sm_out;
+            if (!wait_warp(c, b_o_done(), (uint32_t)(w.nkv - 1) & 1u, kRoleSoftmax)) goto sm_out;
+            ptx::tc_fence_after();
+            const float inv = 1.0f / l_run;
+            const uint32_t stage = sbase + (uint32_t)kStageOff + (uint32_t)warp * 4096u;
+            uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)w.bh * p.n * D;
+            const int row0 = w.qt * kBM + warp * 32;
+#pragma unroll 1
+            for (int pc = 0; pc < D / 64; ++pc) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)(pc * 64 + h * 32), o);
+                    uint32_t wv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) wv[e] = pack2<F16>(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint32_t chunk = (uint32_t)(h * 4 + e) ^ (uint32_t)(lane & 7);
+                        ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, wv[4 * e],
+                                          wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+                    }
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = 4 * k + (lane >> 3);
+                    const int ch = lane & 7;
+                    const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)rr * 128u +
+                                                      (uint32_t)((ch ^ (rr & 7)) * 16));
+                    if (row0 + rr < p.n)
+                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + rr) * D + pc * 64 + ch * 8) = v;
+                }
+                __syncwarp();
+            }
+            if (i < p.n) p.lse[(size_t)w.bh * p.n + i] = (m_run + log2f(l_run)) * kLn2;
+        }
+    sm_out:;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tm, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t tc256_prepare(bool causal, bool f16) {
+    auto set = [](const void* fn) {
+        return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    };
+    if (causal) return f16 ? set((const void*)fa_tc256_kernel<true, true>)
+                           : set((const void*)fa_tc256_kernel<true, false>);
+    return f16 ? set((const void*)fa_tc256_kernel<false, true>)
+               : set((const void*)fa_tc256_kernel<false, false>);
+}
+
+cudaError_t tc256_launch(bool causal, bool f16, const TcParams& p, cudaStream_t stream) {
+    const long long ctas = (long long)p.bh * ((p.n + kBM - 1) / kBM);
+    if (ctas < 1 || ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)ctas);
+    if (causal) {
+        if (f16) fa_tc256_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        else fa_tc256_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    } else {
+        if (f16) fa_tc256_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        else fa_tc256_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t tc256_status_read_reset(uint32_t out[4]) {
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int) * 4);
+    if (e != cudaSuccess) return e;
+    const unsigned int zero[4] = {0, 0, 0, 0};
+    return cudaMemcpyToSymbol(g_status, zero, sizeof(zero));
+}
+
+}  // namespace fa

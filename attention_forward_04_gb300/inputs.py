@@ -51,7 +51,7 @@ class Workload:
 
 TORCH_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}
 
-# The five workloads; seeds are 1000*c + {0,1,2} for workload number c.
+# The workloads; seeds are 1000*c + {0,1,2} for workload number c.
 WORKLOADS = {
     "fp32_b1h1n256d64": Workload("fp32_b1h1n256d64", 1, 1, 256, 64, "fp32", False, 1000),
     "bf16_b2h8n1024d64": Workload("bf16_b2h8n1024d64", 2, 8, 1024, 64, "bf16", False, 2000),
@@ -62,6 +62,11 @@ WORKLOADS = {
                                         False, 5000, 2.0),
     "bf16_b1h32n16384d128_x2_causal": Workload("bf16_b1h32n16384d128_x2_causal", 1, 32, 16384,
                                                128, "bf16", True, 5000, 2.0),
+    # head dimension 256 (the largest head dimension the pages name), same FLOPs as the
+    # headline workload
+    "bf16_b4h8n4096d256": Workload("bf16_b4h8n4096d256", 4, 8, 4096, 256, "bf16", False, 6000),
+    "bf16_b4h8n4096d256_causal": Workload("bf16_b4h8n4096d256_causal", 4, 8, 4096, 256, "bf16",
+                                          True, 6000),
 }
 
 # The workload the throughput metric is quoted on.

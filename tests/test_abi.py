@@ -63,7 +63,8 @@ def call(lib, q=BASE, k=BASE + SZ, v=BASE + 2 * SZ, o=BASE + 3 * SZ, lse=BASE + 
     (dict(causal=2), INVALID), (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID), (dict(scale=-0.5), INVALID),
     (dict(dtype=7), INVALID), (dict(dtype=-1), INVALID),
-    (dict(D=96), UNSUPPORTED), (dict(D=32), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=32), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
+    (dict(D=256, dtype=0), UNSUPPORTED),          # D = 256: 16-bit storage only
     (dict(q=BASE + 8), MISALIGNED), (dict(o=BASE + 3 * SZ + 4), MISALIGNED),
     (dict(lse=BASE + 4 * SZ + 2), MISALIGNED),
     (dict(o=BASE), INVALID),                       # o aliases q
@@ -100,6 +101,10 @@ def test_varlen_and_bnhd_argument_checks(lib):
                            2, 128, 4, 96, 0.1, 0, 1, None) == UNSUPPORTED
     assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
                            2, 0, 4, 128, 0.1, 0, 1, None) == INVALID
+    # D = 256 is served for the [B, H, N, D] layout only
+    assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
+                           2, 128, 4, 256, 0.1, 0, 1, None) == UNSUPPORTED
+    assert varlen(D=256) == UNSUPPORTED
 
 
 def test_watchdog_control_validation(lib):

@@ -139,6 +139,31 @@ def test_non_default_stream():
     assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16")
 
 
+# ------------------------------------------------------------ head dimension 256
+EDGE_N_256 = [1, 17, 63, 64, 65, 127, 128, 129, 300, 640, 1000]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", EDGE_N_256)
+def test_d256_bf16_edge_shapes(N, causal):
+    q, k, v = make_shape(1, 2, N, 256, "bf16", seed=N * 5 + 256)
+    full_compare(q, k, v, 1.0 / 16.0, causal, "bf16", "D=256 N=%d causal=%d" % (N, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 200, 513])
+def test_d256_fp16(N, causal):
+    q, k, v = make_shape(2, 1, N, 256, "fp16", seed=N * 3 + 257)
+    full_compare(q, k, v, 1.0 / 16.0, causal, "fp16", "fp16 D=256 N=%d causal=%d" % (N, causal))
+
+
+def test_d256_large_scores_force_rescales():
+    # Q, K x4: the running maximum rises often, so O is rescaled in TMEM repeatedly
+    q, k, v = make_shape(1, 2, 1000, 256, "bf16", seed=77, qk_mult=4.0)
+    for causal in (False, True):
+        full_compare(q, k, v, 1.0 / 16.0, causal, "bf16", "D=256 x4 causal=%d" % causal)
+
+
 # ------------------------------------------------------------ the five workloads
 def sampled_rows(N, seed, extra=24):
     rows = {0, 1, N - 1, N - 2}
@@ -157,7 +182,8 @@ def test_small_workloads_full(name):
 
 
 @pytest.mark.parametrize("name", ["bf16_b4h16n4096d128", "bf16_b8h32n4096d128_causal",
-                                  "bf16_b1h32n16384d128_x2", "bf16_b1h32n16384d128_x2_causal"])
+                                  "bf16_b1h32n16384d128_x2", "bf16_b1h32n16384d128_x2_causal",
+                                  "bf16_b4h8n4096d256", "bf16_b4h8n4096d256_causal"])
 def test_full_size_workloads_sampled(name):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)
