@@ -29,8 +29,8 @@ struct DeviceInfo {
     cudaError_t err = cudaSuccess;
     int sm_count = 0;
     int major = 0, minor = 0;
-    std::once_flag prepared[2][2][2];  // [D==128][causal][f16]
-    cudaError_t prepare_err[2][2][2] = {};
+    std::once_flag prepared[3][2][2];  // [D = 32, 64, 128][causal][f16]
+    cudaError_t prepare_err[3][2][2] = {};
     std::once_flag bwd_prepared[2][2][2];
     cudaError_t bwd_prepare_err[2][2][2] = {};
     std::once_flag prepared256[2][2];  // [causal][f16]
@@ -66,6 +66,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 // 64 head-dim values (128 bytes, 128-byte swizzle), which the tensor-core kernel expects.
 //   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, rows, 1} (rows = 128, or 64 for the
 //   D = 256 kernel); rows past N read as zero.
+//   D = 32: the box is 32 values wide and lands as 64-byte rows with the 64-byte swizzle.
 //   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, 128}; tokens past T read
 //   as zero (tokens of the next packed sequence are masked by the kernel instead).
 bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int64_t n, int64_t h,
@@ -76,16 +77,17 @@ bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int6
     if (layout == 0) {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)n; dims[2] = (cuuint64_t)bh;
         strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(n * d * 2);
-        box[0] = 64; box[1] = rows; box[2] = 1;
+        box[0] = d < 64 ? (cuuint32_t)d : 64; box[1] = rows; box[2] = 1;
     } else {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)h; dims[2] = (cuuint64_t)t;
         strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(h * d * 2);
-        box[0] = 64; box[1] = 1; box[2] = 128;
+        box[0] = d < 64 ? (cuuint32_t)d : 64; box[1] = 1; box[2] = 128;
     }
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    d < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -164,7 +166,7 @@ int forward(const Request& r) {
     if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
     if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
+    if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
     // D = 256: 16-bit storage, [B, H, N, D] layout only
     if (r.D == 256 && (r.dtype == FA_FP32 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;
@@ -222,7 +224,7 @@ int forward(const Request& r) {
     }
 
     const bool f16 = r.dtype == FA_FP16;
-    const int di128 = r.D == 128, dic = r.causal != 0, dif = f16;
+    const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = f16;
     if (r.D == 256) {
         std::call_once(di.prepared256[dic][dif],
                        [&] { di.prepare256_err[dic][dif] = fa::tc256_prepare(dic, f16); });
@@ -245,10 +247,10 @@ int forward(const Request& r) {
         e = fa::tc256_launch(dic, f16, p, st);
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch (D = 256)");
     }
-    std::call_once(di.prepared[di128][dic][dif],
-                   [&] { di.prepare_err[di128][dic][dif] = fa::tc_prepare((int)r.D, dic, f16); });
-    if (di.prepare_err[di128][dic][dif] != cudaSuccess)
-        return fail_cuda(di.prepare_err[di128][dic][dif], "cudaFuncSetAttribute");
+    std::call_once(di.prepared[dix][dic][dif],
+                   [&] { di.prepare_err[dix][dic][dif] = fa::tc_prepare((int)r.D, dic, f16); });
+    if (di.prepare_err[dix][dic][dif] != cudaSuccess)
+        return fail_cuda(di.prepare_err[dix][dic][dif], "cudaFuncSetAttribute");
 
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
     if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");

@@ -149,6 +149,9 @@ cudaError_t launch(const float* q, const float* k, const float* v, float* o, flo
 cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, const float* v,
                         float* o, float* lse, int bh, const SliceLayout& g, float scale,
                         cudaStream_t stream) {
+    if (D == 32)
+        return causal ? launch<32, true>(q, k, v, o, lse, bh, g, scale, stream)
+                      : launch<32, false>(q, k, v, o, lse, bh, g, scale, stream);
     if (D == 64)
         return causal ? launch<64, true>(q, k, v, o, lse, bh, g, scale, stream)
                       : launch<64, false>(q, k, v, o, lse, bh, g, scale, stream);

@@ -68,6 +68,12 @@ __device__ unsigned int g_status[4];
 
 template <int D>
 struct Geo {
+    // Shared-memory rows: 64 head-dim values (128 bytes, 128-byte swizzle) per panel, or
+    // for D = 32 one panel of 64-byte rows (64-byte swizzle).
+    static constexpr int kPanelCols = D < 64 ? D : 64;
+    static constexpr int kRowBytes = kPanelCols * 2;
+    static constexpr int kPanelBytes = 128 * kRowBytes;        // 128 rows of one panel
+    static constexpr uint32_t kSBO = 8u * kRowBytes;            // 8-row group stride
     static constexpr int kPanels = D / kPanelCols;
     static constexpr int kTileBytes = kPanels * kPanelBytes;   // one 128 x D tile
     static constexpr int kSlots = (D == 128) ? 4 : 8;          // K/V ring depth
@@ -206,15 +212,26 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, const Item& it, i
 }
 
 // ----------------------------------------------------------------- MMA issue
+// Shared-memory descriptor of a tile with D-dependent rows: 128-byte swizzle (layout type
+// 2) for 128-byte rows, 64-byte swizzle (layout type 4) for the 64-byte rows of D = 32.
+template <int D>
+__device__ __forceinline__ uint64_t tile_desc(uint32_t saddr, uint32_t lbo) {
+    const uint64_t layout = Geo<D>::kRowBytes == 128 ? 2ull : 4ull;
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((Geo<D>::kSBO >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+
 // Descriptors are built once per buffer; a K step only adds a constant to the start
 // address field (addresses stay below 256 KB, so the 14-bit field never carries).
 // All lanes of the MMA warp execute these; one elected lane issues.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc,
                                          uint32_t idesc) {
+    using G = Geo<D>;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = ((uint64_t)(kk / 4) * kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
+        // 16 values = 32 bytes per K step inside a row; the next panel after 4 (128-byte rows)
+        const uint64_t off = ((uint64_t)(kk / 4) * G::kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
         ptx::mma_ss_elect(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
@@ -222,12 +239,14 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint6
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          uint32_t idesc, bool accumulate) {
+    using G = Geo<D>;
 #pragma unroll
     for (int kk = 0; kk < kBN / 16; ++kk) {
-        // V tile: rows = keys (K dimension), 128 B = 64 head-dim values per row (MN-major);
-        // 16 keys = 2048 B per K step; 64-column panels kPanelBytes apart (LBO).
-        ptx::mma_ts_elect(d_tmem, p_tmem + (uint32_t)kk * 8u, v_desc + (uint64_t)((kk * 2048) >> 4),
-                          idesc, (accumulate || kk > 0) ? 1u : 0u);
+        // V tile: rows = keys (K dimension), one row of head-dim values per key (MN-major);
+        // 16 keys = 16 rows per K step; panels kPanelBytes apart (LBO).
+        ptx::mma_ts_elect(d_tmem, p_tmem + (uint32_t)kk * 8u,
+                          v_desc + (uint64_t)((kk * 16 * G::kRowBytes) >> 4), idesc,
+                          (accumulate || kk > 0) ? 1u : 0u);
     }
 }
 
@@ -238,10 +257,10 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
     using G = Geo<D>;
     constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false, F16);
     constexpr uint32_t idesc_pv = make_idesc(kBM, D, true, F16);
-    const uint64_t dQ[2] = {sw128_desc(sbase, 16, 1024),
-                            sw128_desc(sbase + (uint32_t)G::kTileBytes, 16, 1024)};
-    const uint64_t dK0 = sw128_desc(sbase + (uint32_t)G::kKVOff, 16, 1024);       // K-major
-    const uint64_t dV0 = sw128_desc(sbase + (uint32_t)G::kKVOff, kPanelBytes, 1024);  // MN-major
+    const uint64_t dQ[2] = {tile_desc<D>(sbase, 16),
+                            tile_desc<D>(sbase + (uint32_t)G::kTileBytes, 16)};
+    const uint64_t dK0 = tile_desc<D>(sbase + (uint32_t)G::kKVOff, 16);                  // K-major
+    const uint64_t dV0 = tile_desc<D>(sbase + (uint32_t)G::kKVOff, (uint32_t)G::kPanelBytes);  // MN-major
     const uint32_t tS[2] = {tmem + G::col_s(0), tmem + G::col_s(1)};
     const uint32_t tP[2] = {tmem + G::col_p(0), tmem + G::col_p(1)};
     const uint32_t tO[2] = {tmem + G::col_o(0), tmem + G::col_o(1)};
@@ -339,7 +358,7 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                 tile_coords<MODE>(p, it, it.pair * 2 * kBM + t * kBM, c1, c2);
 #pragma unroll
                 for (int pc = 0; pc < G::kPanels; ++pc)
-                    ptx::tma_load_3d(sQ[t] + (uint32_t)pc * kPanelBytes, &p.tmap_q, fb, pc * kPanelCols,
+                    ptx::tma_load_3d(sQ[t] + (uint32_t)pc * G::kPanelBytes, &p.tmap_q, fb, pc * G::kPanelCols,
                                      c1, c2);
                 ++q_issued[t];
                 return true;
@@ -356,8 +375,8 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                         tile_coords<MODE>(p, it, j * kBN, c1, c2);
 #pragma unroll
                         for (int pc = 0; pc < G::kPanels; ++pc)
-                            ptx::tma_load_3d(slot(kv) + (uint32_t)pc * kPanelBytes, map, fb,
-                                             pc * kPanelCols, c1, c2);
+                            ptx::tma_load_3d(slot(kv) + (uint32_t)pc * G::kPanelBytes, map, fb,
+                                             pc * G::kPanelCols, c1, c2);
                     }
                     ++kv;
                     if (j == 0 && w == 0 && !load_q(1)) goto out;
@@ -513,6 +532,32 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +
                               (MODE == 0 ? (size_t)it.bh * (size_t)p.n * D
                                          : ((size_t)it.tok0 * p.heads + it.h) * D);
+            if constexpr (D == 32) {
+                // one 64-byte row per thread: 4 chunks staged, then 8 rows x 4 chunks per store
+                uint32_t o[32];
+                ptx::tmem_ld32_wait(tO, o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<F16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t chunk = (uint32_t)i ^ (uint32_t)(lane & 7);
+                    ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
+                                      w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = 8 * k + (lane >> 2);   // row within the warp's 32
+                    const int ch = lane & 3;             // 16-byte chunk within the 64-byte row
+                    const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u +
+                                                      (uint32_t)((ch ^ (r & 7)) * 16));
+                    if (row0 + r < (MODE == 0 ? p.n : it.len))
+                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * ostride + ch * 8) = v;
+                }
+                __syncwarp();
+            }
 #pragma unroll 1
             for (int pc = 0; pc < D / 64; ++pc) {
 #pragma unroll
@@ -660,15 +705,19 @@ int tc_units(int bh, int n, bool causal) {
     return u > 0x7FFFFFFFLL ? -1 : (int)u;
 }
 
-int tc_smem_bytes(int D) { return D == 64 ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes; }
+int tc_smem_bytes(int D) {
+    return D == 32 ? Geo<32>::kSmemBytes : D == 64 ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes;
+}
 
 cudaError_t tc_prepare(int D, bool causal, bool f16) {
+    if (D == 32) return dispatch<32>(causal, f16, 0, true, nullptr, 0, nullptr);
     return D == 64 ? dispatch<64>(causal, f16, 0, true, nullptr, 0, nullptr)
                    : dispatch<128>(causal, f16, 0, true, nullptr, 0, nullptr);
 }
 
 cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
                       cudaStream_t stream) {
+    if (D == 32) return dispatch<32>(causal, f16, p.layout, false, &p, grid, stream);
     return D == 64 ? dispatch<64>(causal, f16, p.layout, false, &p, grid, stream)
                    : dispatch<128>(causal, f16, p.layout, false, &p, grid, stream);
 }

@@ -67,6 +67,8 @@ WORKLOADS = {
     "bf16_b4h8n4096d256": Workload("bf16_b4h8n4096d256", 4, 8, 4096, 256, "bf16", False, 6000),
     "bf16_b4h8n4096d256_causal": Workload("bf16_b4h8n4096d256_causal", 4, 8, 4096, 256, "bf16",
                                           True, 6000),
+    # head dimension 32 (the "第 13 课" exercise's d), same FLOPs as the headline workload
+    "bf16_b8h32n4096d32": Workload("bf16_b8h32n4096d32", 8, 32, 4096, 32, "bf16", False, 7000),
 }
 
 # The workload the throughput metric is quoted on.

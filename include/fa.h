@@ -48,7 +48,7 @@ typedef enum {
  *   lse     : device pointer, [B, H, N] contiguous fp32; written fully.
  *   B, H, N : >= 1.  B*H < 2^31 and N < 2^31.  Any N is accepted (a ragged last tile is
  *             masked; keys >= N never contribute).
- *   D       : head dimension, 64 or 128.
+ *   D       : head dimension: 32, 64 or 128; 256 for bf16/fp16 storage (fa_fwd only).
  *   scale   : finite, >= 0 (normally 1/sqrt(D)).
  *   causal  : 0 = all keys; 1 = key j <= query i (square N x N).
  *   dtype   : an fa_dtype value.

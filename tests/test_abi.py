@@ -63,7 +63,7 @@ def call(lib, q=BASE, k=BASE + SZ, v=BASE + 2 * SZ, o=BASE + 3 * SZ, lse=BASE + 
     (dict(causal=2), INVALID), (dict(scale=float("nan")), INVALID),
     (dict(scale=float("inf")), INVALID), (dict(scale=-0.5), INVALID),
     (dict(dtype=7), INVALID), (dict(dtype=-1), INVALID),
-    (dict(D=96), UNSUPPORTED), (dict(D=32), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=48), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
     (dict(D=256, dtype=0), UNSUPPORTED),          # D = 256: 16-bit storage only
     (dict(q=BASE + 8), MISALIGNED), (dict(o=BASE + 3 * SZ + 4), MISALIGNED),
     (dict(lse=BASE + 4 * SZ + 2), MISALIGNED),

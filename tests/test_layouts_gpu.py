@@ -33,7 +33,7 @@ def check(o, lse, o_ref, lse_ref, dtype, what):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp32"])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 def test_bnhd_matches_oracle(D, causal, dtype):
     B, N, H = 2, 333, 3
     q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in make_shape(B, H, N, D, dtype, seed=D + 5))
@@ -72,7 +72,7 @@ def run_varlen(lengths, H, D, dtype, causal, seed):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("mix", range(len(LENGTH_MIXES)))
 def test_varlen_bf16(mix, D, causal):
     run_varlen(LENGTH_MIXES[mix], 2, D, "bf16", causal, seed=mix * 10 + D)

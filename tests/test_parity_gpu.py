@@ -139,6 +139,27 @@ def test_non_default_stream():
     assert_close(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, "bf16")
 
 
+# ------------------------------------------------------------ head dimension 32
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 17, 127, 128, 129, 256, 300, 1000])
+def test_d32_bf16_edge_shapes(N, causal):
+    q, k, v = make_shape(1, 2, N, 32, "bf16", seed=N * 7 + 32)
+    full_compare(q, k, v, 1.0 / math.sqrt(32), causal, "bf16", "D=32 N=%d causal=%d" % (N, causal))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "fp32"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d32_other_dtypes(dtype, causal):
+    q, k, v = make_shape(2, 1, 300, 32, dtype, seed=32 + causal)
+    full_compare(q, k, v, 1.0 / math.sqrt(32), causal, dtype, "%s D=32 causal=%d" % (dtype, causal))
+
+
+def test_d32_large_scores_force_rescales():
+    q, k, v = make_shape(1, 2, 700, 32, "bf16", seed=33, qk_mult=4.0)
+    for causal in (False, True):
+        full_compare(q, k, v, 1.0 / math.sqrt(32), causal, "bf16", "D=32 x4 causal=%d" % causal)
+
+
 # ------------------------------------------------------------ head dimension 256
 EDGE_N_256 = [1, 17, 63, 64, 65, 127, 128, 129, 300, 640, 1000]
 
@@ -183,7 +204,8 @@ def test_small_workloads_full(name):
 
 @pytest.mark.parametrize("name", ["bf16_b4h16n4096d128", "bf16_b8h32n4096d128_causal",
                                   "bf16_b1h32n16384d128_x2", "bf16_b1h32n16384d128_x2_causal",
-                                  "bf16_b4h8n4096d256", "bf16_b4h8n4096d256_causal"])
+                                  "bf16_b4h8n4096d256", "bf16_b4h8n4096d256_causal",
+                                  "bf16_b8h32n4096d32"])
 def test_full_size_workloads_sampled(name):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)
