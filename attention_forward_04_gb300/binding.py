@@ -31,6 +31,9 @@ SIGNATURES = {
     "fa_fwd_varlen": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                  _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
                                  _c.c_int64, _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_fwd_fp8": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                              _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_float,
+                              _c.c_int, _c.c_float, _c.c_float, _c.c_float, _c.c_void_p]),
     "fa_bwd_workspace_bytes": (_c.c_int64, [_c.c_int64, _c.c_int64, _c.c_int64]),
     "fa_bwd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                           _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
@@ -128,6 +131,33 @@ def fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
     with torch.cuda.device(q.device):
         _check(fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                        B, H, N, D, scale, causal, _dtype_code(q), handle))
+    return out, lse
+
+
+def fwd_fp8(q, k, v, q_descale, k_descale, v_descale, scale=None, causal=False, out=None,
+            lse=None, stream=None):
+    """Forward pass on fp8 e4m3 inputs (fa_fwd_fp8).
+
+    q, k, v: contiguous CUDA tensors [B, H, N, D] of torch.float8_e4m3fn; the descale factors
+    are the per-tensor dequantisation multipliers.  Returns (o [B, H, N, D] bf16, lse fp32)."""
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must share one [B, H, N, D] shape")
+    for t in (q, k, v):
+        if t.dtype != torch.float8_e4m3fn or not t.is_contiguous():
+            raise TypeError("q, k, v must be contiguous torch.float8_e4m3fn tensors")
+    B, H, N, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=q.device) if out is None else out
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                             out.data_ptr(), lse.data_ptr(), B, H, N, D,
+                                             float(scale), int(causal), float(q_descale),
+                                             float(k_descale), float(v_descale),
+                                             _stream_handle(q, stream))))
     return out, lse
 
 

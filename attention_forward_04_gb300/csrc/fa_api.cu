@@ -29,8 +29,8 @@ struct DeviceInfo {
     cudaError_t err = cudaSuccess;
     int sm_count = 0;
     int major = 0, minor = 0;
-    std::once_flag prepared[3][2][2];  // [D = 32, 64, 128][causal][f16]
-    cudaError_t prepare_err[3][2][2] = {};
+    std::once_flag prepared[3][2][3];  // [D = 32, 64, 128][causal][bf16, fp16, fp8]
+    cudaError_t prepare_err[3][2][3] = {};
     std::once_flag bwd_prepared[2][2][2];
     cudaError_t bwd_prepare_err[2][2][2] = {};
     std::once_flag prepared256[2][2];  // [causal][f16]
@@ -70,25 +70,32 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 //   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, 128}; tokens past T read
 //   as zero (tokens of the next packed sequence are masked by the kernel instead).
 bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int64_t n, int64_t h,
-                int64_t t, int64_t d, bool f16, PFN_cuTensorMapEncodeTiled_v12000 fn,
+                int64_t t, int64_t d, int et, PFN_cuTensorMapEncodeTiled_v12000 fn,
                 cuuint32_t rows = 128) {
+    // et: 0 bf16, 1 fp16, 2 fp8 e4m3 (raw bytes).  The box spans one panel: 128-byte rows
+    // (128-byte swizzle), or whole rows of 64 bytes (64-byte swizzle).
+    const int64_t eb = et == 2 ? 1 : 2;
+    const int64_t row_bytes = d * eb < 128 ? d * eb : 128;
+    const cuuint32_t box0 = (cuuint32_t)(row_bytes / eb);
     cuuint64_t dims[3], strides[2];
     cuuint32_t box[3];
     if (layout == 0) {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)n; dims[2] = (cuuint64_t)bh;
-        strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(n * d * 2);
-        box[0] = d < 64 ? (cuuint32_t)d : 64; box[1] = rows; box[2] = 1;
+        strides[0] = (cuuint64_t)(d * eb); strides[1] = (cuuint64_t)(n * d * eb);
+        box[0] = box0; box[1] = rows; box[2] = 1;
     } else {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)h; dims[2] = (cuuint64_t)t;
-        strides[0] = (cuuint64_t)(d * 2); strides[1] = (cuuint64_t)(h * d * 2);
-        box[0] = d < 64 ? (cuuint32_t)d : 64; box[1] = 1; box[2] = 128;
+        strides[0] = (cuuint64_t)(d * eb); strides[1] = (cuuint64_t)(h * d * eb);
+        box[0] = box0; box[1] = 1; box[2] = 128;
     }
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
-                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    d < 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUtensorMapDataType type = et == 2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                     : et == 1 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult r = fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    row_bytes < 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -101,7 +108,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
-int fa_version(void) { return 120; }
+int fa_version(void) { return 130; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -152,9 +159,12 @@ struct Request {
     int layout;            // 0: [B, H, N, D]; 1: token-major [T, H, D]
     const int* cu;         // packed sequences: [B + 1] token offsets (device), else null
     float scale;
-    int causal, dtype;
+    int causal, dtype;     // dtype: an fa_dtype, or kFp8 (e4m3 in, bf16 out)
     void* stream;
+    float descale[3];      // fp8: dequantisation factors of Q, K, V (else 1)
 };
+
+constexpr int kFp8 = 3;
 
 int forward(const Request& r) {
     // ---- argument checks: no CUDA call before these pass
@@ -165,21 +175,29 @@ int forward(const Request& r) {
         return FA_ERR_INVALID_ARG;
     if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
-    if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16 && r.dtype != kFp8)
+        return FA_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+        if (!std::isfinite(r.descale[i]) || !(r.descale[i] > 0.0f)) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(r.scale * r.descale[0] * r.descale[1])) return FA_ERR_INVALID_ARG;
     if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
     // D = 256: 16-bit storage, [B, H, N, D] layout only
-    if (r.D == 256 && (r.dtype == FA_FP32 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
+    if (r.D == 256 && (r.dtype == FA_FP32 || r.dtype == kFp8 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
+    // fp8: D = 64 or 128, [B, H, N, D] layout only
+    if (r.dtype == kFp8 && ((r.D != 64 && r.D != 128) || r.layout != 0)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;
-    const size_t esize = r.dtype == FA_FP32 ? 4 : 2;
+    const size_t esize = r.dtype == FA_FP32 ? 4 : r.dtype == kFp8 ? 1 : 2;   // Q, K, V
+    const size_t osize = r.dtype == FA_FP32 ? 4 : 2;                          // O
     const int64_t rows = r.layout == 0 ? BH * r.N : r.T * r.H;   // rows of D elements
     if (rows / r.H != (r.layout == 0 ? r.B * r.N : r.T)) return FA_ERR_INVALID_ARG;
     const size_t tbytes = (size_t)rows * (size_t)r.D * esize;
+    const size_t obytes = (size_t)rows * (size_t)r.D * osize;
     const size_t lbytes = (size_t)(r.cu ? r.T * r.H : BH * r.N) * sizeof(float);
-    if (tbytes / esize / (size_t)r.D != (size_t)rows) return FA_ERR_INVALID_ARG;
-    if (overlaps(r.o, tbytes, r.q, tbytes) || overlaps(r.o, tbytes, r.k, tbytes) ||
-        overlaps(r.o, tbytes, r.v, tbytes) || overlaps(r.lse, lbytes, r.q, tbytes) ||
+    if (obytes / osize / (size_t)r.D != (size_t)rows) return FA_ERR_INVALID_ARG;
+    if (overlaps(r.o, obytes, r.q, tbytes) || overlaps(r.o, obytes, r.k, tbytes) ||
+        overlaps(r.o, obytes, r.v, tbytes) || overlaps(r.lse, lbytes, r.q, tbytes) ||
         overlaps(r.lse, lbytes, r.k, tbytes) || overlaps(r.lse, lbytes, r.v, tbytes) ||
-        overlaps(r.lse, lbytes, r.o, tbytes))
+        overlaps(r.lse, lbytes, r.o, obytes))
         return FA_ERR_INVALID_ARG;
     for (const void* ptr : {r.q, r.k, r.v, static_cast<const void*>(r.o)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_MISALIGNED;
@@ -224,7 +242,8 @@ int forward(const Request& r) {
     }
 
     const bool f16 = r.dtype == FA_FP16;
-    const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = f16;
+    const int et = r.dtype == kFp8 ? 2 : f16 ? 1 : 0;   // element type of Q, K, V
+    const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = et;
     if (r.D == 256) {
         std::call_once(di.prepared256[dic][dif],
                        [&] { di.prepare256_err[dic][dif] = fa::tc256_prepare(dic, f16); });
@@ -234,21 +253,22 @@ int forward(const Request& r) {
         if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
         fa::TcParams p;
         std::memset(&p, 0, sizeof(p));
-        if (!encode_map(&p.tmap_q, r.q, 0, BH, r.N, r.H, r.T, r.D, f16, fn, 64) ||
-            !encode_map(&p.tmap_k, r.k, 0, BH, r.N, r.H, r.T, r.D, f16, fn, 64) ||
-            !encode_map(&p.tmap_v, r.v, 0, BH, r.N, r.H, r.T, r.D, f16, fn, 64))
+        if (!encode_map(&p.tmap_q, r.q, 0, BH, r.N, r.H, r.T, r.D, et, fn, 64) ||
+            !encode_map(&p.tmap_k, r.k, 0, BH, r.N, r.H, r.T, r.D, et, fn, 64) ||
+            !encode_map(&p.tmap_v, r.v, 0, BH, r.N, r.H, r.T, r.D, et, fn, 64))
             return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
         p.o = r.o;
         p.lse = r.lse;
         p.n = (int)r.N;
         p.bh = (int)BH;
         p.scale_log2 = r.scale * 1.4426950408889634f;
+        p.o_scale = 1.0f;
         p.wait_limit = g_wait_limit.load();
         e = fa::tc256_launch(dic, f16, p, st);
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch (D = 256)");
     }
     std::call_once(di.prepared[dix][dic][dif],
-                   [&] { di.prepare_err[dix][dic][dif] = fa::tc_prepare((int)r.D, dic, f16); });
+                   [&] { di.prepare_err[dix][dic][dif] = fa::tc_prepare((int)r.D, dic, et); });
     if (di.prepare_err[dix][dic][dif] != cudaSuccess)
         return fail_cuda(di.prepare_err[dix][dic][dif], "cudaFuncSetAttribute");
 
@@ -256,9 +276,9 @@ int forward(const Request& r) {
     if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
     fa::TcParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, f16, fn) ||
-        !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, f16, fn) ||
-        !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, f16, fn))
+    if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
+        !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
+        !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, et, fn))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     p.o = r.o;
     p.lse = r.lse;
@@ -271,11 +291,12 @@ int forward(const Request& r) {
     p.npairs = (int)((r.N + 255) / 256);
     p.nkv = (int)((r.N + 127) / 128);
     p.units = units;
-    p.scale_log2 = r.scale * 1.4426950408889634f;
+    p.scale_log2 = r.scale * r.descale[0] * r.descale[1] * 1.4426950408889634f;
+    p.o_scale = r.descale[2];
     p.wait_limit = g_wait_limit.load();
     p.inject_stall = g_inject_stall.load();
     const int grid = units < di.sm_count ? units : di.sm_count;
-    e = fa::tc_launch((int)r.D, dic, f16, p, grid, st);
+    e = fa::tc_launch((int)r.D, dic, et, p, grid, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch");
 }
 
@@ -285,13 +306,25 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B, int64_t H,
            int64_t N, int64_t D, float scale, int causal, int dtype, void* stream) {
-    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 0, nullptr, scale, causal, dtype, stream};
+    if (dtype == kFp8) return FA_ERR_INVALID_ARG;   // e4m3 input only through fa_fwd_fp8
+    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 0, nullptr, scale, causal, dtype, stream,
+                    {1.0f, 1.0f, 1.0f}};
+    return forward(r);
+}
+
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
+               int64_t H, int64_t N, int64_t D, float scale, int causal, float q_descale,
+               float k_descale, float v_descale, void* stream) {
+    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 0, nullptr, scale, causal, kFp8, stream,
+                    {q_descale, k_descale, v_descale}};
     return forward(r);
 }
 
 int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse, int64_t B,
                 int64_t N, int64_t H, int64_t D, float scale, int causal, int dtype, void* stream) {
-    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 1, nullptr, scale, causal, dtype, stream};
+    if (dtype == kFp8) return FA_ERR_INVALID_ARG;   // e4m3 input only through fa_fwd_fp8
+    const Request r{q, k, v, o, lse, B, H, N, D, B * N, 1, nullptr, scale, causal, dtype, stream,
+                    {1.0f, 1.0f, 1.0f}};
     return forward(r);
 }
 
@@ -367,10 +400,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
 
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!encode_map(&p.tmap_q, q, 0, BH, N, H, B * N, D, f16, fn) ||
-        !encode_map(&p.tmap_k, k, 0, BH, N, H, B * N, D, f16, fn) ||
-        !encode_map(&p.tmap_v, v, 0, BH, N, H, B * N, D, f16, fn) ||
-        !encode_map(&p.tmap_do, dout, 0, BH, N, H, B * N, D, f16, fn))
+    const int et = f16 ? 1 : 0;
+    if (!encode_map(&p.tmap_q, q, 0, BH, N, H, B * N, D, et, fn) ||
+        !encode_map(&p.tmap_k, k, 0, BH, N, H, B * N, D, et, fn) ||
+        !encode_map(&p.tmap_v, v, 0, BH, N, H, B * N, D, et, fn) ||
+        !encode_map(&p.tmap_do, dout, 0, BH, N, H, B * N, D, et, fn))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     p.lse = lse;
     p.delta = static_cast<const float*>(workspace);
@@ -393,8 +427,9 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
                   const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total,
                   int64_t H, int64_t D, float scale, int causal, int dtype, void* stream) {
     if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+    if (dtype == kFp8) return FA_ERR_INVALID_ARG;   // e4m3 input only through fa_fwd_fp8
     const Request r{q, k, v, o, lse, batch, H, max_seqlen, D, total, 1, cu_seqlens, scale, causal,
-                    dtype, stream};
+                    dtype, stream, {1.0f, 1.0f, 1.0f}};
     return forward(r);
 }
 

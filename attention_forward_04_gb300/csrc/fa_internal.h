@@ -24,7 +24,8 @@ struct TcParams {
     int npairs;          // ceil(N / 256): query-tile pairs per slice (at most)
     int nkv;             // ceil(N / 128): key/value tiles per slice (at most)
     int units;           // work units of the persistent schedule
-    float scale_log2;    // scale * log2(e)
+    float scale_log2;    // scale * log2(e) (times the Q and K dequantisation factors for fp8)
+    float o_scale;       // factor applied to O at the end: V's dequantisation factor (fp8), else 1
     unsigned long long wait_limit;  // cycles a single wait may spin before giving up
     int inject_stall;    // failure-detection test hook (see fa_set_watchdog)
 };
@@ -65,10 +66,11 @@ int tc_units(int bh, int n, bool causal);
 int tc_smem_bytes(int D);
 
 // One-time per device: raise the dynamic shared-memory limit of the kernel instance.
-cudaError_t tc_prepare(int D, bool causal, bool f16);
+// et: element type of Q, K, V: 0 bf16, 1 fp16, 2 fp8 e4m3 (D = 64 or 128, layout 0 only).
+cudaError_t tc_prepare(int D, bool causal, int et);
 
 // Launch the tensor-core kernel with `grid` persistent CTAs on `stream`.
-cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
+cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, int grid,
                       cudaStream_t stream);
 
 // Copy the device status word (4 words) of the tensor-core kernels to `out` and clear it.

@@ -60,23 +60,30 @@ constexpr uint32_t kTmemCols = 512;
 // The running reference is raised only when a tile max exceeds it by more than this many
 // log2 units, so stored P values stay below 2^kRescaleLog2: 16 for bf16 P (exponent range
 // of fp32), 8 for fp16 P (largest fp16 is 65504).
-template <bool F16> struct Lazy { static constexpr float kRescaleLog2 = F16 ? 8.0f : 16.0f; };
+// Element type of Q, K, V (and P): 0 = bf16, 1 = fp16, 2 = fp8 e4m3 (O is then bf16).
+// e4m3 P tops out at 448, so its reference is raised by 2^8 as for fp16.
+template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 16.0f : 8.0f; };
+template <int ET> struct Elem {
+    static constexpr int kBytes = ET == 2 ? 1 : 2;
+};
 
 
 // Device status word: [0] flags (1 = a wait ran out), [1] role, [2] CTA, [3] wait id.
 __device__ unsigned int g_status[4];
 
-template <int D>
+template <int D, int EB>
 struct Geo {
-    // Shared-memory rows: 64 head-dim values (128 bytes, 128-byte swizzle) per panel, or
-    // for D = 32 one panel of 64-byte rows (64-byte swizzle).
-    static constexpr int kPanelCols = D < 64 ? D : 64;
-    static constexpr int kRowBytes = kPanelCols * 2;
+    // Shared-memory rows of D elements of EB bytes, split into panels of 128-byte rows
+    // (128-byte swizzle), or one panel of 64-byte rows (64-byte swizzle) when a whole row
+    // is 64 bytes (D = 32 at 16 bits, D = 64 at 8 bits).
+    static constexpr int kRowBytesAll = D * EB;
+    static constexpr int kRowBytes = kRowBytesAll < 128 ? kRowBytesAll : 128;
+    static constexpr int kPanelCols = kRowBytes / EB;          // elements per panel row
     static constexpr int kPanelBytes = 128 * kRowBytes;        // 128 rows of one panel
     static constexpr uint32_t kSBO = 8u * kRowBytes;            // 8-row group stride
-    static constexpr int kPanels = D / kPanelCols;
+    static constexpr int kPanels = kRowBytesAll / kRowBytes;
     static constexpr int kTileBytes = kPanels * kPanelBytes;   // one 128 x D tile
-    static constexpr int kSlots = (D == 128) ? 4 : 8;          // K/V ring depth
+    static constexpr int kSlots = kTileBytes >= 32768 ? 4 : 8; // K/V ring depth
     static constexpr int kKVOff = 2 * kTileBytes;               // after Q_A, Q_B
     // O staging: one 4 KB slot per softmax warp (its 32 rows x one 64-column panel, rows
     // of 128 B with the 16-byte chunks XOR-swizzled by row so both the row-wise writes and
@@ -96,18 +103,18 @@ struct Geo {
 };
 
 // Barrier indices.
-template <int D> __device__ __forceinline__ int b_q_full(int t) { return t; }
-template <int D> __device__ __forceinline__ int b_q_empty(int t) { return 2 + t; }
-template <int D> __device__ __forceinline__ int b_kv_full(uint32_t i) { return 4 + (int)(i % Geo<D>::kSlots); }
-template <int D> __device__ __forceinline__ int b_kv_empty(uint32_t i) { return 4 + Geo<D>::kSlots + (int)(i % Geo<D>::kSlots); }
-template <int D> __device__ __forceinline__ int b_s_full(int t) { return 4 + 2 * Geo<D>::kSlots + t; }
-template <int D> __device__ __forceinline__ int b_p_full(int t) { return 6 + 2 * Geo<D>::kSlots + t; }
-template <int D> __device__ __forceinline__ int b_o_done(int t) { return 8 + 2 * Geo<D>::kSlots + t; }
-template <int D> __device__ __forceinline__ int b_drain() { return 10 + 2 * Geo<D>::kSlots; }
+template <int D, int EB> __device__ __forceinline__ int b_q_full(int t) { return t; }
+template <int D, int EB> __device__ __forceinline__ int b_q_empty(int t) { return 2 + t; }
+template <int D, int EB> __device__ __forceinline__ int b_kv_full(uint32_t i) { return 4 + (int)(i % Geo<D, EB>::kSlots); }
+template <int D, int EB> __device__ __forceinline__ int b_kv_empty(uint32_t i) { return 4 + Geo<D, EB>::kSlots + (int)(i % Geo<D, EB>::kSlots); }
+template <int D, int EB> __device__ __forceinline__ int b_s_full(int t) { return 4 + 2 * Geo<D, EB>::kSlots + t; }
+template <int D, int EB> __device__ __forceinline__ int b_p_full(int t) { return 6 + 2 * Geo<D, EB>::kSlots + t; }
+template <int D, int EB> __device__ __forceinline__ int b_o_done(int t) { return 8 + 2 * Geo<D, EB>::kSlots + t; }
+template <int D, int EB> __device__ __forceinline__ int b_drain() { return 10 + 2 * Geo<D, EB>::kSlots; }
 
 // Ring position i -> phase parity of its slot.
-template <int D> __device__ __forceinline__ uint32_t ring_parity(uint32_t i) {
-    return (i / Geo<D>::kSlots) & 1u;
+template <int D, int EB> __device__ __forceinline__ uint32_t ring_parity(uint32_t i) {
+    return (i / Geo<D, EB>::kSlots) & 1u;
 }
 
 // ----------------------------------------------------------------- work schedule
@@ -214,53 +221,70 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, const Item& it, i
 // ----------------------------------------------------------------- MMA issue
 // Shared-memory descriptor of a tile with D-dependent rows: 128-byte swizzle (layout type
 // 2) for 128-byte rows, 64-byte swizzle (layout type 4) for the 64-byte rows of D = 32.
-template <int D>
+template <int D, int EB>
 __device__ __forceinline__ uint64_t tile_desc(uint32_t saddr, uint32_t lbo) {
-    const uint64_t layout = Geo<D>::kRowBytes == 128 ? 2ull : 4ull;
+    using G = Geo<D, EB>;
+    const uint64_t layout = G::kRowBytes == 128 ? 2ull : 4ull;
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)((Geo<D>::kSBO >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+           ((uint64_t)((G::kSBO >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
+}
+
+// Instruction descriptor for the element type: kind::f16 (bf16 or fp16 operands) or
+// kind::f8f6f4 with both operands e4m3 (format code 0).
+template <int ET>
+__host__ __device__ constexpr uint32_t idesc_of(int M, int N, bool b_mn_major) {
+    return ET == 2 ? ((1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+                      ((uint32_t)(M >> 4) << 24))
+                   : make_idesc(M, N, b_mn_major, ET == 1);
 }
 
 // Descriptors are built once per buffer; a K step only adds a constant to the start
 // address field (addresses stay below 256 KB, so the 14-bit field never carries).
 // All lanes of the MMA warp execute these; one elected lane issues.
-template <int D>
+template <int D, int ET>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc,
                                          uint32_t idesc) {
-    using G = Geo<D>;
+    using G = Geo<D, Elem<ET>::kBytes>;
+    constexpr int kSteps = G::kRowBytesAll / 32;   // 32 bytes (16 or 32 values) per K step
+    constexpr int kPerPanel = G::kRowBytes / 32;
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        // 16 values = 32 bytes per K step inside a row; the next panel after 4 (128-byte rows)
-        const uint64_t off = ((uint64_t)(kk / 4) * G::kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
-        ptx::mma_ss_elect(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < kSteps; ++kk) {
+        const uint64_t off = ((uint64_t)(kk / kPerPanel) * G::kPanelBytes +
+                              (uint64_t)(kk % kPerPanel) * 32u) >> 4;
+        if (ET == 2) ptx::mma_ss_f8_elect(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+        else ptx::mma_ss_elect(d_tmem, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
     }
 }
 
-template <int D>
+template <int D, int ET>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                          uint32_t idesc, bool accumulate) {
-    using G = Geo<D>;
+    using G = Geo<D, Elem<ET>::kBytes>;
+    constexpr int kKeys = 32 / Elem<ET>::kBytes;   // keys per K step (32 bytes of P per row)
 #pragma unroll
-    for (int kk = 0; kk < kBN / 16; ++kk) {
-        // V tile: rows = keys (K dimension), one row of head-dim values per key (MN-major);
-        // 16 keys = 16 rows per K step; panels kPanelBytes apart (LBO).
-        ptx::mma_ts_elect(d_tmem, p_tmem + (uint32_t)kk * 8u,
-                          v_desc + (uint64_t)((kk * 16 * G::kRowBytes) >> 4), idesc,
-                          (accumulate || kk > 0) ? 1u : 0u);
+    for (int kk = 0; kk < kBN / kKeys; ++kk) {
+        // P: 8 TMEM columns per K step.  V tile: rows = keys (K dimension), one row of
+        // head-dim values per key (MN-major); kKeys rows per K step; panels kPanelBytes
+        // apart (LBO).
+        const uint64_t b = v_desc + (uint64_t)((kk * kKeys * G::kRowBytes) >> 4);
+        const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+        if (ET == 2) ptx::mma_ts_f8_elect(d_tmem, p_tmem + (uint32_t)kk * 8u, b, idesc, acc);
+        else ptx::mma_ts_elect(d_tmem, p_tmem + (uint32_t)kk * 8u, b, idesc, acc);
     }
 }
 
 // ----------------------------------------------------------------- roles
 // MMA issuer: the whole warp runs this loop (waits are warp-uniform), one lane issues.
-template <int D, bool CAUSAL, bool F16, int MODE>
+template <int D, bool CAUSAL, int ET, int MODE>
 __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_t sbase) {
-    using G = Geo<D>;
-    constexpr uint32_t idesc_qk = make_idesc(kBM, kBN, false, F16);
-    constexpr uint32_t idesc_pv = make_idesc(kBM, D, true, F16);
-    const uint64_t dQ[2] = {tile_desc<D>(sbase, 16),
-                            tile_desc<D>(sbase + (uint32_t)G::kTileBytes, 16)};
-    const uint64_t dK0 = tile_desc<D>(sbase + (uint32_t)G::kKVOff, 16);                  // K-major
-    const uint64_t dV0 = tile_desc<D>(sbase + (uint32_t)G::kKVOff, (uint32_t)G::kPanelBytes);  // MN-major
+    constexpr int EB = Elem<ET>::kBytes;
+    using G = Geo<D, EB>;
+    constexpr uint32_t idesc_qk = idesc_of<ET>(kBM, kBN, false);
+    constexpr uint32_t idesc_pv = idesc_of<ET>(kBM, D, true);
+    const uint64_t dQ[2] = {tile_desc<D, EB>(sbase, 16),
+                            tile_desc<D, EB>(sbase + (uint32_t)G::kTileBytes, 16)};
+    const uint64_t dK0 = tile_desc<D, EB>(sbase + (uint32_t)G::kKVOff, 16);                  // K-major
+    const uint64_t dV0 = tile_desc<D, EB>(sbase + (uint32_t)G::kKVOff, (uint32_t)G::kPanelBytes);  // MN-major
     const uint32_t tS[2] = {tmem + G::col_s(0), tmem + G::col_s(1)};
     const uint32_t tP[2] = {tmem + G::col_p(0), tmem + G::col_p(1)};
     const uint32_t tO[2] = {tmem + G::col_o(0), tmem + G::col_o(1)};
@@ -273,55 +297,55 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
         const int nsub = unit_count<CAUSAL, MODE>(p, u);
         for (int sub = 0; sub < nsub; ++sub) {
             const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
-            if (!wait_warp(c, b_q_full<D>(0), q_cnt & 1u, kRoleMma)) goto out;
-            if (!wait_warp(c, b_kv_full<D>(kv), ring_parity<D>(kv), kRoleMma)) goto out;
+            if (!wait_warp(c, b_q_full<D, EB>(0), q_cnt & 1u, kRoleMma)) goto out;
+            if (!wait_warp(c, b_kv_full<D, EB>(kv), ring_parity<D, EB>(kv), kRoleMma)) goto out;
             ptx::tc_fence_after();
-            issue_qk<D>(tS[0], dQ[0], dK0 + slot_off(kv), idesc_qk);
-            ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(0)));
-            if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(0)));
-            if (!wait_warp(c, b_q_full<D>(1), q_cnt & 1u, kRoleMma)) goto out;
+            issue_qk<D, ET>(tS[0], dQ[0], dK0 + slot_off(kv), idesc_qk);
+            ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(0)));
+            if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
+            if (!wait_warp(c, b_q_full<D, EB>(1), q_cnt & 1u, kRoleMma)) goto out;
             ++q_cnt;
             ptx::tc_fence_after();
-            issue_qk<D>(tS[1], dQ[1], dK0 + slot_off(kv), idesc_qk);
-            ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(1)));
-            if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(1)));
-            ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(kv)));
+            issue_qk<D, ET>(tS[1], dQ[1], dK0 + slot_off(kv), idesc_qk);
+            ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(1)));
+            if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+            ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kv)));
             ++kv;
 
             for (int j = 0; j < it.nB; ++j) {
                 const uint32_t vpos = kv;        // V_j
                 const uint32_t kpos = kv + 1;    // K_{j+1}
                 const bool more = j + 1 < it.nB;
-                if (!wait_warp(c, b_kv_full<D>(vpos), ring_parity<D>(vpos), kRoleMma)) goto out;
+                if (!wait_warp(c, b_kv_full<D, EB>(vpos), ring_parity<D, EB>(vpos), kRoleMma)) goto out;
                 ptx::tc_fence_after();
                 if (j < it.nA) {
-                    if (!wait_warp(c, b_p_full<D>(0), p_cnt0 & 1u, kRoleMma)) goto out;
+                    if (!wait_warp(c, b_p_full<D, EB>(0), p_cnt0 & 1u, kRoleMma)) goto out;
                     ++p_cnt0;
                     ptx::tc_fence_after();
-                    issue_pv<D>(tO[0], tP[0], dV0 + slot_off(vpos), idesc_pv, j > 0);
-                    ptx::mma_commit_elect(bar_addr(c, b_o_done<D>(0)));
+                    issue_pv<D, ET>(tO[0], tP[0], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                    ptx::mma_commit_elect(bar_addr(c, b_o_done<D, EB>(0)));
                 }
                 if (more) {
-                    if (!wait_warp(c, b_kv_full<D>(kpos), ring_parity<D>(kpos), kRoleMma)) goto out;
+                    if (!wait_warp(c, b_kv_full<D, EB>(kpos), ring_parity<D, EB>(kpos), kRoleMma)) goto out;
                     ptx::tc_fence_after();
                 }
                 if (j + 1 < it.nA) {
-                    issue_qk<D>(tS[0], dQ[0], dK0 + slot_off(kpos), idesc_qk);
-                    ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(0)));
-                    if (j + 2 == it.nA) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(0)));
+                    issue_qk<D, ET>(tS[0], dQ[0], dK0 + slot_off(kpos), idesc_qk);
+                    ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(0)));
+                    if (j + 2 == it.nA) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
                 }
-                if (!wait_warp(c, b_p_full<D>(1), p_cnt1 & 1u, kRoleMma)) goto out;
+                if (!wait_warp(c, b_p_full<D, EB>(1), p_cnt1 & 1u, kRoleMma)) goto out;
                 ++p_cnt1;
                 ptx::tc_fence_after();
-                issue_pv<D>(tO[1], tP[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
-                ptx::mma_commit_elect(bar_addr(c, b_o_done<D>(1)));
-                ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(vpos)));
+                issue_pv<D, ET>(tO[1], tP[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                ptx::mma_commit_elect(bar_addr(c, b_o_done<D, EB>(1)));
+                ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(vpos)));
                 ++kv;
                 if (more) {
-                    issue_qk<D>(tS[1], dQ[1], dK0 + slot_off(kpos), idesc_qk);
-                    ptx::mma_commit_elect(bar_addr(c, b_s_full<D>(1)));
-                    if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D>(1)));
-                    ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D>(kpos)));
+                    issue_qk<D, ET>(tS[1], dQ[1], dK0 + slot_off(kpos), idesc_qk);
+                    ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(1)));
+                    if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+                    ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kpos)));
                     ++kv;
                 }
             }
@@ -329,14 +353,14 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
     }
 out:
     // Every product issued so far must finish before TMEM is released.
-    ptx::mma_commit_elect(bar_addr(c, b_drain<D>()));
-    wait_drain(bar_addr(c, b_drain<D>()), 0, c.limit);
+    ptx::mma_commit_elect(bar_addr(c, b_drain<D, EB>()));
+    wait_drain(bar_addr(c, b_drain<D, EB>()), 0, c.limit);
     __syncwarp();
 }
 
-template <int D, bool CAUSAL, int MODE>
+template <int D, int EB, bool CAUSAL, int MODE>
 __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
-    using G = Geo<D>;
+    using G = Geo<D, EB>;
     const uint32_t sQ[2] = {sbase, sbase + (uint32_t)G::kTileBytes};
     auto slot = [&](uint32_t i) {
         return sbase + (uint32_t)G::kKVOff + (i % G::kSlots) * (uint32_t)G::kTileBytes;
@@ -351,8 +375,8 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
             const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
             // Q_A first, then K_0 (so S_A(0) can start), then Q_B, then V_0, K_1, V_1, ...
             auto load_q = [&](int t) -> bool {
-                if (!wait(c, b_q_empty<D>(t), (q_cnt & 1u) ^ 1u, kRoleLoad)) return false;
-                const uint32_t fb = bar_addr(c, b_q_full<D>(t));
+                if (!wait(c, b_q_empty<D, EB>(t), (q_cnt & 1u) ^ 1u, kRoleLoad)) return false;
+                const uint32_t fb = bar_addr(c, b_q_full<D, EB>(t));
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
                 int c1, c2;
                 tile_coords<MODE>(p, it, it.pair * 2 * kBM + t * kBM, c1, c2);
@@ -366,9 +390,9 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
             if (!load_q(0)) goto out;
             for (int j = 0; j < it.nB; ++j) {
                 for (int w = 0; w < 2; ++w) {  // K_j then V_j
-                    if (!wait(c, b_kv_empty<D>(kv), ring_parity<D>(kv) ^ 1u, kRoleLoad)) goto out;
+                    if (!wait(c, b_kv_empty<D, EB>(kv), ring_parity<D, EB>(kv) ^ 1u, kRoleLoad)) goto out;
                     if (kv != skipped) {
-                        const uint32_t fb = bar_addr(c, b_kv_full<D>(kv));
+                        const uint32_t fb = bar_addr(c, b_kv_full<D, EB>(kv));
                         ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
                         const CUtensorMap* map = (w == 0) ? &p.tmap_k : &p.tmap_v;
                         int c1, c2;
@@ -389,9 +413,9 @@ out:
     // No TMA copy may still be writing shared memory when the CTA exits: wait for the
     // last fill of every ring slot and of both query buffers.
     for (uint32_t i = (kv > (uint32_t)G::kSlots ? kv - G::kSlots : 0u); i < kv; ++i)
-        if (i != skipped) wait_drain(bar_addr(c, b_kv_full<D>(i)), ring_parity<D>(i), c.limit);
+        if (i != skipped) wait_drain(bar_addr(c, b_kv_full<D, EB>(i)), ring_parity<D, EB>(i), c.limit);
     for (int t = 0; t < 2; ++t)
-        if (q_issued[t] > 0) wait_drain(bar_addr(c, b_q_full<D>(t)), (q_issued[t] - 1u) & 1u, c.limit);
+        if (q_issued[t] > 0) wait_drain(bar_addr(c, b_q_full<D, EB>(t)), (q_issued[t] - 1u) & 1u, c.limit);
 }
 
 // Row maximum of the raw scores of one 128-key tile; invisible keys (kbase + c >= limit)
@@ -416,59 +440,71 @@ __device__ __forceinline__ float tile_row_max(const uint32_t (&s)[128], int kbas
     return fmaxf(ptx::max3(mx[0], mx[1], mx[2]), fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
-// p = 2^(s * sl2 - m) for columns [C0, C0 + 64), packed to 16-bit pairs into pk[C0/2 ...],
-// partial row sums into acc (four fp32 pairs).  Invisible keys give p = 0.
-template <int C0, bool MASK, bool F16>
+// p = 2^(s * sl2 - m) for columns [C0, C0 + 64), partial row sums into acc (four fp32
+// pairs), and P packed for TMEM: 16-bit pairs into pk[C0/2 ...], or for e4m3 four values
+// per word into pk[C0/4 ...].  Invisible keys give p = 0.
+template <int C0, bool MASK, int ET>
 __device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[128], int kbase, int limit,
                                               float sl2, float neg_m, float (&acc)[8],
                                               uint32_t (&pk)[64]) {
 #pragma unroll
-    for (int c = C0; c < C0 + 64; c += 2) {
-        float x0, x1;
-        ptx::fma2(x0, x1, u2f(s[c]), u2f(s[c + 1]), sl2, neg_m);
-        float p0 = ptx::ex2(x0);
-        float p1 = ptx::ex2(x1);
-        if (MASK) {
-            if (kbase + c >= limit) p0 = 0.f;
-            if (kbase + c + 1 >= limit) p1 = 0.f;
+    for (int c = C0; c < C0 + 64; c += 4) {
+        float x[4], pr[4];
+        ptx::fma2(x[0], x[1], u2f(s[c]), u2f(s[c + 1]), sl2, neg_m);
+        ptx::fma2(x[2], x[3], u2f(s[c + 2]), u2f(s[c + 3]), sl2, neg_m);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            pr[e] = ptx::ex2(x[e]);
+            if (MASK && kbase + c + e >= limit) pr[e] = 0.f;
         }
         const int a = ((c >> 1) & 3) * 2;
-        ptx::add2(acc[a], acc[a + 1], p0, p1);
-        pk[c >> 1] = pack2<F16>(p0, p1);
+        ptx::add2(acc[a], acc[a + 1], pr[0], pr[1]);
+        ptx::add2(acc[a + 2], acc[a + 3], pr[2], pr[3]);
+        if constexpr (ET == 2) {
+            pk[c >> 2] = pack4_e4m3(pr[0], pr[1], pr[2], pr[3]);
+        } else {
+            pk[c >> 1] = pack2<ET == 1>(pr[0], pr[1]);
+            pk[(c >> 1) + 1] = pack2<ET == 1>(pr[2], pr[3]);
+        }
     }
 }
 
 // One 128-key tile of one row: running-max update (raised only when the tile max exceeds
-// it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tP (64
-// columns, two 16-bit values per column) in two halves.  Returns the O rescale factor.
-template <bool MASK, bool F16>
+// it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tP in two
+// halves (64 columns of 16-bit pairs, or 32 columns of e4m3 quadruples).  Returns the O
+// rescale factor.
+template <bool MASK, int ET>
 __device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
                                               float sl2, float& m_run, float& l_run,
                                               uint32_t tP) {
     const float mt = tile_row_max<MASK>(s, kbase, limit) * sl2;  // log2 units
     float alpha = 1.0f;
-    if (mt > m_run + Lazy<F16>::kRescaleLog2) {
+    if (mt > m_run + Lazy<ET>::kRescaleLog2) {
         alpha = ptx::ex2(m_run - mt);   // m_run = -inf on the first tile: alpha = 0
         m_run = mt;
     }
     const float neg_m = -m_run;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     uint32_t pk[64];
-    tile_exp_half<0, MASK, F16>(s, kbase, limit, sl2, neg_m, acc, pk);
+    tile_exp_half<0, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
     __syncwarp();
-    ptx::tmem_st32p(tP, &pk[0]);
-    tile_exp_half<64, MASK, F16>(s, kbase, limit, sl2, neg_m, acc, pk);
+    if constexpr (ET == 2) ptx::tmem_st16(tP, &pk[0]);
+    else ptx::tmem_st32p(tP, &pk[0]);
+    tile_exp_half<64, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
     __syncwarp();
-    ptx::tmem_st32p(tP + 32, &pk[32]);
+    if constexpr (ET == 2) ptx::tmem_st16(tP + 16, &pk[16]);
+    else ptx::tmem_st32p(tP + 32, &pk[32]);
     const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     l_run = l_run * alpha + sum;
     return alpha;
 }
 
-template <int D, bool CAUSAL, bool F16, int MODE>
+template <int D, bool CAUSAL, int ET, int MODE>
 __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int warp, int lane,
                              uint32_t stage) {
-    using G = Geo<D>;
+    constexpr int EB = Elem<ET>::kBytes;
+    constexpr bool kOutF16 = ET == 1;   // O storage: fp16, else bf16
+    using G = Geo<D, EB>;
     const int t = warp / 4;                       // 0: tile A, 1: tile B
     const int lane_base = (warp % 4) * 32;        // this warp's TMEM lane quarter
     const uint32_t tl = (uint32_t)lane_base << 16;
@@ -489,10 +525,10 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             float m_run = -INFINITY, l_run = 0.0f;
 
             for (int j = 0; j < n; ++j) {
-                if (!wait_warp(c, b_s_full<D>(t), s_cnt & 1u, kRoleSoftmax)) return;
+                if (!wait_warp(c, b_s_full<D, EB>(t), s_cnt & 1u, kRoleSoftmax)) return;
                 ++s_cnt;
                 if (j > 0) {  // O_t += P(j-1) V(j-1) is complete before S(j) is (issue order)
-                    if (!wait_warp(c, b_o_done<D>(t), o_cnt & 1u, kRoleSoftmax)) return;
+                    if (!wait_warp(c, b_o_done<D, EB>(t), o_cnt & 1u, kRoleSoftmax)) return;
                     ++o_cnt;
                 }
                 ptx::tc_fence_after();
@@ -501,8 +537,8 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                 const int kbase = j * kBN;
                 const bool mask = __any_sync(0xFFFFFFFFu, kbase + kBN > limit);
                 const float alpha =
-                    mask ? softmax_tile<true, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tP)
-                         : softmax_tile<false, F16>(s, kbase, limit, p.scale_log2, m_run, l_run, tP);
+                    mask ? softmax_tile<true, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP)
+                         : softmax_tile<false, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP);
                 if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                     // The running max rose: rescale this row of O by alpha in TMEM.
 #pragma unroll 1
@@ -516,16 +552,16 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                 }
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
-                ptx::mbar_arrive(bar_addr(c, b_p_full<D>(t)));
+                ptx::mbar_arrive(bar_addr(c, b_p_full<D, EB>(t)));
             }
 
             // Epilogue: O / l, one 64-column panel at a time through this warp's staging
             // slot, so the global stores are row-contiguous: each store instruction writes
             // four whole 128-byte lines (rows past N are skipped); LSE from registers.
-            if (!wait_warp(c, b_o_done<D>(t), o_cnt & 1u, kRoleSoftmax)) return;
+            if (!wait_warp(c, b_o_done<D, EB>(t), o_cnt & 1u, kRoleSoftmax)) return;
             ++o_cnt;
             ptx::tc_fence_after();
-            const float inv_l = 1.0f / l_run;
+            const float inv_l = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
             const int row0 = it.pair * 2 * kBM + t * kBM + lane_base;   // first row of the warp
             // row r of the slice: obase + r * ostride (elements)
             const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
@@ -539,7 +575,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
-                    w[i] = pack2<F16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+                    w[i] = pack2<kOutF16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t chunk = (uint32_t)i ^ (uint32_t)(lane & 7);
@@ -567,7 +603,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        w[i] = pack2<F16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+                        w[i] = pack2<kOutF16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const uint32_t chunk = (uint32_t)(h * 4 + i) ^ (uint32_t)(lane & 7);
@@ -599,9 +635,10 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
     }
 }
 
-template <int D, bool CAUSAL, bool F16, int MODE>
+template <int D, bool CAUSAL, int ET, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constant__ TcParams p) {
-    using G = Geo<D>;
+    constexpr int EB = Elem<ET>::kBytes;
+    using G = Geo<D, EB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -619,17 +656,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
 
     if (threadIdx.x == 0) {
         for (int t = 0; t < 2; ++t) {
-            ptx::mbar_init(bar_addr(c, b_q_full<D>(t)), 1);
-            ptx::mbar_init(bar_addr(c, b_q_empty<D>(t)), 1);
-            ptx::mbar_init(bar_addr(c, b_s_full<D>(t)), 1);
-            ptx::mbar_init(bar_addr(c, b_p_full<D>(t)), 128);
-            ptx::mbar_init(bar_addr(c, b_o_done<D>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_q_full<D, EB>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_q_empty<D, EB>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_s_full<D, EB>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_p_full<D, EB>(t)), 128);
+            ptx::mbar_init(bar_addr(c, b_o_done<D, EB>(t)), 1);
         }
         for (int s = 0; s < G::kSlots; ++s) {
-            ptx::mbar_init(bar_addr(c, b_kv_full<D>(s)), 1);
-            ptx::mbar_init(bar_addr(c, b_kv_empty<D>(s)), 1);
+            ptx::mbar_init(bar_addr(c, b_kv_full<D, EB>(s)), 1);
+            ptx::mbar_init(bar_addr(c, b_kv_empty<D, EB>(s)), 1);
         }
-        ptx::mbar_init(bar_addr(c, b_drain<D>()), 1);
+        ptx::mbar_init(bar_addr(c, b_drain<D, EB>()), 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -648,12 +685,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kSoftmaxWarps) {
-        softmax_role<D, CAUSAL, F16, MODE>(p, c, tmem, warp, lane,
+        softmax_role<D, CAUSAL, ET, MODE>(p, c, tmem, warp, lane,
                                      sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
     } else if (warp == kMmaWarp) {
-        mma_role<D, CAUSAL, F16, MODE>(p, c, tmem, sbase);
+        mma_role<D, CAUSAL, ET, MODE>(p, c, tmem, sbase);
     } else {
-        if (lane == 0) load_role<D, CAUSAL, MODE>(p, c, sbase);
+        if (lane == 0) load_role<D, EB, CAUSAL, MODE>(p, c, sbase);
         __syncwarp();
     }
 
@@ -665,36 +702,52 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     }
 }
 
-template <int D, bool CAUSAL, bool F16, int MODE>
+template <int D, bool CAUSAL, int ET, int MODE>
 cudaError_t prepare_one() {
-    return cudaFuncSetAttribute(fa_tc_kernel<D, CAUSAL, F16, MODE>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSmemBytes);
+    return cudaFuncSetAttribute(fa_tc_kernel<D, CAUSAL, ET, MODE>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Geo<D, Elem<ET>::kBytes>::kSmemBytes);
 }
 
-template <int D, bool CAUSAL, bool F16, int MODE>
+template <int D, bool CAUSAL, int ET, int MODE>
 cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t stream) {
-    fa_tc_kernel<D, CAUSAL, F16, MODE><<<grid, kThreads, Geo<D>::kSmemBytes, stream>>>(p);
+    fa_tc_kernel<D, CAUSAL, ET, MODE>
+        <<<grid, kThreads, Geo<D, Elem<ET>::kBytes>::kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 
-template <int D, bool CAUSAL, bool F16>
+// 16-bit storage: both layouts; e4m3: [B, H, N, D] only.
+template <int D, bool CAUSAL, int ET>
 cudaError_t dispatch_mode(int mode, bool prepare, const TcParams* p, int grid, cudaStream_t stream) {
-    if (prepare) {
-        cudaError_t e = prepare_one<D, CAUSAL, F16, 0>();
-        return e != cudaSuccess ? e : prepare_one<D, CAUSAL, F16, 1>();
+    if constexpr (ET == 2) {
+        if (prepare) return prepare_one<D, CAUSAL, ET, 0>();
+        return mode == 0 ? launch_one<D, CAUSAL, ET, 0>(*p, grid, stream) : cudaErrorInvalidValue;
+    } else {
+        if (prepare) {
+            cudaError_t e = prepare_one<D, CAUSAL, ET, 0>();
+            return e != cudaSuccess ? e : prepare_one<D, CAUSAL, ET, 1>();
+        }
+        return mode == 0 ? launch_one<D, CAUSAL, ET, 0>(*p, grid, stream)
+                         : launch_one<D, CAUSAL, ET, 1>(*p, grid, stream);
     }
-    return mode == 0 ? launch_one<D, CAUSAL, F16, 0>(*p, grid, stream)
-                     : launch_one<D, CAUSAL, F16, 1>(*p, grid, stream);
+}
+
+template <int D, int ET>
+cudaError_t dispatch_et(bool causal, int mode, bool prepare, const TcParams* p, int grid,
+                        cudaStream_t stream) {
+    return causal ? dispatch_mode<D, true, ET>(mode, prepare, p, grid, stream)
+                  : dispatch_mode<D, false, ET>(mode, prepare, p, grid, stream);
 }
 
 template <int D>
-cudaError_t dispatch(bool causal, bool f16, int mode, bool prepare, const TcParams* p, int grid,
+cudaError_t dispatch(bool causal, int et, int mode, bool prepare, const TcParams* p, int grid,
                      cudaStream_t stream) {
-    if (causal)
-        return f16 ? dispatch_mode<D, true, true>(mode, prepare, p, grid, stream)
-                   : dispatch_mode<D, true, false>(mode, prepare, p, grid, stream);
-    return f16 ? dispatch_mode<D, false, true>(mode, prepare, p, grid, stream)
-               : dispatch_mode<D, false, false>(mode, prepare, p, grid, stream);
+    if (et == 1) return dispatch_et<D, 1>(causal, mode, prepare, p, grid, stream);
+    if (et == 2) {
+        if constexpr (D == 64 || D == 128) return dispatch_et<D, 2>(causal, mode, prepare, p, grid, stream);
+        return cudaErrorInvalidValue;
+    }
+    return dispatch_et<D, 0>(causal, mode, prepare, p, grid, stream);
 }
 
 }  // namespace
@@ -706,20 +759,20 @@ int tc_units(int bh, int n, bool causal) {
 }
 
 int tc_smem_bytes(int D) {
-    return D == 32 ? Geo<32>::kSmemBytes : D == 64 ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes;
+    return D == 32 ? Geo<32, 2>::kSmemBytes : D == 64 ? Geo<64, 2>::kSmemBytes : Geo<128, 2>::kSmemBytes;
 }
 
-cudaError_t tc_prepare(int D, bool causal, bool f16) {
-    if (D == 32) return dispatch<32>(causal, f16, 0, true, nullptr, 0, nullptr);
-    return D == 64 ? dispatch<64>(causal, f16, 0, true, nullptr, 0, nullptr)
-                   : dispatch<128>(causal, f16, 0, true, nullptr, 0, nullptr);
+cudaError_t tc_prepare(int D, bool causal, int et) {
+    if (D == 32) return dispatch<32>(causal, et, 0, true, nullptr, 0, nullptr);
+    return D == 64 ? dispatch<64>(causal, et, 0, true, nullptr, 0, nullptr)
+                   : dispatch<128>(causal, et, 0, true, nullptr, 0, nullptr);
 }
 
-cudaError_t tc_launch(int D, bool causal, bool f16, const TcParams& p, int grid,
+cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, int grid,
                       cudaStream_t stream) {
-    if (D == 32) return dispatch<32>(causal, f16, p.layout, false, &p, grid, stream);
-    return D == 64 ? dispatch<64>(causal, f16, p.layout, false, &p, grid, stream)
-                   : dispatch<128>(causal, f16, p.layout, false, &p, grid, stream);
+    if (D == 32) return dispatch<32>(causal, et, p.layout, false, &p, grid, stream);
+    return D == 64 ? dispatch<64>(causal, et, p.layout, false, &p, grid, stream)
+                   : dispatch<128>(causal, et, p.layout, false, &p, grid, stream);
 }
 
 cudaError_t tc_status_read_reset(uint32_t out[4]) {

@@ -105,6 +105,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// Four fp32 values rounded to fp8 e4m3 (saturating at +-448) in one 32-bit word, the
+// first value in the lowest byte.  cvt...e4m3x2 puts its first source in the upper byte.
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+    uint16_t lo, hi;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(b), "f"(a));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
 }  // namespace
 }  // namespace tc
 }  // namespace fa

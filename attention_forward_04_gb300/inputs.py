@@ -28,7 +28,7 @@ class Workload:
     H: int
     N: int
     D: int
-    dtype: str          # "fp32" or "bf16" (storage and I/O type)
+    dtype: str          # "fp32", "bf16", "fp16" or "fp8" (e4m3 Q, K, V; bf16 O)
     causal: bool
     seed: int           # seed base: Q uses seed, K seed+1, V seed+2
     qk_mult: float = 1.0
@@ -49,7 +49,8 @@ class Workload:
         return Workload(**d)
 
 
-TORCH_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16}
+TORCH_DTYPES = {"fp32": torch.float32, "bf16": torch.bfloat16, "fp16": torch.float16,
+                "fp8": torch.float8_e4m3fn}
 
 # The workloads; seeds are 1000*c + {0,1,2} for workload number c.
 WORKLOADS = {
@@ -67,6 +68,10 @@ WORKLOADS = {
     "bf16_b4h8n4096d256": Workload("bf16_b4h8n4096d256", 4, 8, 4096, 256, "bf16", False, 6000),
     "bf16_b4h8n4096d256_causal": Workload("bf16_b4h8n4096d256_causal", 4, 8, 4096, 256, "bf16",
                                           True, 6000),
+    # fp8 e4m3 inputs (per-tensor scales), the headline shape
+    "fp8_b4h16n4096d128": Workload("fp8_b4h16n4096d128", 4, 16, 4096, 128, "fp8", False, 8000),
+    "fp8_b8h32n4096d128_causal": Workload("fp8_b8h32n4096d128_causal", 8, 32, 4096, 128, "fp8",
+                                          True, 8100),
     # head dimension 32 (the "第 13 课" exercise's d), same FLOPs as the headline workload
     "bf16_b8h32n4096d32": Workload("bf16_b8h32n4096d32", 8, 32, 4096, 32, "bf16", False, 7000),
 }
@@ -86,6 +91,31 @@ def make_qkv(w: Workload, seed_offset: int = 0):
             x = x * w.qk_mult
         out.append(x.to(TORCH_DTYPES[w.dtype]).contiguous())
     return tuple(out)
+
+
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor fp8 e4m3 quantisation of an fp32 tensor: returns (x8, descale) with
+    x8 = round(x / descale) in torch.float8_e4m3fn and descale = max|x| / 448, so that
+    descale * x8 is the value the fp8 path computes on."""
+    amax = float(x.abs().max())
+    descale = amax / 448.0 if amax > 0 else 1.0
+    return (x / descale).to(torch.float8_e4m3fn).contiguous(), descale
+
+
+def make_qkv_fp8(w: Workload, seed_offset: int = 0):
+    """Q, K, V drawn as make_qkv draws them (fp32, before the cast), then quantised per
+    tensor to e4m3: returns ((q8, k8, v8), (q_descale, k_descale, v_descale))."""
+    shape = (w.B, w.H, w.N, w.D)
+    out, scales = [], []
+    for t in range(3):
+        g = torch.Generator().manual_seed(w.seed + seed_offset + t)
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if t < 2 and w.qk_mult != 1.0:
+            x = x * w.qk_mult
+        x8, ds = quantize_e4m3(x)
+        out.append(x8)
+        scales.append(ds)
+    return tuple(out), tuple(scales)
 
 
 def make_shape(B, H, N, D, dtype="bf16", seed=7, qk_mult=1.0):

@@ -252,7 +252,7 @@ def config_of(w, gpus):
             "dtype": w.dtype, "scale": w.scale, "qk_mult": w.qk_mult,
             "layout": "[B,H,N,D] contiguous", "parallelism": "replicas x%d" % gpus,
             "l2": "two alternating input sets of %.0f MiB each (> 129 MB L2); no flush"
-                  % (3 * w.B * w.H * w.N * w.D * (4 if w.dtype == "fp32" else 2) / 2**20)}
+                  % (3 * w.B * w.H * w.N * w.D * {"fp32": 4, "fp8": 1}.get(w.dtype, 2) / 2**20)}
 
 
 # ------------------------------------------------------------------ backward
@@ -508,7 +508,7 @@ def main():
     import torch
     import torch.distributed as dist
     from attention_forward_04_gb300 import binding, build
-    from attention_forward_04_gb300.inputs import TORCH_DTYPES, make_qkv
+    from attention_forward_04_gb300.inputs import TORCH_DTYPES, make_qkv, make_qkv_fp8
 
     if rank == 0:
         build.build()
@@ -522,21 +522,36 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    code = {"fp32": binding.FA_FP32, "bf16": binding.FA_BF16, "fp16": binding.FA_FP16}[w.dtype]
+    fp8 = w.dtype == "fp8"
+    code = {"fp32": binding.FA_FP32, "bf16": binding.FA_BF16, "fp16": binding.FA_FP16,
+            "fp8": -1}[w.dtype]
     B, H, N, D = w.B, w.H, w.N, w.D
+    lib = binding.load_library()
 
-    sets = []
+    def inputs(seed_offset):
+        # fp8: e4m3 tensors and their per-tensor dequantisation factors
+        if fp8:
+            return make_qkv_fp8(w, seed_offset=seed_offset)
+        return make_qkv(w, seed_offset=seed_offset), (1.0, 1.0, 1.0)
+
+    sets, descales = [], None
     for s in range(2):
-        q, k, v = make_qkv(w, seed_offset=100 * s + 10 * rank)
+        (q, k, v), descales = inputs(100 * s + 10 * rank)
         sets.append(tuple(t.to(dev) for t in (q, k, v)))
-    host_set = make_qkv(w, seed_offset=10 * rank)
-    o = torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype], device=dev)
+    host_set, host_descales = inputs(10 * rank)
+    o = torch.empty((B, H, N, D), dtype=torch.bfloat16 if fp8 else TORCH_DTYPES[w.dtype],
+                    device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
 
     def step(i):
         q, k, v = sets[i & 1]
-        st = binding.fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                             lse.data_ptr(), B, H, N, D, w.scale, int(w.causal), code, sh)
+        if fp8:
+            st = lib.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), B, H, N, D, w.scale, int(w.causal), descales[0],
+                                descales[1], descales[2], sh)
+        else:
+            st = binding.fwd_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), B, H, N, D, w.scale, int(w.causal), code, sh)
         if st != 0:
             raise binding.FaError(st)
 
@@ -584,7 +599,7 @@ def main():
 
     # ---- end to end through the public API: pinned host inputs -> device -> fa.fwd -> host
     hq, hk, hv = (t.pin_memory() for t in host_set)
-    ho = torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype]).pin_memory()
+    ho = torch.empty((B, H, N, D), dtype=o.dtype).pin_memory()
     hl = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     dq, dk, dv = (torch.empty_like(t, device=dev) for t in host_set)
 
@@ -592,7 +607,11 @@ def main():
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
         dv.copy_(hv, non_blocking=True)
-        binding.fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)
+        if fp8:
+            binding.fwd_fp8(dq, dk, dv, *host_descales, scale=w.scale, causal=w.causal, out=o,
+                            lse=lse, stream=stream)
+        else:
+            binding.fwd(dq, dk, dv, scale=w.scale, causal=w.causal, out=o, lse=lse, stream=stream)
         ho.copy_(o, non_blocking=True)
         hl.copy_(lse, non_blocking=True)
 
@@ -630,12 +649,16 @@ def main():
                 "frac": achieved / alu_peak, "traffic": traffic,
                 "peak_source": "derived: %d SMs x 128 fp32 lanes x 2 FLOP x max SM clock" % sms}
     else:
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": "%s bf16 dense burst (MEASURED_PEAKS.json)" % peak_src
-                if peak_src == "measured" else "fallback 1.9 PFLOP/s",
-                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", 1700.0)),
-                "hbm_gbs_algorithmic": (3 + 1) * B * H * N * D * 2 / (per_launch_ms / 1e3) / 1e9}
+        # e4m3 products run at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense), so
+        # their peak is the measured bf16 peak times 2
+        ratio = 2.0 if fp8 else 1.0
+        src = ("%s bf16 dense burst (MEASURED_PEAKS.json)" % peak_src
+               if peak_src == "measured" else "fallback 1.9 PFLOP/s")
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak * ratio, "unit": "TFLOP/s",
+                "frac": achieved / (peak * ratio), "traffic": traffic,
+                "peak_source": src + (" x 2 (e4m3 : bf16 nominal dense ratio)" if fp8 else ""),
+                "frac_of_sustained": achieved / (ratio * float(peaks.get("bf16_tflops_sustained", 1700.0))),
+                "hbm_gbs_algorithmic": (3 * (1 if fp8 else 2) + 2) * B * H * N * D / (per_launch_ms / 1e3) / 1e9}
 
     cpu = None
     if args.cpu_budget > 0:
@@ -654,8 +677,9 @@ def main():
         "metric": "attention fwd TFLOPS (4*B*H*N^2*D/t)",
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
-        "data": "synthetic (seeded torch.randn, cast to %s)" % w.dtype,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else w.dtype,
+        "data": ("synthetic (seeded torch.randn, per-tensor e4m3 quantisation; O bf16)" if fp8
+                 else "synthetic (seeded torch.randn, cast to %s)" % w.dtype),
         "config": config_of(w, world),
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
@@ -664,7 +688,7 @@ def main():
         "roofline": roof,
         "cpu_baseline": cpu,
         "clocks": clocks,
-        "pct_of_peak": 100.0 * achieved / peak if w.dtype != "fp32" else None,
+        "pct_of_peak": 100.0 * roof["frac"] if w.dtype != "fp32" else None,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -105,6 +105,27 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
 
 /* Human-readable name of a status code (static string; never NULL). */
 /*
+ * fa_fwd_fp8 -- the forward pass on fp8 inputs (FlashAttention-3's direction, which
+ * "第 13 课" names after FlashAttention-2), asynchronous on `stream`.
+ *
+ *   q, k, v : device pointers, [B, H, N, D] contiguous fp8 e4m3 (1 byte per element); the
+ *             values are q_descale * Q, k_descale * K, v_descale * V (per-tensor factors).
+ *   o       : device pointer, [B, H, N, D] contiguous bf16; written fully.
+ *   lse     : device pointer, [B, H, N] fp32; written fully.
+ *   B, H, N, scale, causal, stream : as for fa_fwd.
+ *   D       : 64 or 128.
+ *   q_descale, k_descale, v_descale : finite, > 0.
+ *
+ * Computes O = softmax(scale * (q_descale Q)(k_descale K)^T) (v_descale V) and its LSE:
+ * Q K^T and P V on the tensor cores from e4m3 operands (kind::f8f6f4) with fp32
+ * accumulation; P is rounded to e4m3 before P V (l is summed from the fp32 values);
+ * O is rounded to bf16.  Errors as fa_fwd.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+               int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
+               float q_descale, float k_descale, float v_descale, void* stream);
+
+/*
  * fa_bwd_workspace_bytes -- bytes of device workspace fa_bwd needs for a [B, H, N, D]
  * problem (one fp32 value per query row, rounded up to 256 bytes); -1 if B, H or N is out
  * of range.  Pure host arithmetic.
@@ -197,7 +218,7 @@ int fa_check_device_status(void* stream, uint32_t* detail);
 int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall);
 
 /* Library ABI version (major * 100 + minor). */
-int fa_version(void);   /* 120: adds fa_bwd and fa_bwd_workspace_bytes */
+int fa_version(void);   /* 130: adds fa_fwd_fp8 */
 
 #ifdef __cplusplus
 }

@@ -158,3 +158,26 @@ def test_bwd_workspace_size(lib):
 ])
 def test_bwd_bad_arguments_rejected_before_cuda(lib, kw, expect):
     assert bwd_call(lib, **kw) == expect
+
+
+def fp8_call(lib, D=128, causal=0, qd=0.01, kd=0.01, vd=0.01, scale=0.1, **ptr):
+    addr = dict(q=BASE, k=BASE + SZ, v=BASE + 2 * SZ, o=BASE + 3 * SZ, lse=BASE + 4 * SZ)
+    addr.update(ptr)
+    return lib.fa_fwd_fp8(addr["q"], addr["k"], addr["v"], addr["o"], addr["lse"], 1, 2, 300, D,
+                          scale, causal, qd, kd, vd, None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=0), INVALID), (dict(lse=0), INVALID), (dict(causal=2), INVALID),
+    (dict(qd=0.0), INVALID), (dict(kd=-1.0), INVALID), (dict(vd=float("nan")), INVALID),
+    (dict(qd=float("inf")), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(D=32), UNSUPPORTED), (dict(D=256), UNSUPPORTED), (dict(D=96), UNSUPPORTED),
+    (dict(o=BASE + SZ + 1024), INVALID),           # o overlaps k
+    (dict(q=BASE + 8), MISALIGNED),
+])
+def test_fp8_bad_arguments_rejected_before_cuda(lib, kw, expect):
+    assert fp8_call(lib, **kw) == expect
+
+
+def test_fp8_dtype_code_not_accepted_by_fa_fwd(lib):
+    assert call(lib, dtype=3) == INVALID
