@@ -105,8 +105,9 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
 
 /* Human-readable name of a status code (static string; never NULL). */
 /*
- * fa_fwd_fp8 -- the forward pass on fp8 inputs (FlashAttention-3's direction, which
- * "第 13 课" names after FlashAttention-2), asynchronous on `stream`.
+ * fa_fwd_fp8 -- the forward pass on fp8 inputs (the FP8 tensor-core direction that
+ * "第 13 课：GPU 内核与 FlashAttention", answer to question 3, names for FlashAttention-3),
+ * asynchronous on `stream`.
  *
  *   q, k, v : device pointers, [B, H, N, D] contiguous fp8 e4m3 (1 byte per element); the
  *             values are q_descale * Q, k_descale * K, v_descale * V (per-tensor factors).
