@@ -76,7 +76,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *                and writing this layout directly saves the [B,N,H,D] <-> [B,H,N,D] copies
  *                around the attention ("pwwt.cn: FlashAttention 与内存墙" §5.2).
  *   lse        : device pointer, [B, H, N] contiguous fp32.
- *   Everything else as fa_fwd (same limits, ownership, errors, asynchrony).
+ *   Everything else as fa_fwd (same limits, ownership, errors, asynchrony), except that
+ *   D = 256 is not served here (FA_ERR_UNSUPPORTED).
  */
 int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse,
                 int64_t B, int64_t N, int64_t H, int64_t D,
@@ -97,13 +98,12 @@ int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse
  *                access outside the tensors; they are not otherwise checked (checking would
  *                need a device-to-host copy).
  *   batch, max_seqlen, total, H : >= 1; batch*H < 2^31; total < 2^31.
- *   Everything else as fa_fwd.
+ *   Everything else as fa_fwd, except that D = 256 is not served here (FA_ERR_UNSUPPORTED).
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total,
                   int64_t H, int64_t D, float scale, int causal, int dtype, void* stream);
 
-/* Human-readable name of a status code (static string; never NULL). */
 /*
  * fa_fwd_fp8 -- the forward pass on fp8 inputs (the FP8 tensor-core direction that
  * "第 13 课：GPU 内核与 FlashAttention", answer to question 3, names for FlashAttention-3),
@@ -191,6 +191,7 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                    int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
                    int dtype, void* stream);
 
+/* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(int status);
 
 /* Text of the last CUDA error seen by this library in the calling thread, or "". */
