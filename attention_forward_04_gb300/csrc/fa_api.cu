@@ -407,7 +407,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
         !encode_map(&p.tmap_do, dout, 0, BH, N, H, B * N, D, et, fn))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     p.lse = lse;
-    p.delta = static_cast<const float*>(workspace);
+    p.o = o;
+    p.delta = static_cast<float*>(workspace);
     p.dq = dq;
     p.dk = dk;
     p.dv = dv;
@@ -417,8 +418,6 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit = g_wait_limit.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    e = fa::bwd_delta_launch((int)D, f16, o, dout, static_cast<float*>(workspace), (long long)BH * N, st);
-    if (e != cudaSuccess) return fail_cuda(e, "backward delta launch");
     e = fa::bwd_launch((int)D, dic, f16, p, (int)BH, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "backward kernel launch");
 }

@@ -6,9 +6,9 @@
 //     P = exp(scale * Q K^T - LSE),  dP = dO V^T,  delta = rowsum(dO * O),
 //     dS = P * (dP - delta),  dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
 //
-// Three kernels, no atomics (results do not depend on scheduling):
-//   * delta: one warp per row, rowsum(dO * O) in fp32;
-//   * dQ: one CTA per 128-query tile.  Q is copied once into TMEM and serves as the A
+// Two kernels, no atomics (results do not depend on scheduling):
+//   * dQ: one CTA per 128-query tile; it also forms delta = rowsum(dO * O) in fp32 for its
+//     rows (dO from its shared tile, O from global memory) and writes it for the next kernel.  Q is copied once into TMEM and serves as the A
 //     operand of S = Q K_j^T (dO stays in shared memory for dP = dO V_j^T); the
 //     elementwise warps (TMEM lane = query row) form P, then dS = P (dP - delta) into a
 //     TMEM region of its own (16-bit), so dP of the next key tile can start while dQ +=
@@ -62,8 +62,10 @@ struct BGeo {
     // epilogue staging (4 KB per elementwise warp) reuses the ring: it starts only after
     // every product, hence every read of the ring, has completed
     static constexpr int kStageOff = kRingOff;
-    static constexpr int kVecOff = kRingOff + kSlots * kTile;  // 2 x 256 floats (dK/dV only)
-    static constexpr int kBarOff = kVecOff + (FIXED == 2 ? 2 * 256 * 4 : 0);
+    // dK/dV: 2 x 256 floats of staged per-column LSE and delta; dQ: 2 x 128 floats of
+    // partial row sums of delta
+    static constexpr int kVecOff = kRingOff + kSlots * kTile;
+    static constexpr int kBarOff = kVecOff + (FIXED == 2 ? 2 * 256 * 4 : 2 * 128 * 4);
     // barriers: fixed_full, ring_full[4], ring_empty[4], then the named ones below
     static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -395,9 +397,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         const bool live = i < p.n;
         const size_t row = (size_t)bh * p.n + (live ? i : 0);
         const float lse2 = live ? p.lse[row] * kLog2e : 0.0f;
-        const float dlt = live ? p.delta[row] : 0.0f;
         const int limit = CAUSAL ? min(i + 1, p.n) : p.n;    // visible keys: key < limit
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
+        float* part = reinterpret_cast<float*>(smem_raw + (su.sbase - ptx::smem_addr(smem_raw)) + G::kVecOff);
+        float dlt = 0.0f;
+        {
+            // delta = sum_d dO * O for this row: this warp's 64 columns from dO (the fixed
+            // shared tile) and O (global; loaded first so the loads overlap the tile loads),
+            // the two halves added through shared memory below
+            const bool mine = live && ch < D / 64;
+            uint4 ovs[8];
+            if (mine) {
+                const uint4* orow = reinterpret_cast<const uint4*>(
+                    static_cast<const uint16_t*>(p.o) + row * D + 64 * ch);
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) ovs[cc] = __ldg(orow + cc);
+            }
+            const bool okd = wait_warp(c, G::fixed_full(), 0, kRoleSoftmax);
+            float acc = 0.0f;
+            if (okd && mine) {
+                const uint32_t drow = su.sbase + (uint32_t)ch * kPanelBytes + (uint32_t)r * 128u;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    const uint4 ov = ovs[cc];
+                    const uint4 dv = ptx::ld_shared_v4(drow + (uint32_t)((cc ^ (r & 7)) * 16));
+                    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc = fmaf(unpack_lo<F16>(ow[e]), unpack_lo<F16>(dw[e]), acc);
+                        acc = fmaf(unpack_hi<F16>(ow[e]), unpack_hi<F16>(dw[e]), acc);
+                    }
+                }
+            }
+            part[ch * kT + r] = acc;
+        }
         {
             // Q rows (streamed tile 0) into TMEM as 16-bit pairs (this warp: one 64-column
             // panel); the ring slot is then released
@@ -420,6 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
                 ptx::mbar_arrive(bar_addr(c, G::ring_empty(0)));
                 ptx::mbar_arrive(bar_addr(c, G::q_ready()));
             }
+            // both partial sums are published by the barrier above
+            dlt = part[r] + part[kT + r];
+            if (live && ch == 0) p.delta[row] = dlt;   // for the dK/dV kernel
         }
         for (int j = 0; j < nkv; ++j) {
             const uint32_t par = (uint32_t)j & 1u;
@@ -648,36 +684,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     teardown_cta(su);
 }
 
-// ----------------------------------------------------------------- delta kernel
-template <int D, bool F16>
-__global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ o,
-                                                       const uint16_t* __restrict__ dout,
-                                                       float* __restrict__ delta, long long rows) {
-    constexpr int E = D / 32;   // elements per lane
-    const int lane = threadIdx.x % 32;
-    const long long warps = (long long)gridDim.x * (blockDim.x / 32);
-    for (long long r = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; r < rows; r += warps) {
-        const uint16_t* a = o + r * D + lane * E;
-        const uint16_t* b = dout + r * D + lane * E;
-        float acc = 0.0f;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            float x, y;
-            if constexpr (F16) {
-                x = __half2float(__ushort_as_half(a[e]));
-                y = __half2float(__ushort_as_half(b[e]));
-            } else {
-                x = __bfloat162float(__ushort_as_bfloat16(a[e]));
-                y = __bfloat162float(__ushort_as_bfloat16(b[e]));
-            }
-            acc = fmaf(x, y, acc);
-        }
-#pragma unroll
-        for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, m);
-        if (lane == 0) delta[r] = acc;
-    }
-}
-
 template <int D, bool CAUSAL, bool F16>
 cudaError_t prepare3() {
     cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL, F16>,
@@ -709,22 +715,6 @@ cudaError_t dispatch(bool causal, bool f16, bool prepare, const BwdParams* p, in
 }
 
 }  // namespace
-
-cudaError_t bwd_delta_launch(int D, bool f16, const void* o, const void* dout, float* delta,
-                             long long rows, cudaStream_t stream) {
-    const long long blocks = (rows + 7) / 8;
-    const unsigned grid = (unsigned)(blocks < 65536 ? blocks : 65536);
-    const uint16_t* a = static_cast<const uint16_t*>(o);
-    const uint16_t* b = static_cast<const uint16_t*>(dout);
-    if (D == 64) {
-        if (f16) bwd_delta_kernel<64, true><<<grid, 256, 0, stream>>>(a, b, delta, rows);
-        else bwd_delta_kernel<64, false><<<grid, 256, 0, stream>>>(a, b, delta, rows);
-    } else {
-        if (f16) bwd_delta_kernel<128, true><<<grid, 256, 0, stream>>>(a, b, delta, rows);
-        else bwd_delta_kernel<128, false><<<grid, 256, 0, stream>>>(a, b, delta, rows);
-    }
-    return cudaGetLastError();
-}
 
 cudaError_t bwd_prepare(int D, bool causal, bool f16) {
     return D == 64 ? dispatch<64>(causal, f16, true, nullptr, 0, nullptr)

@@ -37,7 +37,8 @@ struct BwdParams {
     CUtensorMap tmap_v;
     CUtensorMap tmap_do;
     const float* lse;     // [B*H, N] natural-log LSE of the forward
-    const float* delta;   // [B*H, N] rowsum(dO * O), written by the first backward kernel
+    const void* o;        // [B*H, N, D] the forward's output (16-bit)
+    float* delta;         // [B*H, N] rowsum(dO * O): written by the dQ kernel, read by dK/dV
     void* dq;             // [B*H, N, D] outputs, input element type
     void* dk;
     void* dv;
@@ -48,12 +49,10 @@ struct BwdParams {
     unsigned long long wait_limit;
 };
 
-// delta[r] = sum_d dO[r, d] * O[r, d] for rows r < rows (fp32 from 16-bit inputs).
-cudaError_t bwd_delta_launch(int D, bool f16, const void* o, const void* dout, float* delta,
-                             long long rows, cudaStream_t stream);
 // Raise the dynamic shared-memory limit of the backward tensor-core kernels (once).
 cudaError_t bwd_prepare(int D, bool causal, bool f16);
-// dQ (one CTA per 128-query tile) and dK, dV (one CTA per 128-key tile), B*H*ntiles CTAs each.
+// dQ (one CTA per 128-query tile; also writes delta) and then dK, dV (one CTA per 128-key
+// tile), B*H*ntiles CTAs each.
 cudaError_t bwd_launch(int D, bool causal, bool f16, const BwdParams& p, int bh,
                        cudaStream_t stream);
 // Status word of the backward kernels (same meaning as the forward's).

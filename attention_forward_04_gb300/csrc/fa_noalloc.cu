@@ -20,8 +20,8 @@ constexpr int64_t kScratchBytes = FA_BWD_NOALLOC_MAX_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 // One copy per device, created when the library's device code is loaded on that device.
-// Nothing in it has to start at zero: the delta kernel writes every row it uses before the
-// dQ and dK/dV kernels read it.
+// Nothing in it has to start at zero: the dQ kernel writes every delta row before the dK/dV
+// kernel reads it.
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
 struct ScratchSlot {

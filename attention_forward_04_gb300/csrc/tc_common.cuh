@@ -105,6 +105,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// The low / high 16-bit value of a packed pair, as fp32.
+template <bool F16>
+__device__ __forceinline__ float unpack_lo(uint32_t w) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+    else return __uint_as_float(w << 16);
+}
+template <bool F16>
+__device__ __forceinline__ float unpack_hi(uint32_t w) {
+    if constexpr (F16) return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    else return __uint_as_float(w & 0xFFFF0000u);
+}
+
 // Four fp32 values rounded to fp8 e4m3 (saturating at +-448) in one 32-bit word, the
 // first value in the lowest byte.  cvt...e4m3x2 puts its first source in the upper byte.
 __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {

@@ -359,7 +359,7 @@ def run_reference_bwd(args, w):
 
 
 def run_bwd(args, w):
-    """Backward pass: a step is one fa_bwd call (delta, dQ and dK/dV kernels) over resident
+    """Backward pass: a step is one fa_bwd call (dQ-with-delta and dK/dV kernels) over resident
     Q, K, V, O, LSE, dO; the forward that produces O and LSE runs before timing."""
     rank, local_rank, world = dist_env()
     import torch
@@ -472,8 +472,8 @@ def run_bwd(args, w):
     achieved = flops_step / (per_call_ms / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "traffic": load_traffic("bwd:" + w.name, "bwd"),
-            "kernel": "whole fa_bwd call (delta, dQ and dK/dV kernels); per-kernel shares "
-                      "in the ncu launch list",
+            "kernel": "whole fa_bwd call (dQ kernel, which also forms delta, and dK/dV "
+                      "kernel); per-kernel shares in the ncu launch list",
             "peak_source": "%s bf16 dense burst" % peak_src,
             "executed_tflops": 3.5 * w.flops / (per_call_ms / 1e3) / 1e12}
     cpu = None
@@ -504,7 +504,7 @@ def run_bwd(args, w):
                 "pipelining": "host->device copies (one stream per input), the call and "
                               "device->host copies of consecutive steps overlap (two device "
                               "buffer sets)"},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,   # dQ (with delta) and dK/dV kernels
         "roofline": roof, "cpu_baseline": cpu,
         "clocks": sampler.summary(t_wall0, t_wall1),
     }
