@@ -264,7 +264,10 @@ int forward(const Request& r) {
         p.scale_log2 = r.scale * 1.4426950408889634f;
         p.o_scale = 1.0f;
         p.wait_limit = g_wait_limit.load();
-        e = fa::tc256_launch(dic, f16, p, st);
+        p.units = fa::tc256_units((int)BH, (int)r.N, dic != 0);
+        if (p.units < 1) return FA_ERR_UNSUPPORTED;
+        const int grid = p.units < di.sm_count ? p.units : di.sm_count;
+        e = fa::tc256_launch(dic, f16, p, grid, st);
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch (D = 256)");
     }
     std::call_once(di.prepared[dix][dic][dif],

@@ -3,7 +3,8 @@
 // Same computation as the D = 64/128 kernel ("08 · FlashAttention" §二: tiles plus the
 // online (m, l, O) softmax; "KingOfEgg" §1.1 for the definition), with a layout sized for
 // D = 256: the two-query-tile schedule of the smaller head dimensions would need 2 x 256
-// TMEM columns of O alone.  Here one CTA owns one 128-row query tile and all 512 columns:
+// TMEM columns of O alone.  Here a persistent CTA (one per SM) takes one 128-row query tile
+// at a time and owns all 512 columns:
 //     Q [0, 128)       the query tile as 16-bit pairs (A operand of S = Q K^T)
 //     S/P buffer 0     [128, 192)   64 keys: fp32 scores, then P (16-bit) over them
 //     S/P buffer 1     [192, 256)
@@ -57,10 +58,8 @@ constexpr int b_q_ready() { return 2 * kSlots + 5; }
 constexpr int b_drain() { return 2 * kSlots + 6; }
 __device__ __forceinline__ uint32_t ring_par(uint32_t pos) { return (pos / kSlots) & 1u; }
 
-// Streamed tiles: 0 and 1 are the two 64-row halves of the Q tile, then K_j = 2 + 2j and
-// V_j = 3 + 2j.
-__device__ __forceinline__ uint32_t pos_k(int j) { return 2u + 2u * (uint32_t)j; }
-__device__ __forceinline__ uint32_t pos_v(int j) { return 3u + 2u * (uint32_t)j; }
+// Streamed tiles of an item, from its first ring position: 0 and 1 are the two 64-row
+// halves of the Q tile, then K_j = 2 + 2j and V_j = 3 + 2j.
 
 template <bool F16> struct Lazy { static constexpr float kRescaleLog2 = F16 ? 8.0f : 16.0f; };
 
@@ -131,24 +130,40 @@ struct Work {
     int bh, qt, nkv;
 };
 
+// Work units of the persistent schedule.  Non-causal: one 128-row query tile per unit,
+// slice-major, so the CTAs running together share a few slices' K and V through L2.
+// Causal: unit (slice, q) holds tiles ntiles-1-q and q of the slice (one tile when they
+// coincide), so units cost about the same; still slice-major.
+__device__ __forceinline__ int ntiles_of(const TcParams& p) { return (p.n + kBM - 1) / kBM; }
+
 template <bool CAUSAL>
-__device__ __forceinline__ Work work_of(const TcParams& p) {
-    const int ntiles = (p.n + kBM - 1) / kBM;
+__device__ __forceinline__ int unit_items(const TcParams& p, int u) {
+    if (!CAUSAL) return 1;
+    const int nt = ntiles_of(p), q = u % ((nt + 1) / 2);
+    return (nt - 1 - q != q) ? 2 : 1;
+}
+
+template <bool CAUSAL>
+__device__ __forceinline__ Work unit_item(const TcParams& p, int u, int sub) {
+    const int nt = ntiles_of(p);
     Work w;
     if (CAUSAL) {
-        // heaviest query tiles first (work grows with the tile index)
-        w.qt = ntiles - 1 - (int)(blockIdx.x / (unsigned)p.bh);
-        w.bh = (int)(blockIdx.x % (unsigned)p.bh);
+        const int half = (nt + 1) / 2;
+        w.bh = u / half;
+        const int q = u % half;
+        w.qt = sub == 0 ? nt - 1 - q : q;
     } else {
-        // slice-major: CTAs resident together share one slice's K and V through L2
-        w.bh = (int)(blockIdx.x / (unsigned)ntiles);
-        w.qt = (int)(blockIdx.x % (unsigned)ntiles);
+        w.bh = u / nt;
+        w.qt = u % nt;
     }
     const int keys = CAUSAL ? min(p.n, (w.qt + 1) * kBM) : p.n;
     w.nkv = (keys + kBN - 1) / kBN;
     return w;
 }
 
+// Every role walks the same items in the same order and keeps running counters: ring
+// position (2 Q halves, then K_j, V_j per item), global step index g (S/P buffer g % 2, its
+// (g / 2)-th use), products of O done, and items.
 template <bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -185,24 +200,30 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tm = *tmem_slot;
-    const Work w = work_of<CAUSAL>(p);
     const uint32_t ring = sbase;
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
-            const uint32_t count = 2u + 2u * (uint32_t)w.nkv;
             uint32_t pos = 0;
-            for (; pos < count; ++pos) {
-                if (!wait(c, b_ring_empty(pos), ring_par(pos) ^ 1u, kRoleLoad)) break;
-                const uint32_t bar = bar_addr(c, b_ring_full(pos));
-                const CUtensorMap* map = pos < 2 ? &p.tmap_q : ((pos & 1u) ? &p.tmap_v : &p.tmap_k);
-                const int row = pos < 2 ? w.qt * kBM + (int)pos * 64 : (int)((pos - 2u) >> 1) * kBN;
-                const uint32_t dst = ring + (pos % kSlots) * (uint32_t)kTile;
-                ptx::mbar_arrive_expect_tx(bar, (uint32_t)kTile);
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const int nsub = unit_items<CAUSAL>(p, u);
+                for (int sub = 0; sub < nsub; ++sub) {
+                    const Work w = unit_item<CAUSAL>(p, u, sub);
+                    const uint32_t count = 2u + 2u * (uint32_t)w.nkv;
+                    for (uint32_t k = 0; k < count; ++k, ++pos) {
+                        if (!wait(c, b_ring_empty(pos), ring_par(pos) ^ 1u, kRoleLoad)) goto load_out;
+                        const uint32_t bar = bar_addr(c, b_ring_full(pos));
+                        const CUtensorMap* map = k < 2 ? &p.tmap_q : ((k & 1u) ? &p.tmap_v : &p.tmap_k);
+                        const int row = k < 2 ? w.qt * kBM + (int)k * 64 : (int)((k - 2u) >> 1) * kBN;
+                        const uint32_t dst = ring + (pos % kSlots) * (uint32_t)kTile;
+                        ptx::mbar_arrive_expect_tx(bar, (uint32_t)kTile);
 #pragma unroll
-                for (int pc = 0; pc < 4; ++pc)
-                    ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, row, w.bh);
+                        for (int pc = 0; pc < 4; ++pc)
+                            ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, row, w.bh);
+                    }
+                }
             }
+        load_out:
             for (uint32_t i = (pos > (uint32_t)kSlots ? pos - kSlots : 0u); i < pos; ++i)
                 wait_drain(bar_addr(c, b_ring_full(i)), ring_par(i), c.limit);
         }
@@ -216,9 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
         auto vdesc = [&](uint32_t pos) {   // the same tile read as the MN-major operand
             return sw128_desc(ring + (pos % kSlots) * (uint32_t)kTile, kPanel64, 1024);
         };
-        // S(j) = Q K_j^T into buffer j % 2; K_j is then done
-        auto issue_s = [&](int j) -> bool {
-            const uint32_t pos = pos_k(j), b = (uint32_t)j & 1u;
+        // S(step g) = Q K^T into buffer g % 2 from the tile at ring position pos; K is then done
+        auto issue_s = [&](uint32_t g, uint32_t pos) -> bool {
+            const uint32_t b = g & 1u;
             if (!wait_warp(c, b_ring_full(pos), ring_par(pos), kRoleMma)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = kdesc(pos);
@@ -231,24 +252,35 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
             ptx::mma_commit_elect(bar_addr(c, b_ring_empty(pos)));
             return true;
         };
-        if (!wait_warp(c, b_q_ready(), 0, kRoleMma)) goto mma_out;
-        ptx::tc_fence_after();
-        if (!issue_s(0)) goto mma_out;
-        if (w.nkv > 1 && !issue_s(1)) goto mma_out;
-        for (int j = 0; j < w.nkv; ++j) {
-            const uint32_t b = (uint32_t)j & 1u, vpos = pos_v(j);
-            if (!wait_warp(c, b_p_full(b), (uint32_t)(j >> 1) & 1u, kRoleMma)) goto mma_out;
-            if (!wait_warp(c, b_ring_full(vpos), ring_par(vpos), kRoleMma)) goto mma_out;
-            ptx::tc_fence_after();
-            const uint64_t vd = vdesc(vpos);
+        uint32_t g = 0, items = 0, base = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const int nsub = unit_items<CAUSAL>(p, u);
+            for (int sub = 0; sub < nsub; ++sub) {
+                const Work w = unit_item<CAUSAL>(p, u, sub);
+                if (!wait_warp(c, b_q_ready(), items & 1u, kRoleMma)) goto mma_out;
+                ++items;
+                ptx::tc_fence_after();
+                if (!issue_s(g, base + 2u)) goto mma_out;
+                if (w.nkv > 1 && !issue_s(g + 1u, base + 4u)) goto mma_out;
+                for (int j = 0; j < w.nkv; ++j) {
+                    const uint32_t gj = g + (uint32_t)j, b = gj & 1u;
+                    const uint32_t vpos = base + 3u + 2u * (uint32_t)j;
+                    if (!wait_warp(c, b_p_full(b), (gj >> 1) & 1u, kRoleMma)) goto mma_out;
+                    if (!wait_warp(c, b_ring_full(vpos), ring_par(vpos), kRoleMma)) goto mma_out;
+                    ptx::tc_fence_after();
+                    const uint64_t vd = vdesc(vpos);
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-                ptx::mma_ts_elect(tm + kColO, tm + kColS + 64u * b + (uint32_t)kk * 8u,
-                                  vd + (uint64_t)((kk * 2048) >> 4), id_pv,
-                                  (j > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit_elect(bar_addr(c, b_o_done()));
-            ptx::mma_commit_elect(bar_addr(c, b_ring_empty(vpos)));
-            if (j + 2 < w.nkv && !issue_s(j + 2)) goto mma_out;
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        ptx::mma_ts_elect(tm + kColO, tm + kColS + 64u * b + (uint32_t)kk * 8u,
+                                          vd + (uint64_t)((kk * 2048) >> 4), id_pv,
+                                          (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_commit_elect(bar_addr(c, b_o_done()));
+                    ptx::mma_commit_elect(bar_addr(c, b_ring_empty(vpos)));
+                    if (j + 2 < w.nkv && !issue_s(gj + 2u, base + 2u + 2u * (uint32_t)(j + 2))) goto mma_out;
+                }
+                g += (uint32_t)w.nkv;
+                base += 2u + 2u * (uint32_t)w.nkv;
+            }
         }
     mma_out:
         ptx::mma_commit_elect(bar_addr(c, b_drain()));
@@ -257,116 +289,126 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
     } else {
         // softmax: thread = query row r (TMEM lane r)
         const int r = warp * 32 + lane;
-        const int i = w.qt * kBM + r;
-        const int limit = CAUSAL ? min(i + 1, p.n) : p.n;      // visible keys: key < limit
         const uint32_t tl = (uint32_t)(warp * 32) << 16;
         const float sl2 = p.scale_log2;
-        {
-            // Q row r into TMEM as 16-bit pairs; the two ring slots are then released
-            const bool ok = wait_warp(c, b_ring_full(0), 0, kRoleSoftmax) &&
-                            wait_warp(c, b_ring_full(1), 0, kRoleSoftmax);
-            if (ok) {
-                const int lr = r & 63;
-                const uint32_t src = ring + (uint32_t)(r >> 6) * kTile + (uint32_t)lr * 128u;
+        const uint32_t stage = sbase + (uint32_t)kStageOff + (uint32_t)warp * 4096u;
+        uint32_t g = 0, base = 0, pv = 0;   // pv: products of O issued before this item
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const int nsub = unit_items<CAUSAL>(p, u);
+            for (int sub = 0; sub < nsub; ++sub) {
+                const Work w = unit_item<CAUSAL>(p, u, sub);
+                const int i = w.qt * kBM + r;
+                const int limit = CAUSAL ? min(i + 1, p.n) : p.n;      // visible keys: key < limit
+                {
+                    // Q row r into TMEM as 16-bit pairs; the two ring slots are then released.
+                    // The previous item's products (which read Q) are complete: its
+                    // epilogue waited for the last of them.
+                    const bool ok = wait_warp(c, b_ring_full(base), ring_par(base), kRoleSoftmax) &&
+                                    wait_warp(c, b_ring_full(base + 1u), ring_par(base + 1u), kRoleSoftmax);
+                    if (ok) {
+                        const int lr = r & 63;
+                        const uint32_t src = ring + ((base + (uint32_t)(r >> 6)) % kSlots) * kTile +
+                                             (uint32_t)lr * 128u;
 #pragma unroll
-                for (int pc = 0; pc < 4; ++pc) {
-                    uint32_t q[32];
+                        for (int pc = 0; pc < 4; ++pc) {
+                            uint32_t q[32];
 #pragma unroll
-                    for (int cc = 0; cc < 8; ++cc) {
-                        const uint4 v = ptx::ld_shared_v4(src + (uint32_t)pc * kPanel64 +
-                                                          (uint32_t)((cc ^ (lr & 7)) * 16));
-                        q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
+                            for (int cc = 0; cc < 8; ++cc) {
+                                const uint4 v = ptx::ld_shared_v4(src + (uint32_t)pc * kPanel64 +
+                                                                  (uint32_t)((cc ^ (lr & 7)) * 16));
+                                q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
+                            }
+                            ptx::tmem_st32(tm + tl + kColQ + 32u * (uint32_t)pc, q);
+                        }
+                        ptx::tmem_wait_st();
                     }
-                    ptx::tmem_st32(tm + tl + kColQ + 32u * (uint32_t)pc, q);
+                    ptx::tc_fence_before();
+                    if (!sm_barrier_and(ok)) goto sm_out;
+                    if (threadIdx.x == 0) {
+                        ptx::mbar_arrive(bar_addr(c, b_ring_empty(base)));
+                        ptx::mbar_arrive(bar_addr(c, b_ring_empty(base + 1u)));
+                        ptx::mbar_arrive(bar_addr(c, b_q_ready()));
+                    }
                 }
-                ptx::tmem_wait_st();
-            }
-            ptx::tc_fence_before();
-            if (!sm_barrier_and(ok)) goto sm_out;
-            if (threadIdx.x == 0) {
-                ptx::mbar_arrive(bar_addr(c, b_ring_empty(0)));
-                ptx::mbar_arrive(bar_addr(c, b_ring_empty(1)));
-                ptx::mbar_arrive(bar_addr(c, b_q_ready()));
-            }
-        }
-        {
-            float m_run = -INFINITY, l_run = 0.0f;   // reference max (log2 units) and row sum
-            for (int j = 0; j < w.nkv; ++j) {
-                const uint32_t b = (uint32_t)j & 1u;
-                const uint32_t tS = tm + tl + kColS + 64u * b;
-                if (!wait_warp(c, b_s_full(b), (uint32_t)(j >> 1) & 1u, kRoleSoftmax)) goto sm_out;
-                ptx::tc_fence_after();
-                uint32_t s[64];
-                ptx::tmem_ld64_wait(tS, s);
-                const int key0 = j * kBN;
-                const bool mask = __any_sync(0xFFFFFFFFu, key0 + kBN > limit);
-                uint32_t pk[32];
-                const float alpha =
-                    mask ? softmax_step<true, F16>(s, key0, limit, sl2, m_run, l_run, pk)
-                         : softmax_step<false, F16>(s, key0, limit, sl2, m_run, l_run, pk);
-                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                    // The reference rose: O += P(j-1) V_{j-1} must be complete, then this
-                    // row of O is rescaled in TMEM.  (O += P(j-2) V is already complete: S(j)
-                    // was issued after it, so the parity wait below cannot be two phases
-                    // behind.)
-                    if (!wait_warp(c, b_o_done(), (uint32_t)(j - 1) & 1u, kRoleSoftmax)) goto sm_out;
+                float m_run = -INFINITY, l_run = 0.0f;   // reference max (log2 units) and row sum
+                for (int j = 0; j < w.nkv; ++j) {
+                    const uint32_t gj = g + (uint32_t)j, b = gj & 1u;
+                    const uint32_t tS = tm + tl + kColS + 64u * b;
+                    if (!wait_warp(c, b_s_full(b), (gj >> 1) & 1u, kRoleSoftmax)) goto sm_out;
                     ptx::tc_fence_after();
+                    uint32_t s[64];
+                    ptx::tmem_ld64_wait(tS, s);
+                    const int key0 = j * kBN;
+                    const bool mask = __any_sync(0xFFFFFFFFu, key0 + kBN > limit);
+                    uint32_t pk[32];
+                    const float alpha =
+                        mask ? softmax_step<true, F16>(s, key0, limit, sl2, m_run, l_run, pk)
+                             : softmax_step<false, F16>(s, key0, limit, sl2, m_run, l_run, pk);
+                    if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                        // The reference rose: O += P(j-1) V_{j-1} must be complete, then this
+                        // row of O is rescaled in TMEM.  (The product before it is already
+                        // complete: S(j) was issued after it, so the parity wait below cannot
+                        // be two phases behind.)
+                        if (!wait_warp(c, b_o_done(), (pv + (uint32_t)j - 1u) & 1u, kRoleSoftmax)) goto sm_out;
+                        ptx::tc_fence_after();
 #pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t o[32];
+                            ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)cc * 32u, o);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+                            ptx::tmem_st32(tm + tl + kColO + (uint32_t)cc * 32u, o);
+                        }
+                    }
+                    __syncwarp();
+                    ptx::tmem_st32(tS, pk);   // P over this buffer's first 32 columns
+                    ptx::tmem_wait_st();
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar_addr(c, b_p_full(b)));
+                }
+                // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.  A parity
+                // wait is only sound while the barrier is at most one phase behind the awaited
+                // one; the item's third-to-last product (or the previous item's last one) is
+                // known complete, so wait for the last two one at a time.
+                pv += (uint32_t)w.nkv;
+                if (w.nkv >= 2 && !wait_warp(c, b_o_done(), (pv - 2u) & 1u, kRoleSoftmax)) goto sm_out;
+                if (!wait_warp(c, b_o_done(), (pv - 1u) & 1u, kRoleSoftmax)) goto sm_out;
+                ptx::tc_fence_after();
+                const float inv = 1.0f / l_run;
+                uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)w.bh * p.n * D;
+                const int row0 = w.qt * kBM + warp * 32;
+#pragma unroll 1
+                for (int pc = 0; pc < D / 64; ++pc) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
                         uint32_t o[32];
-                        ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)cc * 32u, o);
+                        ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)(pc * 64 + h * 32), o);
+                        uint32_t wv[16];
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
-                        ptx::tmem_st32(tm + tl + kColO + (uint32_t)cc * 32u, o);
+                        for (int e = 0; e < 16; ++e) wv[e] = pack2<F16>(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const uint32_t chunk = (uint32_t)(h * 4 + e) ^ (uint32_t)(lane & 7);
+                            ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, wv[4 * e],
+                                              wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+                        }
                     }
-                }
-                __syncwarp();
-                ptx::tmem_st32(tS, pk);   // P over this buffer's first 32 columns
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar_addr(c, b_p_full(b)));
-            }
-            // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.
-            // A parity wait is only sound while the barrier is at most one phase behind the
-            // awaited one.  Here O += P(nkv-3) V is known complete (S(nkv-1) was issued
-            // after it), so wait for the last two products one at a time.
-            if (w.nkv >= 2 && !wait_warp(c, b_o_done(), (uint32_t)(w.nkv - 2) & 1u, kRoleSoftmax))
-                goto sm_out;
-            if (!wait_warp(c, b_o_done(), (uint32_t)(w.nkv - 1) & 1u, kRoleSoftmax)) goto sm_out;
-            ptx::tc_fence_after();
-            const float inv = 1.0f / l_run;
-            const uint32_t stage = sbase + (uint32_t)kStageOff + (uint32_t)warp * 4096u;
-            uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)w.bh * p.n * D;
-            const int row0 = w.qt * kBM + warp * 32;
-#pragma unroll 1
-            for (int pc = 0; pc < D / 64; ++pc) {
+                    __syncwarp();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t o[32];
-                    ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)(pc * 64 + h * 32), o);
-                    uint32_t wv[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) wv[e] = pack2<F16>(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint32_t chunk = (uint32_t)(h * 4 + e) ^ (uint32_t)(lane & 7);
-                        ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, wv[4 * e],
-                                          wv[4 * e + 1], wv[4 * e + 2], wv[4 * e + 3]);
+                    for (int k = 0; k < 8; ++k) {
+                        const int rr = 4 * k + (lane >> 3);
+                        const int ch = lane & 7;
+                        const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)rr * 128u +
+                                                          (uint32_t)((ch ^ (rr & 7)) * 16));
+                        if (row0 + rr < p.n)
+                            *reinterpret_cast<uint4*>(obase + (size_t)(row0 + rr) * D + pc * 64 + ch * 8) = v;
                     }
+                    __syncwarp();
                 }
-                __syncwarp();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int rr = 4 * k + (lane >> 3);
-                    const int ch = lane & 7;
-                    const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)rr * 128u +
-                                                      (uint32_t)((ch ^ (rr & 7)) * 16));
-                    if (row0 + rr < p.n)
-                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + rr) * D + pc * 64 + ch * 8) = v;
-                }
-                __syncwarp();
+                if (i < p.n) p.lse[(size_t)w.bh * p.n + i] = (m_run + log2f(l_run)) * kLn2;
+                g += (uint32_t)w.nkv;
+                base += 2u + 2u * (uint32_t)w.nkv;
             }
-            if (i < p.n) p.lse[(size_t)w.bh * p.n + i] = (m_run + log2f(l_run)) * kLn2;
         }
     sm_out:;
     }
@@ -390,10 +432,14 @@ cudaError_t tc256_prepare(bool causal, bool f16) {
                : set((const void*)fa_tc256_kernel<false, false>);
 }
 
-cudaError_t tc256_launch(bool causal, bool f16, const TcParams& p, cudaStream_t stream) {
-    const long long ctas = (long long)p.bh * ((p.n + kBM - 1) / kBM);
-    if (ctas < 1 || ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    const dim3 grid((unsigned)ctas);
+int tc256_units(int bh, int n, bool causal) {
+    const long long nt = (n + kBM - 1) / kBM;
+    const long long u = (long long)bh * (causal ? (nt + 1) / 2 : nt);
+    return u > 0x7FFFFFFFLL ? -1 : (int)u;
+}
+
+cudaError_t tc256_launch(bool causal, bool f16, const TcParams& p, int grid, cudaStream_t stream) {
+    if (grid < 1 || p.units < 1) return cudaErrorInvalidConfiguration;
     if (causal) {
         if (f16) fa_tc256_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
         else fa_tc256_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
