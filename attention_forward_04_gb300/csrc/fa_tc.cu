@@ -92,14 +92,25 @@ struct Geo {
     static constexpr int kStageSlot = 4096;
     static constexpr int kBarOff = kStageOff + kSoftmaxWarps * kStageSlot;
     // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2] o_done[2] drain
-    static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 1;
+    // s_read[2]
+    static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 2 + 2 + 1 + 2;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;     // tmem base, abort flag
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;     // + alignment slack
+    static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+    // TMEM columns of one tile's P: 16-bit pairs or e4m3 quadruples of kBN keys
+    static constexpr uint32_t kPCols = (uint32_t)(kBN * EB / 4);
+    // Where TMEM has room (D <= 64 at 16 bits, D = 64 at 8 bits), P gets columns of its own,
+    // so the next S product can be issued as soon as the softmax has read S, without waiting
+    // for P V.  Otherwise P overwrites the upper 64 columns of its S region (S columns 0-63
+    // stay readable until the next S product).
+    static constexpr bool kSepP = 2 * kBN + 2 * kPCols + 2 * D <= 512;
     static constexpr uint32_t col_s(int t) { return (uint32_t)t * kBN; }
-    // P (16-bit pairs) overwrites the upper 64 columns of its S region, so S columns 0-63
-    // stay readable until the next S product
-    static constexpr uint32_t col_p(int t) { return (uint32_t)t * kBN + 64u; }
-    static constexpr uint32_t col_o(int t) { return 2u * kBN + (uint32_t)t * D; }
+    static constexpr uint32_t col_p(int t) {
+        return kSepP ? 2u * kBN + (uint32_t)t * kPCols : (uint32_t)t * kBN + 64u;
+    }
+    static constexpr uint32_t col_o(int t) {
+        return (kSepP ? 2u * kBN + 2u * kPCols : 2u * kBN) + (uint32_t)t * D;
+    }
 };
 
 // Barrier indices.
@@ -111,6 +122,7 @@ template <int D, int EB> __device__ __forceinline__ int b_s_full(int t) { return
 template <int D, int EB> __device__ __forceinline__ int b_p_full(int t) { return 6 + 2 * Geo<D, EB>::kSlots + t; }
 template <int D, int EB> __device__ __forceinline__ int b_o_done(int t) { return 8 + 2 * Geo<D, EB>::kSlots + t; }
 template <int D, int EB> __device__ __forceinline__ int b_drain() { return 10 + 2 * Geo<D, EB>::kSlots; }
+template <int D, int EB> __device__ __forceinline__ int b_s_read(int t) { return 11 + 2 * Geo<D, EB>::kSlots + t; }
 
 // Ring position i -> phase parity of its slot.
 template <int D, int EB> __device__ __forceinline__ uint32_t ring_parity(uint32_t i) {
@@ -358,6 +370,89 @@ out:
     __syncwarp();
 }
 
+// MMA issuer when P has TMEM columns of its own: each tile's next S product is issued as soon
+// as the softmax has read the current S (s_read), ahead of O += P V.  Per 128-key step:
+// S_A(j+1) S_B(j+1) | PV_A(j) PV_B(j).  The whole warp runs this loop; one lane issues.
+template <int D, bool CAUSAL, int ET, int MODE>
+__device__ void mma_role_sep(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_t sbase) {
+    constexpr int EB = Elem<ET>::kBytes;
+    using G = Geo<D, EB>;
+    constexpr uint32_t idesc_qk = idesc_of<ET>(kBM, kBN, false);
+    constexpr uint32_t idesc_pv = idesc_of<ET>(kBM, D, true);
+    const uint64_t dQ[2] = {tile_desc<D, EB>(sbase, 16),
+                            tile_desc<D, EB>(sbase + (uint32_t)G::kTileBytes, 16)};
+    const uint64_t dK0 = tile_desc<D, EB>(sbase + (uint32_t)G::kKVOff, 16);                       // K-major
+    const uint64_t dV0 = tile_desc<D, EB>(sbase + (uint32_t)G::kKVOff, (uint32_t)G::kPanelBytes);  // MN-major
+    const uint32_t tS[2] = {tmem + G::col_s(0), tmem + G::col_s(1)};
+    const uint32_t tP[2] = {tmem + G::col_p(0), tmem + G::col_p(1)};
+    const uint32_t tO[2] = {tmem + G::col_o(0), tmem + G::col_o(1)};
+    auto slot_off = [&](uint32_t i) { return (uint64_t)((i % G::kSlots) * (uint32_t)G::kTileBytes) >> 4; };
+    uint32_t kv = 0, q_cnt = 0, p_cnt[2] = {0, 0}, sr_cnt[2] = {0, 0}, s_issued[2] = {0, 0};
+    // S into tile t's region: the softmax must have read the previous S there
+    auto issue_s = [&](int t, uint32_t kpos) -> bool {
+        if (s_issued[t] > 0) {
+            if (!wait_warp(c, b_s_read<D, EB>(t), sr_cnt[t] & 1u, kRoleMma)) return false;
+            ++sr_cnt[t];
+        }
+        ptx::tc_fence_after();
+        issue_qk<D, ET>(tS[t], dQ[t], dK0 + slot_off(kpos), idesc_qk);
+        ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(t)));
+        ++s_issued[t];
+        return true;
+    };
+    auto issue_o = [&](int t, uint32_t vpos, bool accumulate) -> bool {   // O_t (+)= P_t V_j
+        if (!wait_warp(c, b_p_full<D, EB>(t), p_cnt[t] & 1u, kRoleMma)) return false;
+        ++p_cnt[t];
+        ptx::tc_fence_after();
+        issue_pv<D, ET>(tO[t], tP[t], dV0 + slot_off(vpos), idesc_pv, accumulate);
+        ptx::mma_commit_elect(bar_addr(c, b_o_done<D, EB>(t)));
+        return true;
+    };
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const int nsub = unit_count<CAUSAL, MODE>(p, u);
+        for (int sub = 0; sub < nsub; ++sub) {
+            const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
+            if (!wait_warp(c, b_q_full<D, EB>(0), q_cnt & 1u, kRoleMma)) goto out;
+            if (!wait_warp(c, b_kv_full<D, EB>(kv), ring_parity<D, EB>(kv), kRoleMma)) goto out;
+            if (!issue_s(0, kv)) goto out;
+            if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
+            if (!wait_warp(c, b_q_full<D, EB>(1), q_cnt & 1u, kRoleMma)) goto out;
+            ++q_cnt;
+            if (!issue_s(1, kv)) goto out;
+            if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+            ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kv)));   // K_0
+            ++kv;
+
+            for (int j = 0; j < it.nB; ++j) {
+                const uint32_t vpos = kv;        // V_j
+                const uint32_t kpos = kv + 1;    // K_{j+1}
+                const bool more = j + 1 < it.nB;
+                if (more) {
+                    if (!wait_warp(c, b_kv_full<D, EB>(kpos), ring_parity<D, EB>(kpos), kRoleMma)) goto out;
+                    if (j + 1 < it.nA) {
+                        if (!issue_s(0, kpos)) goto out;
+                        if (j + 2 == it.nA) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
+                    }
+                    if (!issue_s(1, kpos)) goto out;
+                    if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+                    ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kpos)));   // K_{j+1}
+                }
+                if (!wait_warp(c, b_kv_full<D, EB>(vpos), ring_parity<D, EB>(vpos), kRoleMma)) goto out;
+                if (j < it.nA && !issue_o(0, vpos, j > 0)) goto out;
+                if (!issue_o(1, vpos, j > 0)) goto out;
+                ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(vpos)));      // V_j
+                kv += more ? 2u : 1u;
+            }
+        }
+    }
+out:
+    // Every product issued so far must finish before TMEM is released.
+    ptx::mma_commit_elect(bar_addr(c, b_drain<D, EB>()));
+    wait_drain(bar_addr(c, b_drain<D, EB>()), 0, c.limit);
+    __syncwarp();
+}
+
 template <int D, int EB, bool CAUSAL, int MODE>
 __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
     using G = Geo<D, EB>;
@@ -471,14 +566,16 @@ __device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[128], int kbas
 
 // One 128-key tile of one row: running-max update (raised only when the tile max exceeds
 // it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tP in two
-// halves (64 columns of 16-bit pairs, or 32 columns of e4m3 quadruples).  Returns the O
-// rescale factor.
-template <bool MASK, int ET>
-__device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
-                                              float sl2, float& m_run, float& l_run,
-                                              uint32_t tP) {
+// halves (64 columns of 16-bit pairs, or 32 columns of e4m3 quadruples).  before_store()
+// runs once, after the first half is computed and before anything is stored; false from
+// it abandons the tile (returns false).  alpha receives the O rescale factor.
+template <bool MASK, int ET, class BeforeStore>
+__device__ __forceinline__ bool softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
+                                             float sl2, float& m_run, float& l_run,
+                                             uint32_t tP, float& alpha,
+                                             BeforeStore&& before_store) {
     const float mt = tile_row_max<MASK>(s, kbase, limit) * sl2;  // log2 units
-    float alpha = 1.0f;
+    alpha = 1.0f;
     if (mt > m_run + Lazy<ET>::kRescaleLog2) {
         alpha = ptx::ex2(m_run - mt);   // m_run = -inf on the first tile: alpha = 0
         m_run = mt;
@@ -487,6 +584,7 @@ __device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbas
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     uint32_t pk[64];
     tile_exp_half<0, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
+    if (!before_store()) return false;
     __syncwarp();
     if constexpr (ET == 2) ptx::tmem_st16(tP, &pk[0]);
     else ptx::tmem_st32p(tP, &pk[0]);
@@ -496,7 +594,7 @@ __device__ __forceinline__ float softmax_tile(const uint32_t (&s)[128], int kbas
     else ptx::tmem_st32p(tP + 32, &pk[32]);
     const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     l_run = l_run * alpha + sum;
-    return alpha;
+    return true;
 }
 
 template <int D, bool CAUSAL, int ET, int MODE>
@@ -527,18 +625,33 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             for (int j = 0; j < n; ++j) {
                 if (!wait_warp(c, b_s_full<D, EB>(t), s_cnt & 1u, kRoleSoftmax)) return;
                 ++s_cnt;
-                if (j > 0) {  // O_t += P(j-1) V(j-1) is complete before S(j) is (issue order)
+                if (!G::kSepP && j > 0) {  // O_t += P(j-1) V(j-1) is complete before S(j) is (issue order)
                     if (!wait_warp(c, b_o_done<D, EB>(t), o_cnt & 1u, kRoleSoftmax)) return;
                     ++o_cnt;
                 }
                 ptx::tc_fence_after();
                 uint32_t s[128];
                 ptx::tmem_ld128_wait(tS, s);
+                if constexpr (G::kSepP) {   // S may now be overwritten by the next S product
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar_addr(c, b_s_read<D, EB>(t)));
+                }
                 const int kbase = j * kBN;
                 const bool mask = __any_sync(0xFFFFFFFFu, kbase + kBN > limit);
-                const float alpha =
-                    mask ? softmax_tile<true, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP)
-                         : softmax_tile<false, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP);
+                // With separate P columns, O_t += P(j-1) V(j-1) must be complete before P is
+                // overwritten (it reads those columns) and before O_t is rescaled below.
+                auto before_store = [&]() -> bool {
+                    if (!G::kSepP || j == 0) return true;
+                    if (!wait_warp(c, b_o_done<D, EB>(t), o_cnt & 1u, kRoleSoftmax)) return false;
+                    ++o_cnt;
+                    ptx::tc_fence_after();
+                    return true;
+                };
+                float alpha;
+                const bool ok =
+                    mask ? softmax_tile<true, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, alpha, before_store)
+                         : softmax_tile<false, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, alpha, before_store);
+                if (!ok) return;
                 if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                     // The running max rose: rescale this row of O by alpha in TMEM.
 #pragma unroll 1
@@ -661,6 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
             ptx::mbar_init(bar_addr(c, b_s_full<D, EB>(t)), 1);
             ptx::mbar_init(bar_addr(c, b_p_full<D, EB>(t)), 128);
             ptx::mbar_init(bar_addr(c, b_o_done<D, EB>(t)), 1);
+            ptx::mbar_init(bar_addr(c, b_s_read<D, EB>(t)), 128);
         }
         for (int s = 0; s < G::kSlots; ++s) {
             ptx::mbar_init(bar_addr(c, b_kv_full<D, EB>(s)), 1);
@@ -688,7 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
         softmax_role<D, CAUSAL, ET, MODE>(p, c, tmem, warp, lane,
                                      sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
     } else if (warp == kMmaWarp) {
-        mma_role<D, CAUSAL, ET, MODE>(p, c, tmem, sbase);
+        if constexpr (G::kSepP) mma_role_sep<D, CAUSAL, ET, MODE>(p, c, tmem, sbase);
+        else mma_role<D, CAUSAL, ET, MODE>(p, c, tmem, sbase);
     } else {
         if (lane == 0) load_role<D, EB, CAUSAL, MODE>(p, c, sbase);
         __syncwarp();

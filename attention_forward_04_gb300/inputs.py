@@ -74,6 +74,9 @@ WORKLOADS = {
                                           True, 8100),
     # head dimension 32 (the "第 13 课" exercise's d), same FLOPs as the headline workload
     "bf16_b8h32n4096d32": Workload("bf16_b8h32n4096d32", 8, 32, 4096, 32, "bf16", False, 7000),
+    # head dimension 64 (the small shape's d) at full size, 16-bit and e4m3 inputs
+    "bf16_b8h16n4096d64": Workload("bf16_b8h16n4096d64", 8, 16, 4096, 64, "bf16", False, 7100),
+    "fp8_b8h16n4096d64": Workload("fp8_b8h16n4096d64", 8, 16, 4096, 64, "fp8", False, 8200),
 }
 
 # The workload the throughput metric is quoted on.

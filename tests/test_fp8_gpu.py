@@ -96,7 +96,8 @@ def test_fp8_large_scores_force_rescales():
         compare(w, what="fp8 x4 causal=%d" % causal)
 
 
-@pytest.mark.parametrize("name", ["fp8_b4h16n4096d128", "fp8_b8h32n4096d128_causal"])
+@pytest.mark.parametrize("name", ["fp8_b4h16n4096d128", "fp8_b8h32n4096d128_causal",
+                                  "fp8_b8h16n4096d64"])
 def test_fp8_full_size_sampled_slices(name):
     w = WORKLOADS[name]
     BH = w.B * w.H

@@ -205,7 +205,7 @@ def test_small_workloads_full(name):
 @pytest.mark.parametrize("name", ["bf16_b4h16n4096d128", "bf16_b8h32n4096d128_causal",
                                   "bf16_b1h32n16384d128_x2", "bf16_b1h32n16384d128_x2_causal",
                                   "bf16_b4h8n4096d256", "bf16_b4h8n4096d256_causal",
-                                  "bf16_b8h32n4096d32"])
+                                  "bf16_b8h32n4096d32", "bf16_b8h16n4096d64"])
 def test_full_size_workloads_sampled(name):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)
