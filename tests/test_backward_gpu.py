@@ -1,7 +1,7 @@
 """GPU parity of the backward (fa_bwd through the C ABI) against the fp64 backward oracle.
 
 Tolerance, derived from the kernel's arithmetic and applied element by element.  With u the
-unit roundoff of the 16-bit storage type (2^-9 bf16, 2^-11 fp16), P and dS the oracle's
+unit roundoff of the 16-bit storage type (2^-8 bf16, 2^-11 fp16: 8 and 11 significant bits), P and dS the oracle's
 probabilities and softmax derivative, and e_p = |LSE_gpu - LSE_oracle| + 1e-4 the relative
 error of the kernel's rebuilt P (its forward LSE error, plus fp32 accumulation of S and ex2):
   * dV = P^T dO with P rounded to 16 bits before the product:
@@ -31,7 +31,7 @@ from oracle.backward import attention_bwd
 
 pytestmark = pytest.mark.gpu
 
-U = {"bf16": 2.0 ** -9, "fp16": 2.0 ** -11}
+U = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -4,11 +4,11 @@ The oracle reads the dequantised inputs descale * x8 exactly (fp8 values times f
 factors, in fp64).  Tolerance, element-wise on O, derived from the kernel's rounding
 points: P is rounded to e4m3 before P V (unit roundoff u8 = 2^-4 for normal values, and at
 most 2^-10 absolute below the smallest normal 2^-6; P never exceeds 2^8 < 448, so nothing
-saturates), then O is rounded to bf16 (u = 2^-9).  With P the oracle's probabilities and
+saturates), then O is rounded to bf16 (u = 2^-8: 8 significant bits).  With P the oracle's probabilities and
 l >= 1 the oracle's row sum relative to the row maximum (the kernel's own sum relative to
 its reference maximum is never smaller):
     |O - O_oracle| <= v_descale * (u8 * sum_j P_ij |v8_j| + 2^-10 * sum_j |v8_j| / l_i)
-                      + 2^-9 |O_oracle| + 1e-4 * sum_j P_ij |v_j|
+                      + 2^-8 |O_oracle| + 1e-4 * sum_j P_ij |v_j|
 (the last term covers fp32 score accumulation and ex2).  The test allows twice the bound
 plus 1e-5.  LSE is formed from fp32 sums and keeps the bf16 path's 1e-3.
 """
@@ -49,7 +49,7 @@ def bound(q, k, v8, vd, scale, causal, o_ref, lse_ref):
     av = np.abs(v8)
     vis = np.tril(np.ones((N, N))) if causal else np.ones((N, N))
     t = vd * (2.0 ** -4 * (P @ av) + 2.0 ** -10 * (vis @ av) / l[:, None])
-    t += 2.0 ** -9 * np.abs(o_ref) + 1e-4 * (P @ (vd * av))
+    t += 2.0 ** -8 * np.abs(o_ref) + 1e-4 * (P @ (vd * av))
     return 2.0 * t + 1e-5
 
 

@@ -85,7 +85,7 @@ def test_131072_tokens_fp8():
         P = np.exp(s - l_ref[n_])
         l = np.exp(l_ref[n_] - s.max())                    # row sum relative to the maximum
         t = vd * (2.0 ** -4 * (P @ av[: r + 1]) + 2.0 ** -10 * av[: r + 1].sum(0) / l)
-        t += 2.0 ** -9 * np.abs(o_ref[n_]) + 1e-4 * vd * (P @ av[: r + 1])
+        t += 2.0 ** -8 * np.abs(o_ref[n_]) + 1e-4 * vd * (P @ av[: r + 1])
         err = np.abs(og[n_] - o_ref[n_])
         assert np.all(err <= 2.0 * t + 1e-5), "fp8 N=131072 row %d: err %.3e" % (r, err.max())
         assert abs(lg[n_] - l_ref[n_]) <= 1e-3, "fp8 N=131072 row %d LSE" % r
