@@ -1,0 +1,117 @@
+"""The rescale condition: a stale running reference is exact after the final division.
+
+"08 · FlashAttention" §五 and "第 13 课：GPU 内核与 FlashAttention" §4B rescale the old
+output by exp(m_old - m_new) whenever a larger maximum appears (the literal reading,
+tau = 0).  The kernels raise the reference only when a 128-key tile's maximum exceeds it by
+more than tau log2 units (tau = 16 for bf16 P, 8 for fp16 and e4m3 P); below that, the
+exponentials are taken against the stale reference.  O and l share the reference, so the
+final division cancels it.
+
+These CPU tests state that recurrence in fp64 (the order of the kernels' steps, not their
+code) and check it against the three-pass fp64 oracle for tau in {0, 8, 16}: exact (to
+fp64 rounding) with P kept in fp64, and within the bf16 / fp16 output tolerances and the
+derived rounding bound with P rounded to the storage type before the P V product, as the
+kernels do.  A planted mistake (the reference raised without rescaling O and l) must fail.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+LOG2E = 1.0 / math.log(2.0)
+
+
+def lazy_attention(q, k, v, scale, causal, tau, p_dtype=None, plant=None, block=128):
+    """One [N, D] slice by the lazy-reference online softmax.  The reference m (log2 units)
+    is raised to the tile maximum only when that maximum exceeds it by more than tau; O and
+    l are then multiplied by 2^(m_old - m_new).  P is optionally rounded to p_dtype before
+    P V (l keeps the unrounded values).  Returns (O, LSE)."""
+    n, d = q.shape
+    O = np.zeros((n, d))
+    l = np.zeros(n)
+    m = np.full(n, -np.inf)
+    rows = np.arange(n)
+    for j0 in range(0, n, block):
+        j1 = min(n, j0 + block)
+        x = scale * LOG2E * (q @ k[j0:j1].T)            # scores in log2 units
+        if causal:
+            x = np.where(np.arange(j0, j1)[None, :] <= rows[:, None], x, -np.inf)
+        live = np.isfinite(x).any(axis=1)
+        tmax = np.where(live, x.max(axis=1, initial=-np.inf), -np.inf)
+        raise_ = live & (tmax > m + tau)
+        alpha = np.where(raise_, np.exp2(np.where(raise_, m - tmax, 0.0)), 1.0)
+        m = np.where(raise_, tmax, m)
+        if plant != "no_rescale":
+            O = O * alpha[:, None]
+            l = l * alpha
+        p = np.where(live[:, None], np.exp2(x - np.where(live, m, 0.0)[:, None]), 0.0)
+        l = l + p.sum(axis=1)
+        if p_dtype is not None:
+            p = torch.from_numpy(p).to(p_dtype).double().numpy()
+        O = O + p @ v[j0:j1]
+    return O / l[:, None], (m + np.log2(l)) * math.log(2.0)
+
+
+def rnd(shape, seed, mult=1.0):
+    return np.random.default_rng(seed).standard_normal(shape) * mult
+
+
+def compare(n, d, causal, mult, seed, tau, p_dtype=None, plant=None):
+    q, k, v = rnd((n, d), seed, mult), rnd((n, d), seed + 1, mult), rnd((n, d), seed + 2)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, l_ref = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], scale, causal)
+    o, lse = lazy_attention(q, k, v, scale, causal, tau, p_dtype, plant)
+    return float(np.max(np.abs(o - o_ref[0, 0]))), float(np.max(np.abs(lse - l_ref[0, 0])))
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("mult", [1.0, 4.0])
+def test_stale_reference_is_exact_in_fp64(tau, causal, mult):
+    # mult = 4 spreads the scores over tens of log2 units, so the reference is raised
+    # several times along each row for every tau
+    eo, el = compare(700, 64, causal, mult, 31, tau)
+    assert eo < 1e-12 and el < 1e-12, (eo, el)
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
+@pytest.mark.parametrize("p_dtype,tol_o", [(torch.bfloat16, 2e-2), (torch.float16, 2e-3)])
+def test_rounded_p_within_tolerance_for_every_tau(tau, p_dtype, tol_o):
+    for causal in (False, True):
+        for mult in (1.0, 4.0):
+            eo, el = compare(600, 128, causal, mult, 57, tau, p_dtype)
+            assert eo < tol_o and el < 1e-6, (causal, mult, eo, el)
+
+
+@pytest.mark.parametrize("tau", [0.0, 8.0, 16.0])
+def test_rounded_p_error_bound(tau):
+    # P rounded to nearest (unit roundoff u) with l summed from the unrounded values and
+    # O accumulated exactly: O_err = sum_j delta_j p_j v_j / l with |delta_j| <= u, so
+    # |O_err| <= u * max_j |v_j| per column, whatever the reference.  A fresh reference
+    # makes the row maximum's p exactly 1 (no rounding), so on peaked rows (scores x4) the
+    # literal reading's error sits well below the bound and the stale reference's nearer
+    # to it; both stay inside it.
+    for p_dtype, u in ((torch.bfloat16, 2.0 ** -8), (torch.float16, 2.0 ** -11)):
+        for causal in (False, True):
+            n, d, seed = 900, 64, 77
+            q, k, v = rnd((n, d), seed, 4.0), rnd((n, d), seed + 1, 4.0), rnd((n, d), seed + 2)
+            scale = 1.0 / math.sqrt(d)
+            o_ref, _ = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], scale, causal)
+            o, _ = lazy_attention(q, k, v, scale, causal, tau, p_dtype)
+            err = np.abs(o - o_ref[0, 0])
+            if causal:   # row i sees keys 0..i only
+                vmax = np.maximum.accumulate(np.abs(v), axis=0)
+            else:
+                vmax = np.broadcast_to(np.abs(v).max(axis=0), v.shape)
+            assert np.all(err <= u * vmax * (1 + 1e-9) + 1e-12), (p_dtype, causal, float(err.max()))
+
+
+@pytest.mark.parametrize("tau", [0.0, 16.0])
+def test_planted_missing_rescale_fails(tau):
+    # raising the reference without rescaling O and l must be caught (scores spread wide
+    # enough that the reference moves after the first tile even with tau = 16)
+    eo, el = compare(700, 64, False, 6.0, 91, tau, plant="no_rescale")
+    assert eo > 1e-3 or el > 1e-3, (eo, el)
