@@ -155,15 +155,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle leg
-def time_oracle(w, budget_s: float, host_qkv):
+def time_oracle(w, budget_s: float, host_qkv, threads: int = 0):
     """Time the fp64 oracle, as it stands, on a bounded sample of the workload: whole
-    (b, h) slices, as many as fit the time budget (at least one).
-    Returns (tflops, seconds, slices, threads)."""
+    (b, h) slices, as many as fit the time budget (at least one), on `threads` host
+    threads (0: all cores).  Returns (tflops, seconds, slices, threads)."""
     import numpy as np
     import oracle
     BH = w.B * w.H
     q, k, v = (t.reshape(1, BH, w.N, w.D) for t in host_qkv)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     # estimate the cost of one slice from a probe of 64 rows spread over the slice
     rows = np.unique(np.linspace(0, w.N - 1, min(w.N, 64)).astype(np.int64))
     q0, k0, v0 = (t[:, :1].double().numpy() for t in (q, k, v))
@@ -695,6 +695,11 @@ def main():
                    "sample": "%d of %d (b,h) slices of %s (N=%d, D=%d, causal=%s), whole "
                              "slices, fp64 three-pass oracle, %.1f s"
                              % (ns, B * H, w.name, N, D, w.causal, secs)}
+            # the same oracle on one host thread, on a sample of its own budget
+            tfl1, secs1, ns1, _ = time_oracle(w, args.cpu_budget / 2, host_set, threads=1)
+            cpu["single_thread"] = {"value": tfl1, "unit": "TFLOPS", "cores": 1,
+                                    "sample": "%d of %d (b,h) slices, whole slices, %.1f s"
+                                              % (ns1, B * H, secs1)}
         except Exception as ex:  # the CPU leg must not hide the GPU number
             cpu = {"value": None, "unit": "TFLOPS", "cores": None, "kind": "oracle",
                    "sample": "failed: %s" % ex}
