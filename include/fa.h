@@ -141,7 +141,7 @@ int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
  *     delta_i = sum_d dO_id O_id,  dS = P * (dO V^T - delta),
  *     dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
  * P is rebuilt from the forward's LSE instead of being stored ("08 · FlashAttention" §三
- * 反向传播; "第 13 课：FlashAttention" §4B); the formulas are the chain rule through the
+ * 反向传播; "第 13 课：GPU 内核与 FlashAttention" §4B); the formulas are the chain rule through the
  * softmax of "KingOfEgg: Flash Attention v1" §1.1.
  *
  *   q, k, v, o, dout : device pointers, [B, H, N, D] contiguous, element type `dtype`;
