@@ -1,0 +1,46 @@
+"""bench.py's contract on the CPU: the reference arm (the fp64 oracle, timed on the host)
+prints one complete JSON line, and the GPU arm fails loudly where there is no GPU instead
+of falling back to anything."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_bench(*args, timeout=300):
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_prints_one_complete_line():
+    r = run_bench("--impl", "reference", "--steps", "1", "--warmup", "0",
+                  "--workload", "bf16_b2h8n1024d64")
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1, lines
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["metric"].startswith("attention fwd TFLOPS")
+    assert d["unit"] == "TFLOPS" and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["n_gpus"] == 1 and d["steps"] == 1
+    assert d["warmup"] >= 3                      # at least three warm-up steps, always
+    assert d["config"]["workload"] == "bf16_b2h8n1024d64"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
+def test_gpu_arm_fails_without_a_gpu():
+    r = run_bench("--steps", "1", "--warmup", "3", "--cpu-budget", "0", timeout=120)
+    assert r.returncode != 0
+    assert not r.stdout.strip()                  # no bench line without the CUDA path
