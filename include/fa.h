@@ -34,7 +34,7 @@ typedef enum {
 typedef enum {
     FA_OK = 0,
     FA_ERR_INVALID_ARG = 1, /* null pointer, size out of range, bad flag, output overlaps an input */
-    FA_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (D, dtype, GPU model)       */
+    FA_ERR_UNSUPPORTED = 2, /* valid request the library does not serve (D, dtype, GPU model)      */
     FA_ERR_MISALIGNED = 3,  /* a tensor pointer is not 16-byte aligned (TMA needs 16 B)             */
     FA_ERR_CUDA = 4,        /* a CUDA runtime call or the kernel launch failed                      */
     FA_ERR_TIMEOUT = 5      /* a kernel wait ran past its limit (reported by fa_check_device_status) */
