@@ -118,13 +118,16 @@ def fwd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None):
         raise TypeError("q, k, v must share one dtype")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous [B, H, N, D]")
+    _same_device(q, k, v)
     B, H, N, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
+    _check_buffer(out, "out", q.shape, q.dtype, q.device)
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check_buffer(lse, "lse", (B, H, N), torch.float32, q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
@@ -148,10 +151,13 @@ def fwd_fp8(q, k, v, q_descale, k_descale, v_descale, scale=None, causal=False, 
     for t in (q, k, v):
         if t.dtype != torch.float8_e4m3fn or not t.is_contiguous():
             raise TypeError("q, k, v must be contiguous torch.float8_e4m3fn tensors")
+    _same_device(q, k, v)
     B, H, N, D = q.shape
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     out = torch.empty((B, H, N, D), dtype=torch.bfloat16, device=q.device) if out is None else out
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_buffer(out, "out", (B, H, N, D), torch.bfloat16, q.device)
+    _check_buffer(lse, "lse", (B, H, N), torch.float32, q.device)
     with torch.cuda.device(q.device):
         _check(int(load_library().fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                              out.data_ptr(), lse.data_ptr(), B, H, N, D,
@@ -170,6 +176,23 @@ def _common(q, k, v, ndim):
         raise TypeError("q, k, v must share one dtype")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
+    _same_device(q, k, v)
+
+
+def _check_buffer(t, name, shape, dtype, device):
+    """A caller-supplied tensor the library writes or reads by pointer: it must have exactly
+    the shape and dtype the call implies, be contiguous, and live on the inputs' device
+    (the library cannot see buffer sizes, so a mismatch is refused here)."""
+    if not t.is_cuda or t.device != device:
+        raise ValueError("%s must be a CUDA tensor on %s" % (name, device))
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous %s tensor of shape %s" % (name, dtype, tuple(shape)))
+
+
+def _same_device(q, *others):
+    for t in others:
+        if t.device != q.device:
+            raise ValueError("all tensors must be on %s" % q.device)
 
 
 def _stream_handle(q, stream):
@@ -189,6 +212,8 @@ def fwd_bnhd(q, k, v, scale=None, causal=False, out=None, lse=None, stream=None)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_buffer(out, "out", q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", (B, H, N), torch.float32, q.device)
     with torch.cuda.device(q.device):
         _check(int(load_library().fa_fwd_bnhd(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                               out.data_ptr(), lse.data_ptr(), B, N, H, D,
@@ -205,13 +230,16 @@ def fwd_varlen(q, k, v, cu_seqlens, max_seqlen, scale=None, causal=False, out=No
     Returns (o [total, H, D], lse [H, total] fp32)."""
     import torch
     _common(q, k, v, 3)
-    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1):
-        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor")
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1
+            and cu_seqlens.is_contiguous() and cu_seqlens.device == q.device):
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor on %s" % q.device)
     T, H, D = q.shape
     batch = cu_seqlens.numel() - 1
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     out = torch.empty_like(q) if out is None else out
     lse = torch.empty((H, T), dtype=torch.float32, device=q.device) if lse is None else lse
+    _check_buffer(out, "out", q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", (H, T), torch.float32, q.device)
     with torch.cuda.device(q.device):
         _check(int(load_library().fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(),
                                                 out.data_ptr(), lse.data_ptr(),
@@ -235,21 +263,23 @@ def bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=No
     """
     import torch
     _common(q, k, v, 4)
-    for t in (o, dout):
-        if not t.is_cuda or t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
-            raise ValueError("o and dout must be contiguous CUDA tensors shaped and typed like q")
     B, H, N, D = q.shape
-    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    _check_buffer(o, "o", q.shape, q.dtype, q.device)
+    _check_buffer(dout, "dout", q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", (B, H, N), torch.float32, q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(q) if dk is None else dk
     dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_buffer(t, name, q.shape, q.dtype, q.device)
     need = bwd_workspace_bytes(B, H, N)
     if need < 0:
         raise FaError(1, "B, H or N out of range")
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if not (workspace.is_cuda and workspace.device == q.device and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on %s" % q.device)
     with torch.cuda.device(q.device):
         _check(int(load_library().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                          dout.data_ptr(), lse.data_ptr(), dq.data_ptr(),
@@ -266,6 +296,9 @@ def bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, str
     import torch
     _common(q, k, v, 4)
     B, H, N, D = q.shape
+    for name, t in (("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_buffer(t, name, q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", (B, H, N), torch.float32, q.device)
     scale = 1.0 / math.sqrt(D) if scale is None else scale
     with torch.cuda.device(q.device):
         _check(int(load_library().fa_bwd_noalloc(
