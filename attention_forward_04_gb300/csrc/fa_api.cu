@@ -31,8 +31,8 @@ struct DeviceInfo {
     int major = 0, minor = 0;
     std::once_flag prepared[3][2][3];  // [D = 32, 64, 128][causal][bf16, fp16, fp8]
     cudaError_t prepare_err[3][2][3] = {};
-    std::once_flag bwd_prepared[2][2][2];
-    cudaError_t bwd_prepare_err[2][2][2] = {};
+    std::once_flag bwd_prepared[3][2][2];   // [D = 32, 64, 128][causal][f16]
+    cudaError_t bwd_prepare_err[3][2][2] = {};
     std::once_flag prepared256[2][2];  // [causal][f16]
     cudaError_t prepare256_err[2][2] = {};
 };
@@ -353,7 +353,7 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
     if (dtype == FA_FP32) return FA_ERR_UNSUPPORTED;   // backward: 16-bit storage only
-    if (D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
+    if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     const int64_t BH = B * H;
     const size_t tbytes = (size_t)BH * (size_t)N * (size_t)D * 2;
     const size_t lbytes = (size_t)BH * (size_t)N * sizeof(float);
@@ -393,11 +393,11 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
     if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;
     const bool f16 = dtype == FA_FP16;
-    const int di128 = D == 128, dic = causal != 0, dif = f16;
-    std::call_once(di.bwd_prepared[di128][dic][dif],
-                   [&] { di.bwd_prepare_err[di128][dic][dif] = fa::bwd_prepare((int)D, dic, f16); });
-    if (di.bwd_prepare_err[di128][dic][dif] != cudaSuccess)
-        return fail_cuda(di.bwd_prepare_err[di128][dic][dif], "cudaFuncSetAttribute (backward)");
+    const int dix = D == 32 ? 0 : D == 64 ? 1 : 2, dic = causal != 0, dif = f16;
+    std::call_once(di.bwd_prepared[dix][dic][dif],
+                   [&] { di.bwd_prepare_err[dix][dic][dif] = fa::bwd_prepare((int)D, dic, f16); });
+    if (di.bwd_prepare_err[dix][dic][dif] != cudaSuccess)
+        return fail_cuda(di.bwd_prepare_err[dix][dic][dif], "cudaFuncSetAttribute (backward)");
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
     if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
 
@@ -411,6 +411,8 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     p.lse = lse;
     p.o = o;
+    p.q = q;
+    p.dout = dout;
     p.delta = static_cast<float*>(workspace);
     p.dq = dq;
     p.dk = dk;

@@ -51,12 +51,32 @@ constexpr int kLoadWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Rows of a 128 x D tile in shared memory: panels of 128-byte rows (128-byte swizzle), or
+// one panel of 64-byte rows (64-byte swizzle) at D = 32, as TMA writes them.
+template <int D>
+struct Rows {
+    static constexpr int kRowBytes = D * 2 < 128 ? D * 2 : 128;
+    static constexpr int kCols = kRowBytes / 2;               // 16-bit values per panel row
+    static constexpr int kPanelBytes = kT * kRowBytes;        // one 128-row panel
+    static constexpr int kPanels = D / kCols;
+    static constexpr uint32_t kSBO = 8u * kRowBytes;          // 8-row group stride
+    static constexpr uint64_t kLayout = kRowBytes == 128 ? 2ull : 4ull;   // descriptor swizzle
+};
+
+// Shared-memory matrix descriptor of a tile with D-dependent rows.
+template <int D>
+__device__ __forceinline__ uint64_t bdesc(uint32_t saddr, uint32_t lbo) {
+    using R = Rows<D>;
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((R::kSBO >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (R::kLayout << 61);
+}
+
 // Shared memory: FIXED fixed 128 x D tiles, a ring of SLOTS streamed tiles, the staged
 // per-column vectors (dK/dV), then the barriers.
 template <int D, int FIXED, int SLOTS>
 struct BGeo {
-    static constexpr int kPanels = D / kPanelCols;
-    static constexpr int kTile = kPanels * kPanelBytes;        // one 128 x D tile
+    static constexpr int kPanels = Rows<D>::kPanels;
+    static constexpr int kTile = kPanels * Rows<D>::kPanelBytes;   // one 128 x D tile
     static constexpr int kSlots = SLOTS;
     static constexpr int kRingOff = FIXED * kTile;
     // epilogue staging (4 KB per elementwise warp) reuses the ring: it starts only after
@@ -101,9 +121,12 @@ __device__ __forceinline__ uint32_t slot_b(int j) { return 2u * (uint32_t)(j & 1
 __device__ __forceinline__ uint32_t slot_par(int j) { return (uint32_t)(j >> 1) & 1u; }
 
 // ----------------------------------------------------------------- MMA helpers
-// K-major B: 16-element K step inside a 128-byte panel row, panels of 16 KB.
+// K-major operand: a 16-element K step is 32 bytes of a panel row; panels follow each other.
+template <int D>
 __device__ __forceinline__ uint64_t kmaj_step(int kk) {
-    return ((uint64_t)(kk / 4) * kPanelBytes + (uint64_t)(kk % 4) * 32u) >> 4;
+    using R = Rows<D>;
+    constexpr int kSteps = R::kRowBytes / 32;   // K steps per panel row
+    return ((uint64_t)(kk / kSteps) * R::kPanelBytes + (uint64_t)(kk % kSteps) * 32u) >> 4;
 }
 
 // D_tmem = A[128 x D] * B[128 x D]^T, A and B K-major in shared memory.
@@ -112,7 +135,7 @@ __device__ __forceinline__ void mma_ss_nt(uint32_t d_tmem, uint64_t a_desc, uint
                                           uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
-        ptx::mma_ss_elect(d_tmem, a_desc + kmaj_step(kk), b_desc + kmaj_step(kk), idesc,
+        ptx::mma_ss_elect(d_tmem, a_desc + kmaj_step<D>(kk), b_desc + kmaj_step<D>(kk), idesc,
                           kk > 0 ? 1u : 0u);
 }
 
@@ -123,22 +146,23 @@ __device__ __forceinline__ void mma_ts_nt(uint32_t d_tmem, uint32_t a_tmem, uint
                                           uint32_t idesc) {
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk)
-        ptx::mma_ts_elect(d_tmem, a_tmem + (uint32_t)kk * 8u, b_desc + kmaj_step(kk), idesc,
+        ptx::mma_ts_elect(d_tmem, a_tmem + (uint32_t)kk * 8u, b_desc + kmaj_step<D>(kk), idesc,
                           kk > 0 ? 1u : 0u);
 }
 
 // acc_tmem (+)= A_tmem[128 x 128] * B, B a 128 x D tile read as the MN-major operand (16
-// rows = 2 KB per K step).  A holds 16-bit values packed two per TMEM column in two blocks
-// of 32 columns (64 values each), one per elementwise warp of the lane quarter, at a_tmem
-// and a_tmem + BLOCK (BLOCK = 32: contiguous; 64: over the first half of each 64-column
-// fp32 block the values were computed from).
-template <uint32_t BLOCK>
+// rows per K step).  A holds 16-bit values packed two per TMEM column in two blocks of 32
+// columns (64 values each), one per elementwise warp of the lane quarter, at a_tmem and
+// a_tmem + BLOCK (BLOCK = 32: contiguous; 64: over the first half of each 64-column fp32
+// block the values were computed from).
+template <int D, uint32_t BLOCK>
 __device__ __forceinline__ void mma_ts_tn(uint32_t acc_tmem, uint32_t a_tmem, uint64_t b_desc,
                                           uint32_t idesc, bool accumulate) {
+    constexpr int kStepBytes = 16 * Rows<D>::kRowBytes;
 #pragma unroll
     for (int kk = 0; kk < kT / 16; ++kk)
         ptx::mma_ts_elect(acc_tmem, a_tmem + (uint32_t)(kk >> 2) * BLOCK + (uint32_t)(kk & 3) * 8u,
-                          b_desc + (uint64_t)((kk * 2048) >> 4), idesc,
+                          b_desc + (uint64_t)((kk * kStepBytes) >> 4), idesc,
                           (accumulate || kk > 0) ? 1u : 0u);
 }
 
@@ -172,6 +196,36 @@ __device__ __forceinline__ void store_rows(uint32_t t_acc, float mul, uint32_t s
         const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) * 16));
         if (row0 + r < nrows)
             *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * D + ch * 8) = v;
+    }
+    __syncwarp();
+}
+
+// D = 32: this warp's 32 TMEM lanes x 32 fp32 columns at t_acc, times mul, rounded to 16
+// bits, to global rows base + r * 32 (64 bytes each; only rows with row0 + r < nrows).  The
+// warp's rows are one contiguous 2 KB block: staged with the 16-byte chunks of row r
+// XOR-swizzled by (r >> 1) & 3 (free of bank conflicts both ways), each store instruction
+// then writes 512 contiguous bytes.
+template <bool F16>
+__device__ __forceinline__ void store_rows32(uint32_t t_acc, float mul, uint32_t stage,
+                                             uint16_t* base, int row0, int nrows, int lane) {
+    uint32_t o[32];
+    ptx::tmem_ld32_wait(t_acc, o);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack2<F16>(u2f(o[2 * i]) * mul, u2f(o[2 * i + 1]) * mul);
+    const uint32_t sw = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc)
+        ptx::st_shared_v4(stage + (uint32_t)lane * 64u + (((uint32_t)cc ^ sw) * 16u), w[4 * cc],
+                          w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = 8 * k + (lane >> 2);
+        const int ch = lane & 3;
+        const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 64u + (uint32_t)((ch ^ ((r >> 1) & 3)) * 16));
+        if (row0 + r < nrows)
+            *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * 32 + ch * 8) = v;
     }
     __syncwarp();
 }
@@ -253,9 +307,10 @@ __device__ __forceinline__ void teardown_cta(const Setup& su) {
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                           int row, int bh) {
+    using R = Rows<D>;
 #pragma unroll
-    for (int pc = 0; pc < D / kPanelCols; ++pc)
-        ptx::tma_load_3d(dst + (uint32_t)pc * kPanelBytes, map, bar, pc * kPanelCols, row, bh);
+    for (int pc = 0; pc < R::kPanels; ++pc)
+        ptx::tma_load_3d(dst + (uint32_t)pc * R::kPanelBytes, map, bar, pc * R::kCols, row, bh);
 }
 
 // dK/dV loader: the two fixed tiles (f0, f1 at fixed_row), then for steps j < steps the
@@ -318,13 +373,15 @@ __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fi
 }
 
 // ----------------------------------------------------------------- dQ kernel
-// TMEM columns: Q [0, D/2), dS [D/2, D/2+64), S [D/2+64, +128), dP [D/2+192, +128),
-// dQ accumulator [D/2+320, +D)  (512 columns at D = 128).
+// TMEM columns: Q [0, D/2), dS [QC, QC+64), S [QC+64, +128), dP [QC+192, +128), dQ
+// accumulator [QC+320, +D) with QC = max(D/2, 32), so every region starts on a multiple of
+// 32 columns (512 columns at D = 128).
 // Shared memory: dO fixed; ring: Q (copied to TMEM, then released), K_j, V_j.
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using G = GeoDq<D>;
-    constexpr uint32_t kColQ = 0, kColDS = D / 2, kColS = D / 2 + 64, kColDP = kColS + 128,
+    constexpr uint32_t kQC = D / 2 < 32 ? 32 : D / 2;
+    constexpr uint32_t kColQ = 0, kColDS = kQC, kColS = kQC + 64, kColDP = kColS + 128,
                        kColAcc = kColDP + 128;
     static_assert(kColAcc + D <= kTmemCols, "TMEM columns");
     extern __shared__ uint8_t smem_raw[];
@@ -342,13 +399,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
         constexpr uint32_t id_tn = make_idesc(kT, D, true, F16);
-        const uint64_t dDO = sw128_desc(su.sbase, 16, 1024);
+        const uint64_t dDO = bdesc<D>(su.sbase, 16);
         const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
         auto kdesc = [&](uint32_t pos) {
-            return sw128_desc(ring + G::cyc_slot(pos) * (uint32_t)G::kTile, 16, 1024);
+            return bdesc<D>(ring + G::cyc_slot(pos) * (uint32_t)G::kTile, 16);
         };
         auto mdesc = [&](uint32_t pos) {
-            return sw128_desc(ring + G::cyc_slot(pos) * (uint32_t)G::kTile, kPanelBytes, 1024);
+            return bdesc<D>(ring + G::cyc_slot(pos) * (uint32_t)G::kTile, (uint32_t)Rows<D>::kPanelBytes);
         };
         auto issue_s = [&](int j) -> bool {    // S = Q K_j^T (Q from TMEM)
             const uint32_t pos = 1u + 2u * (uint32_t)j;
@@ -380,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             if (!wait_warp(c, G::ds_ready(), par, kRoleMma)) goto mma_out;
             ptx::tc_fence_after();
             const uint32_t kpos = 1u + 2u * (uint32_t)j;
-            mma_ts_tn<32>(tm + kColAcc, tm + kColDS, mdesc(kpos), id_tn, j > 0);   // dQ += dS K_j
+            mma_ts_tn<D, 32>(tm + kColAcc, tm + kColDS, mdesc(kpos), id_tn, j > 0);   // dQ += dS K_j
             ptx::mma_commit_elect(bar_addr(c, G::ds_free()));
             ptx::mma_commit_elect(bar_addr(c, G::ring_empty(G::cyc_slot(kpos))));
         }
@@ -401,7 +458,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
         float* part = reinterpret_cast<float*>(smem_raw + (su.sbase - ptx::smem_addr(smem_raw)) + G::kVecOff);
         float dlt = 0.0f;
-        {
+        if constexpr (D == 32) {
+            // delta = sum_d dO * O for this row, both rows (64 bytes each) read from global
+            // memory by the first warp of the lane quarter
+            const bool mine = live && ch == 0;
+            float acc = 0.0f;
+            if (mine) {
+                const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + row * D);
+                const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + row * D);
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    const uint4 ov = __ldg(orow + cc), dv = __ldg(drow + cc);
+                    const uint32_t ow[4] = {ov.x, ov.y, ov.z, ov.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        acc = fmaf(unpack_lo<F16>(ow[e]), unpack_lo<F16>(dw[e]), acc);
+                        acc = fmaf(unpack_hi<F16>(ow[e]), unpack_hi<F16>(dw[e]), acc);
+                    }
+                }
+            }
+            part[ch * kT + r] = acc;
+        } else {
             // delta = sum_d dO * O for this row: this warp's 64 columns from dO (the fixed
             // shared tile) and O (global; loaded first so the loads overlap the tile loads),
             // the two halves added through shared memory below
@@ -433,9 +510,22 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
         {
             // Q rows (streamed tile 0) into TMEM as 16-bit pairs (this warp: one 64-column
-            // panel); the ring slot is then released
+            // panel; at D = 32 the first warp of the lane quarter copies the 64-byte row
+            // from global memory, zeros past N); the ring slot is then released
             const bool ok = wait_warp(c, G::ring_full(0), 0, kRoleSoftmax);
-            if (ok && ch < D / 64) {
+            if constexpr (D == 32) {
+                if (ok && ch == 0) {
+                    uint32_t w[16];
+                    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + row * D);
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        const uint4 v = live ? __ldg(qrow + cc) : make_uint4(0u, 0u, 0u, 0u);
+                        w[4 * cc] = v.x; w[4 * cc + 1] = v.y; w[4 * cc + 2] = v.z; w[4 * cc + 3] = v.w;
+                    }
+                    ptx::tmem_st16(tm + tl + kColQ, w);
+                    ptx::tmem_wait_st();
+                }
+            } else if (ok && ch < D / 64) {
                 const uint32_t src = su.sbase + (uint32_t)G::kRingOff + (uint32_t)ch * kPanelBytes +
                                      (uint32_t)r * 128u;
                 uint32_t w[32];
@@ -508,18 +598,26 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         }
         if (!wait_warp(c, G::done(), 0, kRoleSoftmax)) goto ew_out;
         ptx::tc_fence_after();
-        if (ch < D / 64)   // one 64-column panel of dQ per warp
+        if constexpr (D == 32) {   // the first warp of each lane quarter stores dQ
+            if (ch == 0)
+                store_rows32<F16>(tm + tl + kColAcc, p.scale,
+                                  su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
+                                  reinterpret_cast<uint16_t*>(p.dq) + (size_t)bh * p.n * D,
+                                  qt * kT + quarter * 32, p.n, lane);
+        } else if (ch < D / 64) {   // one 64-column panel of dQ per warp
             store_rows<D, F16>(tm + tl + kColAcc + 64u * (uint32_t)ch, p.scale,
                                su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
                                reinterpret_cast<uint16_t*>(p.dq) + (size_t)bh * p.n * D + 64 * ch,
                                qt * kT + quarter * 32, p.n, lane);
+        }
     ew_out:;
     }
     teardown_cta(su);
 }
 
 // ----------------------------------------------------------------- dK, dV kernel
-// TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256+D), dK [256+D, 256+2D).
+// TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256+D), dK [256+D, 256+2D)
+// (D = 32: dK at 288, a multiple of 32 columns as every other region).
 // Shared memory: K, V fixed; ring A_s = Q_i, B_s = dO_i for query tile i = i0 + s.
 template <int D, bool CAUSAL, bool F16>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
@@ -542,11 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
         constexpr uint32_t id_tn = make_idesc(kT, D, true, F16);
-        const uint64_t dK = sw128_desc(su.sbase, 16, 1024);
-        const uint64_t dV = sw128_desc(su.sbase + (uint32_t)G::kTile, 16, 1024);
+        const uint64_t dK = bdesc<D>(su.sbase, 16);
+        const uint64_t dV = bdesc<D>(su.sbase + (uint32_t)G::kTile, 16);
         const uint32_t ring = su.sbase + (uint32_t)G::kRingOff;
-        auto kdesc = [&](uint32_t slot) { return sw128_desc(ring + slot * (uint32_t)G::kTile, 16, 1024); };
-        auto mdesc = [&](uint32_t slot) { return sw128_desc(ring + slot * (uint32_t)G::kTile, kPanelBytes, 1024); };
+        auto kdesc = [&](uint32_t slot) { return bdesc<D>(ring + slot * (uint32_t)G::kTile, 16); };
+        auto mdesc = [&](uint32_t slot) {
+            return bdesc<D>(ring + slot * (uint32_t)G::kTile, (uint32_t)Rows<D>::kPanelBytes);
+        };
         auto issue_st = [&](int s) -> bool {    // S^T = K Q_i^T
             if (!wait_warp(c, G::ring_full(slot_a(s)), slot_par(s), kRoleMma)) return false;
             ptx::tc_fence_after();
@@ -567,12 +667,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
             const uint32_t par = (uint32_t)s & 1u;
             if (!wait_warp(c, G::x_ready(), par, kRoleMma)) goto mma_out;   // P^T stored
             ptx::tc_fence_after();
-            mma_ts_tn<64>(tm + kColDV, tm + kColS, mdesc(slot_b(s)), id_tn, s > 0);   // dV += P^T dO_i
+            mma_ts_tn<D, 64>(tm + kColDV, tm + kColS, mdesc(slot_b(s)), id_tn, s > 0);   // dV += P^T dO_i
             ptx::mma_commit_elect(bar_addr(c, G::ring_empty(slot_b(s))));
             if (s + 1 < nq && !issue_st(s + 1)) goto mma_out;
             if (!wait_warp(c, G::ds_ready(), par, kRoleMma)) goto mma_out;
             ptx::tc_fence_after();
-            mma_ts_tn<64>(tm + kColDK, tm + kColDP, mdesc(slot_a(s)), id_tn, s > 0);   // dK += dS^T Q_i
+            mma_ts_tn<D, 64>(tm + kColDK, tm + kColDP, mdesc(slot_a(s)), id_tn, s > 0);   // dK += dS^T Q_i
             ptx::mma_commit_elect(bar_addr(c, G::ring_empty(slot_a(s))));
             if (s + 1 < nq && !issue_dpt(s + 1)) goto mma_out;
         }
@@ -670,7 +770,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if (failed) goto ew_out;
         if (!wait_warp(c, G::done(), 0, kRoleSoftmax)) goto ew_out;
         ptx::tc_fence_after();
-        if (ch < D / 64) {   // one 64-column panel of dV and of dK per warp
+        if constexpr (D == 32) {   // dV by the first, dK by the second warp of each quarter
+            const uint32_t stage = su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u;
+            const int row0 = kt * kT + quarter * 32;
+            const size_t off = (size_t)bh * p.n * D;
+            if (ch == 0)
+                store_rows32<F16>(tm + tl + kColDV, 1.0f, stage,
+                                  reinterpret_cast<uint16_t*>(p.dv) + off, row0, p.n, lane);
+            else
+                store_rows32<F16>(tm + tl + kColDK, p.scale, stage,
+                                  reinterpret_cast<uint16_t*>(p.dk) + off, row0, p.n, lane);
+        } else if (ch < D / 64) {   // one 64-column panel of dV and of dK per warp
             const uint32_t stage = su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u;
             const int row0 = kt * kT + quarter * 32;
             const size_t off = (size_t)bh * p.n * D + 64 * ch;
@@ -717,11 +827,13 @@ cudaError_t dispatch(bool causal, bool f16, bool prepare, const BwdParams* p, in
 }  // namespace
 
 cudaError_t bwd_prepare(int D, bool causal, bool f16) {
+    if (D == 32) return dispatch<32>(causal, f16, true, nullptr, 0, nullptr);
     return D == 64 ? dispatch<64>(causal, f16, true, nullptr, 0, nullptr)
                    : dispatch<128>(causal, f16, true, nullptr, 0, nullptr);
 }
 
 cudaError_t bwd_launch(int D, bool causal, bool f16, const BwdParams& p, int bh, cudaStream_t stream) {
+    if (D == 32) return dispatch<32>(causal, f16, false, &p, bh, stream);
     return D == 64 ? dispatch<64>(causal, f16, false, &p, bh, stream)
                    : dispatch<128>(causal, f16, false, &p, bh, stream);
 }

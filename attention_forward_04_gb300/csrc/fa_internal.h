@@ -38,6 +38,8 @@ struct BwdParams {
     CUtensorMap tmap_do;
     const float* lse;     // [B*H, N] natural-log LSE of the forward
     const void* o;        // [B*H, N, D] the forward's output (16-bit)
+    const void* q;        // [B*H, N, D] Q and dO (16-bit), read row by row where D = 32
+    const void* dout;
     float* delta;         // [B*H, N] rowsum(dO * O): written by the dQ kernel, read by dK/dV
     void* dq;             // [B*H, N, D] outputs, input element type
     void* dk;

@@ -153,7 +153,7 @@ int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
  *                      16-byte aligned; scratch for delta, needs no initialisation, and
  *                      must not be shared by two calls in flight at once.
  *   B, H, N, scale, causal, stream : as for fa_fwd.
- *   D                : 64 or 128.
+ *   D                : 32, 64 or 128.
  *   dtype            : FA_BF16 or FA_FP16 (FA_FP32 returns FA_ERR_UNSUPPORTED).
  *
  * Arithmetic: products on the tensor cores from 16-bit operands (P and dS are rounded to

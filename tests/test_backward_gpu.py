@@ -100,7 +100,7 @@ EDGE_N = [1, 17, 127, 128, 129, 256, 300, 640, 1000]
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("N", EDGE_N)
 def test_bf16_backward_edge_shapes(N, D, causal):
     q, k, v = make_shape(1, 2, N, D, "bf16", seed=N * 13 + D)
@@ -110,7 +110,7 @@ def test_bf16_backward_edge_shapes(N, D, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("N", [1, 200, 384])
 def test_fp16_backward(N, D, causal):
     q, k, v = make_shape(2, 1, N, D, "fp16", seed=N * 17 + D)
@@ -119,11 +119,12 @@ def test_fp16_backward(N, D, causal):
                    "fp16 N=%d D=%d causal=%d" % (N, D, causal))
 
 
-def test_backward_scale_zero_and_large_scores():
+@pytest.mark.parametrize("D", [32, 128])
+def test_backward_scale_zero_and_large_scores(D):
     # scale 0: P is uniform over the visible keys; scores x4: a peaked softmax
-    q, k, v = make_shape(1, 2, 300, 128, "bf16", seed=91, qk_mult=4.0)
-    do = make_shape_dout(1, 2, 300, 128, "bf16", seed=91)
-    for scale in (0.0, 1.0 / math.sqrt(128)):
+    q, k, v = make_shape(1, 2, 300, D, "bf16", seed=91, qk_mult=4.0)
+    do = make_shape_dout(1, 2, 300, D, "bf16", seed=91)
+    for scale in (0.0, 1.0 / math.sqrt(D)):
         for causal in (False, True):
             compare_slices(q, k, v, do, scale, causal, "bf16", [(0, 0), (0, 1)],
                            "scale=%g causal=%d" % (scale, causal))
@@ -131,7 +132,7 @@ def test_backward_scale_zero_and_large_scores():
 
 # ------------------------------------------------------------ full-size workloads, sampled
 @pytest.mark.parametrize("name", ["bf16_b2h8n1024d64", "bf16_b4h16n4096d128",
-                                  "bf16_b8h32n4096d128_causal"])
+                                  "bf16_b8h32n4096d128_causal", "bf16_b8h32n4096d32"])
 def test_backward_full_size_sampled_slices(name):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)
