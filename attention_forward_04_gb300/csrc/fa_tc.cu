@@ -1,7 +1,8 @@
 // fa_tc.cu -- FlashAttention forward on the GB300 5th-generation tensor cores.
 //
 // What it computes: O = softmax(scale * Q K^T) V and LSE per row, for every (b, h) slice
-// of [B, H, N, D] bf16/fp16 tensors ("KingOfEgg: Flash Attention v1" §1.1-§1.2), tile
+// of [B, H, N, D] bf16/fp16 (or e4m3, O in bf16) tensors, D = 32, 64 or 128, or of the
+// token-major layouts ("KingOfEgg: Flash Attention v1" §1.1-§1.2), tile
 // by tile with the online-softmax (m, l, O) recurrence so that no N x N matrix ever
 // reaches HBM ("08 · FlashAttention" §二; "第 13 课：GPU 内核与 FlashAttention"
 // Figure 13-2: query blocks outside, key/value blocks inside, O written once).
@@ -13,11 +14,15 @@
 //     here as TMA + mbarrier instead of cp.async groups).
 //   * warp 8 (MMA issuer, one thread): tcgen05.mma  S_t = Q_t K_j^T  into TMEM, and
 //     O_t += P_t V_j  with P_t read straight from TMEM; completion is signalled with
-//     tcgen05.commit onto mbarriers.  Issue order S_A(0) S_B(0) | PV_A(j) S_A(j+1)
-//     PV_B(j) S_B(j+1) | ... so the softmax of one tile overlaps the products of the other.
+//     tcgen05.commit onto mbarriers.  Where P is written over S (D = 128), issue order
+//     S_A(0) S_B(0) | PV_A(j) S_A(j+1) PV_B(j) S_B(j+1) | ... so the softmax of one tile
+//     overlaps the products of the other.  Where TMEM has room for P in columns of its
+//     own (D <= 64 at 16 bits, D = 64 at e4m3), S(j+1) is issued as soon as the softmax has
+//     loaded S(j), ahead of P(j) V_j.
 //   * warps 0-3 / 4-7 (softmax of tile A / tile B): one thread per query row (TMEM lane =
 //     row).  Running max m and sum l stay in registers; exp2 with scale*log2(e) folded
-//     into one FMA; P is rounded to the input type and stored back into TMEM over S.
+//     into one FMA; P is rounded to the input type and stored into TMEM (over S, or into
+//     its own columns).
 //     The max is only raised when it grows by more than 2^16 (2^8 for fp16), and only then
 //     is O rescaled in TMEM ("08 · FlashAttention" §五 and "第 13 课" §4B: old output
 //     multiplied by exp(m_old - m_new) when a larger maximum appears; keeping a stale

@@ -62,10 +62,16 @@ def load_peaks():
 
 
 def kernel_hash(op: str = "fwd") -> str:
+    """sha256[:16] of the kernel sources' code: comments and whitespace are left out, so an
+    edit to a comment does not retire a traffic capture of unchanged code."""
+    import re
     h = hashlib.sha256()
     for path in KERNEL_SRCS[op]:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                  # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 
