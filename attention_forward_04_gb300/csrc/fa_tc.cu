@@ -138,9 +138,10 @@ template <int D, int EB> __device__ __forceinline__ uint32_t ring_parity(uint32_
 struct Item {
     int bh;    // slice b*H + h
     int h;     // head
-    int pair;  // query rows [256*pair, 256*pair + 256): tile A = first 128, tile B = next 128
+    int pair;  // query rows [256*pair, 256*pair + 256): tile t holds rows 128*(t ^ sw).. of it
+    int sw;    // 0: tile A = first 128 rows, tile B = next 128; 1: the other way round
     int nA;    // key/value tiles tile A visits
-    int nB;    // key/value tiles tile B visits (nB >= nA)
+    int nB;    // key/value tiles tile B visits
     int len;   // sequence length of the slice
     int tok0;  // token-major layout: token index of row 0 of the slice
 };
@@ -169,7 +170,10 @@ __device__ __forceinline__ void slice_geometry(const TcParams& p, int bh, int& l
 
 // Work units: non-causal, one unit per (slice, pair), slice-major so concurrently running
 // CTAs share the K/V of a few slices in L2.  Causal: unit (slice, q) holds pairs
-// npairs-1-q and q of that slice, heavy first, so every unit costs about the same.  Units
+// npairs-1-q and q of that slice, heavy first, so every unit costs about the same; the
+// second pair's rows are swapped between the tiles, so that each tile visits the one
+// extra (diagonal) key tile of the upper rows once per unit and neither tile runs a step
+// longer than the other over the unit.  Units
 // past the end of a (shorter) packed sequence hold nothing.  unit_count gives the number of
 // items of unit u, unit_item the s-th one (computed on demand to keep registers free).
 template <bool CAUSAL, int MODE>
@@ -200,8 +204,11 @@ __device__ __forceinline__ Item unit_item(const TcParams& p, int u, int s) {
         it.len = p.n;
         it.tok0 = 0;
         it.pair = CAUSAL ? ((s == 0) ? (p.npairs - 1 - q) : q) : q;
-        it.nA = CAUSAL ? min(2 * it.pair + 1, p.nkv) : p.nkv;
-        it.nB = CAUSAL ? min(2 * it.pair + 2, p.nkv) : p.nkv;
+        it.sw = (CAUSAL && s == 1) ? 1 : 0;
+        const int n_lo = CAUSAL ? min(2 * it.pair + 1, p.nkv) : p.nkv;   // rows 256 pair..
+        const int n_hi = CAUSAL ? min(2 * it.pair + 2, p.nkv) : p.nkv;   // rows 256 pair + 128..
+        it.nA = it.sw ? n_hi : n_lo;
+        it.nB = it.sw ? n_lo : n_hi;
         return it;
     }
     it.bh = u / per_slice;
@@ -212,12 +219,15 @@ __device__ __forceinline__ Item unit_item(const TcParams& p, int u, int s) {
     const int nkv = (it.len + kBN - 1) / kBN;
     if (!CAUSAL) {
         it.pair = q;
+        it.sw = 0;
         it.nA = nkv;
         it.nB = nkv;
     } else {
         it.pair = (s == 0) ? (npairs - 1 - q) : q;
-        it.nA = min(2 * it.pair + 1, nkv);
-        it.nB = min(2 * it.pair + 2, nkv);
+        it.sw = s == 1 ? 1 : 0;
+        const int n_lo = min(2 * it.pair + 1, nkv), n_hi = min(2 * it.pair + 2, nkv);
+        it.nA = it.sw ? n_hi : n_lo;
+        it.nB = it.sw ? n_lo : n_hi;
     }
     return it;
 }
@@ -329,10 +339,11 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
             ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kv)));
             ++kv;
 
-            for (int j = 0; j < it.nB; ++j) {
+            const int nmax = max(it.nA, it.nB);
+            for (int j = 0; j < nmax; ++j) {
                 const uint32_t vpos = kv;        // V_j
                 const uint32_t kpos = kv + 1;    // K_{j+1}
-                const bool more = j + 1 < it.nB;
+                const bool more = j + 1 < nmax;
                 if (!wait_warp(c, b_kv_full<D, EB>(vpos), ring_parity<D, EB>(vpos), kRoleMma)) goto out;
                 ptx::tc_fence_after();
                 if (j < it.nA) {
@@ -351,17 +362,21 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
                     ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(0)));
                     if (j + 2 == it.nA) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
                 }
-                if (!wait_warp(c, b_p_full<D, EB>(1), p_cnt1 & 1u, kRoleMma)) goto out;
-                ++p_cnt1;
-                ptx::tc_fence_after();
-                issue_pv<D, ET>(tO[1], tP[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
-                ptx::mma_commit_elect(bar_addr(c, b_o_done<D, EB>(1)));
+                if (j < it.nB) {
+                    if (!wait_warp(c, b_p_full<D, EB>(1), p_cnt1 & 1u, kRoleMma)) goto out;
+                    ++p_cnt1;
+                    ptx::tc_fence_after();
+                    issue_pv<D, ET>(tO[1], tP[1], dV0 + slot_off(vpos), idesc_pv, j > 0);
+                    ptx::mma_commit_elect(bar_addr(c, b_o_done<D, EB>(1)));
+                }
                 ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(vpos)));
                 ++kv;
-                if (more) {
+                if (j + 1 < it.nB) {
                     issue_qk<D, ET>(tS[1], dQ[1], dK0 + slot_off(kpos), idesc_qk);
                     ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(1)));
                     if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+                }
+                if (more) {
                     ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kpos)));
                     ++kv;
                 }
@@ -429,23 +444,26 @@ __device__ void mma_role_sep(const TcParams& p, const Ctl& c, uint32_t tmem, uin
             ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kv)));   // K_0
             ++kv;
 
-            for (int j = 0; j < it.nB; ++j) {
+            const int nmax = max(it.nA, it.nB);
+            for (int j = 0; j < nmax; ++j) {
                 const uint32_t vpos = kv;        // V_j
                 const uint32_t kpos = kv + 1;    // K_{j+1}
-                const bool more = j + 1 < it.nB;
+                const bool more = j + 1 < nmax;
                 if (more) {
                     if (!wait_warp(c, b_kv_full<D, EB>(kpos), ring_parity<D, EB>(kpos), kRoleMma)) goto out;
                     if (j + 1 < it.nA) {
                         if (!issue_s(0, kpos)) goto out;
                         if (j + 2 == it.nA) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
                     }
-                    if (!issue_s(1, kpos)) goto out;
-                    if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+                    if (j + 1 < it.nB) {
+                        if (!issue_s(1, kpos)) goto out;
+                        if (j + 2 == it.nB) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+                    }
                     ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kpos)));   // K_{j+1}
                 }
                 if (!wait_warp(c, b_kv_full<D, EB>(vpos), ring_parity<D, EB>(vpos), kRoleMma)) goto out;
                 if (j < it.nA && !issue_o(0, vpos, j > 0)) goto out;
-                if (!issue_o(1, vpos, j > 0)) goto out;
+                if (j < it.nB && !issue_o(1, vpos, j > 0)) goto out;
                 ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(vpos)));      // V_j
                 kv += more ? 2u : 1u;
             }
@@ -479,7 +497,7 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                 const uint32_t fb = bar_addr(c, b_q_full<D, EB>(t));
                 ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTileBytes);
                 int c1, c2;
-                tile_coords<MODE>(p, it, it.pair * 2 * kBM + t * kBM, c1, c2);
+                tile_coords<MODE>(p, it, it.pair * 2 * kBM + (t ^ it.sw) * kBM, c1, c2);
 #pragma unroll
                 for (int pc = 0; pc < G::kPanels; ++pc)
                     ptx::tma_load_3d(sQ[t] + (uint32_t)pc * G::kPanelBytes, &p.tmap_q, fb, pc * G::kPanelCols,
@@ -488,7 +506,8 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                 return true;
             };
             if (!load_q(0)) goto out;
-            for (int j = 0; j < it.nB; ++j) {
+            const int nmax = max(it.nA, it.nB);
+            for (int j = 0; j < nmax; ++j) {
                 for (int w = 0; w < 2; ++w) {  // K_j then V_j
                     if (!wait(c, b_kv_empty<D, EB>(kv), ring_parity<D, EB>(kv) ^ 1u, kRoleLoad)) goto out;
                     if (kv != skipped) {
@@ -621,7 +640,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
         for (int sub = 0; sub < nsub; ++sub) {
             const Item it = unit_item<CAUSAL, MODE>(p, u, sub);
             const int n = t == 0 ? it.nA : it.nB;
-            const int row = it.pair * 2 * kBM + t * kBM + lane_base + lane;
+            const int row = it.pair * 2 * kBM + (t ^ it.sw) * kBM + lane_base + lane;
             // sequence length: the kernel parameter for [B, H, N, D] (no register held)
             const int len = MODE == 0 ? p.n : it.len;
             const int limit = CAUSAL ? min(row + 1, len) : len;   // visible keys: j < limit
@@ -680,7 +699,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             ++o_cnt;
             ptx::tc_fence_after();
             const float inv_l = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
-            const int row0 = it.pair * 2 * kBM + t * kBM + lane_base;   // first row of the warp
+            const int row0 = it.pair * 2 * kBM + (t ^ it.sw) * kBM + lane_base;   // first row of the warp
             // row r of the slice: obase + r * ostride (elements)
             const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
             uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +
