@@ -67,7 +67,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 //   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, rows, 1} (rows = 128, or 64 for the
 //   D = 256 kernel); rows past N read as zero.
 //   D = 32: the box is 32 values wide and lands as 64-byte rows with the 64-byte swizzle.
-//   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, 128}; tokens past T read
+//   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, rows}; tokens past T read
 //   as zero (tokens of the next packed sequence are masked by the kernel instead).
 bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int64_t n, int64_t h,
                 int64_t t, int64_t d, int et, PFN_cuTensorMapEncodeTiled_v12000 fn,
@@ -86,7 +86,7 @@ bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int6
     } else {
         dims[0] = (cuuint64_t)d; dims[1] = (cuuint64_t)h; dims[2] = (cuuint64_t)t;
         strides[0] = (cuuint64_t)(d * eb); strides[1] = (cuuint64_t)(h * d * eb);
-        box[0] = box0; box[1] = 1; box[2] = 128;
+        box[0] = box0; box[1] = 1; box[2] = rows;
     }
     cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType type = et == 2   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
@@ -182,7 +182,7 @@ int forward(const Request& r) {
     if (!std::isfinite(r.scale * r.descale[0] * r.descale[1])) return FA_ERR_INVALID_ARG;
     if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
     // D = 256: 16-bit storage, [B, H, N, D] layout only
-    if (r.D == 256 && (r.dtype == FA_FP32 || r.dtype == kFp8 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
+    if (r.D == 256 && (r.dtype == FA_FP32 || r.dtype == kFp8)) return FA_ERR_UNSUPPORTED;
     // fp8: D = 64 or 128, [B, H, N, D] layout only
     if (r.dtype == kFp8 && ((r.D != 64 && r.D != 128) || r.layout != 0)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;
@@ -253,12 +253,16 @@ int forward(const Request& r) {
         if (!fn) return fail_cuda(e, "cuTensorMapEncodeTiled entry point");
         fa::TcParams p;
         std::memset(&p, 0, sizeof(p));
-        if (!encode_map(&p.tmap_q, r.q, 0, BH, r.N, r.H, r.T, r.D, et, fn, 64) ||
-            !encode_map(&p.tmap_k, r.k, 0, BH, r.N, r.H, r.T, r.D, et, fn, 64) ||
-            !encode_map(&p.tmap_v, r.v, 0, BH, r.N, r.H, r.T, r.D, et, fn, 64))
+        if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, 64) ||
+            !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, 64) ||
+            !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, 64))
             return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
         p.o = r.o;
         p.lse = r.lse;
+        p.layout = r.layout;
+        p.cu_seqlens = r.cu;
+        p.heads = (int)r.H;
+        p.total = (int)r.T;
         p.n = (int)r.N;
         p.bh = (int)BH;
         p.scale_log2 = r.scale * 1.4426950408889634f;

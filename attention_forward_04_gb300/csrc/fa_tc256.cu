@@ -128,35 +128,68 @@ __device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0,
 
 struct Work {
     int bh, qt, nkv;
+    int len;    // sequence length of the slice
+    int tok0;   // token-major layouts: token of row 0 of the slice
+    int h;      // head
 };
+
+// Length and first token of slice bh.  MODE 0, [B, H, N, D]: every slice has N rows.
+// MODE 1, token-major [tokens, H, D]: fixed length N (tokens b*N..), or packed sequences
+// with offsets cu_seqlens, clamped to [0, total] and lengths to the declared maximum, so
+// malformed offsets cannot move an access out of bounds.
+template <int MODE>
+__device__ __forceinline__ void slice_of(const TcParams& p, int bh, int& len, int& tok0) {
+    if (MODE == 0) {
+        len = p.n;
+        tok0 = 0;
+        return;
+    }
+    const int b = bh / p.heads;
+    if (p.cu_seqlens != nullptr) {
+        int s0 = __ldg(p.cu_seqlens + b), s1 = __ldg(p.cu_seqlens + b + 1);
+        s0 = min(max(s0, 0), p.total);
+        s1 = min(max(s1, s0), p.total);
+        len = min(s1 - s0, p.n);
+        tok0 = s0;
+    } else {
+        len = p.n;
+        tok0 = b * p.n;
+    }
+}
 
 // Work units of the persistent schedule.  Non-causal: one 128-row query tile per unit,
 // slice-major, so the CTAs running together share a few slices' K and V through L2.
 // Causal: unit (slice, q) holds tiles ntiles-1-q and q of the slice (one tile when they
-// coincide), so units cost about the same; still slice-major.
-__device__ __forceinline__ int ntiles_of(const TcParams& p) { return (p.n + kBM - 1) / kBM; }
+// coincide), so units cost about the same; still slice-major.  Units are laid out for
+// slices of N (the maximum) rows; a shorter packed sequence leaves some of its units with
+// fewer items or none.
+__device__ __forceinline__ int ntiles_of(int n) { return (n + kBM - 1) / kBM; }
 
-template <bool CAUSAL>
+template <bool CAUSAL, int MODE>
 __device__ __forceinline__ int unit_items(const TcParams& p, int u) {
-    if (!CAUSAL) return 1;
-    const int nt = ntiles_of(p), q = u % ((nt + 1) / 2);
-    return (nt - 1 - q != q) ? 2 : 1;
+    const int nt = ntiles_of(p.n);
+    const int per_slice = CAUSAL ? (nt + 1) / 2 : nt;
+    const int q = u % per_slice;
+    int len = p.n, tok0 = 0;
+    if (MODE == 1) slice_of<MODE>(p, u / per_slice, len, tok0);
+    const int ntl = ntiles_of(len);   // tiles of this slice
+    if (!CAUSAL) return q < ntl ? 1 : 0;
+    if (q >= (ntl + 1) / 2) return 0;
+    return (ntl - 1 - q != q) ? 2 : 1;
 }
 
-template <bool CAUSAL>
+template <bool CAUSAL, int MODE>
 __device__ __forceinline__ Work unit_item(const TcParams& p, int u, int sub) {
-    const int nt = ntiles_of(p);
+    const int nt = ntiles_of(p.n);
+    const int per_slice = CAUSAL ? (nt + 1) / 2 : nt;
     Work w;
-    if (CAUSAL) {
-        const int half = (nt + 1) / 2;
-        w.bh = u / half;
-        const int q = u % half;
-        w.qt = sub == 0 ? nt - 1 - q : q;
-    } else {
-        w.bh = u / nt;
-        w.qt = u % nt;
-    }
-    const int keys = CAUSAL ? min(p.n, (w.qt + 1) * kBM) : p.n;
+    w.bh = u / per_slice;
+    const int q = u % per_slice;
+    slice_of<MODE>(p, w.bh, w.len, w.tok0);
+    w.h = MODE == 1 ? w.bh % p.heads : 0;
+    const int ntl = ntiles_of(w.len);
+    w.qt = CAUSAL ? (sub == 0 ? ntl - 1 - q : q) : q;
+    const int keys = CAUSAL ? min(w.len, (w.qt + 1) * kBM) : w.len;
     w.nkv = (keys + kBN - 1) / kBN;
     return w;
 }
@@ -164,7 +197,7 @@ __device__ __forceinline__ Work unit_item(const TcParams& p, int u, int sub) {
 // Every role walks the same items in the same order and keeps running counters: ring
 // position (2 Q halves, then K_j, V_j per item), global step index g (S/P buffer g % 2, its
 // (g / 2)-th use), products of O done, and items.
-template <bool CAUSAL, bool F16>
+template <bool CAUSAL, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -206,9 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
         if (lane == 0) {
             uint32_t pos = 0;
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-                const int nsub = unit_items<CAUSAL>(p, u);
+                const int nsub = unit_items<CAUSAL, MODE>(p, u);
                 for (int sub = 0; sub < nsub; ++sub) {
-                    const Work w = unit_item<CAUSAL>(p, u, sub);
+                    const Work w = unit_item<CAUSAL, MODE>(p, u, sub);
                     const uint32_t count = 2u + 2u * (uint32_t)w.nkv;
                     for (uint32_t k = 0; k < count; ++k, ++pos) {
                         if (!wait(c, b_ring_empty(pos), ring_par(pos) ^ 1u, kRoleLoad)) goto load_out;
@@ -218,8 +251,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         const uint32_t dst = ring + (pos % kSlots) * (uint32_t)kTile;
                         ptx::mbar_arrive_expect_tx(bar, (uint32_t)kTile);
 #pragma unroll
-                        for (int pc = 0; pc < 4; ++pc)
-                            ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, row, w.bh);
+                        for (int pc = 0; pc < 4; ++pc) {
+                            if (MODE == 0)
+                                ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, row, w.bh);
+                            else   // token-major: dims {D, H, tokens}
+                                ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, w.h,
+                                                 w.tok0 + row);
+                        }
                     }
                 }
             }
@@ -254,9 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
         };
         uint32_t g = 0, items = 0, base = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const int nsub = unit_items<CAUSAL>(p, u);
+            const int nsub = unit_items<CAUSAL, MODE>(p, u);
             for (int sub = 0; sub < nsub; ++sub) {
-                const Work w = unit_item<CAUSAL>(p, u, sub);
+                const Work w = unit_item<CAUSAL, MODE>(p, u, sub);
                 if (!wait_warp(c, b_q_ready(), items & 1u, kRoleMma)) goto mma_out;
                 ++items;
                 ptx::tc_fence_after();
@@ -294,11 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
         const uint32_t stage = sbase + (uint32_t)kStageOff + (uint32_t)warp * 4096u;
         uint32_t g = 0, base = 0, pv = 0;   // pv: products of O issued before this item
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const int nsub = unit_items<CAUSAL>(p, u);
+            const int nsub = unit_items<CAUSAL, MODE>(p, u);
             for (int sub = 0; sub < nsub; ++sub) {
-                const Work w = unit_item<CAUSAL>(p, u, sub);
-                const int i = w.qt * kBM + r;
-                const int limit = CAUSAL ? min(i + 1, p.n) : p.n;      // visible keys: key < limit
+                const Work w = unit_item<CAUSAL, MODE>(p, u, sub);
+                const int i = w.qt * kBM + r;   // row within the slice
+                const int limit = CAUSAL ? min(i + 1, w.len) : w.len;  // visible keys: key < limit
                 {
                     // Q row r into TMEM as 16-bit pairs; the two ring slots are then released.
                     // The previous item's products (which read Q) are complete: its
@@ -375,7 +413,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                 if (!wait_warp(c, b_o_done(), (pv - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                 ptx::tc_fence_after();
                 const float inv = 1.0f / l_run;
-                uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)w.bh * p.n * D;
+                // row rr of the slice: obase + rr * ostride (elements)
+                const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
+                uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +
+                                  (MODE == 0 ? (size_t)w.bh * p.n * D : ((size_t)w.tok0 * p.heads + w.h) * D);
                 const int row0 = w.qt * kBM + warp * 32;
 #pragma unroll 1
                 for (int pc = 0; pc < D / 64; ++pc) {
@@ -400,12 +441,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         const int ch = lane & 7;
                         const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)rr * 128u +
                                                           (uint32_t)((ch ^ (rr & 7)) * 16));
-                        if (row0 + rr < p.n)
-                            *reinterpret_cast<uint4*>(obase + (size_t)(row0 + rr) * D + pc * 64 + ch * 8) = v;
+                        if (row0 + rr < w.len)
+                            *reinterpret_cast<uint4*>(obase + (size_t)(row0 + rr) * ostride + pc * 64 + ch * 8) = v;
                     }
                     __syncwarp();
                 }
-                if (i < p.n) p.lse[(size_t)w.bh * p.n + i] = (m_run + log2f(l_run)) * kLn2;
+                if (i < w.len) {
+                    // [B, H, N] rows, or [H, total] for packed sequences
+                    const size_t lrow = (MODE == 1 && p.cu_seqlens != nullptr)
+                                            ? (size_t)w.h * (size_t)p.total + (size_t)w.tok0 + (size_t)i
+                                            : (size_t)w.bh * (size_t)p.n + (size_t)i;
+                    p.lse[lrow] = (m_run + log2f(l_run)) * kLn2;
+                }
                 g += (uint32_t)w.nkv;
                 base += 2u + 2u * (uint32_t)w.nkv;
             }
@@ -420,16 +467,26 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
     }
 }
 
-}  // namespace
-
-cudaError_t tc256_prepare(bool causal, bool f16) {
+template <bool CAUSAL, bool F16>
+cudaError_t prepare_modes() {
     auto set = [](const void* fn) {
         return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     };
-    if (causal) return f16 ? set((const void*)fa_tc256_kernel<true, true>)
-                           : set((const void*)fa_tc256_kernel<true, false>);
-    return f16 ? set((const void*)fa_tc256_kernel<false, true>)
-               : set((const void*)fa_tc256_kernel<false, false>);
+    const cudaError_t e = set((const void*)fa_tc256_kernel<CAUSAL, F16, 0>);
+    return e != cudaSuccess ? e : set((const void*)fa_tc256_kernel<CAUSAL, F16, 1>);
+}
+
+template <bool CAUSAL, bool F16>
+void launch_mode(int mode, const TcParams& p, int grid, cudaStream_t stream) {
+    if (mode == 0) fa_tc256_kernel<CAUSAL, F16, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    else fa_tc256_kernel<CAUSAL, F16, 1><<<grid, kThreads, kSmemBytes, stream>>>(p);
+}
+
+}  // namespace
+
+cudaError_t tc256_prepare(bool causal, bool f16) {
+    if (causal) return f16 ? prepare_modes<true, true>() : prepare_modes<true, false>();
+    return f16 ? prepare_modes<false, true>() : prepare_modes<false, false>();
 }
 
 int tc256_units(int bh, int n, bool causal) {
@@ -440,12 +497,13 @@ int tc256_units(int bh, int n, bool causal) {
 
 cudaError_t tc256_launch(bool causal, bool f16, const TcParams& p, int grid, cudaStream_t stream) {
     if (grid < 1 || p.units < 1) return cudaErrorInvalidConfiguration;
+    const int mode = p.layout;   // 0: [B, H, N, D]; 1: token-major
     if (causal) {
-        if (f16) fa_tc256_kernel<true, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
-        else fa_tc256_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        if (f16) launch_mode<true, true>(mode, p, grid, stream);
+        else launch_mode<true, false>(mode, p, grid, stream);
     } else {
-        if (f16) fa_tc256_kernel<false, true><<<grid, kThreads, kSmemBytes, stream>>>(p);
-        else fa_tc256_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(p);
+        if (f16) launch_mode<false, true>(mode, p, grid, stream);
+        else launch_mode<false, false>(mode, p, grid, stream);
     }
     return cudaGetLastError();
 }

@@ -48,7 +48,7 @@ typedef enum {
  *   lse     : device pointer, [B, H, N] contiguous fp32; written fully.
  *   B, H, N : >= 1.  B*H < 2^31 and N < 2^31.  Any N is accepted (a ragged last tile is
  *             masked; keys >= N never contribute).
- *   D       : head dimension: 32, 64 or 128; 256 for bf16/fp16 storage (fa_fwd only).
+ *   D       : head dimension: 32, 64 or 128; 256 for bf16/fp16 storage.
  *   scale   : finite, >= 0 (normally 1/sqrt(D)).
  *   causal  : 0 = all keys; 1 = key j <= query i (square N x N).
  *   dtype   : an fa_dtype value.
@@ -76,8 +76,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *                and writing this layout directly saves the [B,N,H,D] <-> [B,H,N,D] copies
  *                around the attention ("pwwt.cn: FlashAttention 与内存墙" §5.2).
  *   lse        : device pointer, [B, H, N] contiguous fp32.
- *   Everything else as fa_fwd (same limits, ownership, errors, asynchrony), except that
- *   D = 256 is not served here (FA_ERR_UNSUPPORTED).
+ *   Everything else as fa_fwd (same limits, ownership, errors, asynchrony).
  */
 int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse,
                 int64_t B, int64_t N, int64_t H, int64_t D,
@@ -98,7 +97,7 @@ int fa_fwd_bnhd(const void* q, const void* k, const void* v, void* o, float* lse
  *                access outside the tensors; they are not otherwise checked (checking would
  *                need a device-to-host copy).
  *   batch, max_seqlen, total, H : >= 1; batch*H < 2^31; total < 2^31.
- *   Everything else as fa_fwd, except that D = 256 is not served here (FA_ERR_UNSUPPORTED).
+ *   Everything else as fa_fwd.
  */
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                   const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen, int64_t total,

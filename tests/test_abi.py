@@ -101,10 +101,10 @@ def test_varlen_and_bnhd_argument_checks(lib):
                            2, 128, 4, 96, 0.1, 0, 1, None) == UNSUPPORTED
     assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
                            2, 0, 4, 128, 0.1, 0, 1, None) == INVALID
-    # D = 256 is served for the [B, H, N, D] layout only
+    # D = 256: 16-bit storage only, in every layout
     assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
-                           2, 128, 4, 256, 0.1, 0, 1, None) == UNSUPPORTED
-    assert varlen(D=256) == UNSUPPORTED
+                           2, 128, 4, 256, 0.1, 0, 0, None) == UNSUPPORTED
+    assert varlen(D=256, dtype=0) == UNSUPPORTED
 
 
 def test_watchdog_control_validation(lib):

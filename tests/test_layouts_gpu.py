@@ -100,3 +100,28 @@ def test_varlen_malformed_offsets_stay_in_bounds():
     torch.cuda.synchronize()
     assert binding.check_device_status()[0] == 0
     assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
+
+
+# ------------------------------------------------------------ head dimension 256
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bnhd_head_dim_256(causal, dtype):
+    B, N, H, D = 2, 333, 3, 256
+    q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in make_shape(B, H, N, D, dtype, seed=261))
+    o, lse = binding.fwd_bnhd(q.cuda(), k.cuda(), v.cuda(), causal=causal)
+    torch.cuda.synchronize()
+    assert binding.check_device_status()[0] == 0
+    to_bhnd = lambda t: t.permute(0, 2, 1, 3).double().numpy()  # noqa: E731
+    o_ref, lse_ref = oracle.attention_fwd(to_bhnd(q), to_bhnd(k), to_bhnd(v), 1 / math.sqrt(D), causal)
+    check(o.permute(0, 2, 1, 3).double().cpu().numpy(), lse.double().cpu().numpy(), o_ref, lse_ref,
+          dtype, "bnhd D=256 causal=%d" % causal)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("mix", range(len(LENGTH_MIXES)))
+def test_varlen_head_dim_256(mix, causal):
+    run_varlen(LENGTH_MIXES[mix], 2, 256, "bf16", causal, seed=mix * 10 + 256)
+
+
+def test_varlen_head_dim_256_fp16_and_empty():
+    run_varlen([0, 65, 0, 190], 2, 256, "fp16", True, seed=257)
