@@ -39,6 +39,15 @@ SIGNATURES = {
                           _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                           _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
                           _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_bwd_bnhd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                               _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                               _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
+                               _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_bwd_varlen": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                 _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                 _c.c_int64, _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64,
+                                 _c.c_int64, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
+                                 _c.c_void_p]),
     "fa_bwd_noalloc": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                   _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                   _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
@@ -287,6 +296,69 @@ def bwd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=No
                                          workspace.numel() * workspace.element_size(), B, H, N,
                                          D, float(scale), int(causal), _dtype_code(q),
                                          _stream_handle(q, stream))))
+    return dq, dk, dv
+
+
+def _bwd_buffers(q, o, dout, lse, lse_shape, dq, dk, dv, workspace, need):
+    """Check and allocate the backward's buffers (shared by the layout variants)."""
+    import torch
+    _check_buffer(o, "o", q.shape, q.dtype, q.device)
+    _check_buffer(dout, "dout", q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", lse_shape, torch.float32, q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(q) if dk is None else dk
+    dv = torch.empty_like(q) if dv is None else dv
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_buffer(t, name, q.shape, q.dtype, q.device)
+    if need < 0:
+        raise FaError(1, "sizes out of range")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if not (workspace.is_cuda and workspace.device == q.device and workspace.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor on %s" % q.device)
+    return dq, dk, dv, workspace
+
+
+def bwd_bnhd(q, k, v, o, lse, dout, scale=None, causal=False, dq=None, dk=None, dv=None,
+             workspace=None, stream=None):
+    """Backward over token-major tensors [B, N, H, D] (fa_bwd_bnhd); lse [B, H, N] as
+    fwd_bnhd returns it.  Returns (dq, dk, dv) in [B, N, H, D]."""
+    import torch
+    _common(q, k, v, 4)
+    B, N, H, D = q.shape
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq, dk, dv, workspace = _bwd_buffers(q, o, dout, lse, (B, H, N), dq, dk, dv, workspace,
+                                         bwd_workspace_bytes(B, H, N))
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_bwd_bnhd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), B, N, H, D, float(scale), int(causal),
+            _dtype_code(q), _stream_handle(q, stream))))
+    return dq, dk, dv
+
+
+def bwd_varlen(q, k, v, o, lse, dout, cu_seqlens, max_seqlen, scale=None, causal=False,
+               dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward over packed sequences (fa_bwd_varlen): q, k, v, o, dout [total, H, D],
+    lse [H, total] as fwd_varlen returns it, the same cu_seqlens.  Returns (dq, dk, dv)."""
+    import torch
+    _common(q, k, v, 3)
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1
+            and cu_seqlens.is_contiguous() and cu_seqlens.device == q.device):
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor on %s" % q.device)
+    T, H, D = q.shape
+    batch = cu_seqlens.numel() - 1
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    dq, dk, dv, workspace = _bwd_buffers(q, o, dout, lse, (H, T), dq, dk, dv, workspace,
+                                         bwd_workspace_bytes(1, H, T))
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_bwd_varlen(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), cu_seqlens.data_ptr(), batch,
+            int(max_seqlen), T, H, D, float(scale), int(causal), _dtype_code(q),
+            _stream_handle(q, stream))))
     return dq, dk, dv
 
 

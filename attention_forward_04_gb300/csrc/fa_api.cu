@@ -108,7 +108,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 
 extern "C" {
 
-int fa_version(void) { return 130; }
+int fa_version(void) { return 140; }
 
 const char* fa_status_string(int status) {
     switch (status) {
@@ -343,42 +343,62 @@ int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N) {
     return (bytes + 255) / 256 * 256;
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-           const float* lse, void* dq, void* dk, void* dv, void* workspace, int64_t workspace_bytes,
-           int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal, int dtype,
-           void* stream) {
+}  // extern "C"
+
+namespace {
+
+// One backward request: [B, H, N, D] (layout 0), token-major [B, N, H, D] (layout 1, cu
+// null, T = B*N) or packed sequences (layout 1, cu set, B = batch, N = max_seqlen, T = total).
+struct BwdRequest {
+    const void *q, *k, *v, *o, *dout;
+    const float* lse;
+    void *dq, *dk, *dv, *workspace;
+    int64_t workspace_bytes, B, H, N, D, T;
+    int layout;
+    const int32_t* cu;
+    float scale;
+    int causal, dtype;
+    void* stream;
+};
+
+int backward(const BwdRequest& r) {
     // ---- argument checks: no CUDA call before these pass
-    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv || !workspace)
+    if (!r.q || !r.k || !r.v || !r.o || !r.dout || !r.lse || !r.dq || !r.dk || !r.dv || !r.workspace)
         return FA_ERR_INVALID_ARG;
-    const int64_t need = fa_bwd_workspace_bytes(B, H, N);
-    if (need < 0) return FA_ERR_INVALID_ARG;
-    if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-    if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;
-    if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (dtype == FA_FP32) return FA_ERR_UNSUPPORTED;   // backward: 16-bit storage only
-    if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
-    const int64_t BH = B * H;
-    const size_t tbytes = (size_t)BH * (size_t)N * (size_t)D * 2;
-    const size_t lbytes = (size_t)BH * (size_t)N * sizeof(float);
-    if (tbytes / 2 / (size_t)D / (size_t)N != (size_t)BH) return FA_ERR_INVALID_ARG;
-    const void* ins[7] = {q, k, v, o, dout, lse, workspace};
+    const bool packed = r.cu != nullptr;
+    if (r.layout == 1 && packed && (r.T < 1 || r.T > 0x7FFFFFFFLL)) return FA_ERR_INVALID_ARG;
+    // delta is indexed like the LSE: [B*H, N], or [H, total] for packed sequences
+    const int64_t need = packed ? fa_bwd_workspace_bytes(1, r.H, r.T) : fa_bwd_workspace_bytes(r.B, r.H, r.N);
+    if (need < 0 || fa_bwd_workspace_bytes(r.B, r.H, r.N) < 0) return FA_ERR_INVALID_ARG;
+    if (r.workspace_bytes < need) return FA_ERR_INVALID_ARG;
+    if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
+    if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
+    if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
+    if (r.dtype == FA_FP32) return FA_ERR_UNSUPPORTED;   // backward: 16-bit storage only
+    if (r.D != 32 && r.D != 64 && r.D != 128) return FA_ERR_UNSUPPORTED;
+    if (r.layout == 1 && !packed && r.B * r.N > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;   // tokens
+    const int64_t BH = r.B * r.H;
+    const int64_t rows = packed ? r.T * r.H : BH * r.N;         // query rows in the tensors
+    const size_t tbytes = (size_t)rows * (size_t)r.D * 2;
+    const size_t lbytes = (size_t)rows * sizeof(float);
+    if (tbytes / 2 / (size_t)r.D != (size_t)rows) return FA_ERR_INVALID_ARG;
+    const void* ins[7] = {r.q, r.k, r.v, r.o, r.dout, r.lse, r.workspace};
     const size_t in_bytes[7] = {tbytes, tbytes, tbytes, tbytes, tbytes, lbytes, (size_t)need};
-    void* outs[3] = {dq, dk, dv};
+    void* outs[3] = {r.dq, r.dk, r.dv};
     for (int a = 0; a < 3; ++a) {
         for (int b = 0; b < 7; ++b)
             if (overlaps(outs[a], tbytes, ins[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
         for (int b = a + 1; b < 3; ++b)
             if (overlaps(outs[a], tbytes, outs[b], tbytes)) return FA_ERR_INVALID_ARG;
     }
-    if (overlaps(workspace, (size_t)need, q, tbytes) || overlaps(workspace, (size_t)need, k, tbytes) ||
-        overlaps(workspace, (size_t)need, v, tbytes) || overlaps(workspace, (size_t)need, o, tbytes) ||
-        overlaps(workspace, (size_t)need, dout, tbytes) || overlaps(workspace, (size_t)need, lse, lbytes))
-        return FA_ERR_INVALID_ARG;
-    for (const void* ptr : {q, k, v, o, dout, static_cast<const void*>(dq),
-                            static_cast<const void*>(dk), static_cast<const void*>(dv)})
+    for (const void* t : {r.q, r.k, r.v, r.o, r.dout, static_cast<const void*>(r.lse)})
+        if (overlaps(r.workspace, (size_t)need, t, t == static_cast<const void*>(r.lse) ? lbytes : tbytes))
+            return FA_ERR_INVALID_ARG;
+    for (const void* ptr : {r.q, r.k, r.v, r.o, r.dout, static_cast<const void*>(r.dq),
+                            static_cast<const void*>(r.dk), static_cast<const void*>(r.dv)})
         if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_MISALIGNED;
-    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+    if ((reinterpret_cast<uintptr_t>(r.lse) & 3u) || (reinterpret_cast<uintptr_t>(r.workspace) & 15u) ||
+        (reinterpret_cast<uintptr_t>(r.cu) & 3u))
         return FA_ERR_MISALIGNED;
 
     // ---- device
@@ -396,10 +416,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     });
     if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
     if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;
-    const bool f16 = dtype == FA_FP16;
-    const int dix = D == 32 ? 0 : D == 64 ? 1 : 2, dic = causal != 0, dif = f16;
+    const bool f16 = r.dtype == FA_FP16;
+    const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = f16;
     std::call_once(di.bwd_prepared[dix][dic][dif],
-                   [&] { di.bwd_prepare_err[dix][dic][dif] = fa::bwd_prepare((int)D, dic, f16); });
+                   [&] { di.bwd_prepare_err[dix][dic][dif] = fa::bwd_prepare((int)r.D, dic, f16); });
     if (di.bwd_prepare_err[dix][dic][dif] != cudaSuccess)
         return fail_cuda(di.bwd_prepare_err[dix][dic][dif], "cudaFuncSetAttribute (backward)");
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
@@ -408,27 +428,66 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
     const int et = f16 ? 1 : 0;
-    if (!encode_map(&p.tmap_q, q, 0, BH, N, H, B * N, D, et, fn) ||
-        !encode_map(&p.tmap_k, k, 0, BH, N, H, B * N, D, et, fn) ||
-        !encode_map(&p.tmap_v, v, 0, BH, N, H, B * N, D, et, fn) ||
-        !encode_map(&p.tmap_do, dout, 0, BH, N, H, B * N, D, et, fn))
+    if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
+        !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
+        !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
+        !encode_map(&p.tmap_do, r.dout, r.layout, BH, r.N, r.H, r.T, r.D, et, fn))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
-    p.lse = lse;
-    p.o = o;
-    p.q = q;
-    p.dout = dout;
-    p.delta = static_cast<float*>(workspace);
-    p.dq = dq;
-    p.dk = dk;
-    p.dv = dv;
-    p.n = (int)N;
-    p.ntiles = (int)((N + 127) / 128);
-    p.scale = scale;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.lse = r.lse;
+    p.o = r.o;
+    p.q = r.q;
+    p.dout = r.dout;
+    p.delta = static_cast<float*>(r.workspace);
+    p.dq = r.dq;
+    p.dk = r.dk;
+    p.dv = r.dv;
+    p.n = (int)r.N;
+    p.ntiles = (int)((r.N + 127) / 128);
+    p.scale = r.scale;
+    p.scale_log2 = r.scale * 1.4426950408889634f;
     p.wait_limit = g_wait_limit.load();
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    e = fa::bwd_launch((int)D, dic, f16, p, (int)BH, st);
+    p.layout = r.layout;
+    p.heads = (int)r.H;
+    p.total = (int)r.T;
+    p.cu_seqlens = r.cu;
+    cudaStream_t st = static_cast<cudaStream_t>(r.stream);
+    e = fa::bwd_launch((int)r.D, dic, f16, p, (int)BH, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "backward kernel launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+           const float* lse, void* dq, void* dk, void* dv, void* workspace, int64_t workspace_bytes,
+           int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal, int dtype,
+           void* stream) {
+    if (B < 1 || N < 1 || B > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+    const BwdRequest r{q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                       B, H, N, D, B * N, 0, nullptr, scale, causal, dtype, stream};
+    return backward(r);
+}
+
+int fa_bwd_bnhd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                int64_t workspace_bytes, int64_t B, int64_t N, int64_t H, int64_t D, float scale,
+                int causal, int dtype, void* stream) {
+    if (B < 1 || N < 1 || B > 0x7FFFFFFFLL || N > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;
+    const BwdRequest r{q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                       B, H, N, D, B * N, 1, nullptr, scale, causal, dtype, stream};
+    return backward(r);
+}
+
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                  int64_t workspace_bytes, const int32_t* cu_seqlens, int64_t batch,
+                  int64_t max_seqlen, int64_t total, int64_t H, int64_t D, float scale,
+                  int causal, int dtype, void* stream) {
+    if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+    const BwdRequest r{q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes,
+                       batch, H, max_seqlen, D, total, 1, cu_seqlens, scale, causal, dtype, stream};
+    return backward(r);
 }
 
 int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -71,6 +71,51 @@ __device__ __forceinline__ uint64_t bdesc(uint32_t saddr, uint32_t lbo) {
            ((uint64_t)((R::kSBO >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (R::kLayout << 61);
 }
 
+// Where the rows of one (b, h) slice live.  MODE 0, [B, H, N, D]: N rows of D elements
+// from element bh*N*D; LSE and delta at bh*N.  MODE 1, token-major [tokens, H, D]: rows H*D
+// elements apart from token tok0 (fixed length N: tok0 = b*N; packed sequences: the
+// clamped offsets of cu_seqlens), LSE and delta at [B, H, N] index bh*N, or [H, total]
+// index h*total + tok0 for packed sequences.  A malformed offset can only give wrong
+// values, never an access outside the tensors.
+struct Slice {
+    int len;          // rows of the slice
+    int h, tok0;      // token-major: TMA coordinates of row 0 (head, token)
+    size_t row0;      // element offset of row 0 in q, k, v, o, dout, dq, dk, dv
+    size_t stride;    // elements from one row to the next
+    size_t vec0;      // index of row 0 in lse and delta
+};
+
+template <int MODE, int D>
+__device__ __forceinline__ Slice slice_at(const BwdParams& p, int bh) {
+    Slice sl;
+    if (MODE == 0) {
+        sl.len = p.n;
+        sl.h = 0;
+        sl.tok0 = 0;
+        sl.row0 = (size_t)bh * (size_t)p.n * D;
+        sl.stride = D;
+        sl.vec0 = (size_t)bh * (size_t)p.n;
+        return sl;
+    }
+    const int b = bh / p.heads;
+    sl.h = bh % p.heads;
+    if (p.cu_seqlens != nullptr) {
+        int s0 = __ldg(p.cu_seqlens + b), s1 = __ldg(p.cu_seqlens + b + 1);
+        s0 = min(max(s0, 0), p.total);
+        s1 = min(max(s1, s0), p.total);
+        sl.len = min(s1 - s0, p.n);
+        sl.tok0 = s0;
+        sl.vec0 = (size_t)sl.h * (size_t)p.total + (size_t)s0;
+    } else {
+        sl.len = p.n;
+        sl.tok0 = b * p.n;
+        sl.vec0 = (size_t)bh * (size_t)p.n;
+    }
+    sl.row0 = ((size_t)sl.tok0 * p.heads + sl.h) * D;
+    sl.stride = (size_t)p.heads * D;
+    return sl;
+}
+
 // Shared memory: FIXED fixed 128 x D tiles, a ring of SLOTS streamed tiles, the staged
 // per-column vectors (dK/dV), then the barriers.
 template <int D, int FIXED, int SLOTS>
@@ -168,12 +213,13 @@ __device__ __forceinline__ void mma_ts_tn(uint32_t acc_tmem, uint32_t a_tmem, ui
 
 // ----------------------------------------------------------------- epilogue
 // This warp's 32 TMEM lanes x 64 fp32 columns at t_acc, times mul, rounded to 16 bits, to
-// global rows base + r * D (r < 32, only rows with row0 + r < nrows; base points at the
-// panel's first column), through a 4 KB staging slot so every store instruction writes
-// whole 128-byte lines.
-template <int D, bool F16>
+// global rows base + (row0 + r) * stride (r < 32, only rows with row0 + r < nrows; base
+// points at the panel's first column), through a 4 KB staging slot so every store
+// instruction writes whole 128-byte lines.
+template <bool F16>
 __device__ __forceinline__ void store_rows(uint32_t t_acc, float mul, uint32_t stage,
-                                           uint16_t* base, int row0, int nrows, int lane) {
+                                           uint16_t* base, size_t stride, int row0, int nrows,
+                                           int lane) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t o[32];
@@ -195,19 +241,20 @@ __device__ __forceinline__ void store_rows(uint32_t t_acc, float mul, uint32_t s
         const int ch = lane & 7;
         const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u + (uint32_t)((ch ^ (r & 7)) * 16));
         if (row0 + r < nrows)
-            *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * D + ch * 8) = v;
+            *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * stride + ch * 8) = v;
     }
     __syncwarp();
 }
 
 // D = 32: this warp's 32 TMEM lanes x 32 fp32 columns at t_acc, times mul, rounded to 16
-// bits, to global rows base + r * 32 (64 bytes each; only rows with row0 + r < nrows).  The
-// warp's rows are one contiguous 2 KB block: staged with the 16-byte chunks of row r
-// XOR-swizzled by (r >> 1) & 3 (free of bank conflicts both ways), each store instruction
-// then writes 512 contiguous bytes.
+// bits, to global rows base + (row0 + r) * stride (64 bytes each; only rows with
+// row0 + r < nrows).  Staged with the 16-byte chunks of row r XOR-swizzled by (r >> 1) & 3
+// (free of bank conflicts both ways); in [B, H, N, D] the warp's rows are one contiguous
+// 2 KB block, so each store instruction then writes 512 contiguous bytes.
 template <bool F16>
 __device__ __forceinline__ void store_rows32(uint32_t t_acc, float mul, uint32_t stage,
-                                             uint16_t* base, int row0, int nrows, int lane) {
+                                             uint16_t* base, size_t stride, int row0, int nrows,
+                                             int lane) {
     uint32_t o[32];
     ptx::tmem_ld32_wait(t_acc, o);
     uint32_t w[16];
@@ -225,7 +272,7 @@ __device__ __forceinline__ void store_rows32(uint32_t t_acc, float mul, uint32_t
         const int ch = lane & 3;
         const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 64u + (uint32_t)((ch ^ ((r >> 1) & 3)) * 16));
         if (row0 + r < nrows)
-            *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * 32 + ch * 8) = v;
+            *reinterpret_cast<uint4*>(base + (size_t)(row0 + r) * stride + ch * 8) = v;
     }
     __syncwarp();
 }
@@ -302,29 +349,35 @@ __device__ __forceinline__ void teardown_cta(const Setup& su) {
     }
 }
 
-// One 128 x D tile (rows row.. of `map`, slice bh) into shared memory at dst, completing
-// on barrier bar (whose expected bytes the caller has set).
-template <int D>
+// One 128 x D tile (rows row.. of the slice) into shared memory at dst, completing on
+// barrier bar (whose expected bytes the caller has set).  Map dims {D, N, B*H} (MODE 0) or
+// {D, H, tokens} (MODE 1).
+template <int D, int MODE>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                          int row, int bh) {
+                                          int row, int bh, const Slice& sl) {
     using R = Rows<D>;
 #pragma unroll
-    for (int pc = 0; pc < R::kPanels; ++pc)
-        ptx::tma_load_3d(dst + (uint32_t)pc * R::kPanelBytes, map, bar, pc * R::kCols, row, bh);
+    for (int pc = 0; pc < R::kPanels; ++pc) {
+        if (MODE == 0)
+            ptx::tma_load_3d(dst + (uint32_t)pc * R::kPanelBytes, map, bar, pc * R::kCols, row, bh);
+        else
+            ptx::tma_load_3d(dst + (uint32_t)pc * R::kPanelBytes, map, bar, pc * R::kCols, sl.h,
+                             sl.tok0 + row);
+    }
 }
 
 // dK/dV loader: the two fixed tiles (f0, f1 at fixed_row), then for steps j < steps the
 // tiles A_j (map ma) and B_j (map mb), rows first_row + 128 j, through the paired ring.
 // Waits for its own copies before returning, so no copy is in flight when the CTA leaves.
-template <int D>
+template <int D, int MODE>
 __device__ void load_pairs(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
                            const CUtensorMap* f1, int fixed_row, const CUtensorMap* ma,
-                           const CUtensorMap* mb, int first_row, int steps, int bh) {
+                           const CUtensorMap* mb, int first_row, int steps, int bh, const Slice& sl) {
     using G = GeoDkdv<D>;
     const uint32_t fb = bar_addr(c, G::fixed_full());
     ptx::mbar_arrive_expect_tx(fb, 2u * G::kTile);
-    load_tile<D>(sbase, f0, fb, fixed_row, bh);
-    load_tile<D>(sbase + (uint32_t)G::kTile, f1, fb, fixed_row, bh);
+    load_tile<D, MODE>(sbase, f0, fb, fixed_row, bh, sl);
+    load_tile<D, MODE>(sbase + (uint32_t)G::kTile, f1, fb, fixed_row, bh, sl);
     int issued = 0;   // tiles issued, A and B alternating
     for (int j = 0; j < steps; ++j) {
         for (int w = 0; w < 2; ++w) {
@@ -332,8 +385,8 @@ __device__ void load_pairs(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
             if (!wait(c, G::ring_empty(slot), slot_par(j) ^ 1u, kRoleLoad)) goto out;
             const uint32_t bar = bar_addr(c, G::ring_full(slot));
             ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
-            load_tile<D>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, w == 0 ? ma : mb,
-                         bar, first_row + j * kT, bh);
+            load_tile<D, MODE>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, w == 0 ? ma : mb,
+                               bar, first_row + j * kT, bh, sl);
             ++issued;
         }
     }
@@ -349,13 +402,13 @@ out:
 // dQ loader: the fixed tile dO (rows fixed_row), then streamed tile 0 = Q (rows fixed_row)
 // and tiles 1 + 2j = K_j, 2 + 2j = V_j (rows 128 j) through the cyclic ring.  Waits for its
 // own copies before returning.
-template <int D>
+template <int D, int MODE>
 __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fixed_row, int nkv,
-                        int bh) {
+                        int bh, const Slice& sl) {
     using G = GeoDq<D>;
     const uint32_t fb = bar_addr(c, G::fixed_full());
     ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTile);
-    load_tile<D>(sbase, &p.tmap_do, fb, fixed_row, bh);
+    load_tile<D, MODE>(sbase, &p.tmap_do, fb, fixed_row, bh, sl);
     const uint32_t count = 1u + 2u * (uint32_t)nkv;
     uint32_t pos = 0;
     for (; pos < count; ++pos) {
@@ -365,7 +418,7 @@ __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fi
         const CUtensorMap* map = pos == 0 ? &p.tmap_q : ((pos & 1u) ? &p.tmap_k : &p.tmap_v);
         const int row = pos == 0 ? fixed_row : (int)((pos - 1u) >> 1) * kT;
         ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
-        load_tile<D>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, map, bar, row, bh);
+        load_tile<D, MODE>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, map, bar, row, bh, sl);
     }
     wait_drain(fb, 0, c.limit);
     for (uint32_t i = (pos > (uint32_t)G::kSlots ? pos - G::kSlots : 0u); i < pos; ++i)
@@ -377,9 +430,13 @@ __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fi
 // accumulator [QC+320, +D) with QC = max(D/2, 32), so every region starts on a multiple of
 // 32 columns (512 columns at D = 128).
 // Shared memory: dO fixed; ring: Q (copied to TMEM, then released), K_j, V_j.
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using G = GeoDq<D>;
+    // query tiles past a (shorter packed) sequence have nothing to do: the whole CTA leaves
+    const int bh = blockIdx.x / p.ntiles, qt = blockIdx.x % p.ntiles;
+    const Slice sl = slice_at<MODE, D>(p, bh);
+    if (qt * kT >= sl.len) return;
     constexpr uint32_t kQC = D / 2 < 32 ? 32 : D / 2;
     constexpr uint32_t kColQ = 0, kColDS = kQC, kColS = kQC + 64, kColDP = kColS + 128,
                        kColAcc = kColDP + 128;
@@ -388,13 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
     const Setup su = setup_cta<G>(smem_raw, p);
     const Ctl& c = su.c;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int bh = blockIdx.x / p.ntiles, qt = blockIdx.x % p.ntiles;
-    const int nkv = CAUSAL ? min(qt + 1, p.ntiles) : p.ntiles;
+    const int ntl = (sl.len + kT - 1) / kT;   // key tiles of the slice
+    const int nkv = CAUSAL ? min(qt + 1, ntl) : ntl;
     const uint32_t tm = su.tmem;
 
     if (warp == kLoadWarp) {
         if (lane == 0)
-            load_dq<D>(c, su.sbase, p, qt * kT, nkv, bh);
+            load_dq<D, MODE>(c, su.sbase, p, qt * kT, nkv, bh, sl);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
@@ -450,11 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
         // elementwise: thread = query row r; this warp's 64 of the 128 keys of each tile
         const int quarter = warp & 3, ch = warp >> 2;
         const int r = quarter * 32 + lane;
-        const int i = qt * kT + r;
-        const bool live = i < p.n;
-        const size_t row = (size_t)bh * p.n + (live ? i : 0);
-        const float lse2 = live ? p.lse[row] * kLog2e : 0.0f;
-        const int limit = CAUSAL ? min(i + 1, p.n) : p.n;    // visible keys: key < limit
+        const int i = qt * kT + r;   // row within the slice
+        const bool live = i < sl.len;
+        const size_t vrow = sl.vec0 + (size_t)(live ? i : 0);                  // lse, delta
+        const size_t erow = sl.row0 + (size_t)(live ? i : 0) * sl.stride;      // q, o, dout
+        const float lse2 = live ? p.lse[vrow] * kLog2e : 0.0f;
+        const int limit = CAUSAL ? min(i + 1, sl.len) : sl.len;    // visible keys: key < limit
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
         float* part = reinterpret_cast<float*>(smem_raw + (su.sbase - ptx::smem_addr(smem_raw)) + G::kVecOff);
         float dlt = 0.0f;
@@ -464,8 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             const bool mine = live && ch == 0;
             float acc = 0.0f;
             if (mine) {
-                const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + row * D);
-                const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + row * D);
+                const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + erow);
+                const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + erow);
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     const uint4 ov = __ldg(orow + cc), dv = __ldg(drow + cc);
@@ -486,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             uint4 ovs[8];
             if (mine) {
                 const uint4* orow = reinterpret_cast<const uint4*>(
-                    static_cast<const uint16_t*>(p.o) + row * D + 64 * ch);
+                    static_cast<const uint16_t*>(p.o) + erow + 64 * ch);
 #pragma unroll
                 for (int cc = 0; cc < 8; ++cc) ovs[cc] = __ldg(orow + cc);
             }
@@ -516,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             if constexpr (D == 32) {
                 if (ok && ch == 0) {
                     uint32_t w[16];
-                    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + row * D);
+                    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + erow);
 #pragma unroll
                     for (int cc = 0; cc < 4; ++cc) {
                         const uint4 v = live ? __ldg(qrow + cc) : make_uint4(0u, 0u, 0u, 0u);
@@ -545,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             }
             // both partial sums are published by the barrier above
             dlt = part[r] + part[kT + r];
-            if (live && ch == 0) p.delta[row] = dlt;   // for the dK/dV kernel
+            if (live && ch == 0) p.delta[vrow] = dlt;   // for the dK/dV kernel
         }
         for (int j = 0; j < nkv; ++j) {
             const uint32_t par = (uint32_t)j & 1u;
@@ -602,13 +660,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
             if (ch == 0)
                 store_rows32<F16>(tm + tl + kColAcc, p.scale,
                                   su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
-                                  reinterpret_cast<uint16_t*>(p.dq) + (size_t)bh * p.n * D,
-                                  qt * kT + quarter * 32, p.n, lane);
+                                  reinterpret_cast<uint16_t*>(p.dq) + sl.row0, sl.stride,
+                                  qt * kT + quarter * 32, sl.len, lane);
         } else if (ch < D / 64) {   // one 64-column panel of dQ per warp
-            store_rows<D, F16>(tm + tl + kColAcc + 64u * (uint32_t)ch, p.scale,
-                               su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
-                               reinterpret_cast<uint16_t*>(p.dq) + (size_t)bh * p.n * D + 64 * ch,
-                               qt * kT + quarter * 32, p.n, lane);
+            store_rows<F16>(tm + tl + kColAcc + 64u * (uint32_t)ch, p.scale,
+                            su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u,
+                            reinterpret_cast<uint16_t*>(p.dq) + sl.row0 + 64 * ch, sl.stride,
+                            qt * kT + quarter * 32, sl.len, lane);
         }
     ew_out:;
     }
@@ -619,23 +677,27 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_consta
 // TMEM columns: S^T [0, 128), dP^T [128, 256), dV [256, 256+D), dK [256+D, 256+2D)
 // (D = 32: dK at 288, a multiple of 32 columns as every other region).
 // Shared memory: K, V fixed; ring A_s = Q_i, B_s = dO_i for query tile i = i0 + s.
-template <int D, bool CAUSAL, bool F16>
+template <int D, bool CAUSAL, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
     using G = GeoDkdv<D>;
+    // key tiles past a (shorter packed) sequence have nothing to do: the whole CTA leaves
+    const int bh = blockIdx.x / p.ntiles, kt = blockIdx.x % p.ntiles;
+    const Slice sl = slice_at<MODE, D>(p, bh);
+    if (kt * kT >= sl.len) return;
     constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     extern __shared__ uint8_t smem_raw[];
     const Setup su = setup_cta<G>(smem_raw, p);
     const Ctl& c = su.c;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int bh = blockIdx.x / p.ntiles, kt = blockIdx.x % p.ntiles;
+    const int ntl = (sl.len + kT - 1) / kT;         // query tiles of the slice
     const int i0 = CAUSAL ? kt : 0;                 // first query tile that sees this key tile
-    const int nq = p.ntiles - i0;
+    const int nq = ntl - i0;
     const uint32_t tm = su.tmem;
 
     if (warp == kLoadWarp) {
         if (lane == 0)
-            load_pairs<D>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, &p.tmap_q, &p.tmap_do,
-                          i0 * kT, nq, bh);
+            load_pairs<D, MODE>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, &p.tmap_q, &p.tmap_do,
+                                i0 * kT, nq, bh, sl);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);
@@ -694,9 +756,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         // delta.  The next tile's value is fetched one step ahead into a register.
         auto fetch = [&](int s) -> float {
             const int q = (i0 + s) * kT + (t & (kT - 1));
-            const bool ok = s < nq && q < p.n;
-            if (t < kT) return ok ? p.lse[(size_t)bh * p.n + q] * kLog2e : INFINITY;   // p = 0 past N
-            return ok ? p.delta[(size_t)bh * p.n + q] : 0.0f;
+            const bool ok = s < nq && q < sl.len;
+            if (t < kT) return ok ? p.lse[sl.vec0 + q] * kLog2e : INFINITY;   // p = 0 past the end
+            return ok ? p.delta[sl.vec0 + q] : 0.0f;
         };
         float next = fetch(0);
         bool failed = false;
@@ -773,45 +835,56 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         if constexpr (D == 32) {   // dV by the first, dK by the second warp of each quarter
             const uint32_t stage = su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u;
             const int row0 = kt * kT + quarter * 32;
-            const size_t off = (size_t)bh * p.n * D;
             if (ch == 0)
                 store_rows32<F16>(tm + tl + kColDV, 1.0f, stage,
-                                  reinterpret_cast<uint16_t*>(p.dv) + off, row0, p.n, lane);
+                                  reinterpret_cast<uint16_t*>(p.dv) + sl.row0, sl.stride, row0, sl.len, lane);
             else
                 store_rows32<F16>(tm + tl + kColDK, p.scale, stage,
-                                  reinterpret_cast<uint16_t*>(p.dk) + off, row0, p.n, lane);
+                                  reinterpret_cast<uint16_t*>(p.dk) + sl.row0, sl.stride, row0, sl.len, lane);
         } else if (ch < D / 64) {   // one 64-column panel of dV and of dK per warp
             const uint32_t stage = su.sbase + (uint32_t)G::kStageOff + (uint32_t)warp * 4096u;
             const int row0 = kt * kT + quarter * 32;
-            const size_t off = (size_t)bh * p.n * D + 64 * ch;
-            store_rows<D, F16>(tm + tl + kColDV + 64u * (uint32_t)ch, 1.0f, stage,
-                               reinterpret_cast<uint16_t*>(p.dv) + off, row0, p.n, lane);
-            store_rows<D, F16>(tm + tl + kColDK + 64u * (uint32_t)ch, p.scale, stage,
-                               reinterpret_cast<uint16_t*>(p.dk) + off, row0, p.n, lane);
+            const size_t off = sl.row0 + 64 * ch;
+            store_rows<F16>(tm + tl + kColDV + 64u * (uint32_t)ch, 1.0f, stage,
+                            reinterpret_cast<uint16_t*>(p.dv) + off, sl.stride, row0, sl.len, lane);
+            store_rows<F16>(tm + tl + kColDK + 64u * (uint32_t)ch, p.scale, stage,
+                            reinterpret_cast<uint16_t*>(p.dk) + off, sl.stride, row0, sl.len, lane);
         }
     ew_out:;
     }
     teardown_cta(su);
 }
 
-template <int D, bool CAUSAL, bool F16>
-cudaError_t prepare3() {
-    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL, F16>,
+template <int D, bool CAUSAL, bool F16, int MODE>
+cudaError_t prepare_mode() {
+    cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<D, CAUSAL, F16, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, GeoDq<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(bwd_dkdv_kernel<D, CAUSAL, F16>,
+    return cudaFuncSetAttribute(bwd_dkdv_kernel<D, CAUSAL, F16, MODE>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, GeoDkdv<D>::kSmemBytes);
+}
+
+template <int D, bool CAUSAL, bool F16>
+cudaError_t prepare3() {
+    const cudaError_t e = prepare_mode<D, CAUSAL, F16, 0>();
+    return e != cudaSuccess ? e : prepare_mode<D, CAUSAL, F16, 1>();
+}
+
+template <int D, bool CAUSAL, bool F16, int MODE>
+cudaError_t launch_mode(const BwdParams& p, unsigned ctas, cudaStream_t stream) {
+    bwd_dq_kernel<D, CAUSAL, F16, MODE><<<ctas, kThreads, GeoDq<D>::kSmemBytes, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    bwd_dkdv_kernel<D, CAUSAL, F16, MODE><<<ctas, kThreads, GeoDkdv<D>::kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
 }
 
 template <int D, bool CAUSAL, bool F16>
 cudaError_t launch3(const BwdParams& p, int bh, cudaStream_t stream) {
     const long long ctas = (long long)bh * p.ntiles;
     if (ctas > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    bwd_dq_kernel<D, CAUSAL, F16><<<(unsigned)ctas, kThreads, GeoDq<D>::kSmemBytes, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    bwd_dkdv_kernel<D, CAUSAL, F16><<<(unsigned)ctas, kThreads, GeoDkdv<D>::kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    return p.layout == 0 ? launch_mode<D, CAUSAL, F16, 0>(p, (unsigned)ctas, stream)
+                         : launch_mode<D, CAUSAL, F16, 1>(p, (unsigned)ctas, stream);
 }
 
 template <int D>

@@ -44,11 +44,15 @@ struct BwdParams {
     void* dq;             // [B*H, N, D] outputs, input element type
     void* dk;
     void* dv;
-    int n;                // sequence length N
+    int n;                // sequence length N (packed sequences: the maximum length)
     int ntiles;           // ceil(N / 128)
     float scale;          // softmax scale
     float scale_log2;     // scale * log2(e)
     unsigned long long wait_limit;
+    int layout;           // 0: [B, H, N, D]; 1: token-major [tokens, H, D] (as the forward's)
+    int heads;            // H
+    int total;            // tokens (token-major layouts)
+    const int* cu_seqlens;   // packed sequences: batch + 1 token offsets; nullptr otherwise
 };
 
 // Raise the dynamic shared-memory limit of the backward tensor-core kernels (once).

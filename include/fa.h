@@ -167,6 +167,30 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const voi
            int causal, int dtype, void* stream);
 
 /*
+ * fa_bwd_bnhd -- the backward pass over token-major tensors: q, k, v, o, dout, dq, dk, dv
+ * are [B, N, H, D] contiguous as for fa_fwd_bnhd, lse is [B, H, N] fp32 (fa_fwd_bnhd's
+ * lse).  Everything else as fa_bwd (workspace of fa_bwd_workspace_bytes(B, H, N) bytes).
+ */
+int fa_bwd_bnhd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                int64_t workspace_bytes, int64_t B, int64_t N, int64_t H, int64_t D, float scale,
+                int causal, int dtype, void* stream);
+
+/*
+ * fa_bwd_varlen -- the backward pass over packed sequences: q, k, v, o, dout, dq, dk, dv
+ * are [total, H, D] and lse [H, total] fp32 as for fa_fwd_varlen (same cu_seqlens,
+ * batch, max_seqlen, total, with the same clamping of malformed offsets).  The workspace
+ * holds delta indexed like lse: at least fa_bwd_workspace_bytes(1, H, total) bytes.
+ * Gradient rows of tokens that belong to no sequence (past cu_seqlens[batch]) are not
+ * written.  Everything else as fa_bwd.
+ */
+int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                  const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                  int64_t workspace_bytes, const int32_t* cu_seqlens, int64_t batch,
+                  int64_t max_seqlen, int64_t total, int64_t H, int64_t D, float scale,
+                  int causal, int dtype, void* stream);
+
+/*
  * fa_bwd_noalloc -- fa_bwd with its scratch taken from a fixed array inside the library
  * instead of from the caller.  The pages have no counterpart: it serves callers that
  * cannot provide or allocate device memory at the call site (a pool holding all free HBM,
@@ -219,7 +243,7 @@ int fa_check_device_status(void* stream, uint32_t* detail);
 int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall);
 
 /* Library ABI version (major * 100 + minor). */
-int fa_version(void);   /* 130: adds fa_fwd_fp8 */
+int fa_version(void);   /* 140: adds fa_bwd_bnhd, fa_bwd_varlen */
 
 #ifdef __cplusplus
 }

@@ -182,3 +182,39 @@ def test_fp8_bad_arguments_rejected_before_cuda(lib, kw, expect):
 
 def test_fp8_dtype_code_not_accepted_by_fa_fwd(lib):
     assert call(lib, dtype=3) == INVALID
+
+
+def test_bwd_layout_variants_argument_checks(lib):
+    names = ["q", "k", "v", "o", "do", "lse", "dq", "dk", "dv", "ws"]
+    a = {n: BASE + i * SZ for i, n in enumerate(names)}
+    cu = BASE + 10 * SZ
+
+    def bnhd(B=2, N=300, H=3, D=128, ws_bytes=None, dtype=1, **kw):
+        x = dict(a, **kw)
+        wsb = lib.fa_bwd_workspace_bytes(B, H, N) if ws_bytes is None else ws_bytes
+        return lib.fa_bwd_bnhd(x["q"], x["k"], x["v"], x["o"], x["do"], x["lse"], x["dq"], x["dk"],
+                               x["dv"], x["ws"], wsb, B, N, H, D, 0.1, 0, dtype, None)
+
+    def varlen(cu=cu, batch=3, maxlen=512, total=1000, H=4, D=128, ws_bytes=None, dtype=1, **kw):
+        x = dict(a, **kw)
+        wsb = lib.fa_bwd_workspace_bytes(1, H, total) if ws_bytes is None else ws_bytes
+        return lib.fa_bwd_varlen(x["q"], x["k"], x["v"], x["o"], x["do"], x["lse"], x["dq"],
+                                 x["dk"], x["dv"], x["ws"], wsb, cu, batch, maxlen, total, H, D, 0.1,
+                                 0, dtype, None)
+    assert bnhd(q=0) == INVALID
+    assert bnhd(D=96) == UNSUPPORTED
+    assert bnhd(dtype=0) == UNSUPPORTED
+    assert bnhd(B=1 << 20, N=1 << 12) == INVALID           # more than 2^31 tokens
+    assert bnhd(ws_bytes=100) == INVALID
+    assert bnhd(dq=BASE) == INVALID                        # dq aliases q
+    assert varlen(cu=0) == INVALID
+    assert varlen(cu=cu + 2) == MISALIGNED
+    assert varlen(total=0) == INVALID
+    # delta is indexed like the [H, total] LSE: the workspace must cover H * total floats
+    assert varlen(ws_bytes=lib.fa_bwd_workspace_bytes(1, 4, 1000) - 16) == INVALID
+    assert varlen(D=256) == UNSUPPORTED
+    assert varlen(do=BASE + 4 * SZ + 8) == MISALIGNED
+
+
+def test_version_reports_layout_backward(lib):
+    assert lib.fa_version() >= 140
