@@ -374,14 +374,14 @@ int backward(const BwdRequest& r) {
     if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
     if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (r.dtype == FA_FP32) return FA_ERR_UNSUPPORTED;   // backward: 16-bit storage only
     if (r.D != 32 && r.D != 64 && r.D != 128) return FA_ERR_UNSUPPORTED;
+    const size_t esize = r.dtype == FA_FP32 ? 4 : 2;
     if (r.layout == 1 && !packed && r.B * r.N > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;   // tokens
     const int64_t BH = r.B * r.H;
     const int64_t rows = packed ? r.T * r.H : BH * r.N;         // query rows in the tensors
-    const size_t tbytes = (size_t)rows * (size_t)r.D * 2;
+    const size_t tbytes = (size_t)rows * (size_t)r.D * esize;
     const size_t lbytes = (size_t)rows * sizeof(float);
-    if (tbytes / 2 / (size_t)r.D != (size_t)rows) return FA_ERR_INVALID_ARG;
+    if (tbytes / esize / (size_t)r.D != (size_t)rows) return FA_ERR_INVALID_ARG;
     const void* ins[7] = {r.q, r.k, r.v, r.o, r.dout, r.lse, r.workspace};
     const size_t in_bytes[7] = {tbytes, tbytes, tbytes, tbytes, tbytes, lbytes, (size_t)need};
     void* outs[3] = {r.dq, r.dk, r.dv};
@@ -416,6 +416,21 @@ int backward(const BwdRequest& r) {
     });
     if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
     if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;
+    if (r.dtype == FA_FP32) {   // fp32 storage: the CUDA-core kernels
+        fa::SliceLayout g;
+        g.layout = r.layout;
+        g.cu_seqlens = r.cu;
+        g.heads = (int)r.H;
+        g.total = (int)r.T;
+        g.n = (int)r.N;
+        e = fa::simt_bwd_launch((int)r.D, r.causal != 0, static_cast<const float*>(r.q),
+                                static_cast<const float*>(r.k), static_cast<const float*>(r.v),
+                                static_cast<const float*>(r.o), static_cast<const float*>(r.dout),
+                                r.lse, static_cast<float*>(r.workspace), static_cast<float*>(r.dq),
+                                static_cast<float*>(r.dk), static_cast<float*>(r.dv), (int)BH, g,
+                                r.scale, static_cast<cudaStream_t>(r.stream));
+        return e == cudaSuccess ? FA_OK : fail_cuda(e, "fp32 backward kernel launch");
+    }
     const bool f16 = r.dtype == FA_FP16;
     const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = f16;
     std::call_once(di.bwd_prepared[dix][dic][dif],

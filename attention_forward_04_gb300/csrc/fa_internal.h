@@ -103,4 +103,11 @@ cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, cons
                         float* o, float* lse, int bh, const SliceLayout& g, float scale,
                         cudaStream_t stream);
 
+// fp32 SIMT backward over the same layouts: dQ (which also writes delta, indexed like the
+// LSE) and then dK, dV, on `stream`.
+cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
+                            const float* o, const float* dout, const float* lse, float* delta,
+                            float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
+                            float scale, cudaStream_t stream);
+
 }  // namespace fa

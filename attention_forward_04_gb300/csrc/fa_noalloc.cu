@@ -45,7 +45,7 @@ extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
     if (!(scale >= 0.0f) || scale > 3.4e38f) return FA_ERR_INVALID_ARG;   // NaN, inf, < 0
-    if (dtype == FA_FP32 || (D != 32 && D != 64 && D != 128)) return FA_ERR_UNSUPPORTED;
+    if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     if (need > kScratchBytes) return FA_ERR_UNSUPPORTED;
 
     int dev = 0;

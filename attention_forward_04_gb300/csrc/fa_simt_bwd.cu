@@ -1,0 +1,234 @@
+// fa_simt_bwd.cu -- fp32 attention backward on the CUDA cores (fp32 storage and arithmetic).
+//
+// The gradients of the forward in fa_simt.cu, with P rebuilt from the forward's LSE
+// ("08 · FlashAttention" §三; "第 13 课：GPU 内核与 FlashAttention" §4B):
+//     P = exp(scale * Q K^T - LSE),  dP = dO V^T,  delta = rowsum(dO * O),
+//     dS = P * (dP - delta),  dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
+// Two kernels, as on the tensor cores, and no atomics:
+//   * dQ: one CTA per 32 query rows; it forms delta for its rows (written to the workspace
+//     for the next kernel), then walks the key tiles with K and V in shared memory;
+//   * dK, dV: one CTA per 32 key rows; it walks the query tiles with Q, dO, LSE and delta
+//     in shared memory.
+// CTA = 128 threads = 32 rows x 4 threads; thread t of a row owns head-dim columns t, t+4,
+// ...; a dot product over D is the four partial sums added with two shuffles.  Layouts as
+// the forward: [B, H, N, D], token-major [tokens, H, D], packed sequences.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fa_internal.h"
+
+namespace fa {
+namespace {
+
+constexpr int kRows = 32;     // rows per CTA and per shared-memory tile
+constexpr int kThreads = 128;
+
+// Length, element offset of row 0, row stride (elements) and LSE / delta index of row 0 of
+// slice bh; packed offsets are clamped to [0, total] and lengths to the declared maximum.
+struct SimtSlice {
+    int len;
+    size_t base, rs, vec0;
+};
+
+template <int D>
+__device__ __forceinline__ SimtSlice simt_slice(const SliceLayout& g, int bh) {
+    const int b = bh / g.heads, h = bh % g.heads;
+    int n = g.n, tok0 = b * g.n;
+    if (g.cu_seqlens != nullptr) {
+        int s0 = g.cu_seqlens[b], s1 = g.cu_seqlens[b + 1];
+        s0 = min(max(s0, 0), g.total);
+        s1 = min(max(s1, s0), g.total);
+        n = min(s1 - s0, g.n);
+        tok0 = s0;
+    }
+    SimtSlice s;
+    s.len = n;
+    s.rs = g.layout == 0 ? (size_t)D : (size_t)g.heads * D;
+    s.base = g.layout == 0 ? (size_t)bh * (size_t)g.n * D : ((size_t)tok0 * g.heads + h) * D;
+    s.vec0 = g.cu_seqlens != nullptr ? (size_t)h * g.total + tok0 : (size_t)bh * g.n;
+    return s;
+}
+
+__device__ __forceinline__ float quad_sum(float x) {
+    x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
+    x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+    return x;
+}
+
+// Cooperative float4 copy of rows r0.. of a slice tensor into a [kRows][D] tile (rows at or
+// past len read as zero).
+template <int D>
+__device__ __forceinline__ void load_rows(float (*dst)[D], const float* __restrict__ src,
+                                          const SimtSlice& s, int r0) {
+    for (int idx = threadIdx.x; idx < kRows * D / 4; idx += kThreads) {
+        const int r = idx / (D / 4);
+        const int c = (idx % (D / 4)) * 4;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r0 + r < s.len) x = *reinterpret_cast<const float4*>(src + s.base + (size_t)(r0 + r) * s.rs + c);
+        *reinterpret_cast<float4*>(&dst[r][c]) = x;
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const float* __restrict__ o, const float* __restrict__ dout, const float* __restrict__ lse,
+    float* __restrict__ delta, float* __restrict__ dq, const SliceLayout g, float scale) {
+    constexpr int DQ = D / 4;
+    __shared__ __align__(16) float Ks[kRows][D];
+    __shared__ __align__(16) float Vs[kRows][D];
+    const int nblk = (g.n + kRows - 1) / kRows;
+    const int bh = (int)(blockIdx.x / (unsigned)nblk), blk = (int)(blockIdx.x % (unsigned)nblk);
+    const SimtSlice s = simt_slice<D>(g, bh);
+    if (blk * kRows >= s.len) return;   // the whole block lies past the end of the sequence
+    const int r = threadIdx.x / 4, qd = threadIdx.x % 4;
+    const int i = blk * kRows + r;
+    const bool live = i < s.len;
+    const size_t row = s.base + (size_t)(live ? i : 0) * s.rs;
+
+    float qv[DQ], dov[DQ], acc[DQ];
+    float dl = 0.0f;
+#pragma unroll
+    for (int c = 0; c < DQ; ++c) {
+        qv[c] = live ? q[row + qd + 4 * c] : 0.0f;
+        dov[c] = live ? dout[row + qd + 4 * c] : 0.0f;
+        dl = fmaf(dov[c], live ? o[row + qd + 4 * c] : 0.0f, dl);
+        acc[c] = 0.0f;
+    }
+    dl = quad_sum(dl);   // delta_i = sum_d dO_id O_id
+    const float li = live ? lse[s.vec0 + i] : 0.0f;
+    if (live && qd == 0) delta[s.vec0 + i] = dl;
+    const int kend = CAUSAL ? min(s.len, (blk + 1) * kRows) : s.len;
+    const int limit = CAUSAL ? min(i + 1, s.len) : s.len;   // visible keys: j < limit
+
+    for (int k0 = 0; k0 < kend; k0 += kRows) {
+        __syncthreads();
+        load_rows<D>(Ks, k, s, k0);
+        load_rows<D>(Vs, v, s, k0);
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < kRows; ++c) {
+            float sp = 0.0f, dp = 0.0f;
+#pragma unroll
+            for (int e = 0; e < DQ; ++e) {
+                sp = fmaf(qv[e], Ks[c][qd + 4 * e], sp);
+                dp = fmaf(dov[e], Vs[c][qd + 4 * e], dp);
+            }
+            sp = quad_sum(sp);
+            dp = quad_sum(dp);
+            const float pij = (k0 + c < limit) ? expf(sp * scale - li) : 0.0f;
+            const float ds = pij * (dp - dl);
+#pragma unroll
+            for (int e = 0; e < DQ; ++e) acc[e] = fmaf(ds, Ks[c][qd + 4 * e], acc[e]);
+        }
+    }
+    if (live) {
+#pragma unroll
+        for (int c = 0; c < DQ; ++c) dq[row + qd + 4 * c] = acc[c] * scale;
+    }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const float* __restrict__ dout, const float* __restrict__ lse,
+    const float* __restrict__ delta, float* __restrict__ dk, float* __restrict__ dv,
+    const SliceLayout g, float scale) {
+    constexpr int DQ = D / 4;
+    __shared__ __align__(16) float Qs[kRows][D];
+    __shared__ __align__(16) float DOs[kRows][D];
+    __shared__ float Ls[kRows], Dl[kRows];
+    const int nblk = (g.n + kRows - 1) / kRows;
+    const int bh = (int)(blockIdx.x / (unsigned)nblk), blk = (int)(blockIdx.x % (unsigned)nblk);
+    const SimtSlice s = simt_slice<D>(g, bh);
+    if (blk * kRows >= s.len) return;
+    const int r = threadIdx.x / 4, qd = threadIdx.x % 4;
+    const int j = blk * kRows + r;   // key row
+    const bool live = j < s.len;
+    const size_t row = s.base + (size_t)(live ? j : 0) * s.rs;
+
+    float kv[DQ], vv[DQ], ak[DQ], av[DQ];
+#pragma unroll
+    for (int c = 0; c < DQ; ++c) {
+        kv[c] = live ? k[row + qd + 4 * c] : 0.0f;
+        vv[c] = live ? v[row + qd + 4 * c] : 0.0f;
+        ak[c] = 0.0f;
+        av[c] = 0.0f;
+    }
+    // queries before this block never see its keys under the causal mask
+    for (int q0 = CAUSAL ? blk * kRows : 0; q0 < s.len; q0 += kRows) {
+        __syncthreads();
+        load_rows<D>(Qs, q, s, q0);
+        load_rows<D>(DOs, dout, s, q0);
+        if (threadIdx.x < kRows) {
+            const int qi = q0 + threadIdx.x;
+            Ls[threadIdx.x] = qi < s.len ? lse[s.vec0 + qi] : 0.0f;
+            Dl[threadIdx.x] = qi < s.len ? delta[s.vec0 + qi] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int c = 0; c < kRows; ++c) {
+            float sp = 0.0f, dp = 0.0f;
+#pragma unroll
+            for (int e = 0; e < DQ; ++e) {
+                sp = fmaf(kv[e], Qs[c][qd + 4 * e], sp);
+                dp = fmaf(vv[e], DOs[c][qd + 4 * e], dp);
+            }
+            sp = quad_sum(sp);
+            dp = quad_sum(dp);
+            const int qi = q0 + c;
+            const bool vis = qi < s.len && (!CAUSAL || qi >= j);
+            const float pij = vis ? expf(sp * scale - Ls[c]) : 0.0f;
+            const float ds = pij * (dp - Dl[c]);
+#pragma unroll
+            for (int e = 0; e < DQ; ++e) {
+                av[e] = fmaf(pij, DOs[c][qd + 4 * e], av[e]);
+                ak[e] = fmaf(ds, Qs[c][qd + 4 * e], ak[e]);
+            }
+        }
+    }
+    if (live) {
+#pragma unroll
+        for (int c = 0; c < DQ; ++c) {
+            dk[row + qd + 4 * c] = ak[c] * scale;
+            dv[row + qd + 4 * c] = av[c];
+        }
+    }
+}
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const float* q, const float* k, const float* v, const float* o,
+                   const float* dout, const float* lse, float* delta, float* dq, float* dk,
+                   float* dv, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
+    const long long blocks = (long long)((g.n + kRows - 1) / kRows) * bh;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
+    simt_bwd_dq_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, dout, lse,
+                                                                           delta, dq, g, scale);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    simt_bwd_dkdv_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, dout, lse,
+                                                                             delta, dk, dv, g, scale);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(bool causal, const float* q, const float* k, const float* v, const float* o,
+                     const float* dout, const float* lse, float* delta, float* dq, float* dk,
+                     float* dv, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
+    return causal ? launch<D, true>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
+                  : launch<D, false>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+}
+
+}  // namespace
+
+cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
+                            const float* o, const float* dout, const float* lse, float* delta,
+                            float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
+                            float scale, cudaStream_t stream) {
+    if (D == 32) return launch_d<32>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    if (D == 64) return launch_d<64>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    return launch_d<128>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+}
+
+}  // namespace fa

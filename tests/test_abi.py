@@ -148,7 +148,7 @@ def test_bwd_workspace_size(lib):
     (dict(q=0), INVALID), (dict(do=0), INVALID), (dict(lse=0), INVALID), (dict(dv=0), INVALID),
     (dict(ws=0), INVALID), (dict(ws_bytes=100), INVALID), (dict(N=0), INVALID),
     (dict(causal=3), INVALID), (dict(scale=float("nan")), INVALID), (dict(dtype=9), INVALID),
-    (dict(dtype=0), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
     (dict(D=16), UNSUPPORTED),
     (dict(dq=BASE), INVALID),                      # dq aliases q
     (dict(dk=BASE + 6 * SZ + 128), INVALID),       # dk overlaps dq
@@ -203,7 +203,6 @@ def test_bwd_layout_variants_argument_checks(lib):
                                  0, dtype, None)
     assert bnhd(q=0) == INVALID
     assert bnhd(D=96) == UNSUPPORTED
-    assert bnhd(dtype=0) == UNSUPPORTED
     assert bnhd(B=1 << 20, N=1 << 12) == INVALID           # more than 2^31 tokens
     assert bnhd(ws_bytes=100) == INVALID
     assert bnhd(dq=BASE) == INVALID                        # dq aliases q

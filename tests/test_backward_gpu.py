@@ -1,9 +1,11 @@
 """GPU parity of the backward (fa_bwd through the C ABI) against the fp64 backward oracle.
 
 Tolerance, derived from the kernel's arithmetic and applied element by element.  With u the
-unit roundoff of the 16-bit storage type (2^-8 bf16, 2^-11 fp16: 8 and 11 significant bits), P and dS the oracle's
-probabilities and softmax derivative, and e_p = |LSE_gpu - LSE_oracle| + 1e-4 the relative
-error of the kernel's rebuilt P (its forward LSE error, plus fp32 accumulation of S and ex2):
+unit roundoff of the storage type (2^-8 bf16, 2^-11 fp16, 2^-24 fp32: 8, 11 and 24
+significant bits), P and dS the oracle's probabilities and softmax derivative, and
+e_p = |LSE_gpu - LSE_oracle| + f the relative error of the kernel's rebuilt P (its forward
+LSE error, plus f = 1e-4 for fp32 accumulation of S and ex2 on the tensor cores, or
+f = 2e-5 for the fp32 kernels' S over D terms and expf):
   * dV = P^T dO with P rounded to 16 bits before the product:
         |err| <= (P (u + e_p))^T |dO| + u |dV|                  (the last term: output rounding)
   * delta is formed from the forward's stored O, so it is off by
@@ -14,8 +16,9 @@ error of the kernel's rebuilt P (its forward LSE error, plus fp32 accumulation o
   * dQ = scale dS K, dK = scale dS^T Q:
         |err_dQ| <= scale (|dS_gpu - dS| bound) |K| + u |dQ|,
         |err_dK| <= scale (|dS_gpu - dS| bound)^T |Q| + u |dK|.
+For fp32 storage nothing is rounded to 16 bits and the same bound holds with u = 2^-24.
 The test allows twice each bound plus 1e-5 absolute.  The oracle reads the same stored
-(16-bit) Q, K, V, dO, converted exactly to fp64; O and LSE come from the GPU forward, as in
+Q, K, V, dO, converted exactly to fp64; O and LSE come from the GPU forward, as in
 training.
 """
 import math
@@ -31,7 +34,10 @@ from oracle.backward import attention_bwd
 
 pytestmark = pytest.mark.gpu
 
-U = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}
+U = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11, "fp32": 2.0 ** -24}
+# floor on the relative error of the rebuilt P beyond the LSE difference: fp32 accumulation of
+# S and exp2 on the tensor cores (16-bit storage); fp32 S over D terms and expf (fp32 storage)
+P_FLOOR = {"bf16": 1e-4, "fp16": 1e-4, "fp32": 2e-5}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -56,7 +62,7 @@ def gpu_fwd_bwd(q, k, v, do, scale, causal):
     return o, lse, dq, dk, dv
 
 
-def bounds(q, k, v, do, scale, causal, o_gpu, lse_gpu, ref, u):
+def bounds(q, k, v, do, scale, causal, o_gpu, lse_gpu, ref, u, p_floor=1e-4):
     """Element-wise error bounds (see the module docstring) for one [N, D] slice."""
     dq_r, dk_r, dv_r, o_r, lse_r, delta_r = ref
     N, D = q.shape
@@ -66,7 +72,7 @@ def bounds(q, k, v, do, scale, causal, o_gpu, lse_gpu, ref, u):
         P = np.where(np.tril(np.ones((N, N), dtype=bool)), P, 0.0)
     dS = P * (do @ v.T - delta_r[:, None])
     gam = D * 2.0 ** -24
-    e_p = np.abs(lse_gpu - lse_r) + 1e-4
+    e_p = np.abs(lse_gpu - lse_r) + p_floor
     e_delta = (np.abs(do) * np.abs(o_gpu - o_r)).sum(1) + gam * (np.abs(do) * np.abs(o_r)).sum(1)
     e_dp = gam * (np.abs(do) @ np.abs(v).T)
     e_ds = P * (e_delta[:, None] + e_dp) + (u + e_p[:, None]) * np.abs(dS)
@@ -85,7 +91,7 @@ def compare_slices(q, k, v, do, scale, causal, dtype, slices, what=""):
         ref = attention_bwd(*args, scale, causal)
         ref = [r[0, 0] for r in ref]
         tol = bounds(*(a[0, 0] for a in args), scale, causal, o_g[b, h], lse_g[b, h], ref,
-                     U[dtype])
+                     U[dtype], P_FLOOR[dtype])
         for name, g, r, t in zip(("dQ", "dK", "dV"), got, ref[:3], tol):
             x = g[b, h]
             assert np.all(np.isfinite(x)), (what, name)
@@ -107,6 +113,16 @@ def test_bf16_backward_edge_shapes(N, D, causal):
     do = make_shape_dout(1, 2, N, D, "bf16", seed=N * 13 + D)
     compare_slices(q, k, v, do, 1.0 / math.sqrt(D), causal, "bf16", [(0, 0), (0, 1)],
                    "N=%d D=%d causal=%d" % (N, D, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("N", [1, 17, 129, 300])
+def test_fp32_backward(N, D, causal):
+    q, k, v = make_shape(2, 1, N, D, "fp32", seed=N * 19 + D)
+    do = make_shape_dout(2, 1, N, D, "fp32", seed=N * 19 + D)
+    compare_slices(q, k, v, do, 1.0 / math.sqrt(D), causal, "fp32", [(0, 0), (1, 0)],
+                   "fp32 N=%d D=%d causal=%d" % (N, D, causal))
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -158,11 +174,9 @@ def test_backward_overwrites_outputs_and_is_deterministic():
         assert torch.equal(a, b)
 
 
-def test_backward_rejects_fp32_and_small_workspace():
+def test_backward_rejects_small_workspace():
     q, k, v = (t.cuda() for t in make_shape(1, 1, 128, 64, "bf16", seed=3))
     o, lse = binding.fwd(q, k, v)
-    with pytest.raises(binding.FaError):
-        binding.bwd(q.float(), k.float(), v.float(), o.float(), lse, o.float())
     ws = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(binding.FaError):
         binding.bwd(q, k, v, o, lse, o.clone(), workspace=ws)

@@ -30,10 +30,10 @@ def f64(t):
 
 def check_slice(q, k, v, do, o, lse, grads, scale, causal, dtype, what):
     """q, k, v, do, o: [N, D] fp64 of one slice; lse [N]; grads: (dq, dk, dv) [N, D]."""
-    from test_backward_gpu import U, bounds
+    from test_backward_gpu import P_FLOOR, U, bounds
     ref = [r[0, 0] for r in attention_bwd(q[None, None], k[None, None], v[None, None],
                                            do[None, None], scale, causal)]
-    tol = bounds(q, k, v, do, scale, causal, o, lse, ref, U[dtype])
+    tol = bounds(q, k, v, do, scale, causal, o, lse, ref, U[dtype], P_FLOOR[dtype])
     for name, g, r, t in zip(("dQ", "dK", "dV"), grads, ref[:3], tol):
         assert np.all(np.isfinite(g)), (what, name)
         err = np.abs(g - r)
@@ -61,18 +61,20 @@ def test_bnhd_backward(D, causal):
                         "bnhd D=%d causal=%d (b=%d, h=%d)" % (D, causal, b, h))
 
 
-def test_bnhd_backward_fp16():
+@pytest.mark.parametrize("dtype", ["fp16", "fp32"])
+def test_bnhd_backward_other_dtypes(dtype):
     B, N, H, D = 1, 200, 2, 64
     to_bnhd = lambda t: t.permute(0, 2, 1, 3).contiguous().cuda()  # noqa: E731
-    q, k, v = (to_bnhd(t) for t in make_shape(B, H, N, D, "fp16", seed=9))
-    do = to_bnhd(make_shape_dout(B, H, N, D, "fp16", seed=9))
+    q, k, v = (to_bnhd(t) for t in make_shape(B, H, N, D, dtype, seed=9))
+    do = to_bnhd(make_shape_dout(B, H, N, D, dtype, seed=9))
     o, lse = binding.fwd_bnhd(q, k, v, causal=True)
     grads = binding.bwd_bnhd(q, k, v, o, lse, do, causal=True)
     torch.cuda.synchronize()
+    assert binding.check_device_status()[0] == 0
     for h in range(H):
         sl = lambda t: f64(t[0, :, h])  # noqa: E731
         check_slice(sl(q), sl(k), sl(v), sl(do), sl(o), f64(lse[0, h]), [sl(g) for g in grads],
-                    1.0 / math.sqrt(D), True, "fp16", "bnhd fp16 h=%d" % h)
+                    1.0 / math.sqrt(D), True, dtype, "bnhd %s h=%d" % (dtype, h))
 
 
 LENGTHS = [[1, 17, 300, 129, 0, 256], [640], [257, 3, 500]]
@@ -82,11 +84,20 @@ LENGTHS = [[1, 17, 300, 129, 0, 256], [640], [257, 3, 500]]
 @pytest.mark.parametrize("D", [32, 128])
 @pytest.mark.parametrize("mix", range(len(LENGTHS)))
 def test_varlen_backward(mix, D, causal):
-    lengths, H = LENGTHS[mix], 2
+    run_varlen_backward(LENGTHS[mix], D, causal, "bf16", 100 + mix * 7 + D)
+
+
+def test_varlen_backward_fp32():
+    run_varlen_backward([0, 40, 129, 7], 64, True, "fp32", 5)
+
+
+def run_varlen_backward(lengths, D, causal, dtype, seed):
+    H = 2
     cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
     T = int(cu[-1])
-    g = torch.Generator().manual_seed(100 + mix * 7 + D)
-    q, k, v, do = (torch.randn((T, H, D), generator=g).to(torch.bfloat16).cuda() for _ in range(4))
+    g = torch.Generator().manual_seed(seed)
+    tdt = {"bf16": torch.bfloat16, "fp32": torch.float32}[dtype]
+    q, k, v, do = (torch.randn((T, H, D), generator=g).to(tdt).cuda() for _ in range(4))
     cu_t = torch.from_numpy(cu).cuda()
     scale = 1.0 / math.sqrt(D)
     o, lse = binding.fwd_varlen(q, k, v, cu_t, max(lengths), scale=scale, causal=causal)
@@ -100,5 +111,5 @@ def test_varlen_backward(mix, D, causal):
         for h in range(H):
             sl = lambda t: f64(t[s0:s1, h])  # noqa: E731
             check_slice(sl(q), sl(k), sl(v), sl(do), sl(o), f64(lse[h, s0:s1]),
-                        [sl(x) for x in grads], scale, causal, "bf16",
+                        [sl(x) for x in grads], scale, causal, dtype,
                         "varlen seq %d (len %d) h=%d D=%d causal=%d" % (b, L, h, D, causal))

@@ -33,7 +33,7 @@ def test_noalloc_refuses_before_cuda(lib):
     assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 128, 128, 0.1, 2, 1, None) == 1
     assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 128, 128, float("nan"), 0, 1, None) == 1
     assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 128, 96, 0.1, 0, 1, None) == 2
-    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 128, 128, 0.1, 0, 0, None) == 2
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 128, 128, 0.1, 0, 7, None) == 1   # unknown dtype
 
 
 def _problem(B, H, N, D, dtype, seed, causal):
