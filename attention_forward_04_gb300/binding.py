@@ -52,6 +52,16 @@ SIGNATURES = {
                                   _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
                                   _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
                                   _c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_bwd_noalloc_bnhd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                       _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                       _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64,
+                                       _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
+                                       _c.c_void_p]),
+    "fa_bwd_noalloc_varlen": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                         _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                                         _c.c_void_p, _c.c_void_p, _c.c_int64, _c.c_int64,
+                                         _c.c_int64, _c.c_int64, _c.c_int64, _c.c_float,
+                                         _c.c_int, _c.c_int, _c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_last_cuda_error": (_c.c_char_p, []),
     "fa_check_device_status": (_c.c_int, [_c.c_void_p, _c.POINTER(_c.c_uint32)]),
@@ -377,6 +387,47 @@ def bwd_noalloc(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, str
             q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
             lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, D,
             float(scale), int(causal), _dtype_code(q), _stream_handle(q, stream))))
+    return dq, dk, dv
+
+
+def bwd_noalloc_bnhd(q, k, v, o, lse, dout, dq, dk, dv, scale=None, causal=False, stream=None):
+    """fa_bwd_noalloc_bnhd: bwd_bnhd with library-owned scratch; the caller provides dq,
+    dk, dv ([B, N, H, D], the dtype of q)."""
+    import torch
+    _common(q, k, v, 4)
+    B, N, H, D = q.shape
+    for name, t in (("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_buffer(t, name, q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", (B, H, N), torch.float32, q.device)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_bwd_noalloc_bnhd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, N, H, D,
+            float(scale), int(causal), _dtype_code(q), _stream_handle(q, stream))))
+    return dq, dk, dv
+
+
+def bwd_noalloc_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens, max_seqlen, scale=None,
+                       causal=False, stream=None):
+    """fa_bwd_noalloc_varlen: bwd_varlen with library-owned scratch; the caller provides
+    dq, dk, dv ([total, H, D], the dtype of q)."""
+    import torch
+    _common(q, k, v, 3)
+    if not (cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int32 and cu_seqlens.dim() == 1
+            and cu_seqlens.is_contiguous() and cu_seqlens.device == q.device):
+        raise ValueError("cu_seqlens must be a contiguous 1-D int32 tensor on %s" % q.device)
+    T, H, D = q.shape
+    for name, t in (("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_buffer(t, name, q.shape, q.dtype, q.device)
+    _check_buffer(lse, "lse", (H, T), torch.float32, q.device)
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    with torch.cuda.device(q.device):
+        _check(int(load_library().fa_bwd_noalloc_varlen(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(),
+            lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), cu_seqlens.data_ptr(),
+            cu_seqlens.numel() - 1, int(max_seqlen), T, H, D, float(scale), int(causal),
+            _dtype_code(q), _stream_handle(q, stream))))
     return dq, dk, dv
 
 

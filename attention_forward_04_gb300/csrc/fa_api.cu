@@ -181,8 +181,8 @@ int forward(const Request& r) {
         if (!std::isfinite(r.descale[i]) || !(r.descale[i] > 0.0f)) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale * r.descale[0] * r.descale[1])) return FA_ERR_INVALID_ARG;
     if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
-    // D = 256: 16-bit storage, [B, H, N, D] layout only
-    if (r.D == 256 && (r.dtype == FA_FP32 || r.dtype == kFp8)) return FA_ERR_UNSUPPORTED;
+    // D = 256: 16-bit storage on the tensor cores, fp32 on the CUDA cores; no e4m3
+    if (r.D == 256 && r.dtype == kFp8) return FA_ERR_UNSUPPORTED;
     // fp8: D = 64 or 128, [B, H, N, D] layout only
     if (r.dtype == kFp8 && ((r.D != 64 && r.D != 128) || r.layout != 0)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;

@@ -31,31 +31,87 @@ struct ScratchSlot {
 };
 ScratchSlot g_scratch[kMaxDevices];
 
-}  // namespace
-
-extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
-                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                              int64_t B, int64_t H, int64_t N, int64_t D, float scale,
-                              int causal, int dtype, void* stream) {
-    // Host checks before any CUDA call; fa_bwd repeats them and adds the overlap and
-    // alignment checks.
-    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
-    const int64_t need = fa_bwd_workspace_bytes(B, H, N);
+// Checks shared by the three entry points, before any CUDA call: pointers, flags, D, and
+// the scratch the call needs (`need`, from fa_bwd_workspace_bytes for its layout).
+int check_common(const void* const* ptrs, int64_t need, int64_t D, float scale, int causal,
+                 int dtype) {
+    for (int a = 0; a < 9; ++a)
+        if (!ptrs[a]) return FA_ERR_INVALID_ARG;
     if (need < 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
     if (!(scale >= 0.0f) || scale > 3.4e38f) return FA_ERR_INVALID_ARG;   // NaN, inf, < 0
     if (D != 32 && D != 64 && D != 128) return FA_ERR_UNSUPPORTED;
     if (need > kScratchBytes) return FA_ERR_UNSUPPORTED;
+    return FA_OK;
+}
 
+// This device's copy of the array (looked up once per device), or null with `status` set.
+void* scratch(int* status) {
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
-    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
-    // Once per device: the address of this device's copy of the array.
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *status = FA_ERR_UNSUPPORTED;
+        return nullptr;
+    }
     ScratchSlot& s = g_scratch[dev];
     std::call_once(s.once, [&] { s.err = cudaGetSymbolAddress(&s.ptr, g_bwd_scratch); });
-    if (s.err != cudaSuccess || !s.ptr) return FA_ERR_CUDA;
-    return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, s.ptr, need, B, H, N, D, scale, causal,
+    if (s.err != cudaSuccess || !s.ptr) {
+        *status = FA_ERR_CUDA;
+        return nullptr;
+    }
+    return s.ptr;
+}
+
+}  // namespace
+
+// fa_bwd, fa_bwd_bnhd and fa_bwd_varlen repeat the host checks and add the overlap and
+// alignment checks.
+extern "C" int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                              const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                              int64_t B, int64_t H, int64_t N, int64_t D, float scale,
+                              int causal, int dtype, void* stream) {
+    const void* ptrs[9] = {q, k, v, o, dout, lse, dq, dk, dv};
+    const int64_t need = fa_bwd_workspace_bytes(B, H, N);
+    int st = check_common(ptrs, need, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    void* ws = scratch(&st);
+    if (!ws) return st;
+    return fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, need, B, H, N, D, scale, causal,
                   dtype, stream);
+}
+
+extern "C" int fa_bwd_noalloc_bnhd(const void* q, const void* k, const void* v, const void* o,
+                                   const void* dout, const float* lse, void* dq, void* dk,
+                                   void* dv, int64_t B, int64_t N, int64_t H, int64_t D,
+                                   float scale, int causal, int dtype, void* stream) {
+    const void* ptrs[9] = {q, k, v, o, dout, lse, dq, dk, dv};
+    const int64_t need = fa_bwd_workspace_bytes(B, H, N);
+    int st = check_common(ptrs, need, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    void* ws = scratch(&st);
+    if (!ws) return st;
+    return fa_bwd_bnhd(q, k, v, o, dout, lse, dq, dk, dv, ws, need, B, N, H, D, scale, causal,
+                       dtype, stream);
+}
+
+extern "C" int fa_bwd_noalloc_varlen(const void* q, const void* k, const void* v, const void* o,
+                                     const void* dout, const float* lse, void* dq, void* dk,
+                                     void* dv, const int32_t* cu_seqlens, int64_t batch,
+                                     int64_t max_seqlen, int64_t total, int64_t H, int64_t D,
+                                     float scale, int causal, int dtype, void* stream) {
+    const void* ptrs[9] = {q, k, v, o, dout, lse, dq, dk, dv};
+    if (!cu_seqlens) return FA_ERR_INVALID_ARG;
+    // delta is indexed like the packed LSE, [H, total]
+    const int64_t need = fa_bwd_workspace_bytes(1, H, total);
+    if (fa_bwd_workspace_bytes(batch, H, max_seqlen) < 0) return FA_ERR_INVALID_ARG;
+    int st = check_common(ptrs, need, D, scale, causal, dtype);
+    if (st != FA_OK) return st;
+    void* ws = scratch(&st);
+    if (!ws) return st;
+    return fa_bwd_varlen(q, k, v, o, dout, lse, dq, dk, dv, ws, need, cu_seqlens, batch,
+                         max_seqlen, total, H, D, scale, causal, dtype, stream);
 }

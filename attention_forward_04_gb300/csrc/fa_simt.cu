@@ -12,7 +12,8 @@
 //
 // CTA = 128 threads = 32 rows x 4 threads.  Thread q of a row owns head-dim columns
 // q, q+4, q+8, ... (interleaved, so the 4 threads of a row hit 4 different banks when
-// reading a shared K/V row).  Per key tile of 32 keys: partial dot products are summed
+// reading a shared K/V row).  Per key tile (32 keys; 16 at D = 256, which keeps the K and V
+// tiles at 32 KB of static shared memory): partial dot products are summed
 // across the 4 threads with two shuffles, then the running max / sum update, exp with
 // the new max, and the O update.  O is divided by l once at the end.
 #include <cuda_runtime.h>
@@ -25,7 +26,6 @@ namespace fa {
 namespace {
 
 constexpr int kRows = 32;     // query rows per CTA
-constexpr int kKeys = 32;     // keys per shared-memory tile
 constexpr int kThreads = 128;
 
 template <int D, bool CAUSAL>
@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
                                                            float* __restrict__ lse,
                                                            const SliceLayout g, float scale) {
     constexpr int DQ = D / 4;  // columns per thread
+    constexpr int kKeys = D == 256 ? 16 : 32;   // keys per shared-memory tile
     __shared__ __align__(16) float Ks[kKeys][D];
     __shared__ __align__(16) float Vs[kKeys][D];
 
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
 
     for (int k0 = 0; k0 < kend; k0 += kKeys) {
         __syncthreads();
-        // Cooperative float4 loads of K and V rows k0..k0+31 (rows >= n read as zero).
+        // Cooperative float4 loads of K and V rows k0..k0+kKeys-1 (rows >= n read as zero).
         for (int idx = tid; idx < kKeys * D / 4; idx += kThreads) {
             const int kr = idx / (D / 4);
             const int kc = (idx % (D / 4)) * 4;
@@ -105,8 +106,9 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
             s[c] = vis ? part * scale : -INFINITY;
             tmax = fmaxf(tmax, s[c]);
         }
-        // Every processed tile holds at least one visible key for a live row; rows
-        // past the end keep finite values and are never stored.
+        // Key 0 lies in the first tile and is visible to every row, so m is finite after
+        // it; a later tile with no visible key for a row leaves that row as it was
+        // (alpha = 1, p = 0).  Rows past the end keep finite values and are never stored.
         const float m_new = fmaxf(m, tmax);
         const float base = (m_new == -INFINITY) ? 0.0f : m_new;
         const float alpha = expf(m - base);   // m = -inf on the first tile -> 0
@@ -155,6 +157,9 @@ cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, cons
     if (D == 64)
         return causal ? launch<64, true>(q, k, v, o, lse, bh, g, scale, stream)
                       : launch<64, false>(q, k, v, o, lse, bh, g, scale, stream);
+    if (D == 256)
+        return causal ? launch<256, true>(q, k, v, o, lse, bh, g, scale, stream)
+                      : launch<256, false>(q, k, v, o, lse, bh, g, scale, stream);
     return causal ? launch<128, true>(q, k, v, o, lse, bh, g, scale, stream)
                   : launch<128, false>(q, k, v, o, lse, bh, g, scale, stream);
 }

@@ -48,7 +48,7 @@ typedef enum {
  *   lse     : device pointer, [B, H, N] contiguous fp32; written fully.
  *   B, H, N : >= 1.  B*H < 2^31 and N < 2^31.  Any N is accepted (a ragged last tile is
  *             masked; keys >= N never contribute).
- *   D       : head dimension: 32, 64 or 128; 256 for bf16/fp16 storage.
+ *   D       : head dimension: 32, 64, 128 or 256.
  *   scale   : finite, >= 0 (normally 1/sqrt(D)).
  *   causal  : 0 = all keys; 1 = key j <= query i (square N x N).
  *   dtype   : an fa_dtype value.
@@ -215,6 +215,30 @@ int fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
                    const void* dout, const float* lse, void* dq, void* dk, void* dv,
                    int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal,
                    int dtype, void* stream);
+
+/*
+ * fa_bwd_noalloc_bnhd -- fa_bwd_bnhd with the scratch of fa_bwd_noalloc: token-major
+ * [B, N, H, D] tensors, lse [B, H, N].  Limit: fa_bwd_workspace_bytes(B, H, N) <=
+ * FA_BWD_NOALLOC_MAX_SCRATCH_BYTES.  Set-up and concurrency as fa_bwd_noalloc (the three
+ * no-alloc entry points share one array per device).
+ */
+int fa_bwd_noalloc_bnhd(const void* q, const void* k, const void* v, const void* o,
+                        const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                        int64_t B, int64_t N, int64_t H, int64_t D, float scale, int causal,
+                        int dtype, void* stream);
+
+/*
+ * fa_bwd_noalloc_varlen -- fa_bwd_varlen with the scratch of fa_bwd_noalloc: packed
+ * [total, H, D] tensors, lse [H, total], the same cu_seqlens.  Limit:
+ * fa_bwd_workspace_bytes(1, H, total) <= FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (H*total <=
+ * 1,048,576).  cu_seqlens == NULL is FA_ERR_INVALID_ARG.  Set-up and concurrency as
+ * fa_bwd_noalloc.
+ */
+int fa_bwd_noalloc_varlen(const void* q, const void* k, const void* v, const void* o,
+                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                          const int32_t* cu_seqlens, int64_t batch, int64_t max_seqlen,
+                          int64_t total, int64_t H, int64_t D, float scale, int causal,
+                          int dtype, void* stream);
 
 /* Human-readable name of a status code (static string; never NULL). */
 const char* fa_status_string(int status);

@@ -64,7 +64,6 @@ def call(lib, q=BASE, k=BASE + SZ, v=BASE + 2 * SZ, o=BASE + 3 * SZ, lse=BASE + 
     (dict(scale=float("inf")), INVALID), (dict(scale=-0.5), INVALID),
     (dict(dtype=7), INVALID), (dict(dtype=-1), INVALID),
     (dict(D=96), UNSUPPORTED), (dict(D=48), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
-    (dict(D=256, dtype=0), UNSUPPORTED),          # D = 256: 16-bit storage only
     (dict(q=BASE + 8), MISALIGNED), (dict(o=BASE + 3 * SZ + 4), MISALIGNED),
     (dict(lse=BASE + 4 * SZ + 2), MISALIGNED),
     (dict(o=BASE), INVALID),                       # o aliases q
@@ -101,10 +100,6 @@ def test_varlen_and_bnhd_argument_checks(lib):
                            2, 128, 4, 96, 0.1, 0, 1, None) == UNSUPPORTED
     assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
                            2, 0, 4, 128, 0.1, 0, 1, None) == INVALID
-    # D = 256: 16-bit storage only, in every layout
-    assert lib.fa_fwd_bnhd(BASE, BASE + SZ, BASE + 2 * SZ, BASE + 3 * SZ, BASE + 4 * SZ,
-                           2, 128, 4, 256, 0.1, 0, 0, None) == UNSUPPORTED
-    assert varlen(D=256, dtype=0) == UNSUPPORTED
 
 
 def test_watchdog_control_validation(lib):

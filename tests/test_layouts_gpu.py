@@ -103,7 +103,7 @@ def test_varlen_malformed_offsets_stay_in_bounds():
 
 
 # ------------------------------------------------------------ head dimension 256
-@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
 @pytest.mark.parametrize("causal", [False, True])
 def test_bnhd_head_dim_256(causal, dtype):
     B, N, H, D = 2, 333, 3, 256
@@ -125,3 +125,8 @@ def test_varlen_head_dim_256(mix, causal):
 
 def test_varlen_head_dim_256_fp16_and_empty():
     run_varlen([0, 65, 0, 190], 2, 256, "fp16", True, seed=257)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_head_dim_256_fp32(causal):
+    run_varlen([1, 17, 300, 0, 129], 2, 256, "fp32", causal, seed=258)

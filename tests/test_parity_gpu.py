@@ -74,7 +74,7 @@ def test_bf16_edge_shapes(N, D, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 33, 200, 256, 300])
 def test_fp32_edge_shapes(N, D, causal):
     q, k, v = make_shape(2, 1, N, D, "fp32", seed=N * 11 + D)
