@@ -33,8 +33,8 @@ struct DeviceInfo {
     cudaError_t prepare_err[3][2][3] = {};
     std::once_flag bwd_prepared[3][2][2];   // [D = 32, 64, 128][causal][f16]
     cudaError_t bwd_prepare_err[3][2][2] = {};
-    std::once_flag prepared256[2][2];  // [causal][f16]
-    cudaError_t prepare256_err[2][2] = {};
+    std::once_flag prepared256[2][3];  // [causal][element type]
+    cudaError_t prepare256_err[2][3] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -181,10 +181,8 @@ int forward(const Request& r) {
         if (!std::isfinite(r.descale[i]) || !(r.descale[i] > 0.0f)) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale * r.descale[0] * r.descale[1])) return FA_ERR_INVALID_ARG;
     if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
-    // D = 256: 16-bit storage on the tensor cores, fp32 on the CUDA cores; no e4m3
-    if (r.D == 256 && r.dtype == kFp8) return FA_ERR_UNSUPPORTED;
-    // fp8: D = 64 or 128, [B, H, N, D] layout only
-    if (r.dtype == kFp8 && ((r.D != 64 && r.D != 128) || r.layout != 0)) return FA_ERR_UNSUPPORTED;
+    // fp8: D = 64, 128 or 256, [B, H, N, D] layout only
+    if (r.dtype == kFp8 && (r.D == 32 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;
     const size_t esize = r.dtype == FA_FP32 ? 4 : r.dtype == kFp8 ? 1 : 2;   // Q, K, V
     const size_t osize = r.dtype == FA_FP32 ? 4 : 2;                          // O
@@ -246,7 +244,7 @@ int forward(const Request& r) {
     const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = et;
     if (r.D == 256) {
         std::call_once(di.prepared256[dic][dif],
-                       [&] { di.prepare256_err[dic][dif] = fa::tc256_prepare(dic, f16); });
+                       [&] { di.prepare256_err[dic][dif] = fa::tc256_prepare(dic, et); });
         if (di.prepare256_err[dic][dif] != cudaSuccess)
             return fail_cuda(di.prepare256_err[dic][dif], "cudaFuncSetAttribute (D = 256)");
         PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
@@ -265,13 +263,13 @@ int forward(const Request& r) {
         p.total = (int)r.T;
         p.n = (int)r.N;
         p.bh = (int)BH;
-        p.scale_log2 = r.scale * 1.4426950408889634f;
-        p.o_scale = 1.0f;
+        p.scale_log2 = r.scale * r.descale[0] * r.descale[1] * 1.4426950408889634f;
+        p.o_scale = r.descale[2];
         p.wait_limit = g_wait_limit.load();
         p.units = fa::tc256_units((int)BH, (int)r.N, dic != 0);
         if (p.units < 1) return FA_ERR_UNSUPPORTED;
         const int grid = p.units < di.sm_count ? p.units : di.sm_count;
-        e = fa::tc256_launch(dic, f16, p, grid, st);
+        e = fa::tc256_launch(dic, et, p, grid, st);
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch (D = 256)");
     }
     std::call_once(di.prepared[dix][dic][dif],

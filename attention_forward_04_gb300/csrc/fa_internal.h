@@ -81,12 +81,12 @@ cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, int grid,
 // Copy the device status word (4 words) of the tensor-core kernels to `out` and clear it.
 cudaError_t tc_status_read_reset(uint32_t out[4]);
 
-// Head dimension 256 ([B*H, N, 256] maps with 64 x 64 boxes): persistent CTAs over the
+// Head dimension 256 (maps with boxes of 64 rows x 128 bytes): persistent CTAs over the
 // units tc256_units gives (query tiles; causal: heavy + light tile pairs).  Uses
-// tmap_q/k/v, o, lse, n, bh, units, scale_log2, wait_limit.
+// tmap_q/k/v, o, lse, n, bh, units, scale_log2, o_scale, wait_limit and the layout fields.
 int tc256_units(int bh, int n, bool causal);
-cudaError_t tc256_prepare(bool causal, bool f16);
-cudaError_t tc256_launch(bool causal, bool f16, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t tc256_prepare(bool causal, int et);   // et: 0 bf16, 1 fp16, 2 e4m3 ([B, H, N, D] only)
+cudaError_t tc256_launch(bool causal, int et, const TcParams& p, int grid, cudaStream_t stream);
 cudaError_t tc256_status_read_reset(uint32_t out[4]);
 
 // Geometry shared by both paths: where row r of slice (b, h) lives.

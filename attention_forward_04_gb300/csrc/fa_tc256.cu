@@ -5,10 +5,14 @@
 // D = 256: the two-query-tile schedule of the smaller head dimensions would need 2 x 256
 // TMEM columns of O alone.  Here a persistent CTA (one per SM) takes one 128-row query tile
 // at a time and owns all 512 columns:
-//     Q [0, 128)       the query tile as 16-bit pairs (A operand of S = Q K^T)
-//     S/P buffer 0     [128, 192)   64 keys: fp32 scores, then P (16-bit) over them
+//     Q [0, 128)       the query tile as 16-bit pairs (A operand of S = Q K^T); e4m3
+//                      quadruples fill [0, 64)
+//     S/P buffer 0     [128, 192)   64 keys: fp32 scores, then P (16-bit pairs, or e4m3
+//                                   quadruples) over them
 //     S/P buffer 1     [192, 256)
 //     O                [256, 512)   fp32 accumulator
+// Element types (ET): 0 bf16, 1 fp16, 2 e4m3 (kind::f8f6f4 products, P rounded to e4m3,
+// O in bf16 times V's dequantisation factor, as in the smaller head dimensions).
 // Keys advance 64 at a time.  S(j+2) is issued right after O += P(j) V_j, so the softmax
 // of step j+1 overlaps both products.  Every product reads only one operand from shared
 // memory (K_j or V_j), which keeps shared-memory bandwidth below the tensor rate.
@@ -38,8 +42,8 @@ constexpr int kBN = 64;                        // keys per step
 constexpr int kThreads = 192;
 constexpr int kMmaWarp = 4, kLoadWarp = 5;
 constexpr int kSlots = 6;
-constexpr int kPanel64 = 64 * 128;             // 64 rows x 64 16-bit columns (8 KB)
-constexpr int kTile = 4 * kPanel64;            // 64 x 256 tile (32 KB)
+constexpr int kPanel64 = 64 * 128;             // 64 rows x 128 bytes (64 16-bit or 128 e4m3 columns)
+constexpr int kTile = 4 * kPanel64;            // ring slot: a 64 x 256 tile (32 KB at 16 bits)
 constexpr int kStageOff = kSlots * kTile;      // 4 warps x 4 KB epilogue staging
 constexpr int kBarOff = kStageOff + 4 * 4096;
 // barriers: ring_full[6], ring_empty[6], s_full[2], p_full[2], o_done, q_ready, drain
@@ -61,7 +65,23 @@ __device__ __forceinline__ uint32_t ring_par(uint32_t pos) { return (pos / kSlot
 // Streamed tiles of an item, from its first ring position: 0 and 1 are the two 64-row
 // halves of the Q tile, then K_j = 2 + 2j and V_j = 3 + 2j.
 
-template <bool F16> struct Lazy { static constexpr float kRescaleLog2 = F16 ? 8.0f : 16.0f; };
+template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 16.0f : 8.0f; };
+
+// Per element type: bytes per value, 128-byte panels per 256-value row, bytes of a tile.
+template <int ET> struct Elem {
+    static constexpr int kBytes = ET == 2 ? 1 : 2;
+    static constexpr int kPanels = D * kBytes / 128;
+    static constexpr int kTileBytes = kPanels * kPanel64;
+};
+
+// Instruction descriptor: kind::f16 (bf16 or fp16), or kind::f8f6f4 with both operands
+// e4m3 (format code 0); fp32 accumulator, A K-major.
+template <int ET>
+__host__ __device__ constexpr uint32_t idesc_of(int M, int N, bool b_mn_major) {
+    return ET == 2 ? ((1u << 4) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+                      ((uint32_t)(M >> 4) << 24))
+                   : make_idesc(M, N, b_mn_major, ET == 1);
+}
 
 // Named barrier 1 over the 128 softmax threads that also ANDs a predicate, so a stop
 // decision is common to the four warps.
@@ -79,11 +99,12 @@ __device__ __forceinline__ bool sm_barrier_and(bool ok) {
 }
 
 // One 64-key step of one row: running-max update (raised only when the step's maximum
-// exceeds it by more than 2^kRescaleLog2), p = 2^(s * sl2 - m), row sum, and P packed to
-// 16-bit pairs.  Keys at or past `limit` count as absent (MASK).  Eight independent max
-// chains and four paired sum chains keep the dependent depth short.  Returns the factor
+// exceeds it by more than 2^kRescaleLog2), p = 2^(s * sl2 - m), row sum (of the fp32
+// values), and P packed to 16-bit pairs in pk[0, 32), or to e4m3 quadruples in pk[0, 16).
+// Keys at or past `limit` count as absent (MASK).  Eight independent max chains and four
+// paired sum chains keep the dependent depth short.  Returns the factor
 // the row's O and l must be scaled by.
-template <bool MASK, bool F16>
+template <bool MASK, int ET>
 __device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0, int limit,
                                               float sl2, float& m_run, float& l_run,
                                               uint32_t (&pk)[32]) {
@@ -102,24 +123,31 @@ __device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0,
     const float mt = fmaxf(ptx::max3(mx[0], mx[1], mx[2]),
                            fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
     float alpha = 1.0f;
-    if (mt > m_run + Lazy<F16>::kRescaleLog2) {
+    if (mt > m_run + Lazy<ET>::kRescaleLog2) {
         alpha = ptx::ex2(m_run - mt);   // 0 on the first step (m_run = -inf)
         m_run = mt;
     }
     const float neg_m = -m_run;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int cc = 0; cc < 64; cc += 2) {
-        float x0, x1;
-        ptx::fma2(x0, x1, u2f(s[cc]), u2f(s[cc + 1]), sl2, neg_m);
-        float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-        if (MASK) {
-            if (key0 + cc >= limit) p0 = 0.0f;
-            if (key0 + cc + 1 >= limit) p1 = 0.0f;
+    for (int cc = 0; cc < 64; cc += 4) {
+        float x[4], pr[4];
+        ptx::fma2(x[0], x[1], u2f(s[cc]), u2f(s[cc + 1]), sl2, neg_m);
+        ptx::fma2(x[2], x[3], u2f(s[cc + 2]), u2f(s[cc + 3]), sl2, neg_m);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            pr[e] = ptx::ex2(x[e]);
+            if (MASK && key0 + cc + e >= limit) pr[e] = 0.0f;
         }
-        const int a = ((cc >> 1) & 3) * 2;
-        ptx::add2(acc[a], acc[a + 1], p0, p1);
-        pk[cc >> 1] = pack2<F16>(p0, p1);
+        const int a = ((cc >> 1) & 3) * 2;   // pairs (cc, cc+1) and (cc+2, cc+3): chains a, a+2
+        ptx::add2(acc[a], acc[a + 1], pr[0], pr[1]);
+        ptx::add2(acc[a + 2], acc[a + 3], pr[2], pr[3]);
+        if constexpr (ET == 2) {
+            pk[cc >> 2] = pack4_e4m3(pr[0], pr[1], pr[2], pr[3]);
+        } else {
+            pk[cc >> 1] = pack2<ET == 1>(pr[0], pr[1]);
+            pk[(cc >> 1) + 1] = pack2<ET == 1>(pr[2], pr[3]);
+        }
     }
     const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     l_run = l_run * alpha + sum;
@@ -197,8 +225,10 @@ __device__ __forceinline__ Work unit_item(const TcParams& p, int u, int sub) {
 // Every role walks the same items in the same order and keeps running counters: ring
 // position (2 Q halves, then K_j, V_j per item), global step index g (S/P buffer g % 2, its
 // (g / 2)-th use), products of O done, and items.
-template <bool CAUSAL, bool F16, int MODE>
+template <bool CAUSAL, int ET, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_constant__ TcParams p) {
+    constexpr int EB = Elem<ET>::kBytes;
+    constexpr int kPanels = Elem<ET>::kPanels;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -249,13 +279,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         const CUtensorMap* map = k < 2 ? &p.tmap_q : ((k & 1u) ? &p.tmap_v : &p.tmap_k);
                         const int row = k < 2 ? w.qt * kBM + (int)k * 64 : (int)((k - 2u) >> 1) * kBN;
                         const uint32_t dst = ring + (pos % kSlots) * (uint32_t)kTile;
-                        ptx::mbar_arrive_expect_tx(bar, (uint32_t)kTile);
+                        ptx::mbar_arrive_expect_tx(bar, (uint32_t)Elem<ET>::kTileBytes);
 #pragma unroll
-                        for (int pc = 0; pc < 4; ++pc) {
+                        for (int pc = 0; pc < kPanels; ++pc) {
+                            // x = the panel's first column: 64 or 128 values, 128 bytes
                             if (MODE == 0)
-                                ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, row, w.bh);
+                                ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * (128 / EB), row,
+                                                 w.bh);
                             else   // token-major: dims {D, H, tokens}
-                                ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * 64, w.h,
+                                ptx::tma_load_3d(dst + (uint32_t)pc * kPanel64, map, bar, pc * (128 / EB), w.h,
                                                  w.tok0 + row);
                         }
                     }
@@ -267,9 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        constexpr uint32_t id_qk = make_idesc(kBM, kBN, false, F16);
-        constexpr uint32_t id_pv = make_idesc(kBM, D, true, F16);
-        auto kdesc = [&](uint32_t pos) {   // K-major 64 x 256 tile
+        constexpr uint32_t id_qk = idesc_of<ET>(kBM, kBN, false);
+        constexpr uint32_t id_pv = idesc_of<ET>(kBM, D, true);
+        constexpr int kKeys = 32 / EB;   // keys per K step of O += P V (32 bytes of P per row)
+        auto kdesc = [&](uint32_t pos) {   // K-major 64 x 256 tile (panels of 128 bytes)
             return sw128_desc(ring + (pos % kSlots) * (uint32_t)kTile, 16, 1024);
         };
         auto vdesc = [&](uint32_t pos) {   // the same tile read as the MN-major operand
@@ -281,11 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
             if (!wait_warp(c, b_ring_full(pos), ring_par(pos), kRoleMma)) return false;
             ptx::tc_fence_after();
             const uint64_t kd = kdesc(pos);
+            // K steps of 32 bytes: Q's 8 TMEM columns, four steps per 128-byte panel of K
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ts_elect(tm + kColS + 64u * b, tm + kColQ + (uint32_t)kk * 8u,
-                                  kd + (((uint64_t)(kk / 4) * kPanel64 + (uint64_t)(kk % 4) * 32u) >> 4),
-                                  id_qk, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D * EB / 32; ++kk) {
+                const uint64_t kb = kd + (((uint64_t)(kk / 4) * kPanel64 + (uint64_t)(kk % 4) * 32u) >> 4);
+                if constexpr (ET == 2)
+                    ptx::mma_ts_f8_elect(tm + kColS + 64u * b, tm + kColQ + (uint32_t)kk * 8u, kb, id_qk,
+                                         kk > 0 ? 1u : 0u);
+                else
+                    ptx::mma_ts_elect(tm + kColS + 64u * b, tm + kColQ + (uint32_t)kk * 8u, kb, id_qk,
+                                      kk > 0 ? 1u : 0u);
+            }
             ptx::mma_commit_elect(bar_addr(c, b_s_full(b)));
             ptx::mma_commit_elect(bar_addr(c, b_ring_empty(pos)));
             return true;
@@ -307,11 +346,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     if (!wait_warp(c, b_ring_full(vpos), ring_par(vpos), kRoleMma)) goto mma_out;
                     ptx::tc_fence_after();
                     const uint64_t vd = vdesc(vpos);
+                    // K steps of kKeys keys: P's 8 TMEM columns, kKeys rows of 128 bytes of V
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        ptx::mma_ts_elect(tm + kColO, tm + kColS + 64u * b + (uint32_t)kk * 8u,
-                                          vd + (uint64_t)((kk * 2048) >> 4), id_pv,
-                                          (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kBN / kKeys; ++kk) {
+                        const uint64_t vb = vd + (uint64_t)((kk * kKeys * 128) >> 4);
+                        const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (ET == 2)
+                            ptx::mma_ts_f8_elect(tm + kColO, tm + kColS + 64u * b + (uint32_t)kk * 8u, vb,
+                                                 id_pv, acc);
+                        else
+                            ptx::mma_ts_elect(tm + kColO, tm + kColS + 64u * b + (uint32_t)kk * 8u, vb,
+                                              id_pv, acc);
+                    }
                     ptx::mma_commit_elect(bar_addr(c, b_o_done()));
                     ptx::mma_commit_elect(bar_addr(c, b_ring_empty(vpos)));
                     if (j + 2 < w.nkv && !issue_s(gj + 2u, base + 2u + 2u * (uint32_t)(j + 2))) goto mma_out;
@@ -338,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                 const int i = w.qt * kBM + r;   // row within the slice
                 const int limit = CAUSAL ? min(i + 1, w.len) : w.len;  // visible keys: key < limit
                 {
-                    // Q row r into TMEM as 16-bit pairs; the two ring slots are then released.
+                    // Q row r into TMEM as 16-bit pairs (e4m3 quadruples); the two ring slots
+                    // are then released.
                     // The previous item's products (which read Q) are complete: its
                     // epilogue waited for the last of them.
                     const bool ok = wait_warp(c, b_ring_full(base), ring_par(base), kRoleSoftmax) &&
@@ -348,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         const uint32_t src = ring + ((base + (uint32_t)(r >> 6)) % kSlots) * kTile +
                                              (uint32_t)lr * 128u;
 #pragma unroll
-                        for (int pc = 0; pc < 4; ++pc) {
+                        for (int pc = 0; pc < kPanels; ++pc) {
                             uint32_t q[32];
 #pragma unroll
                             for (int cc = 0; cc < 8; ++cc) {
@@ -380,8 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     const bool mask = __any_sync(0xFFFFFFFFu, key0 + kBN > limit);
                     uint32_t pk[32];
                     const float alpha =
-                        mask ? softmax_step<true, F16>(s, key0, limit, sl2, m_run, l_run, pk)
-                             : softmax_step<false, F16>(s, key0, limit, sl2, m_run, l_run, pk);
+                        mask ? softmax_step<true, ET>(s, key0, limit, sl2, m_run, l_run, pk)
+                             : softmax_step<false, ET>(s, key0, limit, sl2, m_run, l_run, pk);
                     if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                         // The reference rose: O += P(j-1) V_{j-1} must be complete, then this
                         // row of O is rescaled in TMEM.  (The product before it is already
@@ -399,7 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         }
                     }
                     __syncwarp();
-                    ptx::tmem_st32(tS, pk);   // P over this buffer's first 32 columns
+                    // P over this buffer's first 32 (e4m3: 16) columns
+                    if constexpr (ET == 2) ptx::tmem_st16(tS, pk);
+                    else ptx::tmem_st32(tS, pk);
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar_addr(c, b_p_full(b)));
@@ -412,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                 if (w.nkv >= 2 && !wait_warp(c, b_o_done(), (pv - 2u) & 1u, kRoleSoftmax)) goto sm_out;
                 if (!wait_warp(c, b_o_done(), (pv - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                 ptx::tc_fence_after();
-                const float inv = 1.0f / l_run;
+                const float inv = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
                 // row rr of the slice: obase + rr * ostride (elements)
                 const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
                 uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +
@@ -426,7 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)(pc * 64 + h * 32), o);
                         uint32_t wv[16];
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) wv[e] = pack2<F16>(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
+                        for (int e = 0; e < 16; ++e)   // fp16 for fp16 storage, else bf16
+                            wv[e] = pack2<ET == 1>(u2f(o[2 * e]) * inv, u2f(o[2 * e + 1]) * inv);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const uint32_t chunk = (uint32_t)(h * 4 + e) ^ (uint32_t)(lane & 7);
@@ -467,26 +517,45 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
     }
 }
 
-template <bool CAUSAL, bool F16>
+// e4m3 is served for [B, H, N, D] tensors only (MODE 0).
+template <bool CAUSAL, int ET>
 cudaError_t prepare_modes() {
     auto set = [](const void* fn) {
         return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     };
-    const cudaError_t e = set((const void*)fa_tc256_kernel<CAUSAL, F16, 0>);
-    return e != cudaSuccess ? e : set((const void*)fa_tc256_kernel<CAUSAL, F16, 1>);
+    const cudaError_t e = set((const void*)fa_tc256_kernel<CAUSAL, ET, 0>);
+    if constexpr (ET == 2) return e;
+    else return e != cudaSuccess ? e : set((const void*)fa_tc256_kernel<CAUSAL, ET, 1>);
 }
 
-template <bool CAUSAL, bool F16>
-void launch_mode(int mode, const TcParams& p, int grid, cudaStream_t stream) {
-    if (mode == 0) fa_tc256_kernel<CAUSAL, F16, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
-    else fa_tc256_kernel<CAUSAL, F16, 1><<<grid, kThreads, kSmemBytes, stream>>>(p);
+template <bool CAUSAL, int ET>
+cudaError_t launch_mode(int mode, const TcParams& p, int grid, cudaStream_t stream) {
+    if (mode == 0) {
+        fa_tc256_kernel<CAUSAL, ET, 0><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    } else {
+        if constexpr (ET == 2) return cudaErrorInvalidValue;
+        else fa_tc256_kernel<CAUSAL, ET, 1><<<grid, kThreads, kSmemBytes, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+template <bool CAUSAL>
+cudaError_t prepare_et(int et) {
+    return et == 2 ? prepare_modes<CAUSAL, 2>() : et == 1 ? prepare_modes<CAUSAL, 1>() : prepare_modes<CAUSAL, 0>();
+}
+
+template <bool CAUSAL>
+cudaError_t launch_et(int et, const TcParams& p, int grid, cudaStream_t stream) {
+    const int mode = p.layout;   // 0: [B, H, N, D]; 1: token-major
+    return et == 2   ? launch_mode<CAUSAL, 2>(mode, p, grid, stream)
+           : et == 1 ? launch_mode<CAUSAL, 1>(mode, p, grid, stream)
+                     : launch_mode<CAUSAL, 0>(mode, p, grid, stream);
 }
 
 }  // namespace
 
-cudaError_t tc256_prepare(bool causal, bool f16) {
-    if (causal) return f16 ? prepare_modes<true, true>() : prepare_modes<true, false>();
-    return f16 ? prepare_modes<false, true>() : prepare_modes<false, false>();
+cudaError_t tc256_prepare(bool causal, int et) {
+    return causal ? prepare_et<true>(et) : prepare_et<false>(et);
 }
 
 int tc256_units(int bh, int n, bool causal) {
@@ -495,17 +564,9 @@ int tc256_units(int bh, int n, bool causal) {
     return u > 0x7FFFFFFFLL ? -1 : (int)u;
 }
 
-cudaError_t tc256_launch(bool causal, bool f16, const TcParams& p, int grid, cudaStream_t stream) {
+cudaError_t tc256_launch(bool causal, int et, const TcParams& p, int grid, cudaStream_t stream) {
     if (grid < 1 || p.units < 1) return cudaErrorInvalidConfiguration;
-    const int mode = p.layout;   // 0: [B, H, N, D]; 1: token-major
-    if (causal) {
-        if (f16) launch_mode<true, true>(mode, p, grid, stream);
-        else launch_mode<true, false>(mode, p, grid, stream);
-    } else {
-        if (f16) launch_mode<false, true>(mode, p, grid, stream);
-        else launch_mode<false, false>(mode, p, grid, stream);
-    }
-    return cudaGetLastError();
+    return causal ? launch_et<true>(et, p, grid, stream) : launch_et<false>(et, p, grid, stream);
 }
 
 cudaError_t tc256_status_read_reset(uint32_t out[4]) {

@@ -77,6 +77,10 @@ WORKLOADS = {
     # head dimension 64 (the small shape's d) at full size, 16-bit and e4m3 inputs
     "bf16_b8h16n4096d64": Workload("bf16_b8h16n4096d64", 8, 16, 4096, 64, "bf16", False, 7100),
     "fp8_b8h16n4096d64": Workload("fp8_b8h16n4096d64", 8, 16, 4096, 64, "fp8", False, 8200),
+    # head dimension 256 with e4m3 inputs
+    "fp8_b4h8n4096d256": Workload("fp8_b4h8n4096d256", 4, 8, 4096, 256, "fp8", False, 8300),
+    "fp8_b4h8n4096d256_causal": Workload("fp8_b4h8n4096d256_causal", 4, 8, 4096, 256, "fp8",
+                                         True, 8300),
 }
 
 # The workload the throughput metric is quoted on.

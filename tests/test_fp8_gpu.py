@@ -83,21 +83,23 @@ def compare(w, slices=None, what=""):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 17, 128, 129, 300, 1000])
 def test_fp8_edge_shapes(N, D, causal):
     w = Workload("adhoc", 1, 2, N, D, "fp8", causal, N * 3 + D)
     compare(w, what="fp8 N=%d D=%d causal=%d" % (N, D, causal))
 
 
-def test_fp8_large_scores_force_rescales():
+@pytest.mark.parametrize("D", [128, 256])
+def test_fp8_large_scores_force_rescales(D):
     for causal in (False, True):
-        w = Workload("adhoc", 1, 2, 700, 128, "fp8", causal, 91, qk_mult=4.0)
-        compare(w, what="fp8 x4 causal=%d" % causal)
+        w = Workload("adhoc", 1, 2, 700, D, "fp8", causal, 91, qk_mult=4.0)
+        compare(w, what="fp8 x4 D=%d causal=%d" % (D, causal))
 
 
 @pytest.mark.parametrize("name", ["fp8_b4h16n4096d128", "fp8_b8h32n4096d128_causal",
-                                  "fp8_b8h16n4096d64"])
+                                  "fp8_b8h16n4096d64", "fp8_b4h8n4096d256",
+                                  "fp8_b4h8n4096d256_causal"])
 def test_fp8_full_size_sampled_slices(name):
     w = WORKLOADS[name]
     BH = w.B * w.H
