@@ -372,7 +372,8 @@ int backward(const BwdRequest& r) {
     if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
     if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (r.D != 32 && r.D != 64 && r.D != 128) return FA_ERR_UNSUPPORTED;
+    // D = 256: fp32 storage (CUDA cores) only
+    if (r.D != 32 && r.D != 64 && r.D != 128 && !(r.D == 256 && r.dtype == FA_FP32)) return FA_ERR_UNSUPPORTED;
     const size_t esize = r.dtype == FA_FP32 ? 4 : 2;
     if (r.layout == 1 && !packed && r.B * r.N > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;   // tokens
     const int64_t BH = r.B * r.H;

@@ -5,13 +5,16 @@
 //     P = exp(scale * Q K^T - LSE),  dP = dO V^T,  delta = rowsum(dO * O),
 //     dS = P * (dP - delta),  dV = P^T dO,  dQ = scale * dS K,  dK = scale * dS^T Q.
 // Two kernels, as on the tensor cores, and no atomics:
-//   * dQ: one CTA per 32 query rows; it forms delta for its rows (written to the workspace
-//     for the next kernel), then walks the key tiles with K and V in shared memory;
-//   * dK, dV: one CTA per 32 key rows; it walks the query tiles with Q, dO, LSE and delta
-//     in shared memory.
-// CTA = 128 threads = 32 rows x 4 threads; thread t of a row owns head-dim columns t, t+4,
-// ...; a dot product over D is the four partial sums added with two shuffles.  Layouts as
-// the forward: [B, H, N, D], token-major [tokens, H, D], packed sequences.
+//   * dQ: one CTA per 32 query rows (16 at D = 256); it forms delta for its rows (written
+//     to the workspace for the next kernel), then walks the key tiles with K and V in
+//     shared memory;
+//   * dK, dV: one CTA per 32 key rows (16 at D = 256); it walks the query tiles with Q,
+//     dO, LSE and delta in shared memory.
+// CTA = 128 threads = 32 rows x 4 threads (16 rows x 8 threads at D = 256, which keeps 32
+// columns per thread and the shared tiles at 32 KB); thread t of a row owns head-dim
+// columns t, t+T, t+2T, ... (T threads per row); a dot product over D is the T partial sums
+// added with shuffles.  Layouts as the forward: [B, H, N, D], token-major [tokens, H, D],
+// packed sequences.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -21,8 +24,14 @@
 namespace fa {
 namespace {
 
-constexpr int kRows = 32;     // rows per CTA and per shared-memory tile
 constexpr int kThreads = 128;
+
+// Rows per CTA (and per shared-memory tile) and threads per row.
+template <int D> struct Shape {
+    static constexpr int kTpr = D == 256 ? 8 : 4;
+    static constexpr int kRows = kThreads / kTpr;
+    static constexpr int kCols = D / kTpr;   // columns per thread
+};
 
 // Length, element offset of row 0, row stride (elements) and LSE / delta index of row 0 of
 // slice bh; packed offsets are clamped to [0, total] and lengths to the declared maximum.
@@ -50,9 +59,11 @@ __device__ __forceinline__ SimtSlice simt_slice(const SliceLayout& g, int bh) {
     return s;
 }
 
-__device__ __forceinline__ float quad_sum(float x) {
-    x += __shfl_xor_sync(0xFFFFFFFFu, x, 1);
-    x += __shfl_xor_sync(0xFFFFFFFFu, x, 2);
+// Sum over the TPR consecutive lanes that share a row.
+template <int TPR>
+__device__ __forceinline__ float row_sum(float x) {
+#pragma unroll
+    for (int m = 1; m < TPR; m <<= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, m);
     return x;
 }
 
@@ -61,6 +72,7 @@ __device__ __forceinline__ float quad_sum(float x) {
 template <int D>
 __device__ __forceinline__ void load_rows(float (*dst)[D], const float* __restrict__ src,
                                           const SimtSlice& s, int r0) {
+    constexpr int kRows = Shape<D>::kRows;
     for (int idx = threadIdx.x; idx < kRows * D / 4; idx += kThreads) {
         const int r = idx / (D / 4);
         const int c = (idx % (D / 4)) * 4;
@@ -75,14 +87,14 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const float* __restrict__ o, const float* __restrict__ dout, const float* __restrict__ lse,
     float* __restrict__ delta, float* __restrict__ dq, const SliceLayout g, float scale) {
-    constexpr int DQ = D / 4;
+    constexpr int kRows = Shape<D>::kRows, TPR = Shape<D>::kTpr, DQ = Shape<D>::kCols;
     __shared__ __align__(16) float Ks[kRows][D];
     __shared__ __align__(16) float Vs[kRows][D];
     const int nblk = (g.n + kRows - 1) / kRows;
     const int bh = (int)(blockIdx.x / (unsigned)nblk), blk = (int)(blockIdx.x % (unsigned)nblk);
     const SimtSlice s = simt_slice<D>(g, bh);
     if (blk * kRows >= s.len) return;   // the whole block lies past the end of the sequence
-    const int r = threadIdx.x / 4, qd = threadIdx.x % 4;
+    const int r = threadIdx.x / TPR, qd = threadIdx.x % TPR;
     const int i = blk * kRows + r;
     const bool live = i < s.len;
     const size_t row = s.base + (size_t)(live ? i : 0) * s.rs;
@@ -91,12 +103,12 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     float dl = 0.0f;
 #pragma unroll
     for (int c = 0; c < DQ; ++c) {
-        qv[c] = live ? q[row + qd + 4 * c] : 0.0f;
-        dov[c] = live ? dout[row + qd + 4 * c] : 0.0f;
-        dl = fmaf(dov[c], live ? o[row + qd + 4 * c] : 0.0f, dl);
+        qv[c] = live ? q[row + qd + TPR * c] : 0.0f;
+        dov[c] = live ? dout[row + qd + TPR * c] : 0.0f;
+        dl = fmaf(dov[c], live ? o[row + qd + TPR * c] : 0.0f, dl);
         acc[c] = 0.0f;
     }
-    dl = quad_sum(dl);   // delta_i = sum_d dO_id O_id
+    dl = row_sum<TPR>(dl);   // delta_i = sum_d dO_id O_id
     const float li = live ? lse[s.vec0 + i] : 0.0f;
     if (live && qd == 0) delta[s.vec0 + i] = dl;
     const int kend = CAUSAL ? min(s.len, (blk + 1) * kRows) : s.len;
@@ -112,20 +124,20 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
             float sp = 0.0f, dp = 0.0f;
 #pragma unroll
             for (int e = 0; e < DQ; ++e) {
-                sp = fmaf(qv[e], Ks[c][qd + 4 * e], sp);
-                dp = fmaf(dov[e], Vs[c][qd + 4 * e], dp);
+                sp = fmaf(qv[e], Ks[c][qd + TPR * e], sp);
+                dp = fmaf(dov[e], Vs[c][qd + TPR * e], dp);
             }
-            sp = quad_sum(sp);
-            dp = quad_sum(dp);
+            sp = row_sum<TPR>(sp);
+            dp = row_sum<TPR>(dp);
             const float pij = (k0 + c < limit) ? expf(sp * scale - li) : 0.0f;
             const float ds = pij * (dp - dl);
 #pragma unroll
-            for (int e = 0; e < DQ; ++e) acc[e] = fmaf(ds, Ks[c][qd + 4 * e], acc[e]);
+            for (int e = 0; e < DQ; ++e) acc[e] = fmaf(ds, Ks[c][qd + TPR * e], acc[e]);
         }
     }
     if (live) {
 #pragma unroll
-        for (int c = 0; c < DQ; ++c) dq[row + qd + 4 * c] = acc[c] * scale;
+        for (int c = 0; c < DQ; ++c) dq[row + qd + TPR * c] = acc[c] * scale;
     }
 }
 
@@ -135,7 +147,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     const float* __restrict__ dout, const float* __restrict__ lse,
     const float* __restrict__ delta, float* __restrict__ dk, float* __restrict__ dv,
     const SliceLayout g, float scale) {
-    constexpr int DQ = D / 4;
+    constexpr int kRows = Shape<D>::kRows, TPR = Shape<D>::kTpr, DQ = Shape<D>::kCols;
     __shared__ __align__(16) float Qs[kRows][D];
     __shared__ __align__(16) float DOs[kRows][D];
     __shared__ float Ls[kRows], Dl[kRows];
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     const int bh = (int)(blockIdx.x / (unsigned)nblk), blk = (int)(blockIdx.x % (unsigned)nblk);
     const SimtSlice s = simt_slice<D>(g, bh);
     if (blk * kRows >= s.len) return;
-    const int r = threadIdx.x / 4, qd = threadIdx.x % 4;
+    const int r = threadIdx.x / TPR, qd = threadIdx.x % TPR;
     const int j = blk * kRows + r;   // key row
     const bool live = j < s.len;
     const size_t row = s.base + (size_t)(live ? j : 0) * s.rs;
@@ -151,8 +163,8 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     float kv[DQ], vv[DQ], ak[DQ], av[DQ];
 #pragma unroll
     for (int c = 0; c < DQ; ++c) {
-        kv[c] = live ? k[row + qd + 4 * c] : 0.0f;
-        vv[c] = live ? v[row + qd + 4 * c] : 0.0f;
+        kv[c] = live ? k[row + qd + TPR * c] : 0.0f;
+        vv[c] = live ? v[row + qd + TPR * c] : 0.0f;
         ak[c] = 0.0f;
         av[c] = 0.0f;
     }
@@ -172,27 +184,27 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
             float sp = 0.0f, dp = 0.0f;
 #pragma unroll
             for (int e = 0; e < DQ; ++e) {
-                sp = fmaf(kv[e], Qs[c][qd + 4 * e], sp);
-                dp = fmaf(vv[e], DOs[c][qd + 4 * e], dp);
+                sp = fmaf(kv[e], Qs[c][qd + TPR * e], sp);
+                dp = fmaf(vv[e], DOs[c][qd + TPR * e], dp);
             }
-            sp = quad_sum(sp);
-            dp = quad_sum(dp);
+            sp = row_sum<TPR>(sp);
+            dp = row_sum<TPR>(dp);
             const int qi = q0 + c;
             const bool vis = qi < s.len && (!CAUSAL || qi >= j);
             const float pij = vis ? expf(sp * scale - Ls[c]) : 0.0f;
             const float ds = pij * (dp - Dl[c]);
 #pragma unroll
             for (int e = 0; e < DQ; ++e) {
-                av[e] = fmaf(pij, DOs[c][qd + 4 * e], av[e]);
-                ak[e] = fmaf(ds, Qs[c][qd + 4 * e], ak[e]);
+                av[e] = fmaf(pij, DOs[c][qd + TPR * e], av[e]);
+                ak[e] = fmaf(ds, Qs[c][qd + TPR * e], ak[e]);
             }
         }
     }
     if (live) {
 #pragma unroll
         for (int c = 0; c < DQ; ++c) {
-            dk[row + qd + 4 * c] = ak[c] * scale;
-            dv[row + qd + 4 * c] = av[c];
+            dk[row + qd + TPR * c] = ak[c] * scale;
+            dv[row + qd + TPR * c] = av[c];
         }
     }
 }
@@ -201,6 +213,7 @@ template <int D, bool CAUSAL>
 cudaError_t launch(const float* q, const float* k, const float* v, const float* o,
                    const float* dout, const float* lse, float* delta, float* dq, float* dk,
                    float* dv, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
+    constexpr int kRows = Shape<D>::kRows;
     const long long blocks = (long long)((g.n + kRows - 1) / kRows) * bh;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
     simt_bwd_dq_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, dout, lse,
@@ -228,6 +241,7 @@ cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, 
                             float scale, cudaStream_t stream) {
     if (D == 32) return launch_d<32>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
     if (D == 64) return launch_d<64>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    if (D == 256) return launch_d<256>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
     return launch_d<128>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
 }
 

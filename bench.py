@@ -223,7 +223,7 @@ def run_reference(args, w):
             "unit": "TFLOPS", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, args.gpus),
+            "config": config_of(w, args.gpus, input_set_bytes(w)),
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -293,12 +293,63 @@ def torch_all_reduce_max(device):
     return f
 
 
-def config_of(w, gpus):
+L2_BYTES = 129 * 10**6          # GB300 L2
+FLUSH_BYTES = 256 * 2**20
+
+
+def l2_note(set_bytes):
+    if set_bytes > L2_BYTES:
+        return ("two alternating input sets of %.0f MiB each (> 129 MB L2); no flush"
+                % (set_bytes / 2**20))
+    return ("input sets of %.2f MiB (< 129 MB L2): L2 flushed before every timed call (a "
+            "256 MiB buffer written between calls, outside the per-call CUDA event pairs)"
+            % (set_bytes / 2**20))
+
+
+def flush_buffer(torch, dev, set_bytes):
+    """A buffer larger than L2 to write between timed calls, when one input set fits in L2."""
+    if set_bytes > L2_BYTES:
+        return None
+    return torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+
+def timed_calls(torch, stream, step, steps, flush):
+    """Device milliseconds of step(0) .. step(steps - 1) on `stream` (the current stream).
+    Without a flush buffer the two alternating input sets evict each other from L2 and one
+    event pair brackets the back-to-back calls.  With one, the buffer is written before every
+    call and each call has its own event pair, so the writes stay outside the timed spans."""
+    def event():
+        return torch.cuda.Event(enable_timing=True)
+    if flush is None:
+        ev0, ev1 = event(), event()
+        ev0.record(stream)
+        for i in range(steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        return ev0.elapsed_time(ev1)
+    pairs = [(event(), event()) for _ in range(steps)]
+    for i, (a, b) in enumerate(pairs):
+        flush.fill_(i & 0x7F)
+        a.record(stream)
+        step(i)
+        b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in pairs)
+
+
+def input_set_bytes(w, op="fwd"):
+    """Bytes of one input set of a step: Q, K, V (forward); Q, K, V, O, dO and LSE (backward)."""
+    n = w.B * w.H * w.N * w.D
+    es = {"fp32": 4, "fp8": 1}.get(w.dtype, 2)
+    return 3 * n * es if op == "fwd" else 5 * n * es + 4 * w.B * w.H * w.N
+
+
+def config_of(w, gpus, set_bytes):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
             "dtype": w.dtype, "scale": w.scale, "qk_mult": w.qk_mult,
             "layout": "[B,H,N,D] contiguous", "parallelism": "replicas x%d" % gpus,
-            "l2": "two alternating input sets of %.0f MiB each (> 129 MB L2); no flush"
-                  % (3 * w.B * w.H * w.N * w.D * {"fp32": 4, "fp8": 1}.get(w.dtype, 2) / 2**20)}
+            "l2": l2_note(set_bytes)}
 
 
 # ------------------------------------------------------------------ backward
@@ -354,7 +405,7 @@ def run_reference_bwd(args, w):
             "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
             "ms_per_step": elapsed / steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": dict(config_of(w, args.gpus), op="bwd"),
+            "config": dict(config_of(w, args.gpus, input_set_bytes(w, "bwd")), op="bwd"),
             "cpu_baseline": {"value": value, "unit": "TFLOPS",
                              "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
                              "sample": sample},
@@ -373,8 +424,6 @@ def run_bwd(args, w):
     from attention_forward_04_gb300 import binding, build
     from attention_forward_04_gb300.inputs import TORCH_DTYPES, make_dout, make_qkv
 
-    if w.dtype == "fp32":
-        raise SystemExit("the backward serves bf16 and fp16 storage only")
     if rank == 0:
         build.build()
     if world > 1:
@@ -387,7 +436,7 @@ def run_bwd(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    code = {"bf16": binding.FA_BF16, "fp16": binding.FA_FP16}[w.dtype]
+    code = {"fp32": binding.FA_FP32, "bf16": binding.FA_BF16, "fp16": binding.FA_FP16}[w.dtype]
     B, H, N, D = w.B, w.H, w.N, w.D
     sets = []
     for s in range(2):
@@ -396,6 +445,7 @@ def run_bwd(args, w):
         o, lse = binding.fwd(q, k, v, scale=w.scale, causal=w.causal)
         sets.append((q, k, v, o, lse, do))
     grads = [torch.empty((B, H, N, D), dtype=TORCH_DTYPES[w.dtype], device=dev) for _ in range(3)]
+    set_bytes = input_set_bytes(w, "bwd")
     wsb = binding.bwd_workspace_bytes(B, H, N)
     ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
 
@@ -422,22 +472,17 @@ def run_bwd(args, w):
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = flush_buffer(torch, dev, set_bytes)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.monotonic()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms_local = timed_calls(torch, stream, step, args.steps, flush)
     t_wall1 = time.monotonic()
     if world > 1:
         dist.barrier()
     time.sleep(0.15)
     sampler.stop()
-    ms_local = ev0.elapsed_time(ev1)
     st, detail = binding.check_device_status()
     if st != 0:
         raise RuntimeError("kernel watchdog in timed region: %d %s" % (st, detail))
@@ -482,6 +527,14 @@ def run_bwd(args, w):
                       "kernel); per-kernel shares in the ncu launch list",
             "peak_source": "%s bf16 dense burst" % peak_src,
             "executed_tflops": 3.5 * w.flops / (per_call_ms / 1e3) / 1e12}
+    if w.dtype == "fp32":
+        # the CUDA-core backward: fp32 FFMA peak, SMs x 128 fp32 lanes x 2 FLOP x max SM clock
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = sms * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+        roof.update({"bound": "alu", "peak": alu_peak, "frac": achieved / alu_peak,
+                     "traffic": None, "kernel": "whole fa_bwd call (the two CUDA-core kernels)",
+                     "peak_source": "derived: %d SMs x 128 fp32 lanes x 2 FLOP x max SM clock"
+                                    % sms})
     cpu = None
     if args.cpu_budget > 0:
         try:
@@ -501,9 +554,7 @@ def run_bwd(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded torch.randn, cast to %s)" % w.dtype,
-        "config": dict(config_of(w, world), op="bwd",
-                       l2="two alternating input sets (Q, K, V, O, dO, LSE) of %.0f MiB each "
-                          "(> 129 MB L2); no flush" % ((5 * D * 2 + 4) * B * H * N / 2**20)),
+        "config": dict(config_of(w, world, set_bytes), op="bwd"),
         "e2e": {"value": e2e_per_s / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "ms_per_step": e2e_ms / args.e2e_steps,
@@ -580,6 +631,7 @@ def main():
         (q, k, v), descales = inputs(100 * s + 10 * rank)
         sets.append(tuple(t.to(dev) for t in (q, k, v)))
     host_set, host_descales = inputs(10 * rank)
+    set_bytes = input_set_bytes(w)
     o = torch.empty((B, H, N, D), dtype=torch.bfloat16 if fp8 else TORCH_DTYPES[w.dtype],
                     device=dev)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -612,22 +664,17 @@ def main():
     sampler.start()
     time.sleep(0.3)
 
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = flush_buffer(torch, dev, set_bytes)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.monotonic()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    ms_local = timed_calls(torch, stream, step, args.steps, flush)
     t_wall1 = time.monotonic()
     if world > 1:
         dist.barrier()
     time.sleep(0.15)
     sampler.stop()
-    ms_local = ev0.elapsed_time(ev1)
     st, detail = binding.check_device_status()
     if st != 0:
         raise RuntimeError("kernel watchdog in timed region: %d %s" % (st, detail))
@@ -718,7 +765,7 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else w.dtype,
         "data": ("synthetic (seeded torch.randn, per-tensor e4m3 quantisation; O bf16)" if fp8
                  else "synthetic (seeded torch.randn, cast to %s)" % w.dtype),
-        "config": config_of(w, world),
+        "config": config_of(w, world, set_bytes),
         "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "ms_per_step": e2e_ms / args.e2e_steps,

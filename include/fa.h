@@ -152,7 +152,7 @@ int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
  *                      16-byte aligned; scratch for delta, needs no initialisation, and
  *                      must not be shared by two calls in flight at once.
  *   B, H, N, scale, causal, stream : as for fa_fwd.
- *   D                : 32, 64 or 128.
+ *   D                : 32, 64 or 128; also 256 for FA_FP32.
  *   dtype            : FA_BF16 or FA_FP16 (tensor cores), or FA_FP32 (CUDA cores, fp32
  *                      arithmetic throughout).
  *

@@ -116,7 +116,7 @@ def test_bf16_backward_edge_shapes(N, D, causal):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
 @pytest.mark.parametrize("N", [1, 17, 129, 300])
 def test_fp32_backward(N, D, causal):
     q, k, v = make_shape(2, 1, N, D, "fp32", seed=N * 19 + D)

@@ -61,9 +61,9 @@ def test_bnhd_backward(D, causal):
                         "bnhd D=%d causal=%d (b=%d, h=%d)" % (D, causal, b, h))
 
 
-@pytest.mark.parametrize("dtype", ["fp16", "fp32"])
-def test_bnhd_backward_other_dtypes(dtype):
-    B, N, H, D = 1, 200, 2, 64
+@pytest.mark.parametrize("dtype,D", [("fp16", 64), ("fp32", 64), ("fp32", 256)])
+def test_bnhd_backward_other_dtypes(dtype, D):
+    B, N, H = 1, 200, 2
     to_bnhd = lambda t: t.permute(0, 2, 1, 3).contiguous().cuda()  # noqa: E731
     q, k, v = (to_bnhd(t) for t in make_shape(B, H, N, D, dtype, seed=9))
     do = to_bnhd(make_shape_dout(B, H, N, D, dtype, seed=9))
@@ -74,7 +74,7 @@ def test_bnhd_backward_other_dtypes(dtype):
     for h in range(H):
         sl = lambda t: f64(t[0, :, h])  # noqa: E731
         check_slice(sl(q), sl(k), sl(v), sl(do), sl(o), f64(lse[0, h]), [sl(g) for g in grads],
-                    1.0 / math.sqrt(D), True, dtype, "bnhd %s h=%d" % (dtype, h))
+                    1.0 / math.sqrt(D), True, dtype, "bnhd %s D=%d h=%d" % (dtype, D, h))
 
 
 LENGTHS = [[1, 17, 300, 129, 0, 256], [640], [257, 3, 500]]
@@ -87,8 +87,9 @@ def test_varlen_backward(mix, D, causal):
     run_varlen_backward(LENGTHS[mix], D, causal, "bf16", 100 + mix * 7 + D)
 
 
-def test_varlen_backward_fp32():
-    run_varlen_backward([0, 40, 129, 7], 64, True, "fp32", 5)
+@pytest.mark.parametrize("D", [64, 256])
+def test_varlen_backward_fp32(D):
+    run_varlen_backward([0, 40, 129, 7], D, True, "fp32", 5)
 
 
 def run_varlen_backward(lengths, D, causal, dtype, seed):

@@ -31,6 +31,7 @@ def test_reference_arm_prints_one_complete_line():
     assert d["n_gpus"] == 1 and d["steps"] == 1
     assert d["warmup"] >= 3                      # at least three warm-up steps, always
     assert d["config"]["workload"] == "bf16_b2h8n1024d64"
+    assert "flushed before every timed call" in d["config"]["l2"]   # 6 MiB sets fit in L2
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
     assert cb["sample"]
