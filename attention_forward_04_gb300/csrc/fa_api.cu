@@ -295,13 +295,17 @@ int forward(const Request& r) {
     p.bh = (int)BH;
     p.npairs = (int)((r.N + 255) / 256);
     p.nkv = (int)((r.N + 127) / 128);
-    p.units = units;
+    // [B, H, N, D] with B*H*ceil(N/128) <= #SM: one query tile per unit, so every tile runs
+    // at once on an SM of its own; otherwise pairs of query tiles.
+    const long long single_units = BH * (long long)p.nkv;
+    const bool single = r.layout == 0 && single_units <= (long long)di.sm_count;
+    p.units = single ? (int)single_units : units;
     p.scale_log2 = r.scale * r.descale[0] * r.descale[1] * 1.4426950408889634f;
     p.o_scale = r.descale[2];
     p.wait_limit = g_wait_limit.load();
     p.inject_stall = g_inject_stall.load();
-    const int grid = units < di.sm_count ? units : di.sm_count;
-    e = fa::tc_launch((int)r.D, dic, et, p, grid, st);
+    const int grid = p.units < di.sm_count ? p.units : di.sm_count;
+    e = fa::tc_launch((int)r.D, dic, et, p, single, grid, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "tensor-core kernel launch");
 }
 

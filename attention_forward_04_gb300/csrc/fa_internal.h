@@ -74,8 +74,10 @@ int tc_smem_bytes(int D);
 // et: element type of Q, K, V: 0 bf16, 1 fp16, 2 fp8 e4m3 (D = 64 or 128, layout 0 only).
 cudaError_t tc_prepare(int D, bool causal, int et);
 
-// Launch the tensor-core kernel with `grid` persistent CTAs on `stream`.
-cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, int grid,
+// Launch the tensor-core kernel with `grid` persistent CTAs on `stream`.  single: one
+// query tile per work unit ([B, H, N, D] only; p.units must then be B*H*nkv) instead of
+// pairs of query tiles.
+cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, bool single, int grid,
                       cudaStream_t stream);
 
 // Copy the device status word (4 words) of the tensor-core kernels to `out` and clear it.

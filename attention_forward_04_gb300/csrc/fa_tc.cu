@@ -150,7 +150,7 @@ struct Item {
 // to the declared maximum, so malformed offsets cannot move any access out of bounds.
 template <int MODE>
 __device__ __forceinline__ void slice_geometry(const TcParams& p, int bh, int& len, int& tok0) {
-    if (MODE == 0) {   // [B, H, N, D]: every slice has N rows
+    if (MODE != 1) {   // [B, H, N, D]: every slice has N rows
         len = p.n;
         tok0 = 0;
         return;
@@ -176,8 +176,15 @@ __device__ __forceinline__ void slice_geometry(const TcParams& p, int bh, int& l
 // longer than the other over the unit.  Units
 // past the end of a (shorter) packed sequence hold nothing.  unit_count gives the number of
 // items of unit u, unit_item the s-th one (computed on demand to keep registers free).
+//
+// MODE 2 is [B, H, N, D] with the single-tile schedule, which the host picks when the
+// B*H*ceil(N/128) query tiles fit on the SMs at once: a pair per SM would leave most SMs
+// idle and make each SM's two query tiles share its sub-partitions' softmax throughput.
+// Unit u is query tile u % nkv of slice u / nkv, placed in tile A; tile B is absent
+// (nB = 0), and its buffers, barriers and softmax warps stay unused for the whole launch.
 template <bool CAUSAL, int MODE>
 __device__ __forceinline__ int unit_count(const TcParams& p, int u) {
+    if (MODE == 2) return 1;
     if (MODE == 0) {   // [B, H, N, D]: every unit is full
         if (!CAUSAL) return 1;
         const int q = u % ((p.npairs + 1) / 2);
@@ -195,8 +202,20 @@ __device__ __forceinline__ int unit_count(const TcParams& p, int u) {
 
 template <bool CAUSAL, int MODE>
 __device__ __forceinline__ Item unit_item(const TcParams& p, int u, int s) {
-    const int per_slice = CAUSAL ? (p.npairs + 1) / 2 : p.npairs;
     Item it;
+    if constexpr (MODE == 2) {
+        const int t = u % p.nkv;   // query tile: rows 128 t ..
+        it.bh = u / p.nkv;
+        it.h = 0;
+        it.len = p.n;
+        it.tok0 = 0;
+        it.pair = t >> 1;
+        it.sw = t & 1;             // tile A holds rows 128 * (t & 1) of the pair
+        it.nA = CAUSAL ? min(t + 1, p.nkv) : p.nkv;
+        it.nB = 0;
+        return it;
+    }
+    const int per_slice = CAUSAL ? (p.npairs + 1) / 2 : p.npairs;
     if (MODE == 0) {   // [B, H, N, D]: slices of N rows, no head or token bookkeeping
         it.bh = u / per_slice;
         const int q = u % per_slice;
@@ -236,7 +255,7 @@ __device__ __forceinline__ Item unit_item(const TcParams& p, int u, int s) {
 template <int MODE>
 __device__ __forceinline__ void tile_coords(const TcParams& p, const Item& it, int row, int& c1,
                                             int& c2) {
-    if (MODE == 0) {
+    if (MODE != 1) {
         c1 = row;
         c2 = it.bh;
     } else {
@@ -330,12 +349,14 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
             issue_qk<D, ET>(tS[0], dQ[0], dK0 + slot_off(kv), idesc_qk);
             ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(0)));
             if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
-            if (!wait_warp(c, b_q_full<D, EB>(1), q_cnt & 1u, kRoleMma)) goto out;
+            if constexpr (MODE != 2) {   // tile B (absent in the single-tile schedule)
+                if (!wait_warp(c, b_q_full<D, EB>(1), q_cnt & 1u, kRoleMma)) goto out;
+                ptx::tc_fence_after();
+                issue_qk<D, ET>(tS[1], dQ[1], dK0 + slot_off(kv), idesc_qk);
+                ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(1)));
+                if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+            }
             ++q_cnt;
-            ptx::tc_fence_after();
-            issue_qk<D, ET>(tS[1], dQ[1], dK0 + slot_off(kv), idesc_qk);
-            ptx::mma_commit_elect(bar_addr(c, b_s_full<D, EB>(1)));
-            if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
             ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kv)));
             ++kv;
 
@@ -437,10 +458,12 @@ __device__ void mma_role_sep(const TcParams& p, const Ctl& c, uint32_t tmem, uin
             if (!wait_warp(c, b_kv_full<D, EB>(kv), ring_parity<D, EB>(kv), kRoleMma)) goto out;
             if (!issue_s(0, kv)) goto out;
             if (it.nA == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(0)));
-            if (!wait_warp(c, b_q_full<D, EB>(1), q_cnt & 1u, kRoleMma)) goto out;
+            if constexpr (MODE != 2) {   // tile B (absent in the single-tile schedule)
+                if (!wait_warp(c, b_q_full<D, EB>(1), q_cnt & 1u, kRoleMma)) goto out;
+                if (!issue_s(1, kv)) goto out;
+                if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
+            }
             ++q_cnt;
-            if (!issue_s(1, kv)) goto out;
-            if (it.nB == 1) ptx::mma_commit_elect(bar_addr(c, b_q_empty<D, EB>(1)));
             ptx::mma_commit_elect(bar_addr(c, b_kv_empty<D, EB>(kv)));   // K_0
             ++kv;
 
@@ -522,7 +545,7 @@ __device__ void load_role(const TcParams& p, const Ctl& c, uint32_t sbase) {
                                              pc * G::kPanelCols, c1, c2);
                     }
                     ++kv;
-                    if (j == 0 && w == 0 && !load_q(1)) goto out;
+                    if (MODE != 2 && j == 0 && w == 0 && !load_q(1)) goto out;
                 }
             }
             ++q_cnt;
@@ -634,6 +657,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
     const uint32_t tP = tmem + tl + G::col_p(t);
     const uint32_t tO = tmem + tl + G::col_o(t);
     uint32_t s_cnt = 0, o_cnt = 0;
+    if (MODE == 2 && t == 1) return;   // tile B is absent in the single-tile schedule
 
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const int nsub = unit_count<CAUSAL, MODE>(p, u);
@@ -642,7 +666,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             const int n = t == 0 ? it.nA : it.nB;
             const int row = it.pair * 2 * kBM + (t ^ it.sw) * kBM + lane_base + lane;
             // sequence length: the kernel parameter for [B, H, N, D] (no register held)
-            const int len = MODE == 0 ? p.n : it.len;
+            const int len = MODE != 1 ? p.n : it.len;
             const int limit = CAUSAL ? min(row + 1, len) : len;   // visible keys: j < limit
             float m_run = -INFINITY, l_run = 0.0f;
 
@@ -701,9 +725,9 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             const float inv_l = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
             const int row0 = it.pair * 2 * kBM + (t ^ it.sw) * kBM + lane_base;   // first row of the warp
             // row r of the slice: obase + r * ostride (elements)
-            const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
+            const size_t ostride = MODE != 1 ? (size_t)D : (size_t)p.heads * D;
             uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +
-                              (MODE == 0 ? (size_t)it.bh * (size_t)p.n * D
+                              (MODE != 1 ? (size_t)it.bh * (size_t)p.n * D
                                          : ((size_t)it.tok0 * p.heads + it.h) * D);
             if constexpr (D == 32) {
                 // one 64-byte row per thread: 4 chunks staged, then 8 rows x 4 chunks per store
@@ -726,7 +750,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                     const int ch = lane & 3;             // 16-byte chunk within the 64-byte row
                     const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u +
                                                       (uint32_t)((ch ^ (r & 7)) * 16));
-                    if (row0 + r < (MODE == 0 ? p.n : it.len))
+                    if (row0 + r < (MODE != 1 ? p.n : it.len))
                         *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * ostride + ch * 8) = v;
                 }
                 __syncwarp();
@@ -755,12 +779,12 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                     const int ch = lane & 7;             // 16-byte chunk within the 128-byte row
                     const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u +
                                                       (uint32_t)((ch ^ (r & 7)) * 16));
-                    if (row0 + r < (MODE == 0 ? p.n : it.len))
+                    if (row0 + r < (MODE != 1 ? p.n : it.len))
                         *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * ostride + pc * 64 + ch * 8) = v;
                 }
                 __syncwarp();
             }
-            if (row < (MODE == 0 ? p.n : it.len)) {
+            if (row < (MODE != 1 ? p.n : it.len)) {
                 // [B, H, N] rows, or [H, total] for packed sequences
                 const size_t lrow = (MODE == 1 && p.cu_seqlens != nullptr)
                                         ? (size_t)it.h * (size_t)p.total + (size_t)it.tok0 + (size_t)row
@@ -855,20 +879,21 @@ cudaError_t launch_one(const TcParams& p, int grid, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-// 16-bit storage: both layouts; e4m3: [B, H, N, D] only.
+// Modes: 0 [B, H, N, D] with query-tile pairs, 2 the same layout with one query tile per
+// unit, 1 token-major (16-bit storage only; e4m3 has the [B, H, N, D] modes alone).
 template <int D, bool CAUSAL, int ET>
 cudaError_t dispatch_mode(int mode, bool prepare, const TcParams* p, int grid, cudaStream_t stream) {
-    if constexpr (ET == 2) {
-        if (prepare) return prepare_one<D, CAUSAL, ET, 0>();
-        return mode == 0 ? launch_one<D, CAUSAL, ET, 0>(*p, grid, stream) : cudaErrorInvalidValue;
-    } else {
-        if (prepare) {
-            cudaError_t e = prepare_one<D, CAUSAL, ET, 0>();
-            return e != cudaSuccess ? e : prepare_one<D, CAUSAL, ET, 1>();
-        }
-        return mode == 0 ? launch_one<D, CAUSAL, ET, 0>(*p, grid, stream)
-                         : launch_one<D, CAUSAL, ET, 1>(*p, grid, stream);
+    if (prepare) {
+        cudaError_t e = prepare_one<D, CAUSAL, ET, 0>();
+        if (e == cudaSuccess) e = prepare_one<D, CAUSAL, ET, 2>();
+        if constexpr (ET != 2)
+            if (e == cudaSuccess) e = prepare_one<D, CAUSAL, ET, 1>();
+        return e;
     }
+    if (mode == 0) return launch_one<D, CAUSAL, ET, 0>(*p, grid, stream);
+    if (mode == 2) return launch_one<D, CAUSAL, ET, 2>(*p, grid, stream);
+    if constexpr (ET != 2) return launch_one<D, CAUSAL, ET, 1>(*p, grid, stream);
+    return cudaErrorInvalidValue;
 }
 
 template <int D, int ET>
@@ -907,11 +932,12 @@ cudaError_t tc_prepare(int D, bool causal, int et) {
                    : dispatch<128>(causal, et, 0, true, nullptr, 0, nullptr);
 }
 
-cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, int grid,
+cudaError_t tc_launch(int D, bool causal, int et, const TcParams& p, bool single, int grid,
                       cudaStream_t stream) {
-    if (D == 32) return dispatch<32>(causal, et, p.layout, false, &p, grid, stream);
-    return D == 64 ? dispatch<64>(causal, et, p.layout, false, &p, grid, stream)
-                   : dispatch<128>(causal, et, p.layout, false, &p, grid, stream);
+    const int mode = p.layout == 0 && single ? 2 : p.layout;
+    if (D == 32) return dispatch<32>(causal, et, mode, false, &p, grid, stream);
+    return D == 64 ? dispatch<64>(causal, et, mode, false, &p, grid, stream)
+                   : dispatch<128>(causal, et, mode, false, &p, grid, stream);
 }
 
 cudaError_t tc_status_read_reset(uint32_t out[4]) {

@@ -72,6 +72,13 @@ def run_varlen(lengths, H, D, dtype, causal, seed):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_varlen_pair_schedule(causal):
+    # 40 heads x 6 sequences x ceil(300 / 128) = 720 single-tile units > 152 SMs: the
+    # paired schedule, with empty, single-token and ragged sequences
+    run_varlen([1, 17, 300, 0, 129, 256], 40, 64, "bf16", causal, seed=41)
+
+
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("mix", range(len(LENGTH_MIXES)))
 def test_varlen_bf16(mix, D, causal):

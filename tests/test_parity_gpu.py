@@ -61,6 +61,30 @@ def full_compare(q, k, v, scale, causal, dtype, what=""):
     assert_close(o, lse, o_ref, lse_ref, dtype, what)
 
 
+# ------------------------------------------------------------ both schedules
+# The library gives each 128-row query tile its own work unit when B*H*ceil(N/128) units
+# fit on the SMs at once (152 on GB300), and pairs of query tiles otherwise.  Most small
+# test shapes take the first schedule; these take the second at small N, ragged tails and
+# N <= 128 included.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("N", [100, 300])
+def test_pair_schedule_small_shapes(N, D, causal):
+    B, H = 8, 20                       # 160 slices: at least 160 single-tile units
+    assert B * H * ((N + 127) // 128) > 152
+    q, k, v = make_shape(B, H, N, D, "bf16", seed=N + D)
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "bf16",
+                 "pair schedule N=%d D=%d causal=%d" % (N, D, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_schedule_uneven_tiles(causal):
+    B, H, N, D = 3, 5, 900, 128        # 15 slices x 8 tiles = 120 single-tile units
+    assert B * H * ((N + 127) // 128) <= 152
+    q, k, v = make_shape(B, H, N, D, "bf16", seed=907)
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "bf16", "split schedule causal=%d" % causal)
+
+
 # ------------------------------------------------------------ small and edge shapes
 EDGE_N = [1, 17, 127, 128, 129, 255, 256, 257, 383, 640, 1000]
 
