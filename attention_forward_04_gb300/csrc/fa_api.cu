@@ -64,8 +64,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 
 // 16-bit tensor viewed as a 3-D TMA map whose box lands in shared memory as 128 rows of
 // 64 head-dim values (128 bytes, 128-byte swizzle), which the tensor-core kernel expects.
-//   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, rows, 1} (rows = 128, or 64 for the
-//   D = 256 kernel); rows past N read as zero.
+//   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, rows, 1} (rows = 128, 64 for the
+//   D = 256 kernel, 32 for the forward's O stores); rows past N read as zero (and are not
+//   written by a store).
 //   D = 32: the box is 32 values wide and lands as 64-byte rows with the 64-byte swizzle.
 //   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, rows}; tokens past T read
 //   as zero (tokens of the next packed sequence are masked by the kernel instead).
@@ -285,6 +286,11 @@ int forward(const Request& r) {
         !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
         !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, et, fn))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
+    // O of [B, H, N, D] problems at D >= 64 leaves through bulk tensor stores of 32-row
+    // panels (O is fp16 for fp16 storage, else bf16)
+    if (r.layout == 0 && r.D >= 64 &&
+        !encode_map(&p.tmap_o, r.o, 0, BH, r.N, r.H, r.T, r.D, f16 ? 1 : 0, fn, 32))
+        return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (O)");
     p.o = r.o;
     p.lse = r.lse;
     p.layout = r.layout;

@@ -13,6 +13,7 @@ struct TcParams {
     CUtensorMap tmap_q;  // 3-D maps over the [B*H, N, D] view, innermost D; box {64, 128, 1},
     CUtensorMap tmap_k;  // 128-byte swizzle, zero fill outside the tensor (ragged N)
     CUtensorMap tmap_v;
+    CUtensorMap tmap_o;  // [B*H, N, D] output map, box {64, 32, 1} (D >= 64, [B, H, N, D] only)
     void* o;             // output, same element type and layout as the inputs
     float* lse;          // fp32 LSE: [B, H, N], or [H, total] for packed sequences
     int layout;          // 0: [B, H, N, D] slices; 1: token-major [tokens, H, D]

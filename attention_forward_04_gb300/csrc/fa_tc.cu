@@ -135,6 +135,33 @@ template <int D, int EB> __device__ __forceinline__ uint32_t ring_parity(uint32_
 }
 
 // ----------------------------------------------------------------- work schedule
+// Bulk tensor store of one staged 32-row panel of O (shared -> global) with its completion
+// tracking, for the [B, H, N, D] epilogue at D >= 64: one lane issues, the copy engine
+// reads the staging slot and writes whole lines; rows past N lie outside the map and are
+// not written.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
+                                             int32_t c1, int32_t c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+                 ::"l"(map), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The issuing thread's stores have finished reading shared memory (the slot may be reused).
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// The issuing thread's stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Shared-memory writes of this thread become visible to the copy engine's reads.
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// O leaves through bulk tensor stores where its rows are [B, H, N, D] rows of 64-column
+// panels; token-major rows past a sequence belong to the next one, so those layouts (and
+// the 64-byte rows of D = 32) keep per-row stores with a length check.
+template <int D, int MODE> struct OStore { static constexpr bool kTma = MODE != 1 && D >= 64; };
+
 struct Item {
     int bh;    // slice b*H + h
     int h;     // head
@@ -757,6 +784,10 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             }
 #pragma unroll 1
             for (int pc = 0; pc < D / 64; ++pc) {
+                if constexpr (OStore<D, MODE>::kTma) {   // the slot's last store has read it
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     uint32_t o[32];
@@ -771,6 +802,16 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                         ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
                                           w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                     }
+                }
+                if constexpr (OStore<D, MODE>::kTma) {
+                    // the slot is the store's 128-byte-swizzled 32 x 64 box
+                    fence_async_shared();
+                    __syncwarp();
+                    if (lane == 0 && row0 < p.n) {
+                        tma_store_3d(&p.tmap_o, stage, pc * 64, row0, it.bh);
+                        bulk_commit();
+                    }
+                    continue;
                 }
                 __syncwarp();
 #pragma unroll
@@ -836,6 +877,7 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
         ptx::prefetch_tensormap(&p.tmap_q);
         ptx::prefetch_tensormap(&p.tmap_k);
         ptx::prefetch_tensormap(&p.tmap_v);
+        if constexpr (OStore<D, MODE>::kTma) ptx::prefetch_tensormap(&p.tmap_o);
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
@@ -849,6 +891,10 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     if (warp < kSoftmaxWarps) {
         softmax_role<D, CAUSAL, ET, MODE>(p, c, tmem, warp, lane,
                                      sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
+        if constexpr (OStore<D, MODE>::kTma) {   // this warp's O stores complete before exit
+            if (lane == 0) bulk_wait_all();
+            __syncwarp();
+        }
     } else if (warp == kMmaWarp) {
         if constexpr (G::kSepP) mma_role_sep<D, CAUSAL, ET, MODE>(p, c, tmem, sbase);
         else mma_role<D, CAUSAL, ET, MODE>(p, c, tmem, sbase);
