@@ -236,7 +236,7 @@ int forward(const Request& r) {
     if (!tc) {
         e = fa::simt_launch((int)r.D, r.causal != 0, static_cast<const float*>(r.q),
                             static_cast<const float*>(r.k), static_cast<const float*>(r.v),
-                            static_cast<float*>(r.o), r.lse, (int)BH, g, r.scale, st);
+                            static_cast<float*>(r.o), r.lse, (int)BH, g, r.scale, di.sm_count, st);
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "fp32 kernel launch");
     }
 

@@ -101,10 +101,10 @@ struct SliceLayout {
     int n;                  // N, or the longest allowed packed length
 };
 
-// fp32 SIMT kernel over the same layouts (fp32 storage).
+// fp32 SIMT kernel over the same layouts (fp32 storage); sm_count picks the CTA shape.
 cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, const float* v,
                         float* o, float* lse, int bh, const SliceLayout& g, float scale,
-                        cudaStream_t stream);
+                        int sm_count, cudaStream_t stream);
 
 // fp32 SIMT backward over the same layouts: dQ (which also writes delta, indexed like the
 // LSE) and then dK, dV, on `stream`.

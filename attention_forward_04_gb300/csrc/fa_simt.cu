@@ -10,12 +10,14 @@
 // Layouts: [B, H, N, D] slices, or token-major [tokens, H, D] (fixed length N, or packed
 // sequences with token offsets cu_seqlens), as in the tensor-core path.
 //
-// CTA = 128 threads = 32 rows x 4 threads.  Thread q of a row owns head-dim columns
-// q, q+4, q+8, ... (interleaved, so the 4 threads of a row hit 4 different banks when
-// reading a shared K/V row).  Per key tile (32 keys; 16 at D = 256, which keeps the K and V
-// tiles at 32 KB of static shared memory): partial dot products are summed
-// across the 4 threads with two shuffles, then the running max / sum update, exp with
-// the new max, and the O update.  O is divided by l once at the end.
+// CTA = 128 threads = 32 rows x 4 threads, or, when that grid would leave SMs idle (a
+// small problem), 8 rows x 16 threads: four times the CTAs and a quarter of the dependent
+// work per thread and key.  Thread q of a row owns head-dim columns q, q+T, q+2T, ... (T
+// threads per row; interleaved, so the threads of a row hit different banks when reading
+// a shared K/V row).  Per key tile (32 keys; 16 at D = 256, which keeps the K and V tiles
+// at 32 KB of static shared memory): partial dot products are summed across the T threads
+// with shuffles, then the running max / sum update, exp with the new max, and the O
+// update.  O is divided by l once at the end.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -25,24 +27,24 @@
 namespace fa {
 namespace {
 
-constexpr int kRows = 32;     // query rows per CTA
 constexpr int kThreads = 128;
 
-template <int D, bool CAUSAL>
+template <int D, int TPR, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restrict__ q,
                                                            const float* __restrict__ k,
                                                            const float* __restrict__ v,
                                                            float* __restrict__ o,
                                                            float* __restrict__ lse,
                                                            const SliceLayout g, float scale) {
-    constexpr int DQ = D / 4;  // columns per thread
+    constexpr int kRows = kThreads / TPR;   // query rows per CTA
+    constexpr int DQ = D / TPR;             // columns per thread
     constexpr int kKeys = D == 256 ? 16 : 32;   // keys per shared-memory tile
     __shared__ __align__(16) float Ks[kKeys][D];
     __shared__ __align__(16) float Vs[kKeys][D];
 
     const int tid = threadIdx.x;
-    const int r = tid / 4;         // row within the CTA
-    const int qd = tid % 4;        // column phase: columns qd + 4*i
+    const int r = tid / TPR;       // row within the CTA
+    const int qd = tid % TPR;      // column phase: columns qd + TPR*i
     const int nblk = (g.n + kRows - 1) / kRows;
     const int bh = (int)(blockIdx.x / (unsigned)nblk);     // slice b*H + h
     const int blk = (int)(blockIdx.x % (unsigned)nblk);    // row block within the slice
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
     float qv[DQ], acc[DQ];
 #pragma unroll
     for (int i = 0; i < DQ; ++i) {
-        qv[i] = live ? q[slice + (size_t)row * rs + qd + 4 * i] : 0.0f;
+        qv[i] = live ? q[slice + (size_t)row * rs + qd + TPR * i] : 0.0f;
         acc[i] = 0.0f;
     }
     float m = -INFINITY, l = 0.0f;
@@ -77,21 +79,45 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
     const int kend = CAUSAL ? min(n, (blk + 1) * kRows) : n;
     const int limit = CAUSAL ? min(row + 1, n) : n;   // visible keys: j < limit
 
-    for (int k0 = 0; k0 < kend; k0 += kKeys) {
-        __syncthreads();
-        // Cooperative float4 loads of K and V rows k0..k0+kKeys-1 (rows >= n read as zero).
-        for (int idx = tid; idx < kKeys * D / 4; idx += kThreads) {
+    // Cooperative float4 loads of K and V rows k0..k0+kKeys-1 (rows >= n read as zero): each
+    // thread moves kLoads float4 of each.  With 16 threads per row (few, short CTAs) the next
+    // tile's loads are issued before the current tile's arithmetic, so their latency hides
+    // behind it; with 4 threads per row the registers go to the longer rows instead.
+    constexpr int kLoads = kKeys * D / 4 / kThreads;
+    constexpr bool kPrefetch = TPR == 16;
+    float4 kx[kLoads], vx[kLoads];
+    auto fetch = [&](int k0) {
+#pragma unroll
+        for (int e = 0; e < kLoads; ++e) {
+            const int idx = tid + e * kThreads;
             const int kr = idx / (D / 4);
             const int kc = (idx % (D / 4)) * 4;
-            float4 kx = make_float4(0.f, 0.f, 0.f, 0.f), vx = kx;
+            kx[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            vx[e] = kx[e];
             if (k0 + kr < n) {
-                kx = *reinterpret_cast<const float4*>(k + slice + (size_t)(k0 + kr) * rs + kc);
-                vx = *reinterpret_cast<const float4*>(v + slice + (size_t)(k0 + kr) * rs + kc);
+                kx[e] = *reinterpret_cast<const float4*>(k + slice + (size_t)(k0 + kr) * rs + kc);
+                vx[e] = *reinterpret_cast<const float4*>(v + slice + (size_t)(k0 + kr) * rs + kc);
             }
-            *reinterpret_cast<float4*>(&Ks[kr][kc]) = kx;
-            *reinterpret_cast<float4*>(&Vs[kr][kc]) = vx;
         }
+    };
+    auto stash = [&]() {
+#pragma unroll
+        for (int e = 0; e < kLoads; ++e) {
+            const int idx = tid + e * kThreads;
+            const int kr = idx / (D / 4);
+            const int kc = (idx % (D / 4)) * 4;
+            *reinterpret_cast<float4*>(&Ks[kr][kc]) = kx[e];
+            *reinterpret_cast<float4*>(&Vs[kr][kc]) = vx[e];
+        }
+    };
+    if (kPrefetch && kend > 0) fetch(0);
+
+    for (int k0 = 0; k0 < kend; k0 += kKeys) {
         __syncthreads();
+        if (!kPrefetch) fetch(k0);
+        stash();
+        __syncthreads();
+        if (kPrefetch && k0 + kKeys < kend) fetch(k0 + kKeys);
 
         float s[kKeys];
         float tmax = -INFINITY;
@@ -99,9 +125,9 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
         for (int c = 0; c < kKeys; ++c) {
             float part = 0.0f;
 #pragma unroll
-            for (int i = 0; i < DQ; ++i) part = fmaf(qv[i], Ks[c][qd + 4 * i], part);
-            part += __shfl_xor_sync(0xFFFFFFFFu, part, 1);
-            part += __shfl_xor_sync(0xFFFFFFFFu, part, 2);
+            for (int i = 0; i < DQ; ++i) part = fmaf(qv[i], Ks[c][qd + TPR * i], part);
+#pragma unroll
+            for (int m = 1; m < TPR; m <<= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, m);
             const bool vis = k0 + c < limit;
             s[c] = vis ? part * scale : -INFINITY;
             tmax = fmaxf(tmax, s[c]);
@@ -123,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
         for (int i = 0; i < DQ; ++i) {
             float a = acc[i] * alpha;
 #pragma unroll
-            for (int c = 0; c < kKeys; ++c) a = fmaf(s[c], Vs[c][qd + 4 * i], a);
+            for (int c = 0; c < kKeys; ++c) a = fmaf(s[c], Vs[c][qd + TPR * i], a);
             acc[i] = a;
         }
         m = m_new;
@@ -132,36 +158,47 @@ __global__ void __launch_bounds__(kThreads) fa_simt_kernel(const float* __restri
     if (live) {
         const float inv_l = 1.0f / l;
 #pragma unroll
-        for (int i = 0; i < DQ; ++i) o[slice + (size_t)row * rs + qd + 4 * i] = acc[i] * inv_l;
+        for (int i = 0; i < DQ; ++i) o[slice + (size_t)row * rs + qd + TPR * i] = acc[i] * inv_l;
         if (qd == 0) lse[lse0 + row] = m + logf(l);
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, int TPR, bool CAUSAL>
 cudaError_t launch(const float* q, const float* k, const float* v, float* o, float* lse, int bh,
                    const SliceLayout& g, float scale, cudaStream_t stream) {
+    constexpr int kRows = kThreads / TPR;
     const long long blocks = (long long)((g.n + kRows - 1) / kRows) * bh;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    fa_simt_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, lse, g, scale);
+    fa_simt_kernel<D, TPR, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, lse, g, scale);
     return cudaGetLastError();
+}
+
+template <int D, int TPR>
+cudaError_t launch_c(bool causal, const float* q, const float* k, const float* v, float* o,
+                     float* lse, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
+    return causal ? launch<D, TPR, true>(q, k, v, o, lse, bh, g, scale, stream)
+                  : launch<D, TPR, false>(q, k, v, o, lse, bh, g, scale, stream);
+}
+
+template <int D>
+cudaError_t launch_d(bool wide, bool causal, const float* q, const float* k, const float* v,
+                     float* o, float* lse, int bh, const SliceLayout& g, float scale,
+                     cudaStream_t stream) {
+    return wide ? launch_c<D, 16>(causal, q, k, v, o, lse, bh, g, scale, stream)
+                : launch_c<D, 4>(causal, q, k, v, o, lse, bh, g, scale, stream);
 }
 
 }  // namespace
 
 cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, const float* v,
                         float* o, float* lse, int bh, const SliceLayout& g, float scale,
-                        cudaStream_t stream) {
-    if (D == 32)
-        return causal ? launch<32, true>(q, k, v, o, lse, bh, g, scale, stream)
-                      : launch<32, false>(q, k, v, o, lse, bh, g, scale, stream);
-    if (D == 64)
-        return causal ? launch<64, true>(q, k, v, o, lse, bh, g, scale, stream)
-                      : launch<64, false>(q, k, v, o, lse, bh, g, scale, stream);
-    if (D == 256)
-        return causal ? launch<256, true>(q, k, v, o, lse, bh, g, scale, stream)
-                      : launch<256, false>(q, k, v, o, lse, bh, g, scale, stream);
-    return causal ? launch<128, true>(q, k, v, o, lse, bh, g, scale, stream)
-                  : launch<128, false>(q, k, v, o, lse, bh, g, scale, stream);
+                        int sm_count, cudaStream_t stream) {
+    // 16 threads per row when 32-row CTAs would not give every SM one
+    const bool wide = (long long)((g.n + 31) / 32) * bh < (long long)sm_count;
+    if (D == 32) return launch_d<32>(wide, causal, q, k, v, o, lse, bh, g, scale, stream);
+    if (D == 64) return launch_d<64>(wide, causal, q, k, v, o, lse, bh, g, scale, stream);
+    if (D == 256) return launch_d<256>(wide, causal, q, k, v, o, lse, bh, g, scale, stream);
+    return launch_d<128>(wide, causal, q, k, v, o, lse, bh, g, scale, stream);
 }
 
 }  // namespace fa

@@ -97,6 +97,17 @@ def test_bf16_edge_shapes(N, D, causal):
     full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "bf16", "N=%d D=%d causal=%d" % (N, D, causal))
 
 
+# The fp32 kernel runs 32-row CTAs of 4 threads per row, or, when those would not give
+# every SM (152 on GB300) a CTA, 8-row CTAs of 16 threads per row.  Small shapes take the
+# second form; this one (4 x 8 slices x 10 row blocks = 320 CTAs) takes the first.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_fp32_narrow_cta_shape(D, causal):
+    q, k, v = make_shape(4, 8, 300, D, "fp32", seed=300 + D)
+    assert 4 * 8 * ((300 + 31) // 32) >= 152
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "fp32", "fp32 32-row CTAs D=%d causal=%d" % (D, causal))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("N", [1, 33, 200, 256, 300])
