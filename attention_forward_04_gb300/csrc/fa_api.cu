@@ -437,7 +437,7 @@ int backward(const BwdRequest& r) {
                                 static_cast<const float*>(r.o), static_cast<const float*>(r.dout),
                                 r.lse, static_cast<float*>(r.workspace), static_cast<float*>(r.dq),
                                 static_cast<float*>(r.dk), static_cast<float*>(r.dv), (int)BH, g,
-                                r.scale, static_cast<cudaStream_t>(r.stream));
+                                r.scale, di.sm_count, static_cast<cudaStream_t>(r.stream));
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "fp32 backward kernel launch");
     }
     const bool f16 = r.dtype == FA_FP16;

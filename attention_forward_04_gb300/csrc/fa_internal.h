@@ -107,10 +107,10 @@ cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, cons
                         int sm_count, cudaStream_t stream);
 
 // fp32 SIMT backward over the same layouts: dQ (which also writes delta, indexed like the
-// LSE) and then dK, dV, on `stream`.
+// LSE) and then dK, dV, on `stream`; sm_count picks the CTA shape.
 cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
                             const float* o, const float* dout, const float* lse, float* delta,
                             float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
-                            float scale, cudaStream_t stream);
+                            float scale, int sm_count, cudaStream_t stream);
 
 }  // namespace fa

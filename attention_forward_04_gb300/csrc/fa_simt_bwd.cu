@@ -11,9 +11,9 @@
 //   * dK, dV: one CTA per 32 key rows (16 at D = 256); it walks the query tiles with Q,
 //     dO, LSE and delta in shared memory.
 // CTA = 128 threads = 32 rows x 4 threads (16 rows x 8 threads at D = 256, which keeps 32
-// columns per thread and the shared tiles at 32 KB); thread t of a row owns head-dim
-// columns t, t+T, t+2T, ... (T threads per row); a dot product over D is the T partial sums
-// added with shuffles.  Layouts as the forward: [B, H, N, D], token-major [tokens, H, D],
+// columns per thread and the shared tiles at 32 KB), or 8 rows x 16 threads when those
+// CTAs would not give every SM one; thread t of a row owns head-dim columns t, t+T, t+2T,
+// ... (T threads per row); a dot product over D is the T partial sums added with shuffles.  Layouts as the forward: [B, H, N, D], token-major [tokens, H, D],
 // packed sequences.
 #include <cuda_runtime.h>
 
@@ -26,11 +26,17 @@ namespace {
 
 constexpr int kThreads = 128;
 
-// Rows per CTA (and per shared-memory tile) and threads per row.
-template <int D> struct Shape {
-    static constexpr int kTpr = D == 256 ? 8 : 4;
+// Threads per row, rows per CTA, columns per thread, and rows per streamed tile (the key
+// tiles of the dQ kernel, the query tiles of the dK/dV kernel; 16 at D = 256 so the two
+// shared tiles stay at 32 KB).  WIDE: 16 threads on 8 rows, for problems whose 32-row
+// (16 at D = 256) CTAs would not give every SM one; the next streamed tile is then fetched
+// into registers during the current tile's arithmetic.
+template <int D, bool WIDE> struct Shape {
+    static constexpr int kTpr = WIDE ? 16 : (D == 256 ? 8 : 4);
     static constexpr int kRows = kThreads / kTpr;
-    static constexpr int kCols = D / kTpr;   // columns per thread
+    static constexpr int kCols = D / kTpr;
+    static constexpr int kTile = D == 256 ? 16 : 32;
+    static constexpr int kLoads = kTile * D / 4 / kThreads;   // float4 per thread per tensor
 };
 
 // Length, element offset of row 0, row stride (elements) and LSE / delta index of row 0 of
@@ -67,29 +73,48 @@ __device__ __forceinline__ float row_sum(float x) {
     return x;
 }
 
-// Cooperative float4 copy of rows r0.. of a slice tensor into a [kRows][D] tile (rows at or
-// past len read as zero).
-template <int D>
-__device__ __forceinline__ void load_rows(float (*dst)[D], const float* __restrict__ src,
+// Two streamed [kTile][D] tiles of one slice (K and V, or Q and dO) through registers:
+// fetch() issues the float4 loads of rows r0.. (rows at or past len read as zero), stash()
+// writes them to shared memory.
+template <int D, bool WIDE>
+struct TilePair {
+    static constexpr int kTile = Shape<D, WIDE>::kTile, kLoads = Shape<D, WIDE>::kLoads;
+    float4 a[kLoads], b[kLoads];
+    __device__ __forceinline__ void fetch(const float* __restrict__ sa, const float* __restrict__ sb,
                                           const SimtSlice& s, int r0) {
-    constexpr int kRows = Shape<D>::kRows;
-    for (int idx = threadIdx.x; idx < kRows * D / 4; idx += kThreads) {
-        const int r = idx / (D / 4);
-        const int c = (idx % (D / 4)) * 4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r0 + r < s.len) x = *reinterpret_cast<const float4*>(src + s.base + (size_t)(r0 + r) * s.rs + c);
-        *reinterpret_cast<float4*>(&dst[r][c]) = x;
+#pragma unroll
+        for (int e = 0; e < kLoads; ++e) {
+            const int idx = (int)threadIdx.x + e * kThreads;
+            const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+            a[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+            b[e] = a[e];
+            if (r0 + r < s.len) {
+                const size_t off = s.base + (size_t)(r0 + r) * s.rs + c;
+                a[e] = *reinterpret_cast<const float4*>(sa + off);
+                b[e] = *reinterpret_cast<const float4*>(sb + off);
+            }
+        }
     }
-}
+    __device__ __forceinline__ void stash(float (*da)[D], float (*db)[D]) const {
+#pragma unroll
+        for (int e = 0; e < kLoads; ++e) {
+            const int idx = (int)threadIdx.x + e * kThreads;
+            const int r = idx / (D / 4), c = (idx % (D / 4)) * 4;
+            *reinterpret_cast<float4*>(&da[r][c]) = a[e];
+            *reinterpret_cast<float4*>(&db[r][c]) = b[e];
+        }
+    }
+};
 
-template <int D, bool CAUSAL>
+template <int D, bool WIDE, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const float* __restrict__ o, const float* __restrict__ dout, const float* __restrict__ lse,
     float* __restrict__ delta, float* __restrict__ dq, const SliceLayout g, float scale) {
-    constexpr int kRows = Shape<D>::kRows, TPR = Shape<D>::kTpr, DQ = Shape<D>::kCols;
-    __shared__ __align__(16) float Ks[kRows][D];
-    __shared__ __align__(16) float Vs[kRows][D];
+    using S = Shape<D, WIDE>;
+    constexpr int kRows = S::kRows, TPR = S::kTpr, DQ = S::kCols, kTile = S::kTile;
+    __shared__ __align__(16) float Ks[kTile][D];
+    __shared__ __align__(16) float Vs[kTile][D];
     const int nblk = (g.n + kRows - 1) / kRows;
     const int bh = (int)(blockIdx.x / (unsigned)nblk), blk = (int)(blockIdx.x % (unsigned)nblk);
     const SimtSlice s = simt_slice<D>(g, bh);
@@ -114,13 +139,16 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     const int kend = CAUSAL ? min(s.len, (blk + 1) * kRows) : s.len;
     const int limit = CAUSAL ? min(i + 1, s.len) : s.len;   // visible keys: j < limit
 
-    for (int k0 = 0; k0 < kend; k0 += kRows) {
+    TilePair<D, WIDE> kvt;
+    if (WIDE) kvt.fetch(k, v, s, 0);
+    for (int k0 = 0; k0 < kend; k0 += kTile) {
         __syncthreads();
-        load_rows<D>(Ks, k, s, k0);
-        load_rows<D>(Vs, v, s, k0);
+        if (!WIDE) kvt.fetch(k, v, s, k0);
+        kvt.stash(Ks, Vs);
         __syncthreads();
+        if (WIDE && k0 + kTile < kend) kvt.fetch(k, v, s, k0 + kTile);
 #pragma unroll 4
-        for (int c = 0; c < kRows; ++c) {
+        for (int c = 0; c < kTile; ++c) {
             float sp = 0.0f, dp = 0.0f;
 #pragma unroll
             for (int e = 0; e < DQ; ++e) {
@@ -141,16 +169,17 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool WIDE, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
     const float* __restrict__ dout, const float* __restrict__ lse,
     const float* __restrict__ delta, float* __restrict__ dk, float* __restrict__ dv,
     const SliceLayout g, float scale) {
-    constexpr int kRows = Shape<D>::kRows, TPR = Shape<D>::kTpr, DQ = Shape<D>::kCols;
-    __shared__ __align__(16) float Qs[kRows][D];
-    __shared__ __align__(16) float DOs[kRows][D];
-    __shared__ float Ls[kRows], Dl[kRows];
+    using S = Shape<D, WIDE>;
+    constexpr int kRows = S::kRows, TPR = S::kTpr, DQ = S::kCols, kTile = S::kTile;
+    __shared__ __align__(16) float Qs[kTile][D];
+    __shared__ __align__(16) float DOs[kTile][D];
+    __shared__ float Ls[kTile], Dl[kTile];
     const int nblk = (g.n + kRows - 1) / kRows;
     const int bh = (int)(blockIdx.x / (unsigned)nblk), blk = (int)(blockIdx.x % (unsigned)nblk);
     const SimtSlice s = simt_slice<D>(g, bh);
@@ -169,18 +198,37 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
         av[c] = 0.0f;
     }
     // queries before this block never see its keys under the causal mask
-    for (int q0 = CAUSAL ? blk * kRows : 0; q0 < s.len; q0 += kRows) {
+    const int qstart = CAUSAL ? blk * kRows : 0;
+    TilePair<D, WIDE> qt;
+    float lsv = 0.0f, dlv = 0.0f;   // LSE and delta of query q0 + threadIdx.x (threads < kTile)
+    auto fetch_vec = [&](int q0) {
+        const int qi = q0 + (int)threadIdx.x;
+        const bool ok = threadIdx.x < (unsigned)kTile && qi < s.len;
+        lsv = ok ? lse[s.vec0 + qi] : 0.0f;
+        dlv = ok ? delta[s.vec0 + qi] : 0.0f;
+    };
+    if (WIDE && qstart < s.len) {
+        qt.fetch(q, dout, s, qstart);
+        fetch_vec(qstart);
+    }
+    for (int q0 = qstart; q0 < s.len; q0 += kTile) {
         __syncthreads();
-        load_rows<D>(Qs, q, s, q0);
-        load_rows<D>(DOs, dout, s, q0);
-        if (threadIdx.x < kRows) {
-            const int qi = q0 + threadIdx.x;
-            Ls[threadIdx.x] = qi < s.len ? lse[s.vec0 + qi] : 0.0f;
-            Dl[threadIdx.x] = qi < s.len ? delta[s.vec0 + qi] : 0.0f;
+        if (!WIDE) {
+            qt.fetch(q, dout, s, q0);
+            fetch_vec(q0);
+        }
+        qt.stash(Qs, DOs);
+        if (threadIdx.x < kTile) {
+            Ls[threadIdx.x] = lsv;
+            Dl[threadIdx.x] = dlv;
         }
         __syncthreads();
+        if (WIDE && q0 + kTile < s.len) {
+            qt.fetch(q, dout, s, q0 + kTile);
+            fetch_vec(q0 + kTile);
+        }
 #pragma unroll 4
-        for (int c = 0; c < kRows; ++c) {
+        for (int c = 0; c < kTile; ++c) {
             float sp = 0.0f, dp = 0.0f;
 #pragma unroll
             for (int e = 0; e < DQ; ++e) {
@@ -209,28 +257,35 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool WIDE, bool CAUSAL>
 cudaError_t launch(const float* q, const float* k, const float* v, const float* o,
                    const float* dout, const float* lse, float* delta, float* dq, float* dk,
                    float* dv, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
-    constexpr int kRows = Shape<D>::kRows;
+    constexpr int kRows = Shape<D, WIDE>::kRows;
     const long long blocks = (long long)((g.n + kRows - 1) / kRows) * bh;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    simt_bwd_dq_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, o, dout, lse,
-                                                                           delta, dq, g, scale);
+    simt_bwd_dq_kernel<D, WIDE, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(
+        q, k, v, o, dout, lse, delta, dq, g, scale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    simt_bwd_dkdv_kernel<D, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(q, k, v, dout, lse,
-                                                                             delta, dk, dv, g, scale);
+    simt_bwd_dkdv_kernel<D, WIDE, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(
+        q, k, v, dout, lse, delta, dk, dv, g, scale);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(bool causal, const float* q, const float* k, const float* v, const float* o,
-                     const float* dout, const float* lse, float* delta, float* dq, float* dk,
-                     float* dv, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
-    return causal ? launch<D, true>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
-                  : launch<D, false>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+cudaError_t launch_d(bool causal, int sm_count, const float* q, const float* k, const float* v,
+                     const float* o, const float* dout, const float* lse, float* delta, float* dq,
+                     float* dk, float* dv, int bh, const SliceLayout& g, float scale,
+                     cudaStream_t stream) {
+    // 16 threads per row when the narrow CTAs would not give every SM one
+    constexpr int kNarrow = Shape<D, false>::kRows;
+    const bool wide = (long long)((g.n + kNarrow - 1) / kNarrow) * bh < (long long)sm_count;
+    if (wide)
+        return causal ? launch<D, true, true>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
+                      : launch<D, true, false>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    return causal ? launch<D, false, true>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
+                  : launch<D, false, false>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
 }
 
 }  // namespace
@@ -238,11 +293,11 @@ cudaError_t launch_d(bool causal, const float* q, const float* k, const float* v
 cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
                             const float* o, const float* dout, const float* lse, float* delta,
                             float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
-                            float scale, cudaStream_t stream) {
-    if (D == 32) return launch_d<32>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    if (D == 64) return launch_d<64>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    if (D == 256) return launch_d<256>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    return launch_d<128>(causal, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+                            float scale, int sm_count, cudaStream_t stream) {
+    if (D == 32) return launch_d<32>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    if (D == 64) return launch_d<64>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    if (D == 256) return launch_d<256>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    return launch_d<128>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
 }
 
 }  // namespace fa

@@ -125,6 +125,19 @@ def test_fp32_backward(N, D, causal):
                    "fp32 N=%d D=%d causal=%d" % (N, D, causal))
 
 
+# The fp32 backward runs 32-row CTAs (16 at D = 256) of 4 (8) threads per row, or 8-row
+# CTAs of 16 threads per row when those would not give every SM (152 on GB300) one; the
+# small shapes above take the second form, these (32 slices) the first.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 256])
+def test_fp32_backward_narrow_cta_shape(D, causal):
+    q, k, v = make_shape(4, 8, 200, D, "fp32", seed=200 + D)
+    do = make_shape_dout(4, 8, 200, D, "fp32", seed=200 + D)
+    assert 4 * 8 * ((200 + 31) // 32) >= 152
+    compare_slices(q, k, v, do, 1.0 / math.sqrt(D), causal, "fp32", [(0, 0), (1, 3), (3, 7)],
+                   "fp32 narrow CTAs D=%d causal=%d" % (D, causal))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [32, 64, 128])
 @pytest.mark.parametrize("N", [1, 200, 384])
