@@ -67,14 +67,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn(cudaError_t* err) {
 //   layout 0, [B*H, N, D]: dims {D, N, B*H}, box {64, rows, 1} (rows = 128, 64 for the
 //   D = 256 kernel, 32 for the forward's O stores); rows past N read as zero (and are not
 //   written by a store).
-//   D = 32: the box is 32 values wide and lands as 64-byte rows with the 64-byte swizzle.
+//   Shorter rows: the box is one whole row wide, 64-byte rows (D = 32 at 16 bits, D = 64
+//   at e4m3) with the 64-byte swizzle, 32-byte rows (D = 32 at e4m3) with the 32-byte one.
 //   layout 1, token-major [T, H, D]: dims {D, H, T}, box {64, 1, rows}; tokens past T read
 //   as zero (tokens of the next packed sequence are masked by the kernel instead).
 bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int64_t n, int64_t h,
                 int64_t t, int64_t d, int et, PFN_cuTensorMapEncodeTiled_v12000 fn,
                 cuuint32_t rows = 128) {
     // et: 0 bf16, 1 fp16, 2 fp8 e4m3 (raw bytes).  The box spans one panel: 128-byte rows
-    // (128-byte swizzle), or whole rows of 64 bytes (64-byte swizzle).
+    // (128-byte swizzle), or whole rows of 64 or 32 bytes (swizzle of the row width).
     const int64_t eb = et == 2 ? 1 : 2;
     const int64_t row_bytes = d * eb < 128 ? d * eb : 128;
     const cuuint32_t box0 = (cuuint32_t)(row_bytes / eb);
@@ -95,7 +96,9 @@ bool encode_map(CUtensorMap* map, const void* base, int layout, int64_t bh, int6
                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUresult r = fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    row_bytes < 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                    row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                      : CU_TENSOR_MAP_SWIZZLE_32B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -182,8 +185,8 @@ int forward(const Request& r) {
         if (!std::isfinite(r.descale[i]) || !(r.descale[i] > 0.0f)) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale * r.descale[0] * r.descale[1])) return FA_ERR_INVALID_ARG;
     if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
-    // fp8: D = 64, 128 or 256, [B, H, N, D] layout only
-    if (r.dtype == kFp8 && (r.D == 32 || r.layout != 0)) return FA_ERR_UNSUPPORTED;
+    // fp8: [B, H, N, D] layout only
+    if (r.dtype == kFp8 && r.layout != 0) return FA_ERR_UNSUPPORTED;
     const int64_t BH = r.B * r.H;
     const size_t esize = r.dtype == FA_FP32 ? 4 : r.dtype == kFp8 ? 1 : 2;   // Q, K, V
     const size_t osize = r.dtype == FA_FP32 ? 4 : 2;                          // O

@@ -72,7 +72,7 @@ int tc_units(int bh, int n, bool causal);
 int tc_smem_bytes(int D);
 
 // One-time per device: raise the dynamic shared-memory limit of the kernel instance.
-// et: element type of Q, K, V: 0 bf16, 1 fp16, 2 fp8 e4m3 (D = 64 or 128, layout 0 only).
+// et: element type of Q, K, V: 0 bf16, 1 fp16, 2 fp8 e4m3 (layout 0 only).
 cudaError_t tc_prepare(int D, bool causal, int et);
 
 // Launch the tensor-core kernel with `grid` persistent CTAs on `stream`.  single: one

@@ -79,8 +79,9 @@ __device__ unsigned int g_status[4];
 template <int D, int EB>
 struct Geo {
     // Shared-memory rows of D elements of EB bytes, split into panels of 128-byte rows
-    // (128-byte swizzle), or one panel of 64-byte rows (64-byte swizzle) when a whole row
-    // is 64 bytes (D = 32 at 16 bits, D = 64 at 8 bits).
+    // (128-byte swizzle), or one panel of whole rows when a row is shorter: 64 bytes
+    // (64-byte swizzle; D = 32 at 16 bits, D = 64 at 8 bits) or 32 bytes (32-byte swizzle;
+    // D = 32 at 8 bits).
     static constexpr int kRowBytesAll = D * EB;
     static constexpr int kRowBytes = kRowBytesAll < 128 ? kRowBytesAll : 128;
     static constexpr int kPanelCols = kRowBytes / EB;          // elements per panel row
@@ -293,11 +294,13 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, const Item& it, i
 
 // ----------------------------------------------------------------- MMA issue
 // Shared-memory descriptor of a tile with D-dependent rows: 128-byte swizzle (layout type
-// 2) for 128-byte rows, 64-byte swizzle (layout type 4) for the 64-byte rows of D = 32.
+// 2) for 128-byte rows, 64-byte swizzle (type 4) for 64-byte rows (D = 32 at 16 bits, D = 64
+// at e4m3), 32-byte swizzle (type 6) for the 32-byte rows of D = 32 at e4m3.
 template <int D, int EB>
 __device__ __forceinline__ uint64_t tile_desc(uint32_t saddr, uint32_t lbo) {
     using G = Geo<D, EB>;
-    const uint64_t layout = G::kRowBytes == 128 ? 2ull : 4ull;
+    static_assert(G::kRowBytes == 128 || G::kRowBytes == 64 || G::kRowBytes == 32, "row width");
+    const uint64_t layout = G::kRowBytes == 128 ? 2ull : G::kRowBytes == 64 ? 4ull : 6ull;
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((G::kSBO >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
 }
@@ -953,10 +956,7 @@ template <int D>
 cudaError_t dispatch(bool causal, int et, int mode, bool prepare, const TcParams* p, int grid,
                      cudaStream_t stream) {
     if (et == 1) return dispatch_et<D, 1>(causal, mode, prepare, p, grid, stream);
-    if (et == 2) {
-        if constexpr (D == 64 || D == 128) return dispatch_et<D, 2>(causal, mode, prepare, p, grid, stream);
-        return cudaErrorInvalidValue;
-    }
+    if (et == 2) return dispatch_et<D, 2>(causal, mode, prepare, p, grid, stream);
     return dispatch_et<D, 0>(causal, mode, prepare, p, grid, stream);
 }
 

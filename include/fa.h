@@ -113,7 +113,7 @@ int fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* l
  *   o       : device pointer, [B, H, N, D] contiguous bf16; written fully.
  *   lse     : device pointer, [B, H, N] fp32; written fully.
  *   B, H, N, scale, causal, stream : as for fa_fwd.
- *   D       : 64, 128 or 256.
+ *   D       : 32, 64, 128 or 256.
  *   q_descale, k_descale, v_descale : finite, > 0.
  *
  * Computes O = softmax(scale * (q_descale Q)(k_descale K)^T) (v_descale V) and its LSE:

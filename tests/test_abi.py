@@ -167,7 +167,7 @@ def fp8_call(lib, D=128, causal=0, qd=0.01, kd=0.01, vd=0.01, scale=0.1, **ptr):
     (dict(q=0), INVALID), (dict(lse=0), INVALID), (dict(causal=2), INVALID),
     (dict(qd=0.0), INVALID), (dict(kd=-1.0), INVALID), (dict(vd=float("nan")), INVALID),
     (dict(qd=float("inf")), INVALID), (dict(scale=float("nan")), INVALID),
-    (dict(D=32), UNSUPPORTED), (dict(D=96), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=512), UNSUPPORTED), (dict(D=16), UNSUPPORTED),
     (dict(o=BASE + SZ + 1024), INVALID),           # o overlaps k
     (dict(q=BASE + 8), MISALIGNED),
 ])

@@ -83,7 +83,7 @@ def compare(w, slices=None, what=""):
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
 @pytest.mark.parametrize("N", [1, 17, 128, 129, 300, 1000])
 def test_fp8_edge_shapes(N, D, causal):
     w = Workload("adhoc", 1, 2, N, D, "fp8", causal, N * 3 + D)
