@@ -45,3 +45,21 @@ def test_gpu_arm_fails_without_a_gpu():
     r = run_bench("--steps", "1", "--warmup", "3", "--cpu-budget", "0", timeout=120)
     assert r.returncode != 0
     assert not r.stdout.strip()                  # no bench line without the CUDA path
+
+
+def test_l2_handling_follows_input_set_size():
+    """Input sets larger than L2 alternate without a flush; smaller ones are flushed before
+    every timed call (the timing rule for inputs that fit in L2)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from attention_forward_04_gb300.inputs import WORKLOADS
+    head = WORKLOADS["bf16_b4h16n4096d128"]
+    assert bench.input_set_bytes(head) == 3 * 4 * 16 * 4096 * 128 * 2
+    assert bench.input_set_bytes(head, "bwd") == 5 * 4 * 16 * 4096 * 128 * 2 + 4 * 4 * 16 * 4096
+    assert bench.input_set_bytes(WORKLOADS["fp8_b4h16n4096d128"]) == 3 * 4 * 16 * 4096 * 128
+    assert bench.input_set_bytes(WORKLOADS["fp32_b1h1n256d64"]) == 3 * 256 * 64 * 4
+    assert "no flush" in bench.l2_note(bench.input_set_bytes(head))
+    for name in ("bf16_b2h8n1024d64", "fp32_b1h1n256d64", "fp8_b4h16n4096d128"):
+        assert "flushed before every timed call" in bench.l2_note(bench.input_set_bytes(WORKLOADS[name]))
+    assert bench.flush_buffer(torch, "cpu", bench.input_set_bytes(head)) is None
+    assert bench.L2_BYTES < bench.FLUSH_BYTES
