@@ -28,13 +28,17 @@
 //     multiplied by exp(m_old - m_new) when a larger maximum appears; keeping a stale
 //     reference is exact after the final division, since O and l share it).
 //   * epilogue: O / l (one division per row at the end, "第 13 课" exercise; "pwwt.cn"
-//     §2.2), staged per warp through shared memory so that every global store writes
-//     whole 128-byte lines; LSE = (m + log2 l) * ln 2.
+//     §2.2), staged per warp through shared memory in the 128-byte-swizzled layout, then
+//     written by one TMA bulk tensor store per 64-column panel ([B, H, N, D], D >= 64) or
+//     by row-contiguous stores of whole 128-byte lines (token-major layouts, D = 32);
+//     LSE = (m + log2 l) * ln 2.
 //   * item prologue: Q_A, then K_0, then Q_B are loaded, so S_A(0) starts as early as
 //     possible when a CTA moves to its next work item.
 //   * causal: key tiles entirely after a query tile are skipped, only the diagonal tile
 //     is masked ("08 · FlashAttention" §四 is_causal).  Work units pair a heavy and a
 //     light query-tile pair of the same slice, so every unit costs about the same.
+//   * small problems (all B*H*ceil(N/128) query tiles fit on the SMs at once, [B, H, N, D]):
+//     a separate instance gives every query tile a CTA of its own (tile B absent).
 //
 // Every mbarrier wait is bounded: a wait that runs past its limit raises a CTA-wide abort
 // flag and a device status word, every role then leaves its loop, in-flight copies and
