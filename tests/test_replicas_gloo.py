@@ -33,7 +33,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_whole_job_value():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()   # no fork of this multi-threaded process
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     for rank in range(world):
         ms, per_s = out[rank]
