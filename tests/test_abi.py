@@ -1,6 +1,5 @@
 """The C ABI without a GPU: the library builds and loads, exports every symbol that
 include/fa.h declares, and rejects bad arguments before any CUDA call."""
-import ctypes
 import os
 import re
 

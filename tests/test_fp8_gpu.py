@@ -12,7 +12,6 @@ its reference maximum is never smaller):
 (the last term covers fp32 score accumulation and ex2).  The test allows twice the bound
 plus 1e-5.  LSE is formed from fp32 sums and keeps the bf16 path's 1e-3.
 """
-import math
 
 import numpy as np
 import pytest

@@ -5,7 +5,6 @@ full oracle's values for the sampled rows.  Tolerances as in test_parity_gpu.py 
 2e-2 on O, 1e-3 on LSE).  N = 131072 is the 128K context the pages cite for O(N) memory
 ("08 · FlashAttention" §五): here 100 MB of inputs, never an N x N buffer.
 """
-import math
 
 import numpy as np
 import pytest
