@@ -9,6 +9,7 @@
 // serves; larger ones are refused before any CUDA call.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 #include <mutex>
 
@@ -24,12 +25,11 @@ constexpr int kMaxDevices = 64;
 // kernel reads it.
 static __device__ __align__(256) unsigned char g_bwd_scratch[kScratchBytes];
 
-struct ScratchSlot {
-    std::once_flag once;
-    cudaError_t err = cudaSuccess;
-    void* ptr = nullptr;
-};
-ScratchSlot g_scratch[kMaxDevices];
+// Per device: the array's address once a lookup has succeeded.  A failed lookup (for
+// instance an out-of-memory error while the driver loads the library's device code, or a
+// call made during stream capture) is not remembered, so a later call retries it.
+std::mutex g_scratch_mu;
+void* g_scratch[kMaxDevices] = {};
 
 // Checks shared by the three entry points, before any CUDA call: pointers, flags, D, and
 // the scratch the call needs (`need`, from fa_bwd_workspace_bytes for its layout).
@@ -40,7 +40,7 @@ int check_common(const void* const* ptrs, int64_t need, int64_t D, float scale, 
     if (need < 0) return FA_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    if (!(scale >= 0.0f) || scale > 3.4e38f) return FA_ERR_INVALID_ARG;   // NaN, inf, < 0
+    if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;   // as fa_bwd
     if (D != 32 && D != 64 && D != 128 && !(D == 256 && dtype == FA_FP32)) return FA_ERR_UNSUPPORTED;
     if (need > kScratchBytes) return FA_ERR_UNSUPPORTED;
     return FA_OK;
@@ -57,13 +57,17 @@ void* scratch(int* status) {
         *status = FA_ERR_UNSUPPORTED;
         return nullptr;
     }
-    ScratchSlot& s = g_scratch[dev];
-    std::call_once(s.once, [&] { s.err = cudaGetSymbolAddress(&s.ptr, g_bwd_scratch); });
-    if (s.err != cudaSuccess || !s.ptr) {
-        *status = FA_ERR_CUDA;
-        return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_bwd_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();   // leave no sticky error behind for the caller's next call
+            *status = FA_ERR_CUDA;
+            return nullptr;
+        }
+        g_scratch[dev] = ptr;
     }
-    return s.ptr;
+    return g_scratch[dev];
 }
 
 }  // namespace

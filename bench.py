@@ -581,6 +581,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of CPU oracle timing (0 skips the CPU leg)")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back calls for the sustained block (0 skips it)")
     ap.add_argument("--op", default="fwd", choices=["fwd", "bwd"],
                     help="fwd: the forward pass (default); bwd: the backward pass (fa_bwd)")
     args = ap.parse_args()
@@ -672,8 +674,6 @@ def main():
     t_wall1 = time.monotonic()
     if world > 1:
         dist.barrier()
-    time.sleep(0.15)
-    sampler.stop()
     st, detail = binding.check_device_status()
     if st != 0:
         raise RuntimeError("kernel watchdog in timed region: %d %s" % (st, detail))
@@ -683,6 +683,27 @@ def main():
     ms, per_s = aggregate_over_ranks(ms_local, flops_step, args.steps, world, reduce_max)
     value = per_s / 1e12
     per_launch_ms = ms_local / args.steps
+
+    # ---- sustained: seconds of back-to-back calls on the same inputs, with the clock samples
+    # that fall inside them (the K-step region above can be too short for the power cap to act)
+    sustained = None
+    if args.sustain_s > 0:
+        n_sus = max(args.steps, int(args.sustain_s * 1e3 / max(per_launch_ms, 1e-3)) + 1)
+        # small inputs are flushed from L2 before every call: bound the host-side work
+        n_sus = min(n_sus, 2000 if flush is not None else 200000)
+        time.sleep(0.25)
+        torch.cuda.synchronize()
+        t_sus0 = time.monotonic()
+        ms_sus = timed_calls(torch, stream, step, n_sus, flush)
+        t_sus1 = time.monotonic()
+        st, detail = binding.check_device_status()
+        if st != 0:
+            raise RuntimeError("kernel watchdog in sustained region: %d %s" % (st, detail))
+        sustained = {"steps": n_sus, "ms_per_step": ms_sus / n_sus,
+                     "value": flops_step / (ms_sus / n_sus / 1e3) / 1e12, "unit": "TFLOPS",
+                     "wall_s": t_sus1 - t_sus0}
+    time.sleep(0.15)
+    sampler.stop()
 
     # ---- end to end through the public API: pinned host inputs -> device -> fa.fwd -> host
     hq, hk, hv = (t.pin_memory() for t in host_set)
@@ -757,6 +778,24 @@ def main():
                    "sample": "failed: %s" % ex}
 
     clocks = sampler.summary(t_wall0, t_wall1)
+    if sustained is not None:
+        sc = sampler.summary(t_sus0, t_sus1)
+        sustained["clocks"] = sc
+        sus_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+        if w.dtype != "fp32":
+            ratio = 2.0 if fp8 else 1.0
+            sustained["frac_of_sustained_peak"] = sustained["value"] / (ratio * sus_peak)
+            sustained["sustained_peak_source"] = (
+                "%s bf16 dense sustained (MEASURED_PEAKS.json)%s"
+                % (peak_src, " x 2 (e4m3 : bf16 nominal dense ratio)" if fp8 else ""))
+            if sc.get("sm_mhz"):
+                # tensor rate per SM and clock: 8192 dense bf16/fp16 FLOP (128x128x16 product
+                # in 64 cycles, measured with a back-to-back tcgen05.mma microbenchmark), twice
+                # that for e4m3
+                sms = torch.cuda.get_device_properties(dev).multi_processor_count
+                clk_peak = sms * 8192 * ratio * sc["sm_mhz"] * 1e6 / 1e12
+                sustained["clock_normalised_peak"] = clk_peak
+                sustained["frac_of_clock_normalised_peak"] = sustained["value"] / clk_peak
     line = {
         "metric": "attention fwd TFLOPS (4*B*H*N^2*D/t)",
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -772,6 +811,9 @@ def main():
                               "device->host copies of consecutive steps overlap (two device "
                               "buffer sets)"},
         "gpu_launches": args.steps,
+        "timing": "value: the K timed steps back to back (a burst); sustained: the same "
+                  "calls for --sustain-s seconds",
+        "sustained": sustained,
         "roofline": roof,
         "cpu_baseline": cpu,
         "clocks": clocks,

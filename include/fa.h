@@ -204,8 +204,12 @@ int fa_bwd_varlen(const void* q, const void* k, const void* v, const void* o, co
  *          any CUDA call.
  *   Allocation: none, by this call or anything it calls.
  *   Set-up: the first call on each device looks up that device's copy of the array
- *          (cudaGetSymbolAddress) and keeps the address; make that first call before any
- *          stream capture begins on the device.
+ *          (cudaGetSymbolAddress) and keeps the address.  That first call may make the
+ *          driver load the library's device code on the device, which itself needs device
+ *          memory (the 4 MiB array among it), so make it early: before a memory pool takes
+ *          all free HBM, and before any stream capture begins on the device.  A lookup that
+ *          fails returns FA_ERR_CUDA and is retried by the next call.
+ *   Scale:  any finite scale >= 0, as fa_bwd.
  *   Concurrency: every call on one device uses the same array.  Two calls whose work can
  *          overlap on the device (different streams not ordered by events, or two host
  *          threads' streams) race on it and give wrong results; order them on one stream.

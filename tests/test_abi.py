@@ -211,3 +211,34 @@ def test_bwd_layout_variants_argument_checks(lib):
 
 def test_version_reports_layout_backward(lib):
     assert lib.fa_version() >= 140
+
+
+def header_text():
+    return re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+
+
+def test_boundary_signatures():
+    """fa_fwd keeps the shape of the boundary; two recorded details differ from a
+    cudaStream_t signature: every stream is a void* (the header includes no CUDA header),
+    and fa_check_device_status adds an optional out-parameter for the status detail."""
+    text = " ".join(header_text().split())
+    assert ("int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, "
+            "int64_t B, int64_t H, int64_t N, int64_t D, float scale, int causal, int dtype, "
+            "void* stream);") in text
+    assert "int fa_check_device_status(void* stream, uint32_t* detail);" in text
+    assert "const char* fa_status_string(int status);" in text
+    streams = re.findall(r"([\w*]+\s*\**)\s*stream\s*[,)]", text)
+    assert streams and all(s.replace(" ", "") == "void*" for s in streams), streams
+    assert not re.search(r"#include\s*<cuda", open(HEADER).read())
+
+
+def test_noalloc_scale_check_matches_backward(lib):
+    """The no-alloc backward accepts every finite scale >= 0, as fa_bwd does: a huge finite
+    scale passes the scale check and the call is refused later, for its head dimension."""
+    a = [BASE + i * SZ for i in range(9)]
+    def call(scale, D=96):
+        return lib.fa_bwd_noalloc(*a, 1, 2, 300, D, scale, 0, 1, None)
+    assert call(3.4028234663852886e38) == UNSUPPORTED
+    assert bwd_call(lib, scale=3.4028234663852886e38, D=96) == UNSUPPORTED
+    for bad in (float("inf"), float("nan"), -1.0):
+        assert call(bad) == INVALID

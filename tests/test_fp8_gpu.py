@@ -36,18 +36,18 @@ def deq(x8, ds):
     return x8.to(torch.float64).numpy() * float(ds)
 
 
-def bound(q, k, v8, vd, scale, causal, o_ref, lse_ref):
-    """Element-wise error bound (module docstring) for one [N, D] slice."""
+def bound(q, k, v8, vd, scale, causal, o_ref, lse_ref, rows=None):
+    """Element-wise error bound (module docstring) for the rows `rows` (default: all) of one
+    [N, D] slice; o_ref and lse_ref hold the oracle's values of those rows."""
     N = q.shape[0]
-    S = scale * (q @ k.T)
-    P = np.exp(S - lse_ref[:, None])
-    if causal:
-        P = np.where(np.tril(np.ones((N, N), dtype=bool)), P, 0.0)
-    m = np.where(np.tril(np.ones((N, N), dtype=bool)) | (not causal), S, -np.inf).max(1)
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    S = scale * (q[rows] @ k.T)
+    vis = (np.arange(N)[None, :] <= rows[:, None]) if causal else np.ones((rows.size, N), dtype=bool)
+    P = np.where(vis, np.exp(S - lse_ref[:, None]), 0.0)
+    m = np.where(vis, S, -np.inf).max(1)
     l = np.exp(lse_ref - m)              # row sum relative to the row maximum (>= 1)
     av = np.abs(v8)
-    vis = np.tril(np.ones((N, N))) if causal else np.ones((N, N))
-    t = vd * (2.0 ** -4 * (P @ av) + 2.0 ** -10 * (vis @ av) / l[:, None])
+    t = vd * (2.0 ** -4 * (P @ av) + 2.0 ** -10 * (vis.astype(np.float64) @ av) / l[:, None])
     t += 2.0 ** -8 * np.abs(o_ref) + 1e-4 * (P @ (vd * av))
     return 2.0 * t + 1e-5
 
@@ -94,15 +94,6 @@ def test_fp8_large_scores_force_rescales(D):
     for causal in (False, True):
         w = Workload("adhoc", 1, 2, 700, D, "fp8", causal, 91, qk_mult=4.0)
         compare(w, what="fp8 x4 D=%d causal=%d" % (D, causal))
-
-
-@pytest.mark.parametrize("name", ["fp8_b4h16n4096d128", "fp8_b8h32n4096d128_causal",
-                                  "fp8_b8h16n4096d64", "fp8_b4h8n4096d256",
-                                  "fp8_b4h8n4096d256_causal"])
-def test_fp8_full_size_sampled_slices(name):
-    w = WORKLOADS[name]
-    BH = w.B * w.H
-    compare(w, slices=[0, BH // 2 + 1, BH - 1], what=name)
 
 
 def test_fp8_rejects_bad_arguments():
