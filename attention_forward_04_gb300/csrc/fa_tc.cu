@@ -23,7 +23,9 @@
 //     row).  Running max m and sum l stay in registers; exp2 with scale*log2(e) folded
 //     into one FMA; P is rounded to the input type and stored into TMEM (over S, or into
 //     its own columns).
-//     The max is only raised when it grows by more than 2^16 (2^8 for fp16), and only then
+//     bf16: the reference max is raised whenever a tile's max exceeds it, so the largest P
+//     of a row is exactly 1 and its bf16 rounding costs nothing; fp16 / e4m3: it is raised
+//     only when it grows by more than 2^8 (finer P rounding leaves room), and only then
 //     is O rescaled in TMEM ("08 · FlashAttention" §五 and "第 13 课" §4B: old output
 //     multiplied by exp(m_old - m_new) when a larger maximum appears; keeping a stale
 //     reference is exact after the final division, since O and l share it).
@@ -66,12 +68,14 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-// The running reference is raised only when a tile max exceeds it by more than this many
-// log2 units, so stored P values stay below 2^kRescaleLog2: 16 for bf16 P (exponent range
-// of fp32), 8 for fp16 P (largest fp16 is 65504).
+// The running reference is raised when a tile max exceeds it by more than this many log2
+// units.  bf16: 0, the literal reading, so the row's largest P is exactly 1: a stale
+// reference would leave it at 2^x for fractional x, and its bf16 rounding (2^-9 relative)
+// times a large |v|, added to the bf16 rounding of O, can pass 2e-2 on strongly peaked rows.
+// fp16 P (11 significant bits, largest value 65504) and e4m3 P (tops out at 448): 8, so
+// stored P stays below 2^8.
 // Element type of Q, K, V (and P): 0 = bf16, 1 = fp16, 2 = fp8 e4m3 (O is then bf16).
-// e4m3 P tops out at 448, so its reference is raised by 2^8 as for fp16.
-template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 16.0f : 8.0f; };
+template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 0.0f : 8.0f; };
 template <int ET> struct Elem {
     static constexpr int kBytes = ET == 2 ? 1 : 2;
 };
@@ -594,23 +598,23 @@ out:
         if (q_issued[t] > 0) wait_drain(bar_addr(c, b_q_full<D, EB>(t)), (q_issued[t] - 1u) & 1u, c.limit);
 }
 
-// Row maximum of the raw scores of one 128-key tile; invisible keys (kbase + c >= limit)
-// are left out.
-template <bool MASK>
-__device__ __forceinline__ float tile_row_max(const uint32_t (&s)[128], int kbase, int limit) {
+// Row maximum of the raw scores of NS keys (a 128-key tile, or one 64-key half of it);
+// invisible keys (kbase + c >= limit) are left out.
+template <bool MASK, int NS>
+__device__ __forceinline__ float tile_row_max(const uint32_t (&s)[NS], int kbase, int limit) {
     float mx[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
     if (MASK) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < NS; ++c) {
             const float x = (kbase + c < limit) ? u2f(s[c]) : -INFINITY;
             mx[c & 7] = fmaxf(mx[c & 7], x);
         }
     } else {
         // eight independent chains keep the dependent depth short
 #pragma unroll
-        for (int c = 0; c < 128; c += 2)
+        for (int c = 0; c < NS; c += 2)
             mx[(c >> 1) & 7] = ptx::max3(mx[(c >> 1) & 7], u2f(s[c]), u2f(s[c + 1]));
     }
     return fmaxf(ptx::max3(mx[0], mx[1], mx[2]), fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
@@ -619,10 +623,11 @@ __device__ __forceinline__ float tile_row_max(const uint32_t (&s)[128], int kbas
 // p = 2^(s * sl2 - m) for columns [C0, C0 + 64), partial row sums into acc (four fp32
 // pairs), and P packed for TMEM: 16-bit pairs into pk[C0/2 ...], or for e4m3 four values
 // per word into pk[C0/4 ...].  Invisible keys give p = 0.
-template <int C0, bool MASK, int ET>
-__device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[128], int kbase, int limit,
+template <int C0, bool MASK, int ET, int NS, int NP>
+__device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[NS], int kbase, int limit,
                                               float sl2, float neg_m, float (&acc)[8],
-                                              uint32_t (&pk)[64]) {
+                                              uint32_t (&pk)[NP]) {
+    static_assert(C0 + 64 <= NS && (ET == 2 ? (C0 + 64) / 4 : (C0 + 64) / 2) <= NP, "ranges");
 #pragma unroll
     for (int c = C0; c < C0 + 64; c += 4) {
         float x[4], pr[4];
@@ -645,8 +650,32 @@ __device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[128], int kbas
     }
 }
 
-// One 128-key tile of one row: running-max update (raised only when the tile max exceeds
-// it by more than 2^kRescaleLog2), exp2, row sum, and P stored into TMEM at tP in two
+// One row of O (NC fp32 columns from TMEM address tO0) times alpha, in place, CH columns
+// per TMEM load and store, packed multiplies in between.  Larger chunks mean fewer serial
+// TMEM round trips; CH is as large as the instance's registers allow without spills (the
+// S and P registers are free once P is stored).
+template <int NC, int CH>
+__device__ __forceinline__ void rescale_o(uint32_t tO0, float alpha) {
+    static_assert(NC % CH == 0, "chunks");
+#pragma unroll 1
+    for (int cc = 0; cc < NC / CH; ++cc) {
+        const uint32_t tO = tO0 + (uint32_t)(cc * CH);
+        uint32_t o[CH];
+        if constexpr (CH == 128) ptx::tmem_ld128_wait(tO, o);
+        else if constexpr (CH == 64) ptx::tmem_ld64_wait(tO, o);
+        else if constexpr (CH == 32) ptx::tmem_ld32_wait(tO, o);
+        else ptx::tmem_ld16_wait(tO, o);
+#pragma unroll
+        for (int i = 0; i < CH; i += 2) ptx::mul2u(o[i], o[i + 1], alpha);
+        if constexpr (CH == 128) ptx::tmem_st128(tO, o);
+        else if constexpr (CH == 64) ptx::tmem_st64(tO, o);
+        else if constexpr (CH == 32) ptx::tmem_st32(tO, o);
+        else ptx::tmem_st16(tO, o);
+    }
+}
+
+// One 128-key tile of one row: running-max update (raised when the tile max exceeds it by
+// more than kRescaleLog2 log2 units), exp2, row sum, and P stored into TMEM at tP in two
 // halves (64 columns of 16-bit pairs, or 32 columns of e4m3 quadruples).  before_store()
 // runs once, after the first half is computed and before anything is stored; false from
 // it abandons the tile (returns false).  alpha receives the O rescale factor.
@@ -655,7 +684,7 @@ __device__ __forceinline__ bool softmax_tile(const uint32_t (&s)[128], int kbase
                                              float sl2, float& m_run, float& l_run,
                                              uint32_t tP, float& alpha,
                                              BeforeStore&& before_store) {
-    const float mt = tile_row_max<MASK>(s, kbase, limit) * sl2;  // log2 units
+    const float mt = tile_row_max<MASK, 128>(s, kbase, limit) * sl2;  // log2 units
     alpha = 1.0f;
     if (mt > m_run + Lazy<ET>::kRescaleLog2) {
         alpha = ptx::ex2(m_run - mt);   // m_run = -inf on the first tile: alpha = 0
@@ -691,7 +720,6 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
     const uint32_t tP = tmem + tl + G::col_p(t);
     const uint32_t tO = tmem + tl + G::col_o(t);
     uint32_t s_cnt = 0, o_cnt = 0;
-    if (MODE == 2 && t == 1) return;   // tile B is absent in the single-tile schedule
 
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
         const int nsub = unit_count<CAUSAL, MODE>(p, u);
@@ -734,17 +762,8 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                     mask ? softmax_tile<true, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, alpha, before_store)
                          : softmax_tile<false, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, alpha, before_store);
                 if (!ok) return;
-                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                    // The running max rose: rescale this row of O by alpha in TMEM.
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32_wait(tO + (uint32_t)cc * 32u, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(u2f(o[i]) * alpha);
-                        ptx::tmem_st32(tO + (uint32_t)cc * 32u, o);
-                    }
-                }
+                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f))
+                    rescale_o<D, D == 128 ? 64 : 32>(tO, alpha);   // the running max rose: this row of O times alpha
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 ptx::mbar_arrive(bar_addr(c, b_p_full<D, EB>(t)));
@@ -844,6 +863,198 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
     }
 }
 
+// ----------------------------------------------------------------- single-tile schedule
+// Named barrier 1 + q over the two softmax warps that share TMEM lane quarter q (warps q and
+// q + 4), ANDing a predicate.  A warp whose wait gave up still arrives here with false, so
+// the pair takes one stop decision and neither warp is left at a barrier the other skips.
+__device__ __forceinline__ bool pair_barrier_and(int q, bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, x;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred x, %2, 64, p;\n\t"
+        "selp.u32 %0, 1, 0, x;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "r"(1 + q)
+        : "memory");
+    return r != 0;
+}
+// The same barrier without a predicate, where neither warp can have given up.
+__device__ __forceinline__ void pair_barrier(int q) {
+    asm volatile("bar.sync %0, 64;" ::"r"(1 + q) : "memory");
+}
+
+// Softmax and epilogue of the single-tile schedule (MODE 2), where tile B is absent.  Its
+// four warps would idle, so every row of tile A is shared by the two warps of its TMEM lane
+// quarter: warp q + 4h (h = 0, 1) takes keys [64h, 64h + 64) of each 128-key tile and O
+// columns [h D/2, h D/2 + D/2).  Per tile the two partial row maxima meet in shared memory
+// (the unused Q_B buffer) at one barrier, so both warps take the same lazy-rescale decision
+// and keep the same running reference; each keeps the row sum of its own keys, and the two
+// sums are added once, in the epilogue.  Each warp's serial work per key tile halves.
+template <int D, bool CAUSAL, int ET>
+__device__ void softmax_role_split(const TcParams& p, const Ctl& c, uint32_t tmem, float* xch,
+                                   uint32_t stage_base, int warp, int lane) {
+    constexpr int EB = Elem<ET>::kBytes;
+    constexpr bool kOutF16 = ET == 1;   // O storage: fp16, else bf16
+    constexpr int kHalfO = D / 2;       // O columns of one warp
+    using G = Geo<D, EB>;
+    const int h = warp / 4;             // key half and O half
+    const int q4 = warp % 4;            // TMEM lane quarter, shared by warps q4 and q4 + 4
+    const int lane_base = q4 * 32;
+    const int r128 = lane_base + lane;  // row within the tile
+    const uint32_t tl = (uint32_t)lane_base << 16;
+    const uint32_t tS = tmem + tl + G::col_s(0) + (uint32_t)(64 * h);
+    const uint32_t tP = tmem + tl + G::col_p(0) + (uint32_t)h * (G::kPCols / 2);
+    const uint32_t tO = tmem + tl + G::col_o(0) + (uint32_t)(kHalfO * h);
+    // exchange area: partial maxima xm[step parity][half][row], then row sums xl[half][row]
+    float* xl = xch + 512;
+    uint32_t s_cnt = 0, o_cnt = 0;
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        const Item it = unit_item<CAUSAL, 2>(p, u, 0);
+        const int n = it.nA;
+        const int row = it.pair * 2 * kBM + it.sw * kBM + r128;
+        const int limit = CAUSAL ? min(row + 1, p.n) : p.n;   // visible keys: j < limit
+        float m_run = -INFINITY, l_half = 0.0f;
+        bool live = true;
+
+        for (int j = 0; j < n; ++j) {
+            bool ok = live && wait_warp(c, b_s_full<D, EB>(0), s_cnt & 1u, kRoleSoftmax);
+            ++s_cnt;
+            if (ok && !G::kSepP && j > 0) {   // O += P(j-1) V(j-1) is complete before S(j) is
+                ok = wait_warp(c, b_o_done<D, EB>(0), o_cnt & 1u, kRoleSoftmax);
+                ++o_cnt;
+            }
+            const int kbase = j * kBN + 64 * h;
+            const bool mask = __any_sync(0xFFFFFFFFu, kbase + 64 > limit);
+            uint32_t s[64];
+            if (ok) {
+                ptx::tc_fence_after();
+                ptx::tmem_ld64_wait(tS, s);
+                if constexpr (G::kSepP) {   // S may now be overwritten by the next S product
+                    ptx::tc_fence_before();
+                    ptx::mbar_arrive(bar_addr(c, b_s_read<D, EB>(0)));
+                }
+                xch[((j & 1) * 2 + h) * 128 + r128] =
+                    mask ? tile_row_max<true, 64>(s, kbase, limit) : tile_row_max<false, 64>(s, kbase, limit);
+            }
+            // Both warps' S loads are complete before either stores P (over S at D = 128).
+            ptx::tc_fence_before();
+            if (!pair_barrier_and(q4, ok)) return;
+            ptx::tc_fence_after();
+            const float mt = fmaxf(xch[((j & 1) * 2) * 128 + r128],
+                                   xch[((j & 1) * 2 + 1) * 128 + r128]) * p.scale_log2;
+            float alpha = 1.0f;
+            if (mt > m_run + Lazy<ET>::kRescaleLog2) {
+                alpha = ptx::ex2(m_run - mt);   // m_run = -inf on the first tile: alpha = 0
+                m_run = mt;
+            }
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[32];
+            if (mask) tile_exp_half<0, true, ET>(s, kbase, limit, p.scale_log2, -m_run, acc, pk);
+            else tile_exp_half<0, false, ET>(s, kbase, limit, p.scale_log2, -m_run, acc, pk);
+            // With separate P columns, O += P(j-1) V(j-1) must be complete before P is
+            // overwritten and before O is rescaled.
+            if (G::kSepP && j > 0) {
+                live = wait_warp(c, b_o_done<D, EB>(0), o_cnt & 1u, kRoleSoftmax);
+                ++o_cnt;
+                if (!live) continue;   // the next barrier ends both warps
+                ptx::tc_fence_after();
+            }
+            __syncwarp();
+            if constexpr (ET == 2) ptx::tmem_st16(tP, &pk[0]);
+            else ptx::tmem_st32p(tP, &pk[0]);
+            const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            l_half = l_half * alpha + sum;
+            if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f))
+                rescale_o<kHalfO, kHalfO>(tO, alpha);   // the running max rose: this warp's half of the O row
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(c, b_p_full<D, EB>(0)));
+        }
+
+        // Epilogue: the last O += P V, then the two halves' row sums meet.
+        bool ok = live && wait_warp(c, b_o_done<D, EB>(0), o_cnt & 1u, kRoleSoftmax);
+        ++o_cnt;
+        xl[h * 128 + r128] = l_half;
+        // At D = 64 both warps stage into warp q4's slot: its last bulk store has read it.
+        if (OStore<D, 2>::kTma && D == 64 && h == 0 && lane == 0) bulk_wait_read_all();
+        if (!pair_barrier_and(q4, ok)) return;
+        ptx::tc_fence_after();
+        const float l_run = xl[r128] + xl[128 + r128];
+        const float inv_l = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
+        const int row0 = it.pair * 2 * kBM + it.sw * kBM + lane_base;   // first row of the pair
+        if constexpr (D == 128) {
+            // one 64-column panel per warp, through the warp's own slot and one bulk store
+            const uint32_t stage = stage_base + (uint32_t)(warp * G::kStageSlot);
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t o[32];
+                ptx::tmem_ld32_wait(tO + (uint32_t)(hh * 32), o);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    w[i] = pack2<kOutF16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t chunk = (uint32_t)(hh * 4 + i) ^ (uint32_t)(lane & 7);
+                    ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
+                                      w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0 && row0 < p.n) {
+                tma_store_3d(&p.tmap_o, stage, h * 64, row0, it.bh);
+                bulk_commit();
+            }
+        } else {
+            // D = 64: one panel, each warp stages its 32 columns (16-byte chunks 4h..4h+3);
+            // D = 32: one 64-byte row, each warp stages its 16 columns (chunks 2h, 2h+1).
+            const uint32_t stage = stage_base + (uint32_t)(q4 * G::kStageSlot);
+            constexpr int kChunks = kHalfO / 8;   // 16-byte chunks of this warp's columns
+            uint32_t o[kHalfO];
+            if constexpr (kHalfO == 32) ptx::tmem_ld32_wait(tO, o);
+            else ptx::tmem_ld16_wait(tO, o);
+            uint32_t w[kHalfO / 2];
+#pragma unroll
+            for (int i = 0; i < kHalfO / 2; ++i)
+                w[i] = pack2<kOutF16>(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+#pragma unroll
+            for (int i = 0; i < kChunks; ++i) {
+                const uint32_t chunk = (uint32_t)(h * kChunks + i) ^ (uint32_t)(lane & 7);
+                ptx::st_shared_v4(stage + (uint32_t)lane * 128u + chunk * 16u, w[4 * i],
+                                  w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
+            if constexpr (OStore<D, 2>::kTma) fence_async_shared();
+            pair_barrier(q4);   // both halves of every row are staged
+            if constexpr (OStore<D, 2>::kTma) {
+                if (h == 0 && lane == 0 && row0 < p.n) {
+                    tma_store_3d(&p.tmap_o, stage, 0, row0, it.bh);
+                    bulk_commit();
+                }
+            } else {
+                // 64-byte rows: 8 rows x 4 chunks per store instruction, two of the four
+                // row groups per warp
+                uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) + (size_t)it.bh * (size_t)p.n * D;
+#pragma unroll
+                for (int k = 2 * h; k < 2 * h + 2; ++k) {
+                    const int r = 8 * k + (lane >> 2);   // row within the warp's 32
+                    const int ch = lane & 3;             // 16-byte chunk within the 64-byte row
+                    const uint4 v = ptx::ld_shared_v4(stage + (uint32_t)r * 128u +
+                                                      (uint32_t)((ch ^ (r & 7)) * 16));
+                    if (row0 + r < p.n)
+                        *reinterpret_cast<uint4*>(obase + (size_t)(row0 + r) * D + ch * 8) = v;
+                }
+            }
+        }
+        if (h == 0 && row < p.n) p.lse[(size_t)it.bh * (size_t)p.n + (size_t)row] = (m_run + log2f(l_run)) * kLn2;
+        __syncwarp();
+    }
+}
+
 template <int D, bool CAUSAL, int ET, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constant__ TcParams p) {
     constexpr int EB = Elem<ET>::kBytes;
@@ -868,9 +1079,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
             ptx::mbar_init(bar_addr(c, b_q_full<D, EB>(t)), 1);
             ptx::mbar_init(bar_addr(c, b_q_empty<D, EB>(t)), 1);
             ptx::mbar_init(bar_addr(c, b_s_full<D, EB>(t)), 1);
-            ptx::mbar_init(bar_addr(c, b_p_full<D, EB>(t)), 128);
+            // the single-tile schedule's tile A is served by all eight softmax warps
+            const uint32_t softmax_threads = (MODE == 2 && t == 0) ? 256u : 128u;
+            ptx::mbar_init(bar_addr(c, b_p_full<D, EB>(t)), softmax_threads);
             ptx::mbar_init(bar_addr(c, b_o_done<D, EB>(t)), 1);
-            ptx::mbar_init(bar_addr(c, b_s_read<D, EB>(t)), 128);
+            ptx::mbar_init(bar_addr(c, b_s_read<D, EB>(t)), softmax_threads);
         }
         for (int s = 0; s < G::kSlots; ++s) {
             ptx::mbar_init(bar_addr(c, b_kv_full<D, EB>(s)), 1);
@@ -896,8 +1109,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_slot;
 
     if (warp < kSoftmaxWarps) {
-        softmax_role<D, CAUSAL, ET, MODE>(p, c, tmem, warp, lane,
-                                     sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
+        if constexpr (MODE == 2)   // the exchange area is the unused Q_B buffer
+            softmax_role_split<D, CAUSAL, ET>(p, c, tmem, reinterpret_cast<float*>(smem + G::kTileBytes),
+                                              sbase + (uint32_t)G::kStageOff, warp, lane);
+        else
+            softmax_role<D, CAUSAL, ET, MODE>(p, c, tmem, warp, lane,
+                                              sbase + (uint32_t)G::kStageOff + (uint32_t)(warp * G::kStageSlot));
         if constexpr (OStore<D, MODE>::kTma) {   // this warp's O stores complete before exit
             if (lane == 0) bulk_wait_all();
             __syncwarp();

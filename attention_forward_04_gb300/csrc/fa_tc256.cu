@@ -65,7 +65,10 @@ __device__ __forceinline__ uint32_t ring_par(uint32_t pos) { return (pos / kSlot
 // Streamed tiles of an item, from its first ring position: 0 and 1 are the two 64-row
 // halves of the Q tile, then K_j = 2 + 2j and V_j = 3 + 2j.
 
-template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 16.0f : 8.0f; };
+// The reference is raised when a step's maximum exceeds it by more than kRescaleLog2 log2
+// units: bf16 0 (the literal reading: the row's largest P is exactly 1, so its bf16
+// rounding costs nothing), fp16 and e4m3 8 (P stays below 2^8).
+template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 0.0f : 8.0f; };
 
 // Per element type: bytes per value, 128-byte panels per 256-value row, bytes of a tile.
 template <int ET> struct Elem {
@@ -98,8 +101,8 @@ __device__ __forceinline__ bool sm_barrier_and(bool ok) {
     return r != 0;
 }
 
-// One 64-key step of one row: running-max update (raised only when the step's maximum
-// exceeds it by more than 2^kRescaleLog2), p = 2^(s * sl2 - m), row sum (of the fp32
+// One 64-key step of one row: running-max update (raised when the step's maximum exceeds
+// it by more than kRescaleLog2 log2 units), p = 2^(s * sl2 - m), row sum (of the fp32
 // values), and P packed to 16-bit pairs in pk[0, 32), or to e4m3 quadruples in pk[0, 16).
 // Keys at or past `limit` count as absent (MASK).  Eight independent max chains and four
 // paired sum chains keep the dependent depth short.  Returns the factor

@@ -39,6 +39,7 @@ _CSRC = os.path.join(ROOT, "attention_forward_04_gb300", "csrc")
 # sources whose change invalidates a stored traffic capture
 KERNEL_SRCS = {"fwd": [os.path.join(_CSRC, f) for f in ("fa_tc.cu", "tc_common.cuh", "ptx.cuh")],
                "fwd256": [os.path.join(_CSRC, f) for f in ("fa_tc256.cu", "tc_common.cuh", "ptx.cuh")],
+               "simt": [os.path.join(_CSRC, "fa_simt.cu")],
                "bwd": [os.path.join(_CSRC, f) for f in ("fa_bwd.cu", "tc_common.cuh", "ptx.cuh")]}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
@@ -740,7 +741,7 @@ def main():
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops_step / (per_launch_ms / 1e3) / 1e12
-    traffic = load_traffic(w.name, "fwd256" if w.D == 256 else "fwd")
+    traffic = load_traffic(w.name, "simt" if w.dtype == "fp32" else "fwd256" if w.D == 256 else "fwd")
     if w.dtype == "fp32":
         # fp32 FFMA peak: SMs x 128 fp32 lanes x 2 FLOP x max SM clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -217,3 +217,38 @@ def test_d256_large_scores_force_rescales():
     q, k, v = make_shape(1, 2, 1000, 256, "bf16", seed=77, qk_mult=4.0)
     for causal in (False, True):
         full_compare(q, k, v, 1.0 / 16.0, causal, "bf16", "D=256 x4 causal=%d" % causal)
+
+
+# ------------------------------------------------------------ a dominant key per row
+# Every row has one dominant key with a large value (7.96875): whether the row's largest P is
+# exactly 1 (a fresh reference) or 2^x for fractional x (a stale one) decides whether bf16
+# stays inside 2e-2 (test_rescale_reading.py: 0.014 against 0.046).  Through every kernel:
+# one slice (single-tile schedules), 160 slices (the paired schedule where it applies), the
+# token-major layout, and head dimensions 32 to 256.
+def dominant_key_inputs(B, H, D, dtype):
+    from test_rescale_reading import dominant_key_slice
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
+    return tuple(torch.from_numpy(x).to(dt).expand(B, H, *x.shape).contiguous()
+                 for x in dominant_key_slice(D))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+@pytest.mark.parametrize("BH", [(1, 1), (8, 20)])
+def test_dominant_key_rows(BH, D, dtype, causal):
+    q, k, v = dominant_key_inputs(*BH, D, dtype)
+    full_compare(q, k, v, 1.0, causal, dtype, "dominant key B,H=%s D=%d %s causal=%d" % (BH, D, dtype, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [32, 64, 128, 256])
+def test_dominant_key_rows_token_major(D, causal):
+    q, k, v = (t.permute(0, 2, 1, 3).contiguous() for t in dominant_key_inputs(2, 3, D, "bf16"))
+    o, lse = binding.fwd_bnhd(q.cuda(), k.cuda(), v.cuda(), scale=1.0, causal=causal)
+    torch.cuda.synchronize()
+    assert binding.check_device_status()[0] == 0
+    to_bhnd = lambda t: t.permute(0, 2, 1, 3).double().numpy()  # noqa: E731
+    o_ref, lse_ref = oracle.attention_fwd(to_bhnd(q), to_bhnd(k), to_bhnd(v), 1.0, causal)
+    assert_close(o.permute(0, 2, 1, 3).double().cpu().numpy(), lse.double().cpu().numpy(), o_ref,
+                 lse_ref, "bf16", "dominant key token-major D=%d causal=%d" % (D, causal))

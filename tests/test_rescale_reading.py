@@ -2,10 +2,13 @@
 
 "08 · FlashAttention" §五 and "第 13 课：GPU 内核与 FlashAttention" §4B rescale the old
 output by exp(m_old - m_new) whenever a larger maximum appears (the literal reading,
-tau = 0).  The kernels raise the reference only when a 128-key tile's maximum exceeds it by
-more than tau log2 units (tau = 16 for bf16 P, 8 for fp16 and e4m3 P); below that, the
-exponentials are taken against the stale reference.  O and l share the reference, so the
-final division cancels it.
+tau = 0).  The kernels take the literal reading for bf16 P, and for fp16 and e4m3 P raise
+the reference only when a key tile's maximum exceeds it by more than tau = 8 log2 units;
+below that, the exponentials are taken against the stale reference.  O and l share the
+reference, so the final division cancels it.  Why bf16 needs tau = 0: with a stale
+reference a row's largest P is 2^x for fractional x, and its bf16 rounding times a large
+|v|, added to the bf16 rounding of O, can pass the 2e-2 tolerance (the constructed row of
+test_literal_reading_on_a_dominant_key).
 
 These CPU tests state that recurrence in fp64 (the order of the kernels' steps, not their
 code) and check it against the three-pass fp64 oracle for tau in {0, 8, 16}: exact (to
@@ -115,3 +118,30 @@ def test_planted_missing_rescale_fails(tau):
     # enough that the reference moves after the first tile even with tau = 16)
     eo, el = compare(700, 64, False, 6.0, 91, tau, plant="no_rescale")
     assert eo > 1e-3 or el > 1e-3, (eo, el)
+
+
+def dominant_key_slice(d=64):
+    """Q = e_0, K = s_j e_0, V = 0.5 except one row: row 0 of K scores 0, row 200 scores
+    6.25 (9.02 log2 units above it: below a 16-unit lazy threshold) with V = 7.96875, every
+    other key scores -100.  Every row then has one dominant key with a large value, stored
+    exactly in bf16."""
+    n = 256
+    q = np.zeros((n, d)); q[:, 0] = 1.0
+    k = np.zeros((n, d)); k[:, 0] = -100.0; k[0, 0] = 0.0; k[200, 0] = 6.25
+    v = np.full((n, d), 0.5); v[200, :] = 7.96875
+    return q, k, v
+
+
+def test_literal_reading_on_a_dominant_key():
+    # The kernels' rounding points for bf16 storage: P to bf16 before P V, O to bf16 at the
+    # end.  With a stale reference (tau = 16) the dominant p is 2^9.02 and its rounding
+    # (unit roundoff 2^-8) moves O by up to 2^-8 * 7.97; with the literal reading (tau = 0)
+    # it is exactly 1 and only the rounding of O itself (half an ulp, 2^-6 near 8) remains.
+    q, k, v = dominant_key_slice()
+    o_ref, _ = oracle.attention_fwd(q[None, None], k[None, None], v[None, None], 1.0, False)
+    err = {}
+    for tau in (0.0, 16.0):
+        o, _ = lazy_attention(q, k, v, 1.0, False, tau, torch.bfloat16)
+        o_bf16 = torch.from_numpy(o).to(torch.bfloat16).double().numpy()
+        err[tau] = float(np.abs(o_bf16 - o_ref[0, 0]).max())
+    assert err[0.0] <= 2.0 ** -6 + 1e-9 < 2e-2 < err[16.0], err
