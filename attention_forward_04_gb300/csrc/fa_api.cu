@@ -385,8 +385,7 @@ int backward(const BwdRequest& r) {
     if (r.causal != 0 && r.causal != 1) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(r.scale) || r.scale < 0.0f) return FA_ERR_INVALID_ARG;
     if (r.dtype != FA_FP32 && r.dtype != FA_BF16 && r.dtype != FA_FP16) return FA_ERR_INVALID_ARG;
-    // D = 256: fp32 storage (CUDA cores) only
-    if (r.D != 32 && r.D != 64 && r.D != 128 && !(r.D == 256 && r.dtype == FA_FP32)) return FA_ERR_UNSUPPORTED;
+    if (r.D != 32 && r.D != 64 && r.D != 128 && r.D != 256) return FA_ERR_UNSUPPORTED;
     const size_t esize = r.dtype == FA_FP32 ? 4 : 2;
     if (r.layout == 1 && !packed && r.B * r.N > 0x7FFFFFFFLL) return FA_ERR_INVALID_ARG;   // tokens
     const int64_t BH = r.B * r.H;
@@ -428,20 +427,18 @@ int backward(const BwdRequest& r) {
     });
     if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
     if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;
-    if (r.dtype == FA_FP32) {   // fp32 storage: the CUDA-core kernels
+    if (r.dtype == FA_FP32 || r.D == 256) {   // fp32 storage, and D = 256: the CUDA-core kernels
         fa::SliceLayout g;
         g.layout = r.layout;
         g.cu_seqlens = r.cu;
         g.heads = (int)r.H;
         g.total = (int)r.T;
         g.n = (int)r.N;
-        e = fa::simt_bwd_launch((int)r.D, r.causal != 0, static_cast<const float*>(r.q),
-                                static_cast<const float*>(r.k), static_cast<const float*>(r.v),
-                                static_cast<const float*>(r.o), static_cast<const float*>(r.dout),
-                                r.lse, static_cast<float*>(r.workspace), static_cast<float*>(r.dq),
-                                static_cast<float*>(r.dk), static_cast<float*>(r.dv), (int)BH, g,
+        const int storage = r.dtype == FA_FP32 ? 0 : r.dtype == FA_BF16 ? 1 : 2;
+        e = fa::simt_bwd_launch((int)r.D, r.causal != 0, storage, r.q, r.k, r.v, r.o, r.dout, r.lse,
+                                static_cast<float*>(r.workspace), r.dq, r.dk, r.dv, (int)BH, g,
                                 r.scale, di.sm_count, static_cast<cudaStream_t>(r.stream));
-        return e == cudaSuccess ? FA_OK : fail_cuda(e, "fp32 backward kernel launch");
+        return e == cudaSuccess ? FA_OK : fail_cuda(e, "CUDA-core backward kernel launch");
     }
     const bool f16 = r.dtype == FA_FP16;
     const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = f16;

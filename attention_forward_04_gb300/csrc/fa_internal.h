@@ -106,11 +106,12 @@ cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, cons
                         float* o, float* lse, int bh, const SliceLayout& g, float scale,
                         int sm_count, cudaStream_t stream);
 
-// fp32 SIMT backward over the same layouts: dQ (which also writes delta, indexed like the
-// LSE) and then dK, dV, on `stream`; sm_count picks the CTA shape.
-cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
-                            const float* o, const float* dout, const float* lse, float* delta,
-                            float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
-                            float scale, int sm_count, cudaStream_t stream);
+// CUDA-core backward over the same layouts (fp32 arithmetic): dQ (which also writes delta,
+// indexed like the LSE) and then dK, dV, on `stream`; sm_count picks the CTA shape.
+// storage: 0 fp32 (D = 32, 64, 128, 256), 1 bf16 or 2 fp16 (D = 256 only).
+cudaError_t simt_bwd_launch(int D, bool causal, int storage, const void* q, const void* k,
+                            const void* v, const void* o, const void* dout, const float* lse,
+                            float* delta, void* dq, void* dk, void* dv, int bh,
+                            const SliceLayout& g, float scale, int sm_count, cudaStream_t stream);
 
 }  // namespace fa

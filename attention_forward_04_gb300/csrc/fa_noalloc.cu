@@ -41,7 +41,7 @@ int check_common(const void* const* ptrs, int64_t need, int64_t D, float scale, 
     if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
     if (dtype != FA_FP32 && dtype != FA_BF16 && dtype != FA_FP16) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || scale < 0.0f) return FA_ERR_INVALID_ARG;   // as fa_bwd
-    if (D != 32 && D != 64 && D != 128 && !(D == 256 && dtype == FA_FP32)) return FA_ERR_UNSUPPORTED;
+    if (D != 32 && D != 64 && D != 128 && D != 256) return FA_ERR_UNSUPPORTED;
     if (need > kScratchBytes) return FA_ERR_UNSUPPORTED;
     return FA_OK;
 }

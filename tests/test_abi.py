@@ -142,7 +142,7 @@ def test_bwd_workspace_size(lib):
     (dict(q=0), INVALID), (dict(do=0), INVALID), (dict(lse=0), INVALID), (dict(dv=0), INVALID),
     (dict(ws=0), INVALID), (dict(ws_bytes=100), INVALID), (dict(N=0), INVALID),
     (dict(causal=3), INVALID), (dict(scale=float("nan")), INVALID), (dict(dtype=9), INVALID),
-    (dict(D=96), UNSUPPORTED), (dict(D=256), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=512), UNSUPPORTED),
     (dict(D=16), UNSUPPORTED),
     (dict(dq=BASE), INVALID),                      # dq aliases q
     (dict(dk=BASE + 6 * SZ + 128), INVALID),       # dk overlaps dq
@@ -205,7 +205,7 @@ def test_bwd_layout_variants_argument_checks(lib):
     assert varlen(total=0) == INVALID
     # delta is indexed like the [H, total] LSE: the workspace must cover H * total floats
     assert varlen(ws_bytes=lib.fa_bwd_workspace_bytes(1, 4, 1000) - 16) == INVALID
-    assert varlen(D=256) == UNSUPPORTED
+    assert varlen(D=512) == UNSUPPORTED
     assert varlen(do=BASE + 4 * SZ + 8) == MISALIGNED
 
 

@@ -148,6 +148,29 @@ def test_fp16_backward(N, D, causal):
                    "fp16 N=%d D=%d causal=%d" % (N, D, causal))
 
 
+# Head dimension 256 with 16-bit storage: the CUDA-core kernels widen the inputs to fp32 and
+# round only the stored gradients, so the tensor-core bound (which also allows the rounding
+# of P and dS) holds with room to spare.  Small shapes take the 8-row CTAs of 16 threads per
+# row, the 32-slice shape the 16-row CTAs of 8 threads per row.
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("N", [1, 17, 129, 300])
+def test_16bit_backward_head_dim_256(N, dtype, causal):
+    q, k, v = make_shape(2, 1, N, 256, dtype, seed=N * 23 + 256)
+    do = make_shape_dout(2, 1, N, 256, dtype, seed=N * 23 + 256)
+    compare_slices(q, k, v, do, 1.0 / 16.0, causal, dtype, [(0, 0), (1, 0)],
+                   "%s D=256 N=%d causal=%d" % (dtype, N, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_16bit_backward_head_dim_256_narrow_ctas(causal):
+    q, k, v = make_shape(4, 8, 200, 256, "bf16", seed=456)
+    do = make_shape_dout(4, 8, 200, 256, "bf16", seed=456)
+    assert 4 * 8 * ((200 + 15) // 16) >= 152
+    compare_slices(q, k, v, do, 1.0 / 16.0, causal, "bf16", [(0, 0), (1, 3), (3, 7)],
+                   "bf16 D=256 narrow CTAs causal=%d" % causal)
+
+
 @pytest.mark.parametrize("D", [32, 128])
 def test_backward_scale_zero_and_large_scores(D):
     # scale 0: P is uniform over the visible keys; scores x4: a peaked softmax
@@ -161,7 +184,8 @@ def test_backward_scale_zero_and_large_scores(D):
 
 # ------------------------------------------------------------ full-size workloads, sampled
 @pytest.mark.parametrize("name", ["bf16_b2h8n1024d64", "bf16_b4h16n4096d128",
-                                  "bf16_b8h32n4096d128_causal", "bf16_b8h32n4096d32"])
+                                  "bf16_b8h32n4096d128_causal", "bf16_b8h32n4096d32",
+                                  "bf16_b4h8n4096d256", "bf16_b4h8n4096d256_causal"])
 def test_backward_full_size_sampled_slices(name):
     w = WORKLOADS[name]
     q, k, v = make_qkv(w)

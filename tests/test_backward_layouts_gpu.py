@@ -61,7 +61,8 @@ def test_bnhd_backward(D, causal):
                         "bnhd D=%d causal=%d (b=%d, h=%d)" % (D, causal, b, h))
 
 
-@pytest.mark.parametrize("dtype,D", [("fp16", 64), ("fp32", 64), ("fp32", 256)])
+@pytest.mark.parametrize("dtype,D", [("fp16", 64), ("fp32", 64), ("fp32", 256), ("bf16", 256),
+                                     ("fp16", 256)])
 def test_bnhd_backward_other_dtypes(dtype, D):
     B, N, H = 1, 200, 2
     to_bnhd = lambda t: t.permute(0, 2, 1, 3).contiguous().cuda()  # noqa: E731
@@ -90,6 +91,11 @@ def test_varlen_backward(mix, D, causal):
 @pytest.mark.parametrize("D", [64, 256])
 def test_varlen_backward_fp32(D):
     run_varlen_backward([0, 40, 129, 7], D, True, "fp32", 5)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_backward_bf16_head_dim_256(causal):
+    run_varlen_backward([0, 40, 129, 7, 300], 256, causal, "bf16", 6)
 
 
 def run_varlen_backward(lengths, D, causal, dtype, seed):
