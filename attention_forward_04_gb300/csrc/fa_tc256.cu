@@ -439,13 +439,15 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         // be two phases behind.)
                         if (!wait_warp(c, b_o_done(), (pv + (uint32_t)j - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                         ptx::tc_fence_after();
+                        // two 128-column TMEM round trips (this kernel's warps have the
+                        // registers), packed multiplies in between
 #pragma unroll 1
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t o[32];
-                            ptx::tmem_ld32_wait(tm + tl + kColO + (uint32_t)cc * 32u, o);
+                        for (int cc = 0; cc < D / 128; ++cc) {
+                            uint32_t o[128];
+                            ptx::tmem_ld128_wait(tm + tl + kColO + (uint32_t)cc * 128u, o);
 #pragma unroll
-                            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
-                            ptx::tmem_st32(tm + tl + kColO + (uint32_t)cc * 32u, o);
+                            for (int e = 0; e < 128; e += 2) ptx::mul2u(o[e], o[e + 1], alpha);
+                            ptx::tmem_st128(tm + tl + kColO + (uint32_t)cc * 128u, o);
                         }
                     }
                     __syncwarp();
