@@ -21,7 +21,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
 
 SOURCES = ["fa_api.cu", "fa_tc.cu", "fa_tc256.cu", "fa_simt.cu", "fa_simt_bwd.cu", "fa_bwd.cu",
-           "fa_noalloc.cu"]
+           "fa_bwd256.cu", "fa_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I" + INCLUDE, "-I" + CSRC]

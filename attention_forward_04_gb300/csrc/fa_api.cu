@@ -31,8 +31,8 @@ struct DeviceInfo {
     int major = 0, minor = 0;
     std::once_flag prepared[3][2][3];  // [D = 32, 64, 128][causal][bf16, fp16, fp8]
     cudaError_t prepare_err[3][2][3] = {};
-    std::once_flag bwd_prepared[3][2][2];   // [D = 32, 64, 128][causal][f16]
-    cudaError_t bwd_prepare_err[3][2][2] = {};
+    std::once_flag bwd_prepared[4][2][2];   // [D = 32, 64, 128, 256][causal][f16]
+    cudaError_t bwd_prepare_err[4][2][2] = {};
     std::once_flag prepared256[2][3];  // [causal][element type]
     cudaError_t prepare256_err[2][3] = {};
 };
@@ -138,13 +138,16 @@ int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall) {
 int fa_check_device_status(void* stream, uint32_t* detail) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(e, "cudaStreamSynchronize");
-    uint32_t w[4] = {0, 0, 0, 0}, wb[4] = {0, 0, 0, 0}, w256[4] = {0, 0, 0, 0};
+    uint32_t w[4] = {0, 0, 0, 0}, wb[4] = {0, 0, 0, 0}, w256[4] = {0, 0, 0, 0},
+             wb256[4] = {0, 0, 0, 0};
     e = fa::tc_status_read_reset(w);
     if (e == cudaSuccess) e = fa::bwd_status_read_reset(wb);
     if (e == cudaSuccess) e = fa::tc256_status_read_reset(w256);
+    if (e == cudaSuccess) e = fa::bwd256_status_read_reset(wb256);
     if (e != cudaSuccess) return fail_cuda(e, "status word");
     if (!(w[0] & 1u) && (wb[0] & 1u)) std::memcpy(w, wb, sizeof(w));   // report the backward's
     if (!(w[0] & 1u) && (w256[0] & 1u)) std::memcpy(w, w256, sizeof(w));
+    if (!(w[0] & 1u) && (wb256[0] & 1u)) std::memcpy(w, wb256, sizeof(w));
     if (detail) std::memcpy(detail, w, sizeof(w));
     return (w[0] & 1u) ? FA_ERR_TIMEOUT : FA_OK;
 }
@@ -427,23 +430,28 @@ int backward(const BwdRequest& r) {
     });
     if (di.err != cudaSuccess) return fail_cuda(di.err, "cudaDeviceGetAttribute");
     if (di.major != 10 || di.minor != 3) return FA_ERR_UNSUPPORTED;
-    if (r.dtype == FA_FP32 || r.D == 256) {   // fp32 storage, and D = 256: the CUDA-core kernels
+    if (r.dtype == FA_FP32) {   // fp32 storage: the CUDA-core kernels
         fa::SliceLayout g;
         g.layout = r.layout;
         g.cu_seqlens = r.cu;
         g.heads = (int)r.H;
         g.total = (int)r.T;
         g.n = (int)r.N;
-        const int storage = r.dtype == FA_FP32 ? 0 : r.dtype == FA_BF16 ? 1 : 2;
-        e = fa::simt_bwd_launch((int)r.D, r.causal != 0, storage, r.q, r.k, r.v, r.o, r.dout, r.lse,
-                                static_cast<float*>(r.workspace), r.dq, r.dk, r.dv, (int)BH, g,
+        e = fa::simt_bwd_launch((int)r.D, r.causal != 0, static_cast<const float*>(r.q),
+                                static_cast<const float*>(r.k), static_cast<const float*>(r.v),
+                                static_cast<const float*>(r.o), static_cast<const float*>(r.dout),
+                                r.lse, static_cast<float*>(r.workspace), static_cast<float*>(r.dq),
+                                static_cast<float*>(r.dk), static_cast<float*>(r.dv), (int)BH, g,
                                 r.scale, di.sm_count, static_cast<cudaStream_t>(r.stream));
         return e == cudaSuccess ? FA_OK : fail_cuda(e, "CUDA-core backward kernel launch");
     }
     const bool f16 = r.dtype == FA_FP16;
-    const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : 2, dic = r.causal != 0, dif = f16;
-    std::call_once(di.bwd_prepared[dix][dic][dif],
-                   [&] { di.bwd_prepare_err[dix][dic][dif] = fa::bwd_prepare((int)r.D, dic, f16); });
+    const bool d256 = r.D == 256;
+    const int dix = r.D == 32 ? 0 : r.D == 64 ? 1 : r.D == 128 ? 2 : 3, dic = r.causal != 0, dif = f16;
+    std::call_once(di.bwd_prepared[dix][dic][dif], [&] {
+        di.bwd_prepare_err[dix][dic][dif] = d256 ? fa::bwd256_prepare(dic, f16)
+                                                 : fa::bwd_prepare((int)r.D, dic, f16);
+    });
     if (di.bwd_prepare_err[dix][dic][dif] != cudaSuccess)
         return fail_cuda(di.bwd_prepare_err[dix][dic][dif], "cudaFuncSetAttribute (backward)");
     PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn(&e);
@@ -452,10 +460,11 @@ int backward(const BwdRequest& r) {
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
     const int et = f16 ? 1 : 0;
-    if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
-        !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
-        !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, et, fn) ||
-        !encode_map(&p.tmap_do, r.dout, r.layout, BH, r.N, r.H, r.T, r.D, et, fn))
+    const cuuint32_t box_rows = d256 ? 64 : 128;   // D = 256 streams 64-row sub-tiles
+    if (!encode_map(&p.tmap_q, r.q, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, box_rows) ||
+        !encode_map(&p.tmap_k, r.k, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, box_rows) ||
+        !encode_map(&p.tmap_v, r.v, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, box_rows) ||
+        !encode_map(&p.tmap_do, r.dout, r.layout, BH, r.N, r.H, r.T, r.D, et, fn, box_rows))
         return fail_cuda(cudaErrorInvalidValue, "cuTensorMapEncodeTiled");
     p.lse = r.lse;
     p.o = r.o;
@@ -475,7 +484,7 @@ int backward(const BwdRequest& r) {
     p.total = (int)r.T;
     p.cu_seqlens = r.cu;
     cudaStream_t st = static_cast<cudaStream_t>(r.stream);
-    e = fa::bwd_launch((int)r.D, dic, f16, p, (int)BH, st);
+    e = d256 ? fa::bwd256_launch(dic, f16, p, (int)BH, st) : fa::bwd_launch((int)r.D, dic, f16, p, (int)BH, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "backward kernel launch");
 }
 

@@ -31,7 +31,7 @@ struct TcParams {
     int inject_stall;    // failure-detection test hook (see fa_set_watchdog)
 };
 
-// Launch parameters of the backward kernels ([B*H, N, D] bf16/fp16, D = 64 or 128).
+// Launch parameters of the backward tensor-core kernels (bf16/fp16, D = 32, 64, 128, 256).
 struct BwdParams {
     CUtensorMap tmap_q;   // 3-D maps over [B*H, N, D] exactly as the forward's
     CUtensorMap tmap_k;
@@ -64,6 +64,12 @@ cudaError_t bwd_launch(int D, bool causal, bool f16, const BwdParams& p, int bh,
                        cudaStream_t stream);
 // Status word of the backward kernels (same meaning as the forward's).
 cudaError_t bwd_status_read_reset(uint32_t out[4]);
+
+// Head dimension 256 (16-bit storage; maps with boxes of 64 rows x 128 bytes): dQ (which
+// also writes delta), dV, then dK, B*H*ntiles CTAs each, on `stream`.
+cudaError_t bwd256_prepare(bool causal, bool f16);
+cudaError_t bwd256_launch(bool causal, bool f16, const BwdParams& p, int bh, cudaStream_t stream);
+cudaError_t bwd256_status_read_reset(uint32_t out[4]);
 
 // Work units of the persistent schedule for a given shape.
 int tc_units(int bh, int n, bool causal);
@@ -106,12 +112,11 @@ cudaError_t simt_launch(int D, bool causal, const float* q, const float* k, cons
                         float* o, float* lse, int bh, const SliceLayout& g, float scale,
                         int sm_count, cudaStream_t stream);
 
-// CUDA-core backward over the same layouts (fp32 arithmetic): dQ (which also writes delta,
-// indexed like the LSE) and then dK, dV, on `stream`; sm_count picks the CTA shape.
-// storage: 0 fp32 (D = 32, 64, 128, 256), 1 bf16 or 2 fp16 (D = 256 only).
-cudaError_t simt_bwd_launch(int D, bool causal, int storage, const void* q, const void* k,
-                            const void* v, const void* o, const void* dout, const float* lse,
-                            float* delta, void* dq, void* dk, void* dv, int bh,
-                            const SliceLayout& g, float scale, int sm_count, cudaStream_t stream);
+// fp32 SIMT backward over the same layouts: dQ (which also writes delta, indexed like the
+// LSE) and then dK, dV, on `stream`; sm_count picks the CTA shape.
+cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
+                            const float* o, const float* dout, const float* lse, float* delta,
+                            float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
+                            float scale, int sm_count, cudaStream_t stream);
 
 }  // namespace fa

@@ -1,7 +1,4 @@
-// fa_simt_bwd.cu -- attention backward on the CUDA cores: fp32 arithmetic, over fp32
-// storage (every head dimension) or 16-bit storage (head dimension 256, where the
-// tensor-core backward's tiles do not fit; values are widened to fp32 on load and rounded to
-// the storage type on the final store).
+// fa_simt_bwd.cu -- fp32 attention backward on the CUDA cores (fp32 storage and arithmetic).
 //
 // The gradients of the forward in fa_simt.cu, with P rebuilt from the forward's LSE
 // ("08 · FlashAttention" §三; "第 13 课：GPU 内核与 FlashAttention" §4B):
@@ -18,12 +15,9 @@
 // CTAs would not give every SM one; thread t of a row owns head-dim columns t, t+T, t+2T,
 // ... (T threads per row); a dot product over D is the T partial sums added with shuffles.  Layouts as the forward: [B, H, N, D], token-major [tokens, H, D],
 // packed sequences.
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <type_traits>
 
 #include "fa_internal.h"
 
@@ -71,28 +65,6 @@ __device__ __forceinline__ SimtSlice simt_slice(const SliceLayout& g, int bh) {
     return s;
 }
 
-// Storage access: T = float, __nv_bfloat16 or __half; arithmetic is always fp32.
-template <class T> __device__ __forceinline__ float ld1(const T* p, size_t i) {
-    if constexpr (sizeof(T) == 4) return p[i];
-    else if constexpr (std::is_same<T, __half>::value) return __half2float(p[i]);
-    else return __bfloat162float(p[i]);
-}
-template <class T> __device__ __forceinline__ void st1(T* p, size_t i, float x) {
-    if constexpr (sizeof(T) == 4) p[i] = x;
-    else if constexpr (std::is_same<T, __half>::value) p[i] = __float2half_rn(x);
-    else p[i] = __float2bfloat16_rn(x);
-}
-// four consecutive values from element i (i a multiple of 4: 16 or 8 bytes, aligned)
-template <class T> __device__ __forceinline__ float4 ld4(const T* p, size_t i) {
-    if constexpr (sizeof(T) == 4) {
-        return *reinterpret_cast<const float4*>(p + i);
-    } else {
-        const uint2 w = *reinterpret_cast<const uint2*>(p + i);
-        const T* h = reinterpret_cast<const T*>(&w);
-        return make_float4(ld1<T>(h, 0), ld1<T>(h, 1), ld1<T>(h, 2), ld1<T>(h, 3));
-    }
-}
-
 // Sum over the TPR consecutive lanes that share a row.
 template <int TPR>
 __device__ __forceinline__ float row_sum(float x) {
@@ -108,8 +80,7 @@ template <int D, bool WIDE>
 struct TilePair {
     static constexpr int kTile = Shape<D, WIDE>::kTile, kLoads = Shape<D, WIDE>::kLoads;
     float4 a[kLoads], b[kLoads];
-    template <class T>
-    __device__ __forceinline__ void fetch(const T* __restrict__ sa, const T* __restrict__ sb,
+    __device__ __forceinline__ void fetch(const float* __restrict__ sa, const float* __restrict__ sb,
                                           const SimtSlice& s, int r0) {
 #pragma unroll
         for (int e = 0; e < kLoads; ++e) {
@@ -119,8 +90,8 @@ struct TilePair {
             b[e] = a[e];
             if (r0 + r < s.len) {
                 const size_t off = s.base + (size_t)(r0 + r) * s.rs + c;
-                a[e] = ld4<T>(sa, off);
-                b[e] = ld4<T>(sb, off);
+                a[e] = *reinterpret_cast<const float4*>(sa + off);
+                b[e] = *reinterpret_cast<const float4*>(sb + off);
             }
         }
     }
@@ -135,11 +106,11 @@ struct TilePair {
     }
 };
 
-template <int D, bool WIDE, bool CAUSAL, class T>
+template <int D, bool WIDE, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
-    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-    const T* __restrict__ o, const T* __restrict__ dout, const float* __restrict__ lse,
-    float* __restrict__ delta, T* __restrict__ dq, const SliceLayout g, float scale) {
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const float* __restrict__ o, const float* __restrict__ dout, const float* __restrict__ lse,
+    float* __restrict__ delta, float* __restrict__ dq, const SliceLayout g, float scale) {
     using S = Shape<D, WIDE>;
     constexpr int kRows = S::kRows, TPR = S::kTpr, DQ = S::kCols, kTile = S::kTile;
     __shared__ __align__(16) float Ks[kTile][D];
@@ -157,9 +128,9 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     float dl = 0.0f;
 #pragma unroll
     for (int c = 0; c < DQ; ++c) {
-        qv[c] = live ? ld1<T>(q, row + qd + TPR * c) : 0.0f;
-        dov[c] = live ? ld1<T>(dout, row + qd + TPR * c) : 0.0f;
-        dl = fmaf(dov[c], live ? ld1<T>(o, row + qd + TPR * c) : 0.0f, dl);
+        qv[c] = live ? q[row + qd + TPR * c] : 0.0f;
+        dov[c] = live ? dout[row + qd + TPR * c] : 0.0f;
+        dl = fmaf(dov[c], live ? o[row + qd + TPR * c] : 0.0f, dl);
         acc[c] = 0.0f;
     }
     dl = row_sum<TPR>(dl);   // delta_i = sum_d dO_id O_id
@@ -194,15 +165,15 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dq_kernel(
     }
     if (live) {
 #pragma unroll
-        for (int c = 0; c < DQ; ++c) st1<T>(dq, row + qd + TPR * c, acc[c] * scale);
+        for (int c = 0; c < DQ; ++c) dq[row + qd + TPR * c] = acc[c] * scale;
     }
 }
 
-template <int D, bool WIDE, bool CAUSAL, class T>
+template <int D, bool WIDE, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
-    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-    const T* __restrict__ dout, const float* __restrict__ lse,
-    const float* __restrict__ delta, T* __restrict__ dk, T* __restrict__ dv,
+    const float* __restrict__ q, const float* __restrict__ k, const float* __restrict__ v,
+    const float* __restrict__ dout, const float* __restrict__ lse,
+    const float* __restrict__ delta, float* __restrict__ dk, float* __restrict__ dv,
     const SliceLayout g, float scale) {
     using S = Shape<D, WIDE>;
     constexpr int kRows = S::kRows, TPR = S::kTpr, DQ = S::kCols, kTile = S::kTile;
@@ -221,8 +192,8 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     float kv[DQ], vv[DQ], ak[DQ], av[DQ];
 #pragma unroll
     for (int c = 0; c < DQ; ++c) {
-        kv[c] = live ? ld1<T>(k, row + qd + TPR * c) : 0.0f;
-        vv[c] = live ? ld1<T>(v, row + qd + TPR * c) : 0.0f;
+        kv[c] = live ? k[row + qd + TPR * c] : 0.0f;
+        vv[c] = live ? v[row + qd + TPR * c] : 0.0f;
         ak[c] = 0.0f;
         av[c] = 0.0f;
     }
@@ -280,64 +251,53 @@ __global__ void __launch_bounds__(kThreads) simt_bwd_dkdv_kernel(
     if (live) {
 #pragma unroll
         for (int c = 0; c < DQ; ++c) {
-            st1<T>(dk, row + qd + TPR * c, ak[c] * scale);
-            st1<T>(dv, row + qd + TPR * c, av[c]);
+            dk[row + qd + TPR * c] = ak[c] * scale;
+            dv[row + qd + TPR * c] = av[c];
         }
     }
 }
 
-template <int D, bool WIDE, bool CAUSAL, class T>
-cudaError_t launch(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                   const float* lse, float* delta, void* dq, void* dk, void* dv, int bh,
-                   const SliceLayout& g, float scale, cudaStream_t stream) {
+template <int D, bool WIDE, bool CAUSAL>
+cudaError_t launch(const float* q, const float* k, const float* v, const float* o,
+                   const float* dout, const float* lse, float* delta, float* dq, float* dk,
+                   float* dv, int bh, const SliceLayout& g, float scale, cudaStream_t stream) {
     constexpr int kRows = Shape<D, WIDE>::kRows;
     const long long blocks = (long long)((g.n + kRows - 1) / kRows) * bh;
     if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidConfiguration;
-    const T *tq = static_cast<const T*>(q), *tk = static_cast<const T*>(k), *tv = static_cast<const T*>(v);
-    simt_bwd_dq_kernel<D, WIDE, CAUSAL, T><<<(unsigned)blocks, kThreads, 0, stream>>>(
-        tq, tk, tv, static_cast<const T*>(o), static_cast<const T*>(dout), lse, delta,
-        static_cast<T*>(dq), g, scale);
+    simt_bwd_dq_kernel<D, WIDE, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(
+        q, k, v, o, dout, lse, delta, dq, g, scale);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    simt_bwd_dkdv_kernel<D, WIDE, CAUSAL, T><<<(unsigned)blocks, kThreads, 0, stream>>>(
-        tq, tk, tv, static_cast<const T*>(dout), lse, delta, static_cast<T*>(dk),
-        static_cast<T*>(dv), g, scale);
+    simt_bwd_dkdv_kernel<D, WIDE, CAUSAL><<<(unsigned)blocks, kThreads, 0, stream>>>(
+        q, k, v, dout, lse, delta, dk, dv, g, scale);
     return cudaGetLastError();
 }
 
-template <int D, class T>
-cudaError_t launch_d(bool causal, int sm_count, const void* q, const void* k, const void* v,
-                     const void* o, const void* dout, const float* lse, float* delta, void* dq,
-                     void* dk, void* dv, int bh, const SliceLayout& g, float scale,
+template <int D>
+cudaError_t launch_d(bool causal, int sm_count, const float* q, const float* k, const float* v,
+                     const float* o, const float* dout, const float* lse, float* delta, float* dq,
+                     float* dk, float* dv, int bh, const SliceLayout& g, float scale,
                      cudaStream_t stream) {
     // 16 threads per row when the narrow CTAs would not give every SM one
     constexpr int kNarrow = Shape<D, false>::kRows;
     const bool wide = (long long)((g.n + kNarrow - 1) / kNarrow) * bh < (long long)sm_count;
     if (wide)
-        return causal ? launch<D, true, true, T>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
-                      : launch<D, true, false, T>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    return causal ? launch<D, false, true, T>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
-                  : launch<D, false, false, T>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+        return causal ? launch<D, true, true>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
+                      : launch<D, true, false>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    return causal ? launch<D, false, true>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream)
+                  : launch<D, false, false>(q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
 }
 
 }  // namespace
 
-cudaError_t simt_bwd_launch(int D, bool causal, int storage, const void* q, const void* k,
-                            const void* v, const void* o, const void* dout, const float* lse,
-                            float* delta, void* dq, void* dk, void* dv, int bh,
-                            const SliceLayout& g, float scale, int sm_count, cudaStream_t stream) {
-    if (storage == 1) {   // bf16 (head dimension 256 only)
-        if (D != 256) return cudaErrorInvalidValue;
-        return launch_d<256, __nv_bfloat16>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    }
-    if (storage == 2) {   // fp16 (head dimension 256 only)
-        if (D != 256) return cudaErrorInvalidValue;
-        return launch_d<256, __half>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    }
-    if (D == 32) return launch_d<32, float>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    if (D == 64) return launch_d<64, float>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    if (D == 256) return launch_d<256, float>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
-    return launch_d<128, float>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+cudaError_t simt_bwd_launch(int D, bool causal, const float* q, const float* k, const float* v,
+                            const float* o, const float* dout, const float* lse, float* delta,
+                            float* dq, float* dk, float* dv, int bh, const SliceLayout& g,
+                            float scale, int sm_count, cudaStream_t stream) {
+    if (D == 32) return launch_d<32>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    if (D == 64) return launch_d<64>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    if (D == 256) return launch_d<256>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
+    return launch_d<128>(causal, sm_count, q, k, v, o, dout, lse, delta, dq, dk, dv, bh, g, scale, stream);
 }
 
 }  // namespace fa

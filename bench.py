@@ -40,7 +40,10 @@ _CSRC = os.path.join(ROOT, "attention_forward_04_gb300", "csrc")
 KERNEL_SRCS = {"fwd": [os.path.join(_CSRC, f) for f in ("fa_tc.cu", "tc_common.cuh", "ptx.cuh")],
                "fwd256": [os.path.join(_CSRC, f) for f in ("fa_tc256.cu", "tc_common.cuh", "ptx.cuh")],
                "simt": [os.path.join(_CSRC, "fa_simt.cu")],
-               "bwd": [os.path.join(_CSRC, f) for f in ("fa_bwd.cu", "tc_common.cuh", "ptx.cuh")]}
+               "bwd": [os.path.join(_CSRC, f) for f in ("fa_bwd.cu", "bwd_common.cuh", "tc_common.cuh",
+                                                         "ptx.cuh")],
+               "bwd256": [os.path.join(_CSRC, f) for f in ("fa_bwd256.cu", "bwd_common.cuh",
+                                                            "tc_common.cuh", "ptx.cuh")]}
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 
 
@@ -521,12 +524,17 @@ def run_bwd(args, w):
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops_step / (per_call_ms / 1e3) / 1e12
+    # executed products: S and dP are formed twice (dQ kernel, dK/dV kernel), 14 N^2 D per
+    # slice; at D = 256 S^T three times (dQ, dV and dK kernels), 16 N^2 D
+    d256 = w.D == 256
     roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "traffic": load_traffic("bwd:" + w.name, "bwd"),
-            "kernel": "whole fa_bwd call (dQ kernel, which also forms delta, and dK/dV "
-                      "kernel); per-kernel shares in the ncu launch list",
+            "frac": achieved / peak,
+            "traffic": load_traffic("bwd:" + w.name, "bwd256" if d256 else "bwd"),
+            "kernel": ("whole fa_bwd call (dQ kernel, which also forms delta, dV kernel and dK "
+                       "kernel)" if d256 else "whole fa_bwd call (dQ kernel, which also forms "
+                       "delta, and dK/dV kernel)") + "; per-kernel shares in the ncu launch list",
             "peak_source": "%s bf16 dense burst" % peak_src,
-            "executed_tflops": 3.5 * w.flops / (per_call_ms / 1e3) / 1e12}
+            "executed_tflops": (4.0 if d256 else 3.5) * w.flops / (per_call_ms / 1e3) / 1e12}
     if w.dtype == "fp32":
         # the CUDA-core backward: fp32 FFMA peak, SMs x 128 fp32 lanes x 2 FLOP x max SM clock
         sms = torch.cuda.get_device_properties(dev).multi_processor_count

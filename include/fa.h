@@ -153,14 +153,14 @@ int64_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t N);
  *                      must not be shared by two calls in flight at once.
  *   B, H, N, scale, causal, stream : as for fa_fwd.
  *   D                : 32, 64, 128 or 256.
- *   dtype            : FA_BF16 or FA_FP16 (tensor cores at D <= 128, CUDA cores at
- *                      D = 256), or FA_FP32 (CUDA cores, fp32 arithmetic throughout).
+ *   dtype            : FA_BF16 or FA_FP16 (tensor cores), or FA_FP32 (CUDA cores, fp32
+ *                      arithmetic throughout).
  *
- * Arithmetic: 16-bit storage at D <= 128: products on the tensor cores from 16-bit operands
- * (P and dS are rounded to `dtype` before their products, like P in the forward), fp32
- * accumulation, results rounded to `dtype`; 16-bit storage at D = 256: the inputs widened
- * to fp32, fp32 arithmetic on the CUDA cores, results rounded to `dtype`; fp32 storage:
- * fp32 throughout.  No atomics: results do not depend on scheduling.
+ * Arithmetic: 16-bit storage: products on the tensor cores from 16-bit operands (P and dS
+ * are rounded to `dtype` before their products, like P in the forward), fp32 accumulation,
+ * results rounded to `dtype` (D <= 128: a dQ and a dK/dV kernel; D = 256: a dQ, a dV and a
+ * dK kernel); fp32 storage: fp32 throughout.  No atomics: results do not depend on
+ * scheduling.
  * Errors: as fa_fwd; additionally FA_ERR_INVALID_ARG when the workspace is too small or any
  * output overlaps an input, the workspace or another output.
  */

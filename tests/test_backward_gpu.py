@@ -148,13 +148,13 @@ def test_fp16_backward(N, D, causal):
                    "fp16 N=%d D=%d causal=%d" % (N, D, causal))
 
 
-# Head dimension 256 with 16-bit storage: the CUDA-core kernels widen the inputs to fp32 and
-# round only the stored gradients, so the tensor-core bound (which also allows the rounding
-# of P and dS) holds with room to spare.  Small shapes take the 8-row CTAs of 16 threads per
-# row, the 32-slice shape the 16-row CTAs of 8 threads per row.
+# Head dimension 256 with 16-bit storage: three tensor-core kernels (dQ, dV, dK), each CTA
+# on one 128-row tile and the other side streamed in 64-row sub-tiles.  The lengths put the
+# sequence end inside and on the edges of both (63/64/65: one sub-tile; 127/128/129 and
+# 191/192/193: the tile edge and the second sub-tile of a tile).
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
-@pytest.mark.parametrize("N", [1, 17, 129, 300])
+@pytest.mark.parametrize("N", [1, 17, 63, 64, 65, 127, 128, 129, 191, 193, 300, 640])
 def test_16bit_backward_head_dim_256(N, dtype, causal):
     q, k, v = make_shape(2, 1, N, 256, dtype, seed=N * 23 + 256)
     do = make_shape_dout(2, 1, N, 256, dtype, seed=N * 23 + 256)
@@ -162,16 +162,16 @@ def test_16bit_backward_head_dim_256(N, dtype, causal):
                    "%s D=256 N=%d causal=%d" % (dtype, N, causal))
 
 
+# 32 slices of 2 tiles: more CTAs than SMs in each of the three kernels.
 @pytest.mark.parametrize("causal", [False, True])
-def test_16bit_backward_head_dim_256_narrow_ctas(causal):
+def test_16bit_backward_head_dim_256_many_slices(causal):
     q, k, v = make_shape(4, 8, 200, 256, "bf16", seed=456)
     do = make_shape_dout(4, 8, 200, 256, "bf16", seed=456)
-    assert 4 * 8 * ((200 + 15) // 16) >= 152
     compare_slices(q, k, v, do, 1.0 / 16.0, causal, "bf16", [(0, 0), (1, 3), (3, 7)],
-                   "bf16 D=256 narrow CTAs causal=%d" % causal)
+                   "bf16 D=256 32 slices causal=%d" % causal)
 
 
-@pytest.mark.parametrize("D", [32, 128])
+@pytest.mark.parametrize("D", [32, 128, 256])
 def test_backward_scale_zero_and_large_scores(D):
     # scale 0: P is uniform over the visible keys; scores x4: a peaked softmax
     q, k, v = make_shape(1, 2, 300, D, "bf16", seed=91, qk_mult=4.0)
@@ -195,9 +195,10 @@ def test_backward_full_size_sampled_slices(name):
 
 
 # ------------------------------------------------------------ contract
-def test_backward_overwrites_outputs_and_is_deterministic():
-    q, k, v = (t.cuda() for t in make_shape(2, 3, 700, 128, "bf16", seed=5))
-    do = make_shape_dout(2, 3, 700, 128, "bf16", seed=5).cuda()
+@pytest.mark.parametrize("D", [128, 256])
+def test_backward_overwrites_outputs_and_is_deterministic(D):
+    q, k, v = (t.cuda() for t in make_shape(2, 3, 700, D, "bf16", seed=5))
+    do = make_shape_dout(2, 3, 700, D, "bf16", seed=5).cuda()
     o, lse = binding.fwd(q, k, v, causal=True)
     first = binding.bwd(q, k, v, o, lse, do, causal=True)
     outs = [torch.full_like(q, float("nan")) for _ in range(3)]
