@@ -620,16 +620,16 @@ __device__ __forceinline__ float tile_row_max(const uint32_t (&s)[NS], int kbase
     return fmaxf(ptx::max3(mx[0], mx[1], mx[2]), fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
 }
 
-// p = 2^(s * sl2 - m) for columns [C0, C0 + 64), partial row sums into acc (four fp32
+// p = 2^(s * sl2 - m) for columns [C0, C0 + W), partial row sums into acc (four fp32
 // pairs), and P packed for TMEM: 16-bit pairs into pk[C0/2 ...], or for e4m3 four values
 // per word into pk[C0/4 ...].  Invisible keys give p = 0.
-template <int C0, bool MASK, int ET, int NS, int NP>
-__device__ __forceinline__ void tile_exp_half(const uint32_t (&s)[NS], int kbase, int limit,
+template <int C0, int W, bool MASK, int ET, int NS, int NP>
+__device__ __forceinline__ void tile_exp_cols(const uint32_t (&s)[NS], int kbase, int limit,
                                               float sl2, float neg_m, float (&acc)[8],
                                               uint32_t (&pk)[NP]) {
-    static_assert(C0 + 64 <= NS && (ET == 2 ? (C0 + 64) / 4 : (C0 + 64) / 2) <= NP, "ranges");
+    static_assert(C0 + W <= NS && (ET == 2 ? (C0 + W) / 4 : (C0 + W) / 2) <= NP, "ranges");
 #pragma unroll
-    for (int c = C0; c < C0 + 64; c += 4) {
+    for (int c = C0; c < C0 + W; c += 4) {
         float x[4], pr[4];
         ptx::fma2(x[0], x[1], u2f(s[c]), u2f(s[c + 1]), sl2, neg_m);
         ptx::fma2(x[2], x[3], u2f(s[c + 2]), u2f(s[c + 3]), sl2, neg_m);
@@ -674,15 +674,46 @@ __device__ __forceinline__ void rescale_o(uint32_t tO0, float alpha) {
     }
 }
 
+// 32 lanes x 32 consecutive 32-bit columns, issued without waiting: the registers hold
+// the values only after tmem_wait_ld32 on the same array, which the compiler sees as
+// rewriting them, so no use can be scheduled between the two.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// One 32-column chunk of this row of O, loaded without waiting: the wait, the multiply
+// by alpha and the store come later, so the load's latency overlaps the exponentials.
+__device__ __forceinline__ void o_chunk_finish(uint32_t tO, uint32_t (&o)[32], float alpha) {
+    tmem_wait_ld32(o);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) ptx::mul2u(o[i], o[i + 1], alpha);
+    ptx::tmem_st32(tO, o);
+}
+
 // One 128-key tile of one row: running-max update (raised when the tile max exceeds it by
 // more than kRescaleLog2 log2 units), exp2, row sum, and P stored into TMEM at tP in two
 // halves (64 columns of 16-bit pairs, or 32 columns of e4m3 quadruples).  before_store()
 // runs once, after the first half is computed and before anything is stored; false from
 // it abandons the tile (returns false).  alpha receives the O rescale factor.
-template <bool MASK, int ET, class BeforeStore>
+// RESC (D = 128, P over S: O is final when the step begins): the 128 columns of O at tO
+// are multiplied by alpha here, in 32-column chunks woven between quarters of the
+// exponentials, every step (alpha = 1 exactly where the reference did not move, and 0 on
+// a tile's first step, whose P V then overwrites O; a branch around the chunks costs more
+// registers than the multiplies cost time).
+template <bool MASK, int ET, bool RESC, class BeforeStore>
 __device__ __forceinline__ bool softmax_tile(const uint32_t (&s)[128], int kbase, int limit,
                                              float sl2, float& m_run, float& l_run,
-                                             uint32_t tP, float& alpha,
+                                             uint32_t tP, uint32_t tO, float& alpha,
                                              BeforeStore&& before_store) {
     const float mt = tile_row_max<MASK, 128>(s, kbase, limit) * sl2;  // log2 units
     alpha = 1.0f;
@@ -693,15 +724,32 @@ __device__ __forceinline__ bool softmax_tile(const uint32_t (&s)[128], int kbase
     const float neg_m = -m_run;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     uint32_t pk[64];
-    tile_exp_half<0, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
+    uint32_t o[32];   // the O chunk in flight (RESC)
+    tile_exp_cols<0, 32, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
+    if constexpr (RESC) tmem_ld32_async(tO, o);
+    tile_exp_cols<32, 32, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
     if (!before_store()) return false;
     __syncwarp();
     if constexpr (ET == 2) ptx::tmem_st16(tP, &pk[0]);
     else ptx::tmem_st32p(tP, &pk[0]);
-    tile_exp_half<64, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
+    if constexpr (RESC) {
+        o_chunk_finish(tO, o, alpha);
+        tmem_ld32_async(tO + 32, o);
+    }
+    tile_exp_cols<64, 32, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
+    if constexpr (RESC) {
+        o_chunk_finish(tO + 32, o, alpha);
+        tmem_ld32_async(tO + 64, o);
+    }
+    tile_exp_cols<96, 32, MASK, ET>(s, kbase, limit, sl2, neg_m, acc, pk);
     __syncwarp();
     if constexpr (ET == 2) ptx::tmem_st16(tP + 16, &pk[16]);
     else ptx::tmem_st32p(tP + 32, &pk[32]);
+    if constexpr (RESC) {
+        o_chunk_finish(tO + 64, o, alpha);
+        tmem_ld32_async(tO + 96, o);
+        o_chunk_finish(tO + 96, o, alpha);
+    }
     const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     l_run = l_run * alpha + sum;
     return true;
@@ -757,12 +805,19 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
                     ptx::tc_fence_after();
                     return true;
                 };
+                // bf16 rows at D = 128 are rescaled at most steps (the reference follows
+                // every rise of the maximum): the rescale is woven into the step.  Other
+                // cases rescale after the step, when some row's reference rose (rarely
+                // for the lazy reference of fp16 and e4m3; at D <= 64 the step waits for
+                // the last P V only before its first P store, and the extra registers of
+                // a woven O chunk there cost more than they save).
+                constexpr bool kWeave = ET == 0 && !G::kSepP;
                 float alpha;
                 const bool ok =
-                    mask ? softmax_tile<true, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, alpha, before_store)
-                         : softmax_tile<false, ET>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, alpha, before_store);
+                    mask ? softmax_tile<true, ET, kWeave>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, tO, alpha, before_store)
+                         : softmax_tile<false, ET, kWeave>(s, kbase, limit, p.scale_log2, m_run, l_run, tP, tO, alpha, before_store);
                 if (!ok) return;
-                if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f))
+                if (!kWeave && j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f))
                     rescale_o<D, D == 128 ? 64 : 32>(tO, alpha);   // the running max rose: this row of O times alpha
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
@@ -951,8 +1006,8 @@ __device__ void softmax_role_split(const TcParams& p, const Ctl& c, uint32_t tme
             }
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             uint32_t pk[32];
-            if (mask) tile_exp_half<0, true, ET>(s, kbase, limit, p.scale_log2, -m_run, acc, pk);
-            else tile_exp_half<0, false, ET>(s, kbase, limit, p.scale_log2, -m_run, acc, pk);
+            if (mask) tile_exp_cols<0, 64, true, ET>(s, kbase, limit, p.scale_log2, -m_run, acc, pk);
+            else tile_exp_cols<0, 64, false, ET>(s, kbase, limit, p.scale_log2, -m_run, acc, pk);
             // With separate P columns, O += P(j-1) V(j-1) must be complete before P is
             // overwritten and before O is rescaled.
             if (G::kSepP && j > 0) {
