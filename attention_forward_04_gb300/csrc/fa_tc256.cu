@@ -432,13 +432,18 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     const float alpha =
                         mask ? softmax_step<true, ET>(s, key0, limit, sl2, m_run, l_run, pk)
                              : softmax_step<false, ET>(s, key0, limit, sl2, m_run, l_run, pk);
-                    if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                        // The reference rose: O += P(j-1) V_{j-1} must be complete, then this
-                        // row of O is rescaled in TMEM.  (The product before it is already
-                        // complete: S(j) was issued after it, so the parity wait below cannot
-                        // be two phases behind.)
+                    // The reference rose for some row: O += P(j-1) V_{j-1} must be complete,
+                    // then this row of O is rescaled in TMEM.  The item's last step waits for
+                    // that product in any case, so the epilogue's single wait is exact.  (The
+                    // product before it is complete: S(j) was issued after it; this step's own
+                    // product waits for its hand-over; so the parity wait sees the barrier at
+                    // most one phase behind and never ahead.)
+                    const bool resc = j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.0f);
+                    if (resc || (j > 0 && j + 1 == w.nkv)) {
                         if (!wait_warp(c, b_o_done(), (pv + (uint32_t)j - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                         ptx::tc_fence_after();
+                    }
+                    if (resc) {
                         // two 128-column TMEM round trips (this kernel's warps have the
                         // registers), packed multiplies in between
 #pragma unroll 1
@@ -458,12 +463,12 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar_addr(c, b_p_full(b)));
                 }
-                // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.  A parity
-                // wait is only sound while the barrier is at most one phase behind the awaited
-                // one; the item's third-to-last product (or the previous item's last one) is
-                // known complete, so wait for the last two one at a time.
+                // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.  The
+                // item's second-to-last product (or the previous item's last one) is known
+                // complete and no later product exists yet, so one parity wait for the last
+                // product is exact.  (Two waits in a row, for the last two products, would
+                // misread the barrier if both had completed before the first.)
                 pv += (uint32_t)w.nkv;
-                if (w.nkv >= 2 && !wait_warp(c, b_o_done(), (pv - 2u) & 1u, kRoleSoftmax)) goto sm_out;
                 if (!wait_warp(c, b_o_done(), (pv - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                 ptx::tc_fence_after();
                 const float inv = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)

@@ -1,0 +1,279 @@
+"""Models of the mbarrier protocols of two tensor-core kernels, run under random timing.
+
+Each model lists, per role of one CTA, the barrier operations the kernel performs in program
+order: waits (for phase k of a barrier, by parity k & 1, exactly as the kernels call
+mbarrier.try_wait.parity), arrivals, and products whose commits arrive later.  A scheduler
+interleaves the roles at random and completes TMA copies in any order and products in
+issue order.  A wait passes iff the barrier's completed-phase count has the other parity,
+which is what the hardware checks; the model reports
+
+  * premature: a wait passed before the phase it stands for had completed (the barrier
+    was two phases behind), and
+  * deadlock: no role can move (in particular a wait whose phase completed but whose
+    parity came round again, the barrier being two phases ahead).
+
+Models: the head-dimension-256 forward (fa_tc256.cu: S double-buffered, O += P V, the
+conditional O rescale, the per-item epilogue) and the head-dimension-256 backward
+(fa_bwd256.cu: the dQ / dK template and the dV kernel with its two S^T buffers and
+rings).  A change to either kernel's barrier order must be mirrored here.  Planted
+mistakes (the epilogue's two waits in a row; a single-buffered dV hand-over) must fail.
+"""
+import random
+
+import pytest
+
+
+class Model:
+    """Barriers with arrival counts; roles as lists of operations; random interleaving."""
+
+    def __init__(self, seed):
+        self.rnd = random.Random(seed)
+        self.need, self.got, self.done = {}, {}, {}
+
+    def bar(self, name, count=1):
+        self.need[name], self.got[name], self.done[name] = count, 0, 0
+
+    def arrive(self, name):
+        self.got[name] += 1
+        if self.got[name] == self.need[name]:
+            self.got[name] = 0
+            self.done[name] += 1
+
+    def run(self, roles, max_moves=200000):
+        """roles: name -> list of ('wait', bar, phase) | ('arrive', bar) |
+        ('copy', bar) (completes later, any order) | ('mma', [bars]) (commits later, in
+        order) | ('group', tag) (named barrier of the roles sharing tag).  Returns 'ok',
+        'premature ...' or 'deadlock ...'."""
+        pc = {r: 0 for r in roles}
+        copies, pipe = [], []
+        group_count = {}
+        for _ in range(max_moves):
+            ready = []
+            for r, prog in roles.items():
+                if pc[r] >= len(prog):
+                    continue
+                op = prog[pc[r]]
+                if op[0] == "wait":
+                    name, k = op[1], op[2]
+                    if (self.done[name] & 1) != (k & 1):
+                        if self.done[name] < k + 1:
+                            return "premature %s phase %d (completed %d)" % (name, k, self.done[name])
+                        ready.append(r)
+                elif op[0] == "group":
+                    tag, n = op[1], op[2]
+                    members = [x for x in roles if x.startswith(tag)]
+                    # passes when every member has reached this instance (or gone past it)
+                    if all(group_count.get(x, 0) > n or
+                           (pc[x] < len(roles[x]) and roles[x][pc[x]][:2] == ("group", tag)
+                            and roles[x][pc[x]][2] == n) for x in members):
+                        ready.append(r)
+                else:
+                    ready.append(r)
+            if copies:
+                ready.append("copy")
+            if pipe:
+                ready.append("pipe")
+            if not ready:
+                if all(pc[r] >= len(p) for r, p in roles.items()) and not copies and not pipe:
+                    return "ok"
+                return "deadlock " + str({r: roles[r][pc[r]] if pc[r] < len(roles[r]) else "end"
+                                          for r in roles})
+            r = self.rnd.choice(ready)
+            if r == "copy":
+                self.arrive(copies.pop(self.rnd.randrange(len(copies))))
+                continue
+            if r == "pipe":
+                for name in pipe.pop(0):
+                    self.arrive(name)
+                continue
+            op = roles[r][pc[r]]
+            if op[0] == "arrive":
+                self.arrive(op[1])
+            elif op[0] == "copy":
+                copies.append(op[1])
+            elif op[0] == "mma":
+                pipe.append(list(op[1]))
+            elif op[0] == "group":
+                group_count[r] = group_count.get(r, 0) + 1
+            pc[r] += 1
+        return "no end"
+
+
+# ----------------------------------------------------------------- D = 256 forward
+def tc256_roles(m, items, rescale_prob, two_epilogue_waits=False):
+    """fa_tc256.cu, one CTA over `items` (key steps per item); loads are taken as ready."""
+    for b in (0, 1):
+        m.bar(("s_full", b))
+        m.bar(("p_full", b))
+    m.bar("o_done")
+    m.bar("q_ready")
+    mma, sm = [], []
+    g = 0
+    for it, nkv in enumerate(items):
+        mma.append(("wait", "q_ready", it))
+        mma.append(("mma", [("s_full", g & 1)]))
+        if nkv > 1:
+            mma.append(("mma", [("s_full", (g + 1) & 1)]))
+        for j in range(nkv):
+            gj = g + j
+            mma.append(("wait", ("p_full", gj & 1), gj >> 1))
+            mma.append(("mma", ["o_done"]))
+            if j + 2 < nkv:
+                mma.append(("mma", [("s_full", (gj + 2) & 1)]))
+        g += nkv
+    g = pv = 0
+    for nkv in items:
+        sm.append(("arrive", "q_ready"))
+        for j in range(nkv):
+            gj = g + j
+            sm.append(("wait", ("s_full", gj & 1), gj >> 1))
+            resc = j > 0 and m.rnd.random() < rescale_prob
+            last_sync = (j > 0 and j + 1 == nkv) and not two_epilogue_waits
+            if resc or last_sync:
+                sm.append(("wait", "o_done", pv + j - 1))
+            sm.append(("arrive", ("p_full", gj & 1)))
+        pv += nkv
+        if two_epilogue_waits and nkv >= 2:
+            sm.append(("wait", "o_done", pv - 2))
+        sm.append(("wait", "o_done", pv - 1))
+        g += nkv
+    return {"mma": mma, "softmax": sm}
+
+
+@pytest.mark.parametrize("rescale_prob", [0.0, 0.5, 1.0])
+def test_tc256_forward_protocol(rescale_prob):
+    for seed in range(300):
+        m = Model(seed)
+        items = [m.rnd.randint(1, 6) for _ in range(m.rnd.randint(1, 4))]
+        res = m.run(tc256_roles(m, items, rescale_prob))
+        assert res == "ok", (seed, items, res)
+
+
+def test_tc256_planted_two_epilogue_waits_fail():
+    # waiting for the last two products one after the other misreads the parity when both
+    # completed before the first wait
+    bad = 0
+    for seed in range(300):
+        m = Model(seed)
+        items = [m.rnd.randint(2, 6) for _ in range(m.rnd.randint(1, 4))]
+        bad += m.run(tc256_roles(m, items, 0.5, two_epilogue_waits=True)) != "ok"
+    assert bad > 0
+
+
+# ----------------------------------------------------------------- D = 256 backward
+def bwd256_roles(m, role, n, slots, single_buffer_dv=False):
+    """fa_bwd256.cu, one CTA: role 'dq' / 'dk' (one template) or 'dv'; n streamed
+    sub-tiles; two elementwise warp groups (ew0, ew1) standing for the eight warps."""
+    fixed = role != "dv"
+    m.bar("fixed")
+    for s in range(slots):
+        m.bar(("full", s))
+        m.bar(("empty", s))
+    for b in (0, 1):
+        m.bar(("s", b))
+        m.bar(("x", b), 2)
+    m.bar("dp")
+    m.bar("ds", 2)
+    m.bar("row")
+    m.bar("done")
+    slot = lambda pos: pos % slots
+    fill = lambda pos: pos // slots
+    # the loader's order of streamed sub-tiles (after the row tile's two halves)
+    if role != "dv":
+        order = [("X" if k % 2 == 0 else "Y", k // 2) for k in range(2 * n)]
+    else:
+        order = [("X", 0)] + ([("X", 1)] if n > 1 else [])
+        for s in range(n):
+            order.append(("Y", s))
+            if s + 2 < n:
+                order.append(("X", s + 2))
+    pos_of = {o: 2 + i for i, o in enumerate(order)}
+    load = [("copy", "fixed")] if fixed else []
+    for pos in range(2 + 2 * n):
+        if pos >= slots:
+            load.append(("wait", ("empty", slot(pos)), fill(pos) - 1))
+        load.append(("copy", ("full", slot(pos))))
+    mma = [("wait", "fixed", 0)] if fixed else []
+    mma.append(("wait", "row", 0))
+
+    def full(o):
+        p = pos_of[o]
+        return ("wait", ("full", slot(p)), fill(p))
+
+    if role != "dv":
+        def issue_s(j):
+            mma.extend([full(("X", j)), ("mma", [("s", 0)])])
+
+        def issue_dp(j):
+            mma.extend([full(("Y", j)), ("mma", ["dp", ("empty", slot(pos_of[("Y", j)]))])])
+
+        issue_s(0)
+        issue_dp(0)
+        for j in range(n):
+            mma.append(("wait", ("x", 0), j))
+            if j + 1 < n:
+                issue_s(j + 1)
+            mma.append(("wait", "ds", j))
+            mma.append(("mma", [("empty", slot(pos_of[("X", j)]))]))
+            if j + 1 < n:
+                issue_dp(j + 1)
+    else:
+        def issue_s(s):
+            b = 0 if single_buffer_dv else s & 1
+            mma.extend([full(("X", s)), ("mma", [("s", b), ("empty", slot(pos_of[("X", s)]))])])
+
+        issue_s(0)
+        if n > 1:
+            issue_s(1)
+        for s in range(n):
+            if single_buffer_dv:
+                mma.append(("wait", ("x", 0), s))
+            else:
+                mma.append(("wait", ("x", s & 1), s >> 1))
+            mma.extend([full(("Y", s)), ("mma", [("empty", slot(pos_of[("Y", s)]))])])
+            if s + 2 < n:
+                issue_s(s + 2)
+    mma.append(("mma", ["done"]))
+
+    def ew(first):
+        e = [("wait", "fixed", 0)] if role == "dq" else []
+        e += [("wait", ("full", slot(0)), 0), ("wait", ("full", slot(1)), 0), ("group", "ew", 0)]
+        if first:
+            e += [("arrive", ("empty", slot(0))), ("arrive", ("empty", slot(1))), ("arrive", "row")]
+        k = 1
+        for j in range(n):
+            if role == "dv":
+                if single_buffer_dv:
+                    e.append(("wait", ("s", 0), j))
+                else:
+                    e.append(("wait", ("s", j & 1), j >> 1))
+                e.append(("group", "ew", k)); k += 1
+                e.append(("arrive", ("x", 0 if single_buffer_dv else j & 1)))
+            else:
+                e.append(("wait", ("s", 0), j))
+                if role == "dk":
+                    e.append(("group", "ew", k)); k += 1
+                e.append(("arrive", ("x", 0)))
+                e.append(("wait", "dp", j))
+                e.append(("arrive", "ds"))
+        e.append(("wait", "done", 0))
+        return e
+
+    return {"load": load, "mma": mma, "ew0": ew(True), "ew1": ew(False)}
+
+
+@pytest.mark.parametrize("role,slots", [("dq", 5), ("dk", 5), ("dv", 6)])
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8])
+def test_bwd256_protocol(role, slots, n):
+    for seed in range(60):
+        m = Model(seed)
+        res = m.run(bwd256_roles(m, role, n, slots))
+        assert res == "ok", (role, n, seed, res)
+
+
+def test_bwd256_planted_single_buffered_dv_fails():
+    bad = 0
+    for seed in range(60):
+        m = Model(seed)
+        bad += m.run(bwd256_roles(m, "dv", 4, 6, single_buffer_dv=True)) != "ok"
+    assert bad > 0
