@@ -483,6 +483,7 @@ int backward(const BwdRequest& r) {
     p.heads = (int)r.H;
     p.total = (int)r.T;
     p.cu_seqlens = r.cu;
+    p.inject_stall = g_inject_stall.load();
     cudaStream_t st = static_cast<cudaStream_t>(r.stream);
     e = d256 ? fa::bwd256_launch(dic, f16, p, (int)BH, st) : fa::bwd_launch((int)r.D, dic, f16, p, (int)BH, st);
     return e == cudaSuccess ? FA_OK : fail_cuda(e, "backward kernel launch");

@@ -276,10 +276,12 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, 
 // dK/dV loader: the two fixed tiles (f0, f1 at fixed_row), then for steps j < steps the
 // tiles A_j (map ma) and B_j (map mb), rows first_row + 128 j, through the paired ring.
 // Waits for its own copies before returning, so no copy is in flight when the CTA leaves.
+// withhold (failure-detection test hook): A_0 is never loaded, so the waits for it run out.
 template <int D, int MODE>
 __device__ void load_pairs(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
                            const CUtensorMap* f1, int fixed_row, const CUtensorMap* ma,
-                           const CUtensorMap* mb, int first_row, int steps, int bh, const Slice& sl) {
+                           const CUtensorMap* mb, int first_row, int steps, int bh, const Slice& sl,
+                           bool withhold) {
     using G = GeoDkdv<D>;
     const uint32_t fb = bar_addr(c, G::fixed_full());
     ptx::mbar_arrive_expect_tx(fb, 2u * G::kTile);
@@ -290,6 +292,10 @@ __device__ void load_pairs(const Ctl& c, uint32_t sbase, const CUtensorMap* f0,
         for (int w = 0; w < 2; ++w) {
             const uint32_t slot = w == 0 ? slot_a(j) : slot_b(j);
             if (!wait(c, G::ring_empty(slot), slot_par(j) ^ 1u, kRoleLoad)) goto out;
+            if (withhold && issued == 0) {
+                ++issued;
+                continue;
+            }
             const uint32_t bar = bar_addr(c, G::ring_full(slot));
             ptx::mbar_arrive_expect_tx(bar, (uint32_t)G::kTile);
             load_tile<D, MODE>(sbase + (uint32_t)G::kRingOff + slot * (uint32_t)G::kTile, w == 0 ? ma : mb,
@@ -301,6 +307,7 @@ out:
     wait_drain(fb, 0, c.limit);
     // copies of the last two steps may still be in flight
     for (int k = (issued > 4 ? issued - 4 : 0); k < issued; ++k) {
+        if (withhold && k == 0) continue;
         const int j = k >> 1;
         wait_drain(bar_addr(c, G::ring_full((k & 1) ? slot_b(j) : slot_a(j))), slot_par(j), c.limit);
     }
@@ -308,7 +315,7 @@ out:
 
 // dQ loader: the fixed tile dO (rows fixed_row), then streamed tile 0 = Q (rows fixed_row)
 // and tiles 1 + 2j = K_j, 2 + 2j = V_j (rows 128 j) through the cyclic ring.  Waits for its
-// own copies before returning.
+// own copies before returning.  Failure-detection test hook: CTA 0 withholds Q.
 template <int D, int MODE>
 __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fixed_row, int nkv,
                         int bh, const Slice& sl) {
@@ -317,10 +324,12 @@ __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fi
     ptx::mbar_arrive_expect_tx(fb, (uint32_t)G::kTile);
     load_tile<D, MODE>(sbase, &p.tmap_do, fb, fixed_row, bh, sl);
     const uint32_t count = 1u + 2u * (uint32_t)nkv;
+    const uint32_t skipped = (p.inject_stall == 1 && blockIdx.x == 0) ? 0u : 0xFFFFFFFFu;
     uint32_t pos = 0;
     for (; pos < count; ++pos) {
         const uint32_t slot = G::cyc_slot(pos);
         if (!wait(c, G::ring_empty(slot), G::cyc_par(pos) ^ 1u, kRoleLoad)) break;
+        if (pos == skipped) continue;
         const uint32_t bar = bar_addr(c, G::ring_full(slot));
         const CUtensorMap* map = pos == 0 ? &p.tmap_q : ((pos & 1u) ? &p.tmap_k : &p.tmap_v);
         const int row = pos == 0 ? fixed_row : (int)((pos - 1u) >> 1) * kT;
@@ -329,7 +338,7 @@ __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fi
     }
     wait_drain(fb, 0, c.limit);
     for (uint32_t i = (pos > (uint32_t)G::kSlots ? pos - G::kSlots : 0u); i < pos; ++i)
-        wait_drain(bar_addr(c, G::ring_full(G::cyc_slot(i))), G::cyc_par(i), c.limit);
+        if (i != skipped) wait_drain(bar_addr(c, G::ring_full(G::cyc_slot(i))), G::cyc_par(i), c.limit);
 }
 
 // ----------------------------------------------------------------- dQ kernel
@@ -604,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
     if (warp == kLoadWarp) {
         if (lane == 0)
             load_pairs<D, MODE>(c, su.sbase, &p.tmap_k, &p.tmap_v, kt * kT, &p.tmap_q, &p.tmap_do,
-                                i0 * kT, nq, bh, sl);
+                                i0 * kT, nq, bh, sl, p.inject_stall == 1 && blockIdx.x == 0);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_nt = make_idesc(kT, kT, false, F16);

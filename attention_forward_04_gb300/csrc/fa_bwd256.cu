@@ -155,11 +155,13 @@ __device__ __forceinline__ void load_rows64(uint32_t dst, uint32_t panel, const 
 // The loader: the fixed tile (dQ: dO, dK: V; rows fix_row..), the row tile's two halves
 // (pos 0, 1; rows row0..), then the streamed sub-tiles in the order the MMA warp takes
 // them: dQ, dK: X_0, Y_0, X_1, Y_1, ...; dV: X_0, X_1, Y_0, X_2, Y_1, X_3, ... (sub-tile
-// t covers rows (s0 + t) * 64..).  Waits for its own copies before returning.
+// t covers rows (s0 + t) * 64..).  Waits for its own copies before returning.  Position
+// `skipped` (failure-detection test hook) is never loaded, so the waits for it run out.
 template <int ROLE, int MODE>
 __device__ void load_role(const Ctl& c, uint32_t sbase, const CUtensorMap* fixed,
                           const CUtensorMap* rowmap, int row0, const CUtensorMap* xmap,
-                          const CUtensorMap* ymap, int s0, int n, int bh, const Slice& sl) {
+                          const CUtensorMap* ymap, int s0, int n, int bh, const Slice& sl,
+                          uint32_t skipped) {
     using G = G256<ROLE>;
     const uint32_t ring = sbase + (uint32_t)G::kRingOff;
     if constexpr (G::kFixed) {
@@ -173,6 +175,7 @@ __device__ void load_role(const Ctl& c, uint32_t sbase, const CUtensorMap* fixed
     for (; pos < count; ++pos) {
         const uint32_t slot = G::slot(pos);
         if (!wait(c, G::ring_empty(slot), G::par(pos) ^ 1u, kRoleLoad)) break;
+        if (pos == skipped) continue;
         const uint32_t bar = bar_addr(c, G::ring_full(slot));
         const CUtensorMap* map;
         int row;
@@ -209,7 +212,7 @@ __device__ void load_role(const Ctl& c, uint32_t sbase, const CUtensorMap* fixed
     }
     if constexpr (G::kFixed) wait_drain(bar_addr(c, G::fixed_full()), 0, c.limit);
     for (uint32_t i = (pos > (uint32_t)G::kSlots ? pos - G::kSlots : 0u); i < pos; ++i)
-        wait_drain(bar_addr(c, G::ring_full(G::slot(i))), G::par(i), c.limit);
+        if (i != skipped) wait_drain(bar_addr(c, G::ring_full(G::slot(i))), G::par(i), c.limit);
 }
 
 // ----------------------------------------------------------------- prologue
@@ -355,12 +358,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_kernel(const __grid_consta
 
     if (warp == kLoadWarp) {
         if (lane == 0) {
+            const uint32_t skipped = (p.inject_stall == 1 && blockIdx.x == 0) ? 0u : 0xFFFFFFFFu;
             if (kDQ)
                 load_role<ROLE, MODE>(c, su.sbase, &p.tmap_do, &p.tmap_q, tile * kT, &p.tmap_k,
-                                      &p.tmap_v, s0, n, bh, sl);
+                                      &p.tmap_v, s0, n, bh, sl, skipped);
             else
                 load_role<ROLE, MODE>(c, su.sbase, &p.tmap_v, &p.tmap_k, tile * kT, &p.tmap_q,
-                                      &p.tmap_do, s0, n, bh, sl);
+                                      &p.tmap_do, s0, n, bh, sl, skipped);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -585,7 +589,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_dv_kernel(const __grid_con
     if (warp == kLoadWarp) {
         if (lane == 0)
             load_role<kRoleDV, MODE>(c, su.sbase, nullptr, &p.tmap_k, tile * kT, &p.tmap_q,
-                                     &p.tmap_do, s0, n, bh, sl);
+                                     &p.tmap_do, s0, n, bh, sl,
+                                     (p.inject_stall == 1 && blockIdx.x == 0) ? 0u : 0xFFFFFFFFu);
         __syncwarp();
     } else if (warp == kMmaWarp) {
         constexpr uint32_t id_s = make_idesc(kT, kSub, false, F16);

@@ -54,6 +54,7 @@ struct BwdParams {
     int heads;            // H
     int total;            // tokens (token-major layouts)
     const int* cu_seqlens;   // packed sequences: batch + 1 token offsets; nullptr otherwise
+    int inject_stall;     // failure-detection test hook (see fa_set_watchdog)
 };
 
 // Raise the dynamic shared-memory limit of the backward tensor-core kernels (once).

@@ -264,11 +264,12 @@ int fa_check_device_status(void* stream, uint32_t* detail);
  * launches made after the call, in this process).
  *   wait_limit_cycles : SM clock cycles any single wait may spin before the kernel gives
  *                       up; 0 restores the default (2^32 cycles, about two seconds).
- *   inject_stall      : 0 = normal.  1 = in CTA 0 the loader withholds the first K/V tile
- *                       load of its first work item, so the waits for it run out.  This
- *                       exists so tests can check that a stuck pipeline ends with
- *                       FA_ERR_TIMEOUT instead of a hang; the outputs of that call are
- *                       then undefined.
+ *   inject_stall      : 0 = normal.  1 = in CTA 0 of each tensor-core kernel the loader
+ *                       withholds one tile (the forward: the first K/V tile of its first
+ *                       work item; the backward kernels: the first tile they stream), so
+ *                       the waits for it run out.  This exists so tests can check that a
+ *                       stuck pipeline ends with FA_ERR_TIMEOUT instead of a hang; the
+ *                       outputs of that call are then undefined.
  * Returns FA_OK, or FA_ERR_INVALID_ARG for an unknown inject_stall value.
  */
 int fa_set_watchdog(uint64_t wait_limit_cycles, int inject_stall);

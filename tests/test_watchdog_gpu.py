@@ -65,3 +65,33 @@ def test_short_limit_alone_does_not_fire():
         binding.set_watchdog(0, 0)
     assert st == FA_OK, detail
     assert bool(torch.isfinite(o).all())
+
+
+# The backward kernels bound their waits the same way: dQ (and, at D = 256, dV and dK) and
+# the dK/dV kernel each withhold one streamed tile in CTA 0.  Every kernel of the call must
+# give up and leave; the next call on the same context must give exactly the results of a
+# call made before the stall (the backward is deterministic).
+@pytest.mark.parametrize("D", [128, 256])
+def test_stalled_backward_reports_timeout_and_context_survives(D):
+    from attention_forward_04_gb300.inputs import make_shape_dout
+    q, k, v = (t.cuda() for t in make_shape(1, 4, 640, D, "bf16", seed=47))
+    do = make_shape_dout(1, 4, 640, D, "bf16", seed=47).cuda()
+    assert binding.check_device_status()[0] == FA_OK
+    o, lse = binding.fwd(q, k, v, causal=True)
+    before = binding.bwd(q, k, v, o, lse, do, causal=True)
+    assert binding.check_device_status()[0] == FA_OK
+    try:
+        binding.set_watchdog(1 << 22, 1)   # ~2 ms per wait; CTA 0 of each kernel withholds a tile
+        binding.bwd(q, k, v, o, lse, do, causal=True)
+        st, detail = binding.check_device_status()
+    finally:
+        binding.set_watchdog(0, 0)
+    assert st == FA_ERR_TIMEOUT, (st, detail)
+    assert detail[0] == 1 and detail[2] == 0, detail   # a wait in CTA 0 gave up
+    assert detail[1] in (1, 2, 3), detail             # elementwise, MMA or loader role
+
+    assert binding.check_device_status()[0] == FA_OK
+    after = binding.bwd(q, k, v, o, lse, do, causal=True)
+    assert binding.check_device_status()[0] == FA_OK
+    for a, b in zip(before, after):
+        assert torch.equal(a, b)
