@@ -349,8 +349,10 @@ __device__ void load_dq(const Ctl& c, uint32_t sbase, const BwdParams& p, int fi
 template <int D, bool CAUSAL, bool F16, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) bwd_dq_kernel(const __grid_constant__ BwdParams p) {
     using G = GeoDq<D>;
-    // query tiles past a (shorter packed) sequence have nothing to do: the whole CTA leaves
-    const int bh = blockIdx.x / p.ntiles, qt = blockIdx.x % p.ntiles;
+    // query tiles past a (shorter packed) sequence have nothing to do: the whole CTA leaves.
+    // Causal: a slice's last query tile sees the most keys, so it is dispatched first.
+    const int bh = blockIdx.x / p.ntiles;
+    const int qt = CAUSAL ? p.ntiles - 1 - blockIdx.x % p.ntiles : blockIdx.x % p.ntiles;
     const Slice sl = slice_at<MODE, D>(p, bh);
     if (qt * kT >= sl.len) return;
     constexpr uint32_t kQC = D / 2 < 32 ? 32 : D / 2;

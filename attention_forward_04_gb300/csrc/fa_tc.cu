@@ -28,7 +28,9 @@
 //     only when it grows by more than 2^8 (finer P rounding leaves room), and only then
 //     is O rescaled in TMEM ("08 · FlashAttention" §五 and "第 13 课" §4B: old output
 //     multiplied by exp(m_old - m_new) when a larger maximum appears; keeping a stale
-//     reference is exact after the final division, since O and l share it).
+//     reference is exact after the final division, since O and l share it).  bf16 at
+//     D = 128 rescales at most steps, so there the row of O is multiplied inside the
+//     softmax step, 32 TMEM columns at a time between quarters of the exponentials.
 //   * epilogue: O / l (one division per row at the end, "第 13 课" exercise; "pwwt.cn"
 //     §2.2), staged per warp through shared memory in the 128-byte-swizzled layout, then
 //     written by one TMA bulk tensor store per 64-column panel ([B, H, N, D], D >= 64) or
