@@ -366,6 +366,12 @@ def bwd_flops(w) -> float:
     return 2.5 * w.flops
 
 
+def bwd_launches_per_call(w) -> int:
+    """Kernels one fa_bwd call launches: dQ (which forms delta) and dK/dV (fp32 on the CUDA
+    cores, and 16-bit at D <= 128), or dQ, dV and dK (16-bit at D = 256)."""
+    return 3 if w.D == 256 and w.dtype != "fp32" else 2
+
+
 def time_oracle_bwd(w, budget_s: float, host):
     """The fp64 backward oracle, as it stands, on whole (b, h) slices within the budget."""
     from oracle.backward import attention_bwd
@@ -569,7 +575,7 @@ def run_bwd(args, w):
                 "pipelining": "host->device copies (one stream per input), the call and "
                               "device->host copies of consecutive steps overlap (two device "
                               "buffer sets)"},
-        "gpu_launches": 2 * args.steps,   # dQ (with delta) and dK/dV kernels
+        "gpu_launches": bwd_launches_per_call(w) * args.steps,
         "roofline": roof, "cpu_baseline": cpu,
         "clocks": sampler.summary(t_wall0, t_wall1),
     }

@@ -1,6 +1,7 @@
 """bench.py's contract on the CPU: the reference arm (the fp64 oracle, timed on the host)
 prints one complete JSON line, and the GPU arm fails loudly where there is no GPU instead
 of falling back to anything."""
+import importlib.util
 import json
 import os
 import subprocess
@@ -63,3 +64,19 @@ def test_l2_handling_follows_input_set_size():
         assert "flushed before every timed call" in bench.l2_note(bench.input_set_bytes(WORKLOADS[name]))
     assert bench.flush_buffer(torch, "cpu", bench.input_set_bytes(head)) is None
     assert bench.L2_BYTES < bench.FLUSH_BYTES
+
+
+def test_backward_launch_count_per_call():
+    # gpu_launches of a backward line counts the kernels of every call
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    argv = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        spec.loader.exec_module(bench)
+    finally:
+        sys.argv = argv
+    from attention_forward_04_gb300.inputs import WORKLOADS
+    assert bench.bwd_launches_per_call(WORKLOADS["bf16_b4h16n4096d128"]) == 2
+    assert bench.bwd_launches_per_call(WORKLOADS["bf16_b4h8n4096d256"]) == 3
+    assert bench.bwd_launches_per_call(WORKLOADS["fp32_b1h1n256d64"]) == 2
