@@ -96,9 +96,12 @@ def test_bf16_edge_shapes(N, D, causal):
     full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "bf16", "N=%d D=%d causal=%d" % (N, D, causal))
 
 
-# The fp32 kernel runs 32-row CTAs of 4 threads per row, or, when those would not give
-# every SM (152 on GB300) a CTA, 8-row CTAs of 16 threads per row.  Small shapes take the
-# second form; this one (4 x 8 slices x 10 row blocks = 320 CTAs) takes the first.
+# The fp32 forward takes one of three CTA forms: at D <= 128, when two-row CTAs fit in two
+# waves (<= 304 on GB300), two rows per CTA with the threads across keys; otherwise 32-row
+# CTAs of 4 threads per row, or, when those would not give every SM a CTA, 8-row CTAs of 16
+# threads per row.  The edge shapes below take the first form (and the third at D = 256),
+# test_fp32_middle_shapes the third, and this one (4 x 8 slices x 10 row blocks = 320
+# CTAs) the second.
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [32, 64, 128, 256])
 def test_fp32_narrow_cta_shape(D, causal):
@@ -112,6 +115,17 @@ def test_fp32_narrow_cta_shape(D, causal):
 @pytest.mark.parametrize("N", [1, 33, 200, 256, 300])
 def test_fp32_edge_shapes(N, D, causal):
     q, k, v = make_shape(2, 1, N, D, "fp32", seed=N * 11 + D)
+    full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "fp32", "N=%d D=%d causal=%d" % (N, D, causal))
+
+
+# 2 slices of 1000 or 2000 rows: too many two-row CTAs for two waves, too few 32-row CTAs
+# for the SMs, so the 8-row CTAs of 16 threads per row (ragged last block at N = 1000)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("N", [1000, 2000])
+def test_fp32_middle_shapes(N, D, causal):
+    assert 2 * ((N + 1) // 2) > 2 * 152 and 2 * ((N + 31) // 32) < 152
+    q, k, v = make_shape(1, 2, N, D, "fp32", seed=N * 13 + D)
     full_compare(q, k, v, 1.0 / math.sqrt(D), causal, "fp32", "N=%d D=%d causal=%d" % (N, D, causal))
 
 
