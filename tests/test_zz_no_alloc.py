@@ -58,6 +58,7 @@ def _problem(B, H, N, D, dtype, seed, causal):
 @pytest.mark.parametrize("shape,dtype,causal", [
     ((2, 3, 700, 128), "bf16", False),
     ((1, 4, 1000, 64), "fp16", True),
+    ((1, 4, 500, 256), "bf16", True),          # head dimension 256: dQ, dV and dK kernels
     ((1, 256, 4096, 64), "bf16", True),        # B*H*N = 1,048,576 rows: exactly the limit
 ])
 def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row(lib, shape, dtype, causal):
