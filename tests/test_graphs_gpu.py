@@ -59,9 +59,10 @@ def test_fp8_forward_graph_replay_matches_eager():
     assert torch.equal(o_g, o_e) and torch.equal(lse_g, lse_e)
 
 
-def test_backward_graph_replay_matches_eager():
-    q, k, v = inputs(4)
-    do = make_shape_dout(2, 3, 700, 128, "bf16", seed=4).cuda()
+@pytest.mark.parametrize("D", [128, 256])
+def test_backward_graph_replay_matches_eager(D):
+    q, k, v = inputs(4, D=D)
+    do = make_shape_dout(2, 3, 700, D, "bf16", seed=4).cuda()
     o, lse = binding.fwd(q, k, v, causal=True)
     binding.bwd(q, k, v, o, lse, do, causal=True)
     torch.cuda.synchronize()
@@ -69,9 +70,9 @@ def test_backward_graph_replay_matches_eager():
     with torch.cuda.graph(g):
         o_g, lse_g = binding.fwd(q, k, v, causal=True)
         grads_g = binding.bwd(q, k, v, o_g, lse_g, do, causal=True)
-    for dst, src in zip((q, k, v), inputs(5)):
+    for dst, src in zip((q, k, v), inputs(5, D=D)):
         dst.copy_(src)
-    do.copy_(make_shape_dout(2, 3, 700, 128, "bf16", seed=5).cuda())
+    do.copy_(make_shape_dout(2, 3, 700, D, "bf16", seed=5).cuda())
     g.replay()
     o_e, lse_e = binding.fwd(q, k, v, causal=True)
     grads_e = binding.bwd(q, k, v, o_e, lse_e, do, causal=True)
