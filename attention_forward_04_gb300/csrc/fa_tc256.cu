@@ -65,10 +65,18 @@ __device__ __forceinline__ uint32_t ring_par(uint32_t pos) { return (pos / kSlot
 // Streamed tiles of an item, from its first ring position: 0 and 1 are the two 64-row
 // halves of the Q tile, then K_j = 2 + 2j and V_j = 3 + 2j.
 
-// The reference is raised when a step's maximum exceeds it by more than kRescaleLog2 log2
-// units: bf16 0 (the literal reading: the row's largest P is exactly 1, so its bf16
-// rounding costs nothing), fp16 and e4m3 8 (P stays below 2^8).
-template <int ET> struct Lazy { static constexpr float kRescaleLog2 = ET == 0 ? 0.0f : 8.0f; };
+// The reference is raised when a step's maximum exceeds it by more than kRescaleLog2 = 8
+// log2 units (P stays below 2^8); otherwise the stale reference is kept, which the final
+// division cancels.  For bf16 P (8 significant bits) a stale reference alone would leave a
+// row's largest P rounded (2^x for fractional x) while the row sum kept the unrounded
+// value; so at bf16 O is divided by a second row sum, of the bf16-rounded P that O += P V
+// multiplies, and the rounding of P cancels in the quotient (the unrounded sum still gives
+// the LSE).  A rescale moves 256 columns of O through TMEM here, four times the work per
+// key of the smaller head dimensions, which take the literal reading for bf16 instead.
+template <int ET> struct Lazy {
+    static constexpr float kRescaleLog2 = 8.0f;
+    static constexpr bool kRoundedSum = ET == 0;
+};
 
 // Per element type: bytes per value, 128-byte panels per 256-value row, bytes of a tile.
 template <int ET> struct Elem {
@@ -102,14 +110,14 @@ __device__ __forceinline__ bool sm_barrier_and(bool ok) {
 }
 
 // One 64-key step of one row: running-max update (raised when the step's maximum exceeds
-// it by more than kRescaleLog2 log2 units), p = 2^(s * sl2 - m), row sum (of the fp32
-// values), and P packed to 16-bit pairs in pk[0, 32), or to e4m3 quadruples in pk[0, 16).
-// Keys at or past `limit` count as absent (MASK).  Eight independent max chains and four
-// paired sum chains keep the dependent depth short.  Returns the factor
-// the row's O and l must be scaled by.
+// it by more than kRescaleLog2 log2 units), p = 2^(s * sl2 - m), row sum l_run (of the fp32
+// values), and P packed to 16-bit pairs in pk[0, 32), or to e4m3 quadruples in pk[0, 16);
+// at bf16 also l_rnd, the row sum of the packed (rounded) values.  Keys at or past `limit`
+// count as absent (MASK).  Eight independent max chains and four paired sum chains keep
+// the dependent depth short.  Returns the factor the row's O and sums must be scaled by.
 template <bool MASK, int ET>
 __device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0, int limit,
-                                              float sl2, float& m_run, float& l_run,
+                                              float sl2, float& m_run, float& l_run, float& l_rnd,
                                               uint32_t (&pk)[32]) {
     float mx[8];
 #pragma unroll
@@ -132,6 +140,7 @@ __device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0,
     }
     const float neg_m = -m_run;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float accr[4] = {0.f, 0.f, 0.f, 0.f};   // bf16: sums of the rounded values
 #pragma unroll
     for (int cc = 0; cc < 64; cc += 4) {
         float x[4], pr[4];
@@ -150,10 +159,17 @@ __device__ __forceinline__ float softmax_step(const uint32_t (&s)[64], int key0,
         } else {
             pk[cc >> 1] = pack2<ET == 1>(pr[0], pr[1]);
             pk[(cc >> 1) + 1] = pack2<ET == 1>(pr[2], pr[3]);
+            if constexpr (Lazy<ET>::kRoundedSum) {
+                const int ar = ((cc >> 2) & 1) * 2;
+                ptx::add2(accr[ar], accr[ar + 1], unpack_lo<false>(pk[cc >> 1]), unpack_hi<false>(pk[cc >> 1]));
+                ptx::add2(accr[ar], accr[ar + 1], unpack_lo<false>(pk[(cc >> 1) + 1]),
+                          unpack_hi<false>(pk[(cc >> 1) + 1]));
+            }
         }
     }
     const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
     l_run = l_run * alpha + sum;
+    if constexpr (Lazy<ET>::kRoundedSum) l_rnd = l_rnd * alpha + ((accr[0] + accr[1]) + (accr[2] + accr[3]));
     return alpha;
 }
 
@@ -342,11 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                 ptx::tc_fence_after();
                 if (!issue_s(g, base + 2u)) goto mma_out;
                 if (w.nkv > 1 && !issue_s(g + 1u, base + 4u)) goto mma_out;
+                if (!wait_warp(c, b_ring_full(base + 3u), ring_par(base + 3u), kRoleMma)) goto mma_out;
                 for (int j = 0; j < w.nkv; ++j) {
                     const uint32_t gj = g + (uint32_t)j, b = gj & 1u;
                     const uint32_t vpos = base + 3u + 2u * (uint32_t)j;
+                    // V_j is resident (waited for before S(j+1) was issued): between the last
+                    // product of S(j+1) entering the tensor queue and the first of O += P V,
+                    // only the hand-over of P is awaited.
                     if (!wait_warp(c, b_p_full(b), (gj >> 1) & 1u, kRoleMma)) goto mma_out;
-                    if (!wait_warp(c, b_ring_full(vpos), ring_par(vpos), kRoleMma)) goto mma_out;
                     ptx::tc_fence_after();
                     const uint64_t vd = vdesc(vpos);
                     // K steps of kKeys keys: P's 8 TMEM columns, kKeys rows of 128 bytes of V
@@ -363,6 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     }
                     ptx::mma_commit_elect(bar_addr(c, b_o_done()));
                     ptx::mma_commit_elect(bar_addr(c, b_ring_empty(vpos)));
+                    if (j + 1 < w.nkv && !wait_warp(c, b_ring_full(vpos + 2u), ring_par(vpos + 2u), kRoleMma))
+                        goto mma_out;
                     if (j + 2 < w.nkv && !issue_s(gj + 2u, base + 2u + 2u * (uint32_t)(j + 2))) goto mma_out;
                 }
                 g += (uint32_t)w.nkv;
@@ -418,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                         ptx::mbar_arrive(bar_addr(c, b_q_ready()));
                     }
                 }
-                float m_run = -INFINITY, l_run = 0.0f;   // reference max (log2 units) and row sum
+                // reference max (log2 units), row sum, and (bf16) row sum of the rounded P
+                float m_run = -INFINITY, l_run = 0.0f, l_rnd = 0.0f;
                 for (int j = 0; j < w.nkv; ++j) {
                     const uint32_t gj = g + (uint32_t)j, b = gj & 1u;
                     const uint32_t tS = tm + tl + kColS + 64u * b;
@@ -430,8 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     const bool mask = __any_sync(0xFFFFFFFFu, key0 + kBN > limit);
                     uint32_t pk[32];
                     const float alpha =
-                        mask ? softmax_step<true, ET>(s, key0, limit, sl2, m_run, l_run, pk)
-                             : softmax_step<false, ET>(s, key0, limit, sl2, m_run, l_run, pk);
+                        mask ? softmax_step<true, ET>(s, key0, limit, sl2, m_run, l_run, l_rnd, pk)
+                             : softmax_step<false, ET>(s, key0, limit, sl2, m_run, l_run, l_rnd, pk);
                     // The reference rose for some row: O += P(j-1) V_{j-1} must be complete,
                     // then this row of O is rescaled in TMEM.  The item's last step waits for
                     // that product in any case, so the epilogue's single wait is exact.  (The
@@ -471,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                 pv += (uint32_t)w.nkv;
                 if (!wait_warp(c, b_o_done(), (pv - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                 ptx::tc_fence_after();
-                const float inv = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
+                // o_scale: V's dequantisation factor (1 at 16 bits)
+                const float inv = p.o_scale / (Lazy<ET>::kRoundedSum ? l_rnd : l_run);
                 // row rr of the slice: obase + rr * ostride (elements)
                 const size_t ostride = MODE == 0 ? (size_t)D : (size_t)p.heads * D;
                 uint16_t* obase = reinterpret_cast<uint16_t*>(p.o) +

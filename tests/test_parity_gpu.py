@@ -239,20 +239,25 @@ def test_d256_large_scores_force_rescales():
 # stays inside 2e-2 (test_rescale_reading.py: 0.014 against 0.046).  Through every kernel:
 # one slice (single-tile schedules), 160 slices (the paired schedule where it applies), the
 # token-major layout, and head dimensions 32 to 256.
-def dominant_key_inputs(B, H, D, dtype):
+def dominant_key_inputs(B, H, D, dtype, score=6.25):
     from test_rescale_reading import dominant_key_slice
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[dtype]
     return tuple(torch.from_numpy(x).to(dt).expand(B, H, *x.shape).contiguous()
-                 for x in dominant_key_slice(D))
+                 for x in dominant_key_slice(D, score))
 
 
+# score 6.25: the dominant key 9.02 log2 units above key 0 (a reference raised at tau = 8);
+# 3.5: 5.05 units above it, inside tau = 8, where the head-dimension-256 kernel keeps the
+# stale reference and its bf16 path rests on the row sum of the rounded P
+@pytest.mark.parametrize("score", [6.25, 3.5])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("D", [32, 64, 128, 256])
 @pytest.mark.parametrize("BH", [(1, 1), (8, 20)])
-def test_dominant_key_rows(BH, D, dtype, causal):
-    q, k, v = dominant_key_inputs(*BH, D, dtype)
-    full_compare(q, k, v, 1.0, causal, dtype, "dominant key B,H=%s D=%d %s causal=%d" % (BH, D, dtype, causal))
+def test_dominant_key_rows(BH, D, dtype, causal, score):
+    q, k, v = dominant_key_inputs(*BH, D, dtype, score)
+    full_compare(q, k, v, 1.0, causal, dtype,
+                 "dominant key %.2f B,H=%s D=%d %s causal=%d" % (score, BH, D, dtype, causal))
 
 
 @pytest.mark.parametrize("causal", [False, True])
