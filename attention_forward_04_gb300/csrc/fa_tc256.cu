@@ -400,45 +400,59 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
         const uint32_t tl = (uint32_t)(warp * 32) << 16;
         const float sl2 = p.scale_log2;
         const uint32_t stage = sbase + (uint32_t)kStageOff + (uint32_t)warp * 4096u;
+        // Q row r of the query tile at ring positions qpos, qpos + 1 into TMEM as 16-bit pairs
+        // (e4m3 quadruples); the two ring slots are then released and the MMA issuer told.
+        // No product that reads the previous Q is pending: the caller has seen the last of
+        // them complete.
+        auto write_q = [&](uint32_t qpos) -> bool {
+            const bool ok = wait_warp(c, b_ring_full(qpos), ring_par(qpos), kRoleSoftmax) &&
+                            wait_warp(c, b_ring_full(qpos + 1u), ring_par(qpos + 1u), kRoleSoftmax);
+            if (ok) {
+                const int lr = r & 63;
+                const uint32_t src = ring + ((qpos + (uint32_t)(r >> 6)) % kSlots) * kTile + (uint32_t)lr * 128u;
+#pragma unroll
+                for (int pc = 0; pc < kPanels; ++pc) {
+                    uint32_t q[32];
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        const uint4 v = ptx::ld_shared_v4(src + (uint32_t)pc * kPanel64 +
+                                                          (uint32_t)((cc ^ (lr & 7)) * 16));
+                        q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
+                    }
+                    ptx::tmem_st32(tm + tl + kColQ + 32u * (uint32_t)pc, q);
+                }
+                ptx::tmem_wait_st();
+            }
+            ptx::tc_fence_before();
+            if (!sm_barrier_and(ok)) return false;
+            if (threadIdx.x == 0) {
+                ptx::mbar_arrive(bar_addr(c, b_ring_empty(qpos)));
+                ptx::mbar_arrive(bar_addr(c, b_ring_empty(qpos + 1u)));
+                ptx::mbar_arrive(bar_addr(c, b_q_ready()));
+            }
+            return true;
+        };
+        // Whether this CTA has an item after item sub of unit u (units of packed sequences
+        // can be empty).
+        auto has_next = [&](int u, int sub, int nsub) -> bool {
+            if (sub + 1 < nsub) return true;
+            for (int u2 = u + (int)gridDim.x; u2 < p.units; u2 += (int)gridDim.x)
+                if (unit_items<CAUSAL, MODE>(p, u2) > 0) return true;
+            return false;
+        };
         uint32_t g = 0, base = 0, pv = 0;   // pv: products of O issued before this item
+        bool q_written = false;             // the current item's Q is in TMEM already
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const int nsub = unit_items<CAUSAL, MODE>(p, u);
             for (int sub = 0; sub < nsub; ++sub) {
                 const Work w = unit_item<CAUSAL, MODE>(p, u, sub);
                 const int i = w.qt * kBM + r;   // row within the slice
                 const int limit = CAUSAL ? min(i + 1, w.len) : w.len;  // visible keys: key < limit
-                {
-                    // Q row r into TMEM as 16-bit pairs (e4m3 quadruples); the two ring slots
-                    // are then released.
-                    // The previous item's products (which read Q) are complete: its
-                    // epilogue waited for the last of them.
-                    const bool ok = wait_warp(c, b_ring_full(base), ring_par(base), kRoleSoftmax) &&
-                                    wait_warp(c, b_ring_full(base + 1u), ring_par(base + 1u), kRoleSoftmax);
-                    if (ok) {
-                        const int lr = r & 63;
-                        const uint32_t src = ring + ((base + (uint32_t)(r >> 6)) % kSlots) * kTile +
-                                             (uint32_t)lr * 128u;
-#pragma unroll
-                        for (int pc = 0; pc < kPanels; ++pc) {
-                            uint32_t q[32];
-#pragma unroll
-                            for (int cc = 0; cc < 8; ++cc) {
-                                const uint4 v = ptx::ld_shared_v4(src + (uint32_t)pc * kPanel64 +
-                                                                  (uint32_t)((cc ^ (lr & 7)) * 16));
-                                q[4 * cc] = v.x; q[4 * cc + 1] = v.y; q[4 * cc + 2] = v.z; q[4 * cc + 3] = v.w;
-                            }
-                            ptx::tmem_st32(tm + tl + kColQ + 32u * (uint32_t)pc, q);
-                        }
-                        ptx::tmem_wait_st();
-                    }
-                    ptx::tc_fence_before();
-                    if (!sm_barrier_and(ok)) goto sm_out;
-                    if (threadIdx.x == 0) {
-                        ptx::mbar_arrive(bar_addr(c, b_ring_empty(base)));
-                        ptx::mbar_arrive(bar_addr(c, b_ring_empty(base + 1u)));
-                        ptx::mbar_arrive(bar_addr(c, b_q_ready()));
-                    }
-                }
+                // A CTA's first item writes its Q here; every later one was written on the
+                // previous item's last step.
+                if (!q_written && !write_q(base)) goto sm_out;
+                q_written = false;
+                const bool next = has_next(u, sub, nsub);
                 // reference max (log2 units), row sum, and (bf16) row sum of the rounded P
                 float m_run = -INFINITY, l_run = 0.0f, l_rnd = 0.0f;
                 for (int j = 0; j < w.nkv; ++j) {
@@ -484,6 +498,13 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     ptx::tmem_wait_st();
                     ptx::tc_fence_before();
                     ptx::mbar_arrive(bar_addr(c, b_p_full(b)));
+                    // The item's last S product, the last to read this Q, is complete (this
+                    // step waited for it): the next item's Q goes into TMEM now, so its first
+                    // two S products run during this item's epilogue.
+                    if (next && j + 1 == w.nkv) {
+                        if (!write_q(base + 2u + 2u * (uint32_t)w.nkv)) goto sm_out;
+                        q_written = true;
+                    }
                 }
                 // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.  The
                 // item's second-to-last product (or the previous item's last one) is known

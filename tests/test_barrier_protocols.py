@@ -10,13 +10,17 @@ which is what the hardware checks; the model reports
   * premature: a wait passed before the phase it stands for had completed (the barrier
     was two phases behind), and
   * deadlock: no role can move (in particular a wait whose phase completed but whose
-    parity came round again, the barrier being two phases ahead).
+    parity came round again, the barrier being two phases ahead), and
+  * hazard: a ('check', predicate, what) step found the model state wrong, e.g. the query
+    tile rewritten in TMEM while a product that reads the old one was still pending.
 
 Models: the head-dimension-256 forward (fa_tc256.cu: S double-buffered, O += P V, the
-conditional O rescale, the per-item epilogue) and the head-dimension-256 backward
+conditional O rescale, the next item's query tile written on the last step, the per-item
+epilogue) and the head-dimension-256 backward
 (fa_bwd256.cu: the dQ / dK template and the dV kernel with its two S^T buffers and
 rings).  A change to either kernel's barrier order must be mirrored here.  Planted
-mistakes (the epilogue's two waits in a row; a single-buffered dV hand-over) must fail.
+mistakes (the epilogue's two waits in a row; the next query tile written before the last
+S product is seen complete; a single-buffered dV hand-over) must fail.
 """
 import random
 
@@ -43,7 +47,7 @@ class Model:
         """roles: name -> list of ('wait', bar, phase) | ('arrive', bar) |
         ('copy', bar) (completes later, any order) | ('mma', [bars]) (commits later, in
         order) | ('group', tag) (named barrier of the roles sharing tag).  Returns 'ok',
-        'premature ...' or 'deadlock ...'."""
+        'premature ...', 'deadlock ...' or 'hazard ...'."""
         pc = {r: 0 for r in roles}
         copies, pipe = [], []
         group_count = {}
@@ -87,7 +91,10 @@ class Model:
                     self.arrive(name)
                 continue
             op = roles[r][pc[r]]
-            if op[0] == "arrive":
+            if op[0] == "check":
+                if not op[1](self):
+                    return "hazard " + op[2]
+            elif op[0] == "arrive":
                 self.arrive(op[1])
             elif op[0] == "copy":
                 copies.append(op[1])
@@ -100,8 +107,12 @@ class Model:
 
 
 # ----------------------------------------------------------------- D = 256 forward
-def tc256_roles(m, items, rescale_prob, two_epilogue_waits=False):
-    """fa_tc256.cu, one CTA over `items` (key steps per item); loads are taken as ready."""
+def tc256_roles(m, items, rescale_prob, two_epilogue_waits=False, early_q=False):
+    """fa_tc256.cu, one CTA over `items` (key steps per item); loads are taken as ready.
+    The softmax writes a CTA's first query tile into TMEM at the start and every later one
+    on the previous item's last step, after that step's S product (the last to read the old
+    tile) is seen complete; a check step asserts exactly that.  early_q plants the write
+    before that wait."""
     for b in (0, 1):
         m.bar(("s_full", b))
         m.bar(("p_full", b))
@@ -122,16 +133,29 @@ def tc256_roles(m, items, rescale_prob, two_epilogue_waits=False):
                 mma.append(("mma", [("s_full", (gj + 2) & 1)]))
         g += nkv
     g = pv = 0
-    for nkv in items:
-        sm.append(("arrive", "q_ready"))
+
+    def s_done_through(n):   # every S product of the first n steps is complete
+        return lambda mm: mm.done[("s_full", 0)] + mm.done[("s_full", 1)] >= n
+
+    for it, nkv in enumerate(items):
+        if it == 0:
+            sm.append(("arrive", "q_ready"))
         for j in range(nkv):
             gj = g + j
+            last_with_next = j + 1 == nkv and it + 1 < len(items)
+            if early_q and last_with_next:
+                sm.append(("check", s_done_through(g + nkv), "query tile rewritten early"))
+                sm.append(("arrive", "q_ready"))
             sm.append(("wait", ("s_full", gj & 1), gj >> 1))
             resc = j > 0 and m.rnd.random() < rescale_prob
             last_sync = (j > 0 and j + 1 == nkv) and not two_epilogue_waits
             if resc or last_sync:
                 sm.append(("wait", "o_done", pv + j - 1))
             sm.append(("arrive", ("p_full", gj & 1)))
+            if last_with_next and not early_q:
+                # the next item's query tile into TMEM, then q_ready
+                sm.append(("check", s_done_through(g + nkv), "query tile rewritten early"))
+                sm.append(("arrive", "q_ready"))
         pv += nkv
         if two_epilogue_waits and nkv >= 2:
             sm.append(("wait", "o_done", pv - 2))
@@ -147,6 +171,17 @@ def test_tc256_forward_protocol(rescale_prob):
         items = [m.rnd.randint(1, 6) for _ in range(m.rnd.randint(1, 4))]
         res = m.run(tc256_roles(m, items, rescale_prob))
         assert res == "ok", (seed, items, res)
+
+
+def test_tc256_planted_early_query_write_fails():
+    # writing the next query tile before the item's last S product is seen complete
+    bad = 0
+    for seed in range(300):
+        m = Model(seed)
+        items = [m.rnd.randint(1, 4) for _ in range(m.rnd.randint(2, 4))]
+        res = m.run(tc256_roles(m, items, 0.5, early_q=True))
+        bad += res.startswith("hazard")
+    assert bad > 0
 
 
 def test_tc256_planted_two_epilogue_waits_fail():
