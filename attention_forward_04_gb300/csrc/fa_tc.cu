@@ -405,7 +405,10 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
                 const uint32_t vpos = kv;        // V_j
                 const uint32_t kpos = kv + 1;    // K_{j+1}
                 const bool more = j + 1 < nmax;
+                // V_j and K_{j+1} (loaded right after it) are awaited before tile A's P, so
+                // that nothing but the hand-over of P stands between O_A += P V_j and S_A(j+1).
                 if (!wait_warp(c, b_kv_full<D, EB>(vpos), ring_parity<D, EB>(vpos), kRoleMma)) goto out;
+                if (more && !wait_warp(c, b_kv_full<D, EB>(kpos), ring_parity<D, EB>(kpos), kRoleMma)) goto out;
                 ptx::tc_fence_after();
                 if (j < it.nA) {
                     if (!wait_warp(c, b_p_full<D, EB>(0), p_cnt0 & 1u, kRoleMma)) goto out;
@@ -413,10 +416,6 @@ __device__ void mma_role(const TcParams& p, const Ctl& c, uint32_t tmem, uint32_
                     ptx::tc_fence_after();
                     issue_pv<D, ET>(tO[0], tP[0], dV0 + slot_off(vpos), idesc_pv, j > 0);
                     ptx::mma_commit_elect(bar_addr(c, b_o_done<D, EB>(0)));
-                }
-                if (more) {
-                    if (!wait_warp(c, b_kv_full<D, EB>(kpos), ring_parity<D, EB>(kpos), kRoleMma)) goto out;
-                    ptx::tc_fence_after();
                 }
                 if (j + 1 < it.nA) {
                     issue_qk<D, ET>(tS[0], dQ[0], dK0 + slot_off(kpos), idesc_qk);
@@ -769,6 +768,7 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
     const uint32_t tS = tmem + tl + G::col_s(t);
     const uint32_t tP = tmem + tl + G::col_p(t);
     const uint32_t tO = tmem + tl + G::col_o(t);
+    // S products read; O products of earlier items (P over S) or O products waited for
     uint32_t s_cnt = 0, o_cnt = 0;
 
     for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
@@ -783,12 +783,11 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             float m_run = -INFINITY, l_run = 0.0f;
 
             for (int j = 0; j < n; ++j) {
+                // Where P overwrites S, S(j) was issued after O_t += P(j-1) V(j-1) by the same
+                // thread, and the commit behind s_full tracks every product that thread issued
+                // before it: O is final once S(j) is complete, and no wait on o_done is needed.
                 if (!wait_warp(c, b_s_full<D, EB>(t), s_cnt & 1u, kRoleSoftmax)) return;
                 ++s_cnt;
-                if (!G::kSepP && j > 0) {  // O_t += P(j-1) V(j-1) is complete before S(j) is (issue order)
-                    if (!wait_warp(c, b_o_done<D, EB>(t), o_cnt & 1u, kRoleSoftmax)) return;
-                    ++o_cnt;
-                }
                 ptx::tc_fence_after();
                 uint32_t s[128];
                 ptx::tmem_ld128_wait(tS, s);
@@ -829,8 +828,13 @@ __device__ void softmax_role(const TcParams& p, const Ctl& c, uint32_t tmem, int
             // Epilogue: O / l, one 64-column panel at a time through this warp's staging
             // slot, so the global stores are row-contiguous: each store instruction writes
             // four whole 128-byte lines (rows past N are skipped); LSE from registers.
-            if (!wait_warp(c, b_o_done<D, EB>(t), o_cnt & 1u, kRoleSoftmax)) return;
-            ++o_cnt;
+            // Where P overwrites S, only the tile's last O product is awaited: the one before
+            // it is complete (S(n-1) was issued after it) and the next item's first one
+            // waits for this warp's P, so the parity wait is exact.
+            if (!wait_warp(c, b_o_done<D, EB>(t), (G::kSepP ? o_cnt : o_cnt + (uint32_t)n - 1u) & 1u,
+                           kRoleSoftmax))
+                return;
+            o_cnt += G::kSepP ? 1u : (uint32_t)n;
             ptx::tc_fence_after();
             const float inv_l = p.o_scale / l_run;   // o_scale: V's dequantisation factor (1 at 16 bits)
             const int row0 = it.pair * 2 * kBM + (t ^ it.sw) * kBM + lane_base;   // first row of the warp
@@ -976,12 +980,11 @@ __device__ void softmax_role_split(const TcParams& p, const Ctl& c, uint32_t tme
         bool live = true;
 
         for (int j = 0; j < n; ++j) {
+            // Where P overwrites S, S(j) was issued after O += P(j-1) V(j-1) by the same
+            // thread, and the commit behind s_full tracks every product issued before it:
+            // O is final once S(j) is complete.
             bool ok = live && wait_warp(c, b_s_full<D, EB>(0), s_cnt & 1u, kRoleSoftmax);
             ++s_cnt;
-            if (ok && !G::kSepP && j > 0) {   // O += P(j-1) V(j-1) is complete before S(j) is
-                ok = wait_warp(c, b_o_done<D, EB>(0), o_cnt & 1u, kRoleSoftmax);
-                ++o_cnt;
-            }
             const int kbase = j * kBN + 64 * h;
             const bool mask = __any_sync(0xFFFFFFFFu, kbase + 64 > limit);
             uint32_t s[64];
@@ -1030,9 +1033,12 @@ __device__ void softmax_role_split(const TcParams& p, const Ctl& c, uint32_t tme
             ptx::mbar_arrive(bar_addr(c, b_p_full<D, EB>(0)));
         }
 
-        // Epilogue: the last O += P V, then the two halves' row sums meet.
-        bool ok = live && wait_warp(c, b_o_done<D, EB>(0), o_cnt & 1u, kRoleSoftmax);
-        ++o_cnt;
+        // Epilogue: the last O += P V, then the two halves' row sums meet.  Where P overwrites
+        // S only that product is awaited (the one before it is complete, S(n-1) having been
+        // issued after it), so the parity wait is exact.
+        bool ok = live && wait_warp(c, b_o_done<D, EB>(0), (G::kSepP ? o_cnt : o_cnt + (uint32_t)n - 1u) & 1u,
+                                    kRoleSoftmax);
+        o_cnt += G::kSepP ? 1u : (uint32_t)n;
         xl[h * 128 + r128] = l_half;
         // At D = 64 both warps stage into warp q4's slot: its last bulk store has read it.
         if (OStore<D, 2>::kTma && D == 64 && h == 0 && lane == 0) bulk_wait_read_all();

@@ -14,7 +14,8 @@ which is what the hardware checks; the model reports
   * hazard: a ('check', predicate, what) step found the model state wrong, e.g. the query
     tile rewritten in TMEM while a product that reads the old one was still pending.
 
-Models: the head-dimension-256 forward (fa_tc256.cu: S double-buffered, O += P V, the
+Models: the paired head-dimension-128 forward (fa_tc.cu: two query tiles, P written over S,
+O final once the next S is complete), the head-dimension-256 forward (fa_tc256.cu: S double-buffered, O += P V, the
 conditional O rescale, the next item's query tile written on the last step, the per-item
 epilogue) and the head-dimension-256 backward
 (fa_bwd256.cu: the dQ / dK template and the dV kernel with its two S^T buffers and
@@ -104,6 +105,71 @@ class Model:
                 group_count[r] = group_count.get(r, 0) + 1
             pc[r] += 1
         return "no end"
+
+
+# ----------------------------------------------------------------- D = 128 forward, paired tiles
+def tc128_roles(m, items, s_before_pv=False):
+    """fa_tc.cu's paired schedule where P overwrites S, one CTA over `items` ((nA, nB) key
+    tiles per item); loads are taken as ready.  The softmax of a tile waits only for S: the
+    commit behind s_full tracks every product the MMA thread issued before S(j), so
+    O += P(j-1) V(j-1) is complete too, which a check step asserts before O is touched.
+    Its epilogue waits once, for the tile's last O product.  s_before_pv plants an issue
+    order with S(j+1) ahead of O += P(j) V(j)."""
+    for t in "AB":
+        m.bar(("s_full", t))
+        m.bar(("p_full", t))
+        m.bar(("o_done", t))
+    mma = []
+    for nA, nB in items:
+        n = {"A": nA, "B": nB}
+        for t in "AB":
+            mma.append(("mma", [("s_full", t)]))
+        for j in range(max(nA, nB)):
+            for t in "AB":
+                pv = [("wait", ("p_full", t), None), ("mma", [("o_done", t)])] if j < n[t] else []
+                s_next = [("mma", [("s_full", t)])] if j + 1 < n[t] else []
+                mma.extend(s_next + pv if s_before_pv else pv + s_next)
+    # the MMA's p_full waits count per tile
+    cnt = {"A": 0, "B": 0}
+    for k, op in enumerate(mma):
+        if op[0] == "wait":
+            t = op[1][1]
+            mma[k] = ("wait", op[1], cnt[t])
+            cnt[t] += 1
+    roles = {"mma": mma}
+    for t in "AB":
+        sm, s_cnt, o_base = [], 0, 0
+        for nA, nB in items:
+            n = nA if t == "A" else nB
+            for j in range(n):
+                sm.append(("wait", ("s_full", t), s_cnt))
+                s_cnt += 1
+                if j > 0:
+                    need = o_base + j   # O += P(j-1) V(j-1) of this item complete
+                    sm.append(("check", lambda mm, t=t, need=need: mm.done[("o_done", t)] >= need,
+                               "tile %s read O before its last product completed" % t))
+                sm.append(("arrive", ("p_full", t)))
+            sm.append(("wait", ("o_done", t), o_base + n - 1))
+            o_base += n
+        roles["softmax_" + t] = sm
+    return roles
+
+
+def test_tc128_paired_protocol():
+    for seed in range(400):
+        m = Model(seed)
+        items = [(m.rnd.randint(1, 5), m.rnd.randint(1, 5)) for _ in range(m.rnd.randint(1, 4))]
+        res = m.run(tc128_roles(m, items))
+        assert res == "ok", (seed, items, res)
+
+
+def test_tc128_planted_s_before_pv_fails():
+    bad = 0
+    for seed in range(200):
+        m = Model(seed)
+        items = [(m.rnd.randint(2, 5), m.rnd.randint(2, 5)) for _ in range(m.rnd.randint(1, 3))]
+        bad += m.run(tc128_roles(m, items, s_before_pv=True)) != "ok"
+    assert bad > 0
 
 
 # ----------------------------------------------------------------- D = 256 forward
