@@ -84,10 +84,10 @@ struct BGeo {
     // epilogue staging (4 KB per elementwise warp) reuses the ring: it starts only after
     // every product, hence every read of the ring, has completed
     static constexpr int kStageOff = kRingOff;
-    // dK/dV: 2 x 256 floats of staged per-column LSE and delta; dQ: 2 x 128 floats of
-    // partial row sums of delta
+    // dK/dV: per elementwise warp 2 x 128 floats of staged per-column LSE and delta; dQ:
+    // 2 x 128 floats of partial row sums of delta
     static constexpr int kVecOff = kRingOff + kSlots * kTile;
-    static constexpr int kBarOff = kVecOff + (FIXED == 2 ? 2 * 256 * 4 : 2 * 128 * 4);
+    static constexpr int kBarOff = kVecOff + (FIXED == 2 ? 8 * 2 * 128 * 4 : 2 * 128 * 4);
     // barriers: fixed_full, ring_full[4], ring_empty[4], then the named ones below
     static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
@@ -667,31 +667,35 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
         const int r = quarter * 32 + lane;
         const int key = kt * kT + r;
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-        const int t = threadIdx.x;   // 0..255
-        float* vec = reinterpret_cast<float*>(smem_raw + (su.sbase - ptx::smem_addr(smem_raw)) + G::kVecOff);
-        // Per-column LSE (log2 units) and delta of each query tile, staged in shared
-        // memory: thread t < 128 stages the LSE of query t of the tile, thread 128 + t its
-        // delta.  The next tile's value is fetched one step ahead into a register.
-        auto fetch = [&](int s) -> float {
-            const int q = (i0 + s) * kT + (t & (kT - 1));
+        // Per-column LSE (log2 units) and delta of this warp's 64 queries of each query tile,
+        // staged in the warp's own area of shared memory, so that no barrier across warps is
+        // needed: lane l holds queries l and l + 32 (k = 0, 1: LSE; k = 2, 3: delta), fetched
+        // one step ahead into registers.
+        float* vw = reinterpret_cast<float*>(smem_raw + (su.sbase - ptx::smem_addr(smem_raw)) + G::kVecOff) +
+                    warp * 256;
+        auto fetch = [&](int s, int k) -> float {
+            const int q = (i0 + s) * kT + 64 * ch + lane + 32 * (k & 1);
             const bool ok = s < nq && q < sl.len;
-            if (t < kT) return ok ? p.lse[sl.vec0 + q] * kLog2e : INFINITY;   // p = 0 past the end
+            if (k < 2) return ok ? p.lse[sl.vec0 + q] * kLog2e : INFINITY;   // p = 0 past the end
             return ok ? p.delta[sl.vec0 + q] : 0.0f;
         };
-        float next = fetch(0);
-        bool failed = false;
+        float nx[4] = {fetch(0, 0), fetch(0, 1), fetch(0, 2), fetch(0, 3)};
         for (int s = 0; s < nq; ++s) {
             const uint32_t par = (uint32_t)s & 1u;
-            float* vl = vec + par * 256;   // [0, 128): LSE * log2 e, [128, 256): delta
-            vl[t] = next;
-            const bool ok = !failed && wait_warp(c, G::s_ready(), par, kRoleSoftmax);
-            if (!ew_barrier_and(ok)) goto ew_out;
+            float* vl = vw + par * 128;   // [0, 64): LSE * log2 e, [64, 128): delta
+            vl[lane] = nx[0];
+            vl[lane + 32] = nx[1];
+            vl[64 + lane] = nx[2];
+            vl[96 + lane] = nx[3];
+            __syncwarp();
+            if (!wait_warp(c, G::s_ready(), par, kRoleSoftmax)) goto ew_out;
             ptx::tc_fence_after();
-            next = fetch(s + 1);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) nx[k] = fetch(s + 1, k);
             const int qbase = (i0 + s) * kT + 64 * ch;
             const bool diag = CAUSAL && (i0 + s == kt);   // queries before this key are masked
-            const float4* l4 = reinterpret_cast<const float4*>(vl + 64 * ch);
-            const float4* d4 = reinterpret_cast<const float4*>(vl + kT + 64 * ch);
+            const float4* l4 = reinterpret_cast<const float4*>(vl);
+            const float4* d4 = reinterpret_cast<const float4*>(vl + 64);
             float pr[64];
             {   // phase a: P^T from S^T, 16-bit over this warp's S^T columns
                 const uint32_t ts = tm + tl + kColS + 64u * (uint32_t)ch;
@@ -723,7 +727,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 ptx::mbar_arrive(bar_addr(c, G::x_ready()));
             }
             {   // phase b: dS^T = P^T (dP^T - delta), 16-bit over this warp's dP^T columns
-                if (!wait_warp(c, G::dp_ready(), par, kRoleSoftmax)) { failed = true; continue; }
+                if (!wait_warp(c, G::dp_ready(), par, kRoleSoftmax)) goto ew_out;
                 ptx::tc_fence_after();
                 const uint32_t tp = tm + tl + kColDP + 64u * (uint32_t)ch;
                 uint32_t dp[64];
@@ -747,7 +751,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_dkdv_kernel(const __grid_cons
                 ptx::mbar_arrive(bar_addr(c, G::ds_ready()));
             }
         }
-        if (failed) goto ew_out;
         if (!wait_warp(c, G::done(), 0, kRoleSoftmax)) goto ew_out;
         ptx::tc_fence_after();
         if constexpr (D == 32) {   // dV by the first, dK by the second warp of each quarter

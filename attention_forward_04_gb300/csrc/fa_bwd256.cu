@@ -77,10 +77,11 @@ struct G256 {
     // epilogue staging (4 KB per elementwise warp) reuses the ring: it starts only after
     // the last product, hence the last read of the ring, has completed
     static constexpr int kStageOff = kRingOff;
-    // dQ: 2 x 128 partial row sums of delta; dK, dV: per query column of the sub-tile
-    // LSE (and, dK, delta), double-buffered (2 x 128 floats)
+    // dQ: 2 x 128 partial row sums of delta; dK: per query column of the sub-tile LSE and
+    // delta, double-buffered (2 x 128 floats); dV: per elementwise warp, the LSE of its 32
+    // query columns, double-buffered (8 x 2 x 32 floats)
     static constexpr int kVecOff = kRingOff + kSlots * kSubBytes;
-    static constexpr int kBarOff = kVecOff + 2 * 128 * 4;
+    static constexpr int kBarOff = kVecOff + (ROLE == kRoleDV ? 8 * 2 * 32 * 4 : 2 * 128 * 4);
     static constexpr int kNumBars = 1 + 2 * kSlots + 9;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kSmemBytes = kMiscOff + 16 + 1024;
@@ -633,30 +634,31 @@ __global__ void __launch_bounds__(kThreads, 1) bwd256_dv_kernel(const __grid_con
         const int r = quarter * 32 + lane;
         const int key = tile * kT + r;
         const uint32_t tl = (uint32_t)(quarter * 32) << 16;
-        const int t = threadIdx.x;
-        float* vec = reinterpret_cast<float*>(su.smem + G::kVecOff);
+        // this warp's staging area: the LSE of its 32 query columns, double-buffered
+        float* vw = reinterpret_cast<float*>(su.smem + G::kVecOff) + warp * 64;
         if (!row_tile_to_tmem<kRoleDV>(c, su.sbase, tm, quarter, ch, lane)) goto ew_out;
         {
-            // LSE (log2 units; +inf past the end) of each query column of the next sub-tile,
-            // fetched one step ahead by threads 0-63
+            // LSE (log2 units; +inf past the end) of this warp's query columns of the next
+            // sub-tile, lane l holding column l, fetched one step ahead; staged per warp, so
+            // no barrier across warps is needed
             auto fetch = [&](int s) -> float {
-                const int q = (s0 + s) * kSub + t;
+                const int q = (s0 + s) * kSub + 32 * ch + lane;
                 return (s < n && q < sl.len) ? p.lse[sl.vec0 + q] * kLog2e : INFINITY;
             };
-            float next = t < kSub ? fetch(0) : 0.0f;
+            float next = fetch(0);
             for (int s = 0; s < n; ++s) {
                 const int b = s & 1;
-                float* vl = vec + b * 128;
-                if (t < kSub) vl[t] = next;
-                const bool ok = wait_warp(c, G::s_ready(b), (uint32_t)(s >> 1) & 1u, kRoleSoftmax);
-                if (!ew_barrier_and(ok)) goto ew_out;
-                if (t < kSub) next = fetch(s + 1);
+                float* vl = vw + b * 32;
+                vl[lane] = next;
+                __syncwarp();
+                if (!wait_warp(c, G::s_ready(b), (uint32_t)(s >> 1) & 1u, kRoleSoftmax)) goto ew_out;
+                next = fetch(s + 1);
                 ptx::tc_fence_after();
                 const int col0 = (s0 + s) * kSub + 32 * ch;   // first query of this warp
                 const uint32_t ts = tm + tl + kColS + 64u * (uint32_t)b + 32u * (uint32_t)ch;
                 uint32_t sv[32];
                 ptx::tmem_ld32_wait(ts, sv);
-                const float4* l4 = reinterpret_cast<const float4*>(vl + 32 * ch);
+                const float4* l4 = reinterpret_cast<const float4*>(vl);
                 float pr[32];
 #pragma unroll
                 for (int c4 = 0; c4 < 8; ++c4) {
