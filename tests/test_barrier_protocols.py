@@ -15,11 +15,14 @@ which is what the hardware checks; the model reports
     tile rewritten in TMEM while a product that reads the old one was still pending.
 
 Models: the paired head-dimension-128 forward (fa_tc.cu: two query tiles, P written over S,
-O final once the next S is complete), the head-dimension-256 forward (fa_tc256.cu: S double-buffered, O += P V, the
+O final once the next S is complete), the head-dimension-32/64 forward (P in TMEM columns of
+its own, S released to the next product once read), the head-dimension-256 forward (fa_tc256.cu: S double-buffered, O += P V, the
 conditional O rescale, the next item's query tile written on the last step, the per-item
 epilogue) and the head-dimension-256 backward
 (fa_bwd256.cu: the dQ / dK template and the dV kernel with its two S^T buffers and
-rings).  A change to either kernel's barrier order must be mirrored here.  Planted
+rings), and the head-dimension-32-128 backward (fa_bwd.cu: the dQ kernel and the dK/dV
+kernel, whose elementwise warps stage their per-column vectors without a barrier across
+warps).  A change to either kernel's barrier order must be mirrored here.  Planted
 mistakes (the epilogue's two waits in a row; the next query tile written before the last
 S product is seen complete; a single-buffered dV hand-over) must fail.
 """
@@ -169,6 +172,80 @@ def test_tc128_planted_s_before_pv_fails():
         m = Model(seed)
         items = [(m.rnd.randint(2, 5), m.rnd.randint(2, 5)) for _ in range(m.rnd.randint(1, 3))]
         bad += m.run(tc128_roles(m, items, s_before_pv=True)) != "ok"
+    assert bad > 0
+
+
+# ----------------------------------------------------------------- D <= 64 forward, P apart
+def tc_sep_roles(m, items, no_s_read_wait=False):
+    """fa_tc.cu's paired schedule where P has TMEM columns of its own (D <= 64): each tile's
+    next S product waits only until the softmax has read the current S (s_read), ahead of
+    O += P V; the softmax waits for the previous O product before it stores P (which that
+    product reads) and before O is rescaled.  Checks: S(j) is still in its region when it is
+    read, and the previous O product is complete when P is stored.  no_s_read_wait plants an
+    MMA issuer that overwrites S without waiting for the read."""
+    for t in "AB":
+        for b in ("s_full", "s_read", "p_full", "o_done"):
+            m.bar((b, t))
+    mma, issued, sr, pc = [], {"A": 0, "B": 0}, {"A": 0, "B": 0}, {"A": 0, "B": 0}
+
+    def issue_s(t):
+        if issued[t] > 0 and not no_s_read_wait:
+            mma.append(("wait", ("s_read", t), sr[t]))
+            sr[t] += 1
+        mma.append(("mma", [("s_full", t)]))
+        issued[t] += 1
+
+    for nA, nB in items:
+        n = {"A": nA, "B": nB}
+        for t in "AB":
+            issue_s(t)
+        for j in range(max(nA, nB)):
+            for t in "AB":
+                if j + 1 < n[t]:
+                    issue_s(t)
+            for t in "AB":
+                if j < n[t]:
+                    mma.append(("wait", ("p_full", t), pc[t]))
+                    pc[t] += 1
+                    mma.append(("mma", [("o_done", t)]))
+    roles = {"mma": mma}
+    for t in "AB":
+        sm, s_cnt, o_cnt = [], 0, 0
+        for nA, nB in items:
+            n = nA if t == "A" else nB
+            o_base = o_cnt
+            for j in range(n):
+                sm.append(("wait", ("s_full", t), s_cnt))
+                s_cnt += 1
+                sm.append(("check", lambda mm, t=t, k=s_cnt: mm.done[("s_full", t)] == k,
+                           "tile %s S overwritten before it was read" % t))
+                sm.append(("arrive", ("s_read", t)))
+                if j > 0:
+                    sm.append(("wait", ("o_done", t), o_cnt))
+                    o_cnt += 1
+                    sm.append(("check", lambda mm, t=t, k=o_base + j: mm.done[("o_done", t)] >= k,
+                               "tile %s P stored before the last O product read it" % t))
+                sm.append(("arrive", ("p_full", t)))
+            sm.append(("wait", ("o_done", t), o_cnt))
+            o_cnt += 1
+        roles["softmax_" + t] = sm
+    return roles
+
+
+def test_tc_sep_protocol():
+    for seed in range(400):
+        m = Model(seed)
+        items = [(m.rnd.randint(1, 5), m.rnd.randint(1, 5)) for _ in range(m.rnd.randint(1, 4))]
+        res = m.run(tc_sep_roles(m, items))
+        assert res == "ok", (seed, items, res)
+
+
+def test_tc_sep_planted_missing_s_read_fails():
+    bad = 0
+    for seed in range(200):
+        m = Model(seed)
+        items = [(m.rnd.randint(2, 5), m.rnd.randint(2, 5)) for _ in range(m.rnd.randint(1, 3))]
+        bad += m.run(tc_sep_roles(m, items, no_s_read_wait=True)).startswith("hazard")
     assert bad > 0
 
 
@@ -377,4 +454,125 @@ def test_bwd256_planted_single_buffered_dv_fails():
     for seed in range(60):
         m = Model(seed)
         bad += m.run(bwd256_roles(m, "dv", 4, 6, single_buffer_dv=True)) != "ok"
+    assert bad > 0
+
+
+# ----------------------------------------------------------------- D <= 128 backward
+def bwd_dq_roles(m, n, no_ds_free_wait=False):
+    """fa_bwd.cu's dQ kernel, one CTA over n key tiles; loads taken as ready; two
+    elementwise groups stand for the eight warps (each barrier they arrive on counts both).
+    S(j+1) is issued once S(j) is read (x_ready), dP(j+1) once dP(j) is read (dp_free), and
+    dQ += dS K_j once dS is stored (ds_ready); the elementwise warps store dS(j) only after
+    the previous dQ product has read dS(j-1) (ds_free).  Checks: S and dP are read before the
+    next product overwrites them, and dS is not overwritten while a dQ product reads it."""
+    m.bar("s_ready")
+    m.bar("dp_ready")
+    m.bar("x_ready", 2)
+    m.bar("dp_free", 2)
+    m.bar("ds_ready", 2)
+    m.bar("ds_free")
+    m.bar("done")
+    mma = [("mma", ["s_ready"]), ("mma", ["dp_ready"])]
+    for j in range(n):
+        mma.append(("wait", "x_ready", j))
+        if j + 1 < n:
+            mma.append(("mma", ["s_ready"]))
+        mma.append(("wait", "dp_free", j))
+        if j + 1 < n:
+            mma.append(("mma", ["dp_ready"]))
+        mma.append(("wait", "ds_ready", j))
+        mma.append(("mma", ["ds_free"]))
+    mma.append(("mma", ["done"]))
+
+    def ew():
+        e = []
+        for j in range(n):
+            e.append(("wait", "s_ready", j))
+            e.append(("check", lambda mm, k=j + 1: mm.done["s_ready"] == k, "S overwritten before it was read"))
+            e.append(("arrive", "x_ready"))
+            e.append(("wait", "dp_ready", j))
+            e.append(("check", lambda mm, k=j + 1: mm.done["dp_ready"] == k, "dP overwritten before it was read"))
+            e.append(("arrive", "dp_free"))
+            if j > 0:
+                if not no_ds_free_wait:
+                    e.append(("wait", "ds_free", j - 1))
+                e.append(("check", lambda mm, k=j: mm.done["ds_free"] >= k, "dS stored while dQ read it"))
+            e.append(("arrive", "ds_ready"))
+        e.append(("wait", "done", 0))
+        return e
+
+    return {"mma": mma, "ew0": ew(), "ew1": ew()}
+
+
+def bwd_dkdv_roles(m, n, no_dp_wait=False):
+    """fa_bwd.cu's dK/dV kernel, one CTA over n query tiles; loads taken as ready; two
+    elementwise groups stand for the eight warps, each staging its per-column vectors on
+    its own (no barrier across warps).  dV += P^T dO_i once P^T is stored over S^T
+    (x_ready), then S^T(i+1); dK += dS^T Q_i once dS^T is stored over dP^T (ds_ready), then
+    dP^T(i+1).  Checks (with two commits the kernel does not need, to observe the products
+    that read P^T and dS^T): a group reads S^T and dP^T of the current tile, and overwrites
+    them only after the previous tile's dV and dK products have read them."""
+    for b in ("s_ready", "dp_ready", "done", "dv_read", "dk_read"):
+        m.bar(b)
+    m.bar("x_ready", 2)
+    m.bar("ds_ready", 2)
+    mma = [("mma", ["s_ready"]), ("mma", ["dp_ready"])]
+    for i in range(n):
+        mma.append(("wait", "x_ready", i))
+        mma.append(("mma", ["dv_read"]))
+        if i + 1 < n:
+            mma.append(("mma", ["s_ready"]))
+        mma.append(("wait", "ds_ready", i))
+        mma.append(("mma", ["dk_read"]))
+        if i + 1 < n:
+            mma.append(("mma", ["dp_ready"]))
+    mma.append(("mma", ["done"]))
+
+    def ew():
+        e = []
+        for i in range(n):
+            e.append(("wait", "s_ready", i))
+            e.append(("check", lambda mm, k=i + 1: mm.done["s_ready"] == k, "S^T not the current tile's"))
+            e.append(("check", lambda mm, k=i: mm.done["dv_read"] >= k, "P^T stored while dV read the last one"))
+            e.append(("arrive", "x_ready"))
+            if not no_dp_wait:
+                e.append(("wait", "dp_ready", i))
+            e.append(("check", lambda mm, k=i + 1: mm.done["dp_ready"] == k, "dP^T not the current tile's"))
+            e.append(("check", lambda mm, k=i: mm.done["dk_read"] >= k, "dS^T stored while dK read the last one"))
+            e.append(("arrive", "ds_ready"))
+        e.append(("wait", "done", 0))
+        return e
+
+    return {"mma": mma, "ew0": ew(), "ew1": ew()}
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 9])
+def test_bwd_dq_protocol(n):
+    for seed in range(150):
+        m = Model(seed)
+        res = m.run(bwd_dq_roles(m, n))
+        assert res == "ok", (n, seed, res)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 9])
+def test_bwd_dkdv_protocol(n):
+    for seed in range(150):
+        m = Model(seed)
+        res = m.run(bwd_dkdv_roles(m, n))
+        assert res == "ok", (n, seed, res)
+
+
+def test_bwd_dq_planted_missing_ds_free_fails():
+    bad = 0
+    for seed in range(200):
+        m = Model(seed)
+        bad += m.run(bwd_dq_roles(m, 4, no_ds_free_wait=True)).startswith("hazard")
+    assert bad > 0
+
+
+def test_bwd_dkdv_planted_missing_dp_wait_fails():
+    bad = 0
+    for seed in range(200):
+        m = Model(seed)
+        bad += m.run(bwd_dkdv_roles(m, 4, no_dp_wait=True)) != "ok"
     assert bad > 0
