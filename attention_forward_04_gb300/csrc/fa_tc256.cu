@@ -507,10 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1) fa_tc256_kernel(const __grid_cons
                     }
                 }
                 // epilogue: O / l, rounded, staged per warp, whole-line stores; LSE.  The
-                // item's second-to-last product (or the previous item's last one) is known
-                // complete and no later product exists yet, so one parity wait for the last
-                // product is exact.  (Two waits in a row, for the last two products, would
-                // misread the barrier if both had completed before the first.)
+                // item's second-to-last O product (or the previous item's last one) is known
+                // complete and no later O product exists yet (the next item's S products may),
+                // so one parity wait for the last O product is exact.  (Two waits in a row, for
+                // the last two products, would misread the barrier if both had completed
+                // before the first.)
                 pv += (uint32_t)w.nkv;
                 if (!wait_warp(c, b_o_done(), (pv - 1u) & 1u, kRoleSoftmax)) goto sm_out;
                 ptx::tc_fence_after();
